@@ -1,0 +1,457 @@
+#!/usr/bin/env python3
+"""Throughput of the liboss hot path on one GB300 (or N, one process each).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Headline workload (``config.workload``): softmax_32k -- os_softmax_rows over a
+32768 x 8192 fp32 matrix of N(0,1) * 10 logits (1 GiB in, 1 GiB out). A step
+is one os_softmax_rows call; ``value`` is algorithmic GB/s (bytes read + bytes
+written by the definition) over all ranks. The same JSON line carries, under
+``extra``, the attention forward (attn_4k, non-causal; attn_causal) in
+TFLOP/s and split-KV decode + merge (decode_64x32) in GB/s, each with its own
+roofline.
+
+Inputs are seeded and synthetic, resident in HBM before the timed region, and
+larger than the 129 MB L2 (no flush needed). Timing: W untimed steps, then K
+steps bracketed by a barrier and a device synchronise, CUDA events on the
+launching stream, max over ranks. ``--impl reference`` times the fp64 CPU
+oracle on the host cores on bounded samples of the same workload.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+from concurrent.futures import ThreadPoolExecutor
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from pass_attention_gb300 import workloads  # noqa: E402
+
+METRIC = "softmax GB/s & attention fwd TFLOP/s on 1 GB300, as fraction of roofline"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+# DRAM traffic per launch from ncu (dram__bytes_read.sum + dram__bytes_write.sum),
+# keyed by kernel, with the sha256 of the kernel's source file when it was
+# captured: a changed source reports null. Summaries live under profiles/.
+NCU_TRAFFIC = {}
+
+
+# ---------------------------------------------------------------------------
+# helpers
+# ---------------------------------------------------------------------------
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {k: float(p[k]) for k in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained")}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def source_sha(rel):
+    with open(os.path.join(ROOT, rel), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()
+
+
+def traffic_for(kernel):
+    rec = NCU_TRAFFIC.get(kernel)
+    if not rec:
+        return None
+    try:
+        if source_sha(rec["source"]) != rec["sha256"]:
+            return None
+    except OSError:
+        return None
+    return rec["bytes_per_launch"]
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 100 ms."""
+
+    FIELDS = ["timestamp", "index", "clocks.sm", "clocks.max.sm", "power.draw",
+              "clocks_event_reasons.active", "clocks_event_reasons.hw_slowdown",
+              "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, index):
+        self.index = index
+        self.samples = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={','.join(self.FIELDS)}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(self.index)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return self
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) == len(self.FIELDS):
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+
+    def summary(self, t0, t1):
+        inside = [p for (t, p) in self.samples if t0 - 0.15 <= t <= t1 + 0.15]
+        window = "timed region"
+        if not inside:
+            inside = [p for (_, p) in self.samples]
+            window = "whole run (timed region shorter than the 100 ms sampling period)"
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "note": "nvidia-smi unavailable"}
+        sm = [float(p[2]) for p in inside if p[2].replace(".", "").isdigit()]
+        smax = [float(p[3]) for p in inside if p[3].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for p in inside for i in range(4) if p[6 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": reasons,
+                "samples": len(inside), "window": window}
+
+
+def device_index_for_smi(local_rank):
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis:
+        ids = [v.strip() for v in vis.split(",") if v.strip()]
+        if local_rank < len(ids) and ids[local_rank].isdigit():
+            return int(ids[local_rank])
+    return local_rank
+
+
+def time_steps(fn, steps, warmup, stream, barrier):
+    """W untimed calls, then K timed calls with per-step events. Returns
+    (total_ms, mean_step_ms, t_wall0, t_wall1)."""
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    t0 = time.time()
+    with torch.cuda.stream(stream):
+        ev[0].record(stream)
+        for i in range(steps):
+            fn()
+            ev[i + 1].record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    barrier()
+    per = [ev[i].elapsed_time(ev[i + 1]) for i in range(steps)]
+    return ev[0].elapsed_time(ev[steps]), sum(per) / len(per), t0, t1
+
+
+# ---------------------------------------------------------------------------
+# workloads on the GPU
+# ---------------------------------------------------------------------------
+
+def softmax_bytes(rows, cols):
+    return rows * cols * 4 * 2 + rows * 4 * 2  # x read, y written, m and l written
+
+
+def attention_flops(B, H, S, D, causal):
+    if causal:
+        return 4 * B * H * D * (S * (S + 1) // 2)
+    return 4 * B * H * S * S * D
+
+
+def decode_bytes(kv_len, H, D, S):
+    B = len(kv_len)
+    kv = int(sum(int(L) for L in kv_len)) * H * D * 2 * 2   # K and V rows read once
+    q = B * H * D * 2
+    parts = B * H * S * (D + 2) * 4                         # written by decode, read by merge
+    out = B * H * (D * 2 + 4 * 3)                           # O bf16, m, l, lse
+    return kv + q + 2 * parts + out
+
+
+def bench_softmax(args, ctx):
+    import pass_attention_gb300 as oss
+    w = workloads.SOFTMAX_32K
+    x = workloads.logits(w.rows, w.cols, w.mult, w.seed + ctx["rank"], device="cuda")
+    y = torch.empty_like(x)
+    m = torch.empty(w.rows, device="cuda")
+    l = torch.empty(w.rows, device="cuda")
+    stream = torch.cuda.current_stream()
+    fn = lambda: oss.softmax_rows(x, w.scale, y=y, m=m, l=l, stream=stream)
+    total_ms, step_ms, t0, t1 = time_steps(fn, args.steps, args.warmup, stream, ctx["barrier"])
+    nbytes = softmax_bytes(w.rows, w.cols)
+    # end to end: pinned host input -> device -> kernel -> pinned host outputs
+    xh = x.cpu().pin_memory()
+    outs = (torch.empty(x.shape, pin_memory=True), torch.empty(w.rows, pin_memory=True),
+            torch.empty(w.rows, pin_memory=True))
+    e2e_steps = max(1, min(args.steps, 10))
+    oss.softmax_rows_from_host(xh, w.scale, out=outs)
+    torch.cuda.synchronize()
+    ctx["barrier"]()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(e2e_steps):
+        oss.softmax_rows_from_host(xh, w.scale, out=outs)
+    e.record()
+    torch.cuda.synchronize()
+    e2e_ms = s.elapsed_time(e) / e2e_steps
+    del xh, outs
+    return {"workload": w, "total_ms": total_ms, "step_ms": step_ms, "t0": t0, "t1": t1,
+            "nbytes": nbytes, "e2e_ms": e2e_ms, "h2d": w.rows * w.cols * 4,
+            "d2h": w.rows * w.cols * 4 + 2 * w.rows * 4}
+
+
+def bench_attention(args, ctx, w):
+    import pass_attention_gb300 as oss
+    q, k, v = workloads.qkv(w.B, w.H, w.S, w.S, w.D, w.seed, device="cuda")
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H, w.S), device="cuda")
+    stream = torch.cuda.current_stream()
+    fn = lambda: oss.attention_fwd(q, k, v, w.scale, w.causal, o=o, lse=lse, stream=stream)
+    steps = max(3, min(args.steps, 50))
+    total_ms, step_ms, _, _ = time_steps(fn, steps, max(3, args.warmup), stream, ctx["barrier"])
+    oss.check_device_error()
+    flops = attention_flops(w.B, w.H, w.S, w.D, w.causal)
+    return step_ms, flops
+
+
+def bench_decode(args, ctx):
+    import pass_attention_gb300 as oss
+    w = workloads.DECODE_64X32
+    q, k, v, kv = workloads.decode_inputs(w.B, w.H, w.Lmax, w.D, w.seed, device="cuda")
+    S = w.num_splits
+    pm = torch.empty((w.B, w.H, S), device="cuda")
+    pl = torch.empty_like(pm)
+    po = torch.empty((w.B, w.H, S, w.D), device="cuda")
+    o = torch.empty((w.B, w.H, w.D), dtype=torch.bfloat16, device="cuda")
+    mo, lo, lseo = (torch.empty((w.B, w.H), device="cuda") for _ in range(3))
+    stream = torch.cuda.current_stream()
+
+    def fn():
+        oss.attention_decode_splitkv(q, k, v, kv, S, w.scale, pm, pl, po, stream=stream)
+        oss.merge_partials(pm, pl, po, True, o, mo, lo, lseo, stream=stream)
+
+    steps = max(3, min(args.steps, 30))
+    total_ms, step_ms, _, _ = time_steps(fn, steps, max(3, args.warmup), stream, ctx["barrier"])
+    # the decode kernel alone (dominant): events around it only
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * steps)]
+    for i in range(steps):
+        ev[2 * i].record(stream)
+        oss.attention_decode_splitkv(q, k, v, kv, S, w.scale, pm, pl, po, stream=stream)
+        ev[2 * i + 1].record(stream)
+    torch.cuda.synchronize()
+    dec_ms = sum(ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(steps)) / steps
+    kvl = kv.cpu().tolist()
+    nbytes = decode_bytes(kvl, w.H, w.D, S)
+    kv_bytes = int(sum(kvl)) * w.H * w.D * 4
+    dec_bytes = kv_bytes + w.B * w.H * w.D * 2 + w.B * w.H * S * (w.D + 2) * 4
+    del k, v
+    return step_ms, nbytes, dec_ms, dec_bytes
+
+
+# ---------------------------------------------------------------------------
+# the oracle on the host cores
+# ---------------------------------------------------------------------------
+
+def oracle_softmax_rate(seconds, x_np=None):
+    """Time the fp64 oracle's softmax on row chunks of the softmax_32k
+    workload across the host cores (numpy releases the GIL in its ufuncs)
+    until about ``seconds`` have passed. Returns (GB/s, cores, rows)."""
+    import oracle
+    w = workloads.SOFTMAX_32K
+    chunk = 256
+    if x_np is None:
+        x_np = workloads.logits(4096, w.cols, w.mult, w.seed).numpy()
+    cores = os.cpu_count() or 1
+    done_rows = 0
+    t0 = time.perf_counter()
+    with ThreadPoolExecutor(max_workers=cores) as ex:
+        while time.perf_counter() - t0 < seconds:
+            starts = [(i * chunk) % x_np.shape[0] for i in range(cores)]
+            list(ex.map(lambda s: oracle.softmax_rows(x_np[s:s + chunk], w.scale), starts))
+            done_rows += chunk * cores
+    dt = time.perf_counter() - t0
+    return softmax_bytes(done_rows, w.cols) / dt / 1e9, cores, done_rows
+
+
+def run_reference(args, rank):
+    if rank != 0:
+        return
+    w = workloads.SOFTMAX_32K
+    x_np = workloads.logits(4096, w.cols, w.mult, w.seed).numpy()
+    per_step_s = 2.0
+    for _ in range(args.warmup):
+        oracle_softmax_rate(0.2, x_np)
+    t0 = time.perf_counter()
+    rates = []
+    rows_total = 0
+    for _ in range(args.steps):
+        r, cores, rows = oracle_softmax_rate(per_step_s, x_np)
+        rates.append(r)
+        rows_total += rows
+    dt = time.perf_counter() - t0
+    value = softmax_bytes(rows_total, w.cols) / dt / 1e9
+    sample = (f"{rows_total} rows of the {w.rows}x{w.cols} workload over {args.steps} steps "
+              f"(~{per_step_s:.0f} s each), 256-row chunks on {cores} threads")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": f"{w.name} {w.rows}x{w.cols} fp32 N(0,1)*{w.mult:g}",
+                                        "rows": w.rows, "cols": w.cols},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# main
+# ---------------------------------------------------------------------------
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--headline-only", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() and args.impl == "ours" else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local_rank)
+        dist.init_process_group(backend)
+
+    if args.impl == "reference":
+        run_reference(args, rank)
+        if dist:
+            dist.destroy_process_group()
+        return
+
+    import pass_attention_gb300 as oss
+    oss.load()  # fails loudly if the library is not built
+    torch.cuda.set_device(local_rank)
+
+    def barrier():
+        if dist:
+            dist.barrier()
+
+    ctx = {"rank": rank, "barrier": barrier}
+    pk, pk_kind = peaks()
+    sampler = ClockSampler(device_index_for_smi(local_rank)).start()
+
+    sm = bench_softmax(args, ctx)
+    total_ms = sm["total_ms"]
+    step_ms = sm["step_ms"]
+    e2e_ms = sm["e2e_ms"]
+    if dist:
+        t = torch.tensor([total_ms, step_ms, e2e_ms], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms, step_ms, e2e_ms = t.tolist()
+    n = world
+    w = sm["workload"]
+    value = sm["nbytes"] * args.steps * n / (total_ms / 1e3) / 1e9
+    achieved = sm["nbytes"] / (sm["step_ms"] / 1e3) / 1e9
+    kname = "softmax_rows_reg_kernel<8>"
+
+    extra = {}
+    if not args.headline_only:
+        for aw in (workloads.ATTN_4K, workloads.ATTN_CAUSAL):
+            try:
+                ms, flops = bench_attention(args, ctx, aw)
+                tf = flops / (ms / 1e3) / 1e12
+                extra[aw.name] = {
+                    "value": tf, "unit": "TFLOP/s", "ms_per_step": ms,
+                    "workload": f"B{aw.B} H{aw.H} S{aw.S} D{aw.D} bf16 {'causal' if aw.causal else 'non-causal'}",
+                    "roofline": {"bound": "tensor", "achieved": tf, "peak": pk["bf16_tflops"],
+                                 "unit": "TFLOP/s", "frac": tf / pk["bf16_tflops"],
+                                 "traffic": traffic_for("attn_fwd_kernel"),
+                                 "peak_kind": f"{pk_kind} bf16 dense (burst)"}}
+            except Exception as e:  # report, do not hide
+                extra[aw.name] = {"unavailable": f"{type(e).__name__}: {e}"}
+        try:
+            ms, nbytes, dec_ms, dec_bytes = bench_decode(args, ctx)
+            gbs = nbytes / (ms / 1e3) / 1e9
+            ach = dec_bytes / (dec_ms / 1e3) / 1e9
+            extra["decode_64x32"] = {
+                "value": gbs, "unit": "GB/s", "ms_per_step": ms,
+                "workload": "B64 H32 D128 bf16, kv_len~U{1..32768}, 16 splits, decode + merge",
+                "roofline": {"bound": "hbm", "kernel": "decode_splitkv_kernel", "achieved": ach,
+                             "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": ach / pk["hbm_gbs"],
+                             "traffic": traffic_for("decode_splitkv_kernel"),
+                             "peak_kind": f"{pk_kind} HBM copy"}}
+        except Exception as e:
+            extra["decode_64x32"] = {"unavailable": f"{type(e).__name__}: {e}"}
+
+    sampler.stop()
+    clocks = sampler.summary(sm["t0"], sm["t1"])
+
+    cpu = None
+    if rank == 0:
+        rate, cores, rows = oracle_softmax_rate(args.cpu_seconds)
+        cpu = {"value": rate, "unit": "GB/s", "cores": cores, "kind": "oracle",
+               "sample": f"{rows} rows of the {w.rows}x{w.cols} workload in 256-row chunks, "
+                         f"~{args.cpu_seconds:g} s on {cores} host threads"}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": n, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": f"{w.name} {w.rows}x{w.cols} fp32 N(0,1)*{w.mult:g}, scale {w.scale:g}",
+                   "rows": w.rows, "cols": w.cols, "per_rank": "one full matrix per rank",
+                   "l2": "inputs larger than L2 (1 GiB per step), no flush"},
+        "clocks": clocks,
+        "e2e": {"value": sm["nbytes"] * n / (e2e_ms / 1e3) / 1e9, "unit": "GB/s",
+                "h2d_bytes_per_step": sm["h2d"], "d2h_bytes_per_step": sm["d2h"]},
+        "gpu_launches": args.steps,
+        "roofline": {"bound": "hbm", "kernel": kname, "achieved": achieved, "peak": pk["hbm_gbs"],
+                     "unit": "GB/s", "frac": achieved / pk["hbm_gbs"],
+                     "traffic": traffic_for(kname), "peak_kind": f"{pk_kind} HBM copy"},
+        "cpu_baseline": cpu,
+        "extra": extra,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

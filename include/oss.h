@@ -1,0 +1,198 @@
+/*
+ * liboss -- online softmax, fused attention forward, split-KV decode and the
+ * (m, l, O) merge on one NVIDIA GB300 (sm_103a).
+ *
+ * The method: a row's softmax is computed block by block while carrying a
+ * running maximum m and a running sum l of exp(x - m); when a block raises
+ * the maximum, l (and, for attention, the output accumulator O) is multiplied
+ * by exp(m_old - m_new) before the block is added. After the last block
+ * O /= l. Sources: roadmapper "Online softmax" ("The recurrence",
+ * "Initialise honestly"), curionode "The Online Softmax." (introduction,
+ * "One pass, exactly"), metalworking "Online Softmax" (the five-line
+ * recurrence and its closing note on split-KV decode).
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - Tensors are DEVICE pointers allocated and owned by the caller. The
+ *   library never allocates, frees or keeps them.
+ * - Layouts are row-major; the attention tensors are dense [B, H, S, D].
+ * - Each call validates its arguments on the host, then enqueues its kernels
+ *   on `stream` (a cudaStream_t passed as void*; NULL = the legacy default
+ *   stream) and returns without synchronising. A non-OK status means nothing
+ *   was enqueued (except OS_ERR_CUDA, which reports a failed launch).
+ * - Outputs must not overlap inputs or each other.
+ * - m is reported in natural units: m = max of scale * x. l is the sum of
+ *   exp(scale * x - m), i.e. the normaliser relative to the maximum
+ *   (curionode "The Online Softmax.", "Workshop"); lse = m + ln(l).
+ * - A fully masked or empty row reports m = -inf, l = 0, lse = -inf and a
+ *   zero output instead of NaN (roadmapper "Online softmax", "Initialise
+ *   honestly", describes the NaN an unguarded empty block produces).
+ * - bf16 tensors are passed as `os_bf16` (the raw 16-bit patterns).
+ * - The library keeps one device error word per device; kernels that wait
+ *   on an mbarrier give up after a bounded number of polls and set it.
+ *   os_check_device_error reads and clears it.
+ */
+#ifndef OSS_H
+#define OSS_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define OSS_ABI_VERSION 1
+
+#if defined(__GNUC__)
+#define OSS_API __attribute__((visibility("default")))
+#else
+#define OSS_API
+#endif
+
+typedef uint16_t os_bf16; /* IEEE-754 binary32 truncated to its top 16 bits (bfloat16) */
+
+typedef enum os_status {
+  OS_OK = 0,
+  OS_ERR_INVALID_ARGUMENT = 1, /* null pointer, non-positive size, ld < cols, bad scale */
+  OS_ERR_MISALIGNED = 2,       /* a base address or leading dimension is not 16-byte aligned */
+  OS_ERR_UNSUPPORTED = 3,      /* a valid request this version does not implement */
+  OS_ERR_CUDA = 4,             /* a CUDA runtime or driver call failed (launch, attribute, ...) */
+  OS_ERR_TIMEOUT = 5           /* a kernel gave up on a bounded wait (os_check_device_error) */
+} os_status;
+
+/*
+ * os_softmax_rows -- one-pass safe softmax of each row of a row-major matrix.
+ *
+ * Defines (curionode "The Online Softmax.", introduction and "One pass,
+ * exactly"; the running pair (m, l) of roadmapper "Online softmax", "The
+ * recurrence"):
+ *     m[r] = max_j fl32(scale * x[r, j])
+ *     l[r] = sum_j exp(scale * x[r, j] - m[r])
+ *     y[r, j] = exp(scale * x[r, j] - m[r]) / l[r]
+ * computed with exp2 and log2(e) folded into the scale once. Each element of
+ * x is read from HBM once and each element of y written once.
+ *
+ *   x     [rows, ld_x] fp32, device. Entries may be -inf (masked); +inf / NaN
+ *         inputs are undefined.
+ *   y     [rows, ld_y] fp32, device, written for j < cols.
+ *   m, l  [rows] fp32, device, or NULL to skip.
+ *   rows  >= 1; cols >= 1; ld_x >= cols, ld_y >= cols (elements).
+ *   scale finite and > 0.
+ * Alignment: x and y 4-byte aligned. When x and y are 16-byte aligned and
+ * ld_x, ld_y are multiples of 4 the kernel uses 16-byte loads and stores and,
+ * for cols <= 16384, holds each row in registers (one read, one write per
+ * element); otherwise it streams the row twice (two reads, one write).
+ * Errors: OS_ERR_INVALID_ARGUMENT, OS_ERR_MISALIGNED, OS_ERR_CUDA.
+ */
+OSS_API os_status os_softmax_rows(const float* x, float* y, float* m, float* l,
+                          int64_t rows, int64_t cols, int64_t ld_x, int64_t ld_y,
+                          float scale, void* stream);
+
+/*
+ * os_attention_fwd -- fused attention forward that never stores a score row.
+ *
+ * Defines (metalworking "Online Softmax", the five-line recurrence;
+ * curionode "The Online Softmax.", "One pass, exactly", on tiling attention
+ * without storing a row of scores):
+ *     S_ij = scale * q_i . k_j            (j <= i only, when causal)
+ *     o_i  = sum_j exp(S_ij - m_i) v_j / l_i,   lse_i = m_i + ln(l_i)
+ * Keys stream through in tiles; per tile the running (m, l, O) is rescaled
+ * by exp2(m_old - m_new) and the tile added (S = Q K^T and O += P V run on
+ * the tcgen05 tensor cores with fp32 accumulation in tensor memory; P is
+ * rounded to bf16 for the P V product, l sums the fp32 P).
+ *
+ *   q    [B, H, Sq, D] bf16, device.   k, v [B, H, Sk, D] bf16, device.
+ *   o    [B, H, Sq, D] bf16, device (round to nearest even).
+ *   lse  [B, H, Sq] fp32, device (natural log), or NULL to skip.
+ *   B, H, Sq, Sk >= 1.  D == 128 (other head sizes: OS_ERR_UNSUPPORTED).
+ *   scale finite and > 0.
+ *   causal != 0: query i attends to keys 0..i; requires Sq == Sk
+ *   (OS_ERR_UNSUPPORTED otherwise).
+ * Alignment: q, k, v, o 16-byte aligned.
+ * Errors: OS_ERR_INVALID_ARGUMENT, OS_ERR_MISALIGNED, OS_ERR_UNSUPPORTED,
+ * OS_ERR_CUDA; a timed-out internal wait is reported by os_check_device_error.
+ */
+OSS_API os_status os_attention_fwd(const os_bf16* q, const os_bf16* k, const os_bf16* v,
+                           os_bf16* o, float* lse,
+                           int32_t B, int32_t H, int32_t Sq, int32_t Sk, int32_t D,
+                           float scale, int causal, void* stream);
+
+/*
+ * os_attention_decode_splitkv -- one query token per (batch, head) against a
+ * padded KV cache, cut into num_splits chunks, each chunk written as a
+ * partial softmax state (metalworking "Online Softmax", closing note: split-KV
+ * decode merges partial softmaxes with the same correction identity instead
+ * of float atomics).
+ *
+ * For batch b with L = kv_len[b] and chunk = ceil(L / num_splits), split j
+ * covers keys [j*chunk, min(L, (j+1)*chunk)). Its partial is
+ *     part_m = max_t scale * q . k_t                     (natural units)
+ *     part_l = sum_t exp(scale * q . k_t - part_m)
+ *     part_o = sum_t exp(scale * q . k_t - part_m) v_t   (NOT divided by l)
+ * An empty split writes (-inf, 0, 0).
+ *
+ *   q       [B, H, D] bf16, device.
+ *   k, v    [B, H, Lmax, D] bf16, device; only rows t < kv_len[b] are read.
+ *   kv_len  [B] int32, DEVICE; each value in 1..Lmax (values outside are
+ *           clamped to [0, Lmax] on the device; 0 gives all-empty splits).
+ *   part_m, part_l  [B, H, num_splits] fp32, device.
+ *   part_o  [B, H, num_splits, D] fp32, device.
+ *   B, H, Lmax >= 1.  D == 128.  1 <= num_splits <= 64.  scale finite, > 0.
+ * Alignment: q, k, v, part_o 16-byte aligned.
+ * Errors: OS_ERR_INVALID_ARGUMENT, OS_ERR_MISALIGNED, OS_ERR_UNSUPPORTED,
+ * OS_ERR_CUDA.
+ */
+OSS_API os_status os_attention_decode_splitkv(const os_bf16* q, const os_bf16* k, const os_bf16* v,
+                                      const int32_t* kv_len,
+                                      int32_t B, int32_t H, int32_t Lmax, int32_t D,
+                                      int32_t num_splits, float scale,
+                                      float* part_m, float* part_l, float* part_o,
+                                      void* stream);
+
+/*
+ * os_merge_partials -- merge num_splits partial states (m, l, O) per group
+ * with the pairwise identity (curionode "The Online Softmax.", "One pass,
+ * exactly": the identity for pairs of partial results is associative, so
+ * they can be merged in any order or tree):
+ *     m = max(m1, m2);  l = l1 e^(m1-m) + l2 e^(m2-m);  O = O1 e^(m1-m) + O2 e^(m2-m)
+ * in a fixed pairwise tree ((0,1),(2,3),...; an odd element is carried up),
+ * with no atomics, so the result is the same on every run. Two empty sides
+ * merge to (-inf, 0, 0).
+ *
+ *   part_m, part_l  [groups, num_splits] fp32, device.
+ *   part_o          [groups, num_splits, D] fp32, device (unnormalised).
+ *   finalize != 0: o_out is bf16 [groups, D] = O / l (0 for an empty group).
+ *   finalize == 0: o_out is fp32 [groups, D] = the merged unnormalised O, so
+ *                  merges can nest (hierarchical or across shards).
+ *   m_out, l_out, lse_out  [groups] fp32, device, each may be NULL.
+ *   groups >= 1.  1 <= num_splits <= 64.  1 <= D <= 256, D % 4 == 0.
+ * Alignment: part_o and o_out 16-byte aligned.
+ * Errors: OS_ERR_INVALID_ARGUMENT, OS_ERR_MISALIGNED, OS_ERR_UNSUPPORTED,
+ * OS_ERR_CUDA.
+ */
+OSS_API os_status os_merge_partials(const float* part_m, const float* part_l, const float* part_o,
+                            int64_t groups, int32_t num_splits, int32_t D, int finalize,
+                            void* o_out, float* m_out, float* l_out, float* lse_out,
+                            void* stream);
+
+/*
+ * os_check_device_error -- synchronise `stream`, then read and clear the
+ * current device's error word. *code receives 0 when no kernel gave up on a
+ * wait since the last check, otherwise an OS_ERR_TIMEOUT detail code
+ * (bits 0..7 = kernel id, bits 8..15 = wait site). Returns OS_ERR_TIMEOUT
+ * when the word was set, OS_ERR_CUDA when a CUDA call failed, OS_OK otherwise.
+ * `code` may be NULL.
+ */
+OSS_API os_status os_check_device_error(void* stream, int32_t* code);
+
+/* Human-readable name of a status (static storage; never NULL). */
+OSS_API const char* os_status_string(os_status status);
+
+/* OSS_ABI_VERSION of the loaded library. */
+OSS_API int32_t os_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* OSS_H */

@@ -1,2 +1,330 @@
-"""liboss: online-softmax row softmax, attention forward, split-KV decode and
-partial merge on one GB300 (sm_103a)."""
+"""liboss: online-softmax row softmax, fused attention forward, split-KV
+decode and the (m, l, O) merge on one GB300 (sm_103a).
+
+This module is the thin Python binding over the C ABI in ``include/oss.h``:
+it checks tensor dtypes and devices, allocates outputs with PyTorch, passes
+raw device pointers and the current CUDA stream to ``liboss.so`` and turns a
+non-OK status into an exception. Every step of the computation runs in the
+library's CUDA kernels; there is no CPU fallback, and a missing library is an
+error.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from typing import Optional
+
+import torch
+
+__all__ = [
+    "OssError",
+    "library_path",
+    "load",
+    "softmax_rows",
+    "softmax_rows_from_host",
+    "attention_fwd",
+    "attention_fwd_from_host",
+    "attention_decode_splitkv",
+    "merge_partials",
+    "decode_from_host",
+    "check_device_error",
+    "abi_version",
+    "EXPORTED_SYMBOLS",
+]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "liboss.so")
+
+OS_OK = 0
+STATUS_NAMES = {
+    0: "OS_OK",
+    1: "OS_ERR_INVALID_ARGUMENT",
+    2: "OS_ERR_MISALIGNED",
+    3: "OS_ERR_UNSUPPORTED",
+    4: "OS_ERR_CUDA",
+    5: "OS_ERR_TIMEOUT",
+}
+
+_vp = ctypes.c_void_p
+_i32 = ctypes.c_int32
+_i64 = ctypes.c_int64
+_f32 = ctypes.c_float
+
+# name -> (restype, argtypes), the signatures of include/oss.h
+_SIGNATURES = {
+    "os_softmax_rows": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _f32, _vp]),
+    "os_attention_fwd": (_i32, [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _f32,
+                                ctypes.c_int, _vp]),
+    "os_attention_decode_splitkv": (_i32, [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32,
+                                           _f32, _vp, _vp, _vp, _vp]),
+    "os_merge_partials": (_i32, [_vp, _vp, _vp, _i64, _i32, _i32, ctypes.c_int, _vp, _vp, _vp,
+                                 _vp, _vp]),
+    "os_check_device_error": (_i32, [_vp, ctypes.POINTER(_i32)]),
+    "os_status_string": (ctypes.c_char_p, [_i32]),
+    "os_abi_version": (_i32, []),
+}
+EXPORTED_SYMBOLS = tuple(_SIGNATURES)
+
+_lib: Optional[ctypes.CDLL] = None
+
+
+class OssError(RuntimeError):
+    """A liboss call returned a non-OK status."""
+
+    def __init__(self, status: int, where: str):
+        self.status = int(status)
+        super().__init__(f"{where}: {STATUS_NAMES.get(self.status, self.status)}")
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load() -> ctypes.CDLL:
+    """Load liboss.so (built by ``pass_attention_gb300.build_lib``)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(
+                f"liboss is not built ({_LIB_PATH} is missing); build it with "
+                "`python -m pass_attention_gb300.build_lib`")
+        lib = ctypes.CDLL(_LIB_PATH)
+        for name, (res, args) in _SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+    return _lib
+
+
+def abi_version() -> int:
+    return int(load().os_abi_version())
+
+
+def _check(status: int, where: str) -> None:
+    if status != OS_OK:
+        raise OssError(status, where)
+
+
+def _stream_ptr(stream) -> int:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else t.data_ptr()
+
+
+def _need(t: torch.Tensor, name: str, dtype: torch.dtype, ndim: int) -> None:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (liboss has no CPU path)")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dimensions, got {t.dim()}")
+
+
+def _dense(t: torch.Tensor, name: str) -> None:
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+# ---------------------------------------------------------------------------
+# os_softmax_rows
+# ---------------------------------------------------------------------------
+
+def softmax_rows(x: torch.Tensor, scale: float = 1.0, y: Optional[torch.Tensor] = None,
+                 m: Optional[torch.Tensor] = None, l: Optional[torch.Tensor] = None,
+                 stream=None):
+    """Row softmax of ``scale * x`` (fp32 [rows, cols], unit column stride).
+
+    Returns ``(y, m, l)``; see ``os_softmax_rows`` in include/oss.h.
+    """
+    _need(x, "x", torch.float32, 2)
+    if x.stride(1) != 1:
+        raise ValueError("x must have unit column stride")
+    rows, cols = x.shape
+    if y is None:
+        y = torch.empty((rows, cols), dtype=torch.float32, device=x.device)
+    _need(y, "y", torch.float32, 2)
+    if y.stride(1) != 1 or tuple(y.shape) != (rows, cols):
+        raise ValueError("y must be [rows, cols] with unit column stride")
+    if m is None:
+        m = torch.empty(rows, dtype=torch.float32, device=x.device)
+    if l is None:
+        l = torch.empty(rows, dtype=torch.float32, device=x.device)
+    _need(m, "m", torch.float32, 1)
+    _need(l, "l", torch.float32, 1)
+    st = load().os_softmax_rows(x.data_ptr(), y.data_ptr(), m.data_ptr(), l.data_ptr(), rows,
+                                cols, x.stride(0), y.stride(0), float(scale),
+                                _stream_ptr(stream))
+    _check(st, "os_softmax_rows")
+    return y, m, l
+
+
+def softmax_rows_from_host(x_host: torch.Tensor, scale: float = 1.0, out=None, device="cuda"):
+    """End-to-end call on host memory: copy x to the GPU, run os_softmax_rows,
+    copy y, m and l back into (pinned) host tensors. Returns host (y, m, l)."""
+    x_dev = x_host.to(device, non_blocking=True)
+    y, m, l = softmax_rows(x_dev, scale)
+    if out is None:
+        out = (torch.empty(y.shape, dtype=y.dtype, pin_memory=True),
+               torch.empty(m.shape, dtype=m.dtype, pin_memory=True),
+               torch.empty(l.shape, dtype=l.dtype, pin_memory=True))
+    for dst, src in zip(out, (y, m, l)):
+        dst.copy_(src, non_blocking=True)
+    torch.cuda.current_stream().synchronize()
+    return out
+
+
+# ---------------------------------------------------------------------------
+# os_attention_fwd
+# ---------------------------------------------------------------------------
+
+def attention_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                  scale: Optional[float] = None, causal: bool = False,
+                  o: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                  stream=None):
+    """Fused attention forward on bf16 [B, H, S, D] tensors.
+
+    Returns ``(o, lse)``; see ``os_attention_fwd`` in include/oss.h.
+    """
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, n, torch.bfloat16, 4)
+        _dense(t, n)
+    B, H, Sq, D = q.shape
+    Sk = k.shape[2]
+    if tuple(k.shape) != (B, H, Sk, D) or tuple(v.shape) != (B, H, Sk, D):
+        raise ValueError("k and v must be [B, H, Sk, D] matching q")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if o is None:
+        o = torch.empty_like(q)
+    _need(o, "o", torch.bfloat16, 4)
+    _dense(o, "o")
+    if lse is None:
+        lse = torch.empty((B, H, Sq), dtype=torch.float32, device=q.device)
+    st = load().os_attention_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                 lse.data_ptr(), B, H, Sq, Sk, D, float(scale), int(bool(causal)),
+                                 _stream_ptr(stream))
+    _check(st, "os_attention_fwd")
+    return o, lse
+
+
+def attention_fwd_from_host(q_host, k_host, v_host, scale=None, causal=False, out=None,
+                            device="cuda"):
+    """End-to-end call on host memory: copy q, k, v to the GPU, run
+    os_attention_fwd, copy o and lse back. Returns host (o, lse)."""
+    q, k, v = (t.to(device, non_blocking=True) for t in (q_host, k_host, v_host))
+    o, lse = attention_fwd(q, k, v, scale, causal)
+    if out is None:
+        out = (torch.empty(o.shape, dtype=o.dtype, pin_memory=True),
+               torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True))
+    out[0].copy_(o, non_blocking=True)
+    out[1].copy_(lse, non_blocking=True)
+    torch.cuda.current_stream().synchronize()
+    return out
+
+
+# ---------------------------------------------------------------------------
+# os_attention_decode_splitkv / os_merge_partials
+# ---------------------------------------------------------------------------
+
+def attention_decode_splitkv(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                             kv_len: torch.Tensor, num_splits: int,
+                             scale: Optional[float] = None, part_m=None, part_l=None,
+                             part_o=None, stream=None):
+    """Split-KV decode partials. q [B, H, D], k/v [B, H, Lmax, D] bf16,
+    kv_len [B] int32 (device). Returns ``(part_m, part_l, part_o)``."""
+    _need(q, "q", torch.bfloat16, 3)
+    _need(k, "k", torch.bfloat16, 4)
+    _need(v, "v", torch.bfloat16, 4)
+    _need(kv_len, "kv_len", torch.int32, 1)
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (kv_len, "kv_len")):
+        _dense(t, n)
+    B, H, D = q.shape
+    Lmax = k.shape[2]
+    if tuple(k.shape) != (B, H, Lmax, D) or tuple(v.shape) != (B, H, Lmax, D):
+        raise ValueError("k and v must be [B, H, Lmax, D] matching q")
+    if kv_len.numel() != B:
+        raise ValueError("kv_len must have B entries")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    S = int(num_splits)
+    dev = q.device
+    if part_m is None:
+        part_m = torch.empty((B, H, S), dtype=torch.float32, device=dev)
+    if part_l is None:
+        part_l = torch.empty((B, H, S), dtype=torch.float32, device=dev)
+    if part_o is None:
+        part_o = torch.empty((B, H, S, D), dtype=torch.float32, device=dev)
+    st = load().os_attention_decode_splitkv(q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                            kv_len.data_ptr(), B, H, Lmax, D, S, float(scale),
+                                            part_m.data_ptr(), part_l.data_ptr(),
+                                            part_o.data_ptr(), _stream_ptr(stream))
+    _check(st, "os_attention_decode_splitkv")
+    return part_m, part_l, part_o
+
+
+def merge_partials(part_m: torch.Tensor, part_l: torch.Tensor, part_o: torch.Tensor,
+                   finalize: bool = True, o_out=None, m_out=None, l_out=None, lse_out=None,
+                   stream=None):
+    """Merge partials over their split axis. part_m/part_l [..., S],
+    part_o [..., S, D] fp32. Returns ``(o, m, l, lse)`` with o bf16 [..., D]
+    (finalize) or fp32 [..., D] (unnormalised, finalize=False)."""
+    for t, n in ((part_m, "part_m"), (part_l, "part_l"), (part_o, "part_o")):
+        if not t.is_cuda or t.dtype != torch.float32:
+            raise TypeError(f"{n} must be a CUDA float32 tensor")
+        _dense(t, n)
+    lead = tuple(part_m.shape[:-1])
+    S = part_m.shape[-1]
+    D = part_o.shape[-1]
+    if tuple(part_l.shape) != tuple(part_m.shape) or tuple(part_o.shape) != lead + (S, D):
+        raise ValueError("partials must be [..., S] and [..., S, D]")
+    groups = 1
+    for n in lead:
+        groups *= n
+    dev = part_m.device
+    if o_out is None:
+        o_out = torch.empty(lead + (D,), dtype=torch.bfloat16 if finalize else torch.float32,
+                            device=dev)
+    if m_out is None:
+        m_out = torch.empty(lead, dtype=torch.float32, device=dev)
+    if l_out is None:
+        l_out = torch.empty(lead, dtype=torch.float32, device=dev)
+    if lse_out is None:
+        lse_out = torch.empty(lead, dtype=torch.float32, device=dev)
+    st = load().os_merge_partials(part_m.data_ptr(), part_l.data_ptr(), part_o.data_ptr(), groups,
+                                  S, D, int(bool(finalize)), o_out.data_ptr(), _ptr(m_out),
+                                  _ptr(l_out), _ptr(lse_out), _stream_ptr(stream))
+    _check(st, "os_merge_partials")
+    return o_out, m_out, l_out, lse_out
+
+
+def decode_from_host(q_host, k_host, v_host, kv_len_host, num_splits, scale=None, out=None,
+                     device="cuda"):
+    """End-to-end split-KV decode on host memory: copy inputs to the GPU, run
+    the decode partials and the merge, copy o and lse back."""
+    q, k, v, kv = (t.to(device, non_blocking=True) for t in (q_host, k_host, v_host, kv_len_host))
+    pm, pl, po = attention_decode_splitkv(q, k, v, kv, num_splits, scale)
+    o, _, _, lse = merge_partials(pm, pl, po, finalize=True)
+    if out is None:
+        out = (torch.empty(o.shape, dtype=o.dtype, pin_memory=True),
+               torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True))
+    out[0].copy_(o, non_blocking=True)
+    out[1].copy_(lse, non_blocking=True)
+    torch.cuda.current_stream().synchronize()
+    return out
+
+
+def check_device_error(stream=None) -> int:
+    """Synchronise ``stream`` and read/clear the device error word; raises
+    OssError(OS_ERR_TIMEOUT) when a kernel gave up on a bounded wait."""
+    code = _i32(0)
+    st = load().os_check_device_error(_stream_ptr(stream), ctypes.byref(code))
+    _check(st, f"os_check_device_error (code {code.value:#x})")
+    return int(code.value)

@@ -1,0 +1,132 @@
+// The C ABI of liboss (include/oss.h): host-side validation, then launch.
+// Nothing here synchronises, allocates or prints.
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+
+#include <cuda_runtime.h>
+
+#include "../../include/oss.h"
+#include "oss_internal.h"
+
+// One error word per device, written by kernels that give up on a bounded
+// wait (first code wins) and read back by os_check_device_error.
+__device__ unsigned int g_oss_error_word;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+unsigned int* g_err_ptr[kMaxDevices];  // device address of g_oss_error_word, per device
+
+unsigned int* error_word() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  if (!g_err_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_oss_error_word) != cudaSuccess) return nullptr;
+    g_err_ptr[dev] = static_cast<unsigned int*>(p);
+  }
+  return g_err_ptr[dev];
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+os_status from_cuda(cudaError_t e) {
+  if (e == cudaSuccess) return OS_OK;
+  if (e == cudaErrorNotSupported) return OS_ERR_UNSUPPORTED;
+  return OS_ERR_CUDA;
+}
+
+bool valid_scale(float s) { return std::isfinite(s) && s > 0.f; }
+
+}  // namespace
+
+extern "C" {
+
+int32_t os_abi_version(void) { return OSS_ABI_VERSION; }
+
+const char* os_status_string(os_status status) {
+  switch (status) {
+    case OS_OK: return "OS_OK";
+    case OS_ERR_INVALID_ARGUMENT: return "OS_ERR_INVALID_ARGUMENT";
+    case OS_ERR_MISALIGNED: return "OS_ERR_MISALIGNED";
+    case OS_ERR_UNSUPPORTED: return "OS_ERR_UNSUPPORTED";
+    case OS_ERR_CUDA: return "OS_ERR_CUDA";
+    case OS_ERR_TIMEOUT: return "OS_ERR_TIMEOUT";
+  }
+  return "OS_ERR_UNKNOWN";
+}
+
+os_status os_softmax_rows(const float* x, float* y, float* m, float* l, int64_t rows,
+                          int64_t cols, int64_t ld_x, int64_t ld_y, float scale, void* stream) {
+  if (!x || !y) return OS_ERR_INVALID_ARGUMENT;
+  if (rows <= 0 || cols <= 0 || ld_x < cols || ld_y < cols) return OS_ERR_INVALID_ARGUMENT;
+  if (cols > (int64_t(1) << 30) || rows > (int64_t(1) << 40)) return OS_ERR_INVALID_ARGUMENT;
+  if (!valid_scale(scale)) return OS_ERR_INVALID_ARGUMENT;
+  if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y)) & 3u) return OS_ERR_MISALIGNED;
+  return from_cuda(oss::launch_softmax_rows(x, y, m, l, rows, cols, ld_x, ld_y, scale,
+                                            static_cast<cudaStream_t>(stream)));
+}
+
+os_status os_attention_fwd(const os_bf16* q, const os_bf16* k, const os_bf16* v, os_bf16* o,
+                           float* lse, int32_t B, int32_t H, int32_t Sq, int32_t Sk, int32_t D,
+                           float scale, int causal, void* stream) {
+  if (!q || !k || !v || !o) return OS_ERR_INVALID_ARGUMENT;
+  if (B <= 0 || H <= 0 || Sq <= 0 || Sk <= 0 || D <= 0) return OS_ERR_INVALID_ARGUMENT;
+  if (!valid_scale(scale)) return OS_ERR_INVALID_ARGUMENT;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return OS_ERR_MISALIGNED;
+  if (D != 128) return OS_ERR_UNSUPPORTED;
+  if (causal && Sq != Sk) return OS_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(B) * H > 65535 * 64) return OS_ERR_UNSUPPORTED;
+  unsigned int* err = error_word();
+  if (!err) return OS_ERR_CUDA;
+  return from_cuda(oss::launch_attention_fwd(q, k, v, o, lse, B, H, Sq, Sk, D, scale,
+                                             causal != 0, err,
+                                             static_cast<cudaStream_t>(stream)));
+}
+
+os_status os_attention_decode_splitkv(const os_bf16* q, const os_bf16* k, const os_bf16* v,
+                                      const int32_t* kv_len, int32_t B, int32_t H, int32_t Lmax,
+                                      int32_t D, int32_t num_splits, float scale, float* part_m,
+                                      float* part_l, float* part_o, void* stream) {
+  if (!q || !k || !v || !kv_len || !part_m || !part_l || !part_o) return OS_ERR_INVALID_ARGUMENT;
+  if (B <= 0 || H <= 0 || Lmax <= 0 || D <= 0 || num_splits <= 0) return OS_ERR_INVALID_ARGUMENT;
+  if (!valid_scale(scale)) return OS_ERR_INVALID_ARGUMENT;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(part_o))
+    return OS_ERR_MISALIGNED;
+  if (D != 128 || num_splits > 64 || B > 65535 || H > 65535) return OS_ERR_UNSUPPORTED;
+  return from_cuda(oss::launch_decode_splitkv(q, k, v, kv_len, B, H, Lmax, D, num_splits, scale,
+                                              part_m, part_l, part_o,
+                                              static_cast<cudaStream_t>(stream)));
+}
+
+os_status os_merge_partials(const float* part_m, const float* part_l, const float* part_o,
+                            int64_t groups, int32_t num_splits, int32_t D, int finalize,
+                            void* o_out, float* m_out, float* l_out, float* lse_out,
+                            void* stream) {
+  if (!part_m || !part_l || !part_o || !o_out) return OS_ERR_INVALID_ARGUMENT;
+  if (groups <= 0 || num_splits <= 0 || D <= 0) return OS_ERR_INVALID_ARGUMENT;
+  if (!aligned16(part_o) || !aligned16(o_out)) return OS_ERR_MISALIGNED;
+  if (num_splits > 64 || D > 256 || (D & 3)) return OS_ERR_UNSUPPORTED;
+  return from_cuda(oss::launch_merge_partials(part_m, part_l, part_o, groups, num_splits, D,
+                                              finalize, o_out, m_out, l_out, lse_out,
+                                              static_cast<cudaStream_t>(stream)));
+}
+
+os_status os_check_device_error(void* stream, int32_t* code) {
+  if (code) *code = 0;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return OS_ERR_CUDA;
+  unsigned int* err = error_word();
+  if (!err) return OS_ERR_CUDA;
+  unsigned int word = 0;
+  if (cudaMemcpyAsync(&word, err, sizeof(word), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return OS_ERR_CUDA;
+  if (cudaMemsetAsync(err, 0, sizeof(word), s) != cudaSuccess) return OS_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return OS_ERR_CUDA;
+  if (code) *code = static_cast<int32_t>(word);
+  return word ? OS_ERR_TIMEOUT : OS_OK;
+}
+
+}  // extern "C"

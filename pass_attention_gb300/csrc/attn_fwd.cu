@@ -1,0 +1,639 @@
+// G2: fused attention forward on the tcgen05 tensor cores (sm_103a).
+//
+// Per tile of scores S the running state of each query row is updated as the
+// metalworking page's five-line recurrence states it ("Online Softmax"):
+//   m_new = max(m, rowmax S);  c = 2^(m - m_new);  P = 2^(S - m_new);
+//   l = l*c + rowsum P;        O = O*c + P V;      m = m_new;
+// and after the last tile O /= l. Scores are kept in base 2 with
+// scale * log2(e) folded in once, and every exponential is exp2, the rescale
+// factor included (roadmapper "Online softmax", "Things that break"). The
+// state starts at m = -inf, l = 0; a row whose keys are all masked so far
+// subtracts 0 instead of -inf, so P = 0 and no NaN appears (roadmapper,
+// "Initialise honestly"). No score row is ever written to memory (curionode
+// "The Online Softmax.", "One pass, exactly").
+//
+// CTA layout (384 threads, one CTA per SM):
+//   * 2 query tiles of 128 rows share every K/V tile of 128 keys.
+//   * warp 0      -- TMA producer: Q once, then K/V tiles into a 2-stage ring.
+//   * warp 1      -- owns tensor memory and issues the MMAs (one thread):
+//                    S_t = Q_t K^T (A, B from shared memory) and
+//                    O_t += P_t V (A = P from tensor memory, B from shared).
+//   * warps 4..7  -- softmax for query tile 0; warps 8..11 for tile 1. Each
+//                    thread owns one query row = one tensor-memory lane.
+// Tensor memory (512 fp32 columns x 128 lanes): S_0 | S_1 | O_0 | O_1, with
+// P_t (bf16 pairs) written over the first 64 columns of S_t.
+//
+// Causal: query i sees keys 0..i (Sq == Sk). KV tiles wholly above the
+// diagonal are skipped; the diagonal tiles are visited first, from the last
+// one down, so query tile 0 meets a KV tile in which all of its rows are
+// masked before it meets any visible key -- the case the guard exists for.
+//
+// Every wait on an mbarrier is bounded: on timeout the thread raises a
+// CTA-wide abort flag and writes the device error word; all roles then drain
+// their own in-flight copies and MMAs (again with a bound), and tensor memory
+// is released before the CTA exits.
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "device_common.cuh"
+#include "oss_internal.h"
+
+namespace oss {
+namespace {
+
+constexpr int kD = 128;           // head dimension
+constexpr int kBM = 128;          // query rows per tile (= tensor-memory lanes)
+constexpr int kTilesPerCta = 2;   // query tiles per CTA
+constexpr int kBN = 128;          // keys per KV tile
+constexpr int kStages = 2;        // K/V ring depth
+constexpr int kThreads = 384;
+constexpr int kSoftmaxWarp0 = 4;
+constexpr int kRowsPerCta = kBM * kTilesPerCta;
+
+// shared memory (bytes from the 1024-aligned base)
+constexpr int kHalfTile = kBM * 64 * 2;            // 128 rows x 64 bf16 = 16 KB
+constexpr int kTileBytes = 2 * kHalfTile;          // 128 x 128 bf16 = 32 KB
+constexpr int kOffQ = 0;                           // Q_0, Q_1
+constexpr int kOffK = kOffQ + kTilesPerCta * kTileBytes;
+constexpr int kOffV = kOffK + kStages * kTileBytes;
+constexpr int kOffEnd = kOffV + kStages * kTileBytes;  // 192 KB
+constexpr int kSmemBytes = kOffEnd + 1024;             // + alignment slack
+
+// tensor-memory columns: S_t at 128 t, O_t at 256 + 128 t
+constexpr uint32_t kTmemCols = 512;
+__device__ __forceinline__ uint32_t col_s(int t) { return 128u * t; }
+__device__ __forceinline__ uint32_t col_o(int t) { return 256u + 128u * t; }
+
+constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s per wait
+constexpr uint64_t kDrainNs = 200000000ull;     // 0.2 s to drain own copies
+
+// wait sites (error word bits 8..15)
+enum Site : unsigned int {
+  kSiteQFull = 1, kSiteKFull, kSiteVFull, kSiteKEmpty, kSiteVEmpty,
+  kSiteSFull, kSitePReady, kSiteODone, kSiteDrain
+};
+
+// ---------------------------------------------------------------------------
+// PTX wrappers
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t global_timer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait. Returns false on timeout (after raising the abort flag and
+// recording the site) or when another thread has already aborted.
+__device__ __noinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                      unsigned int* err, unsigned int site) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer();
+  for (uint32_t n = 1;; ++n) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if ((n & 63u) == 0 && global_timer() - t0 > kTimeoutNs) {
+      *abort_flag = 1;
+      report_error(err, kKernelAttnFwd | (site << 8));
+      return false;
+    }
+  }
+}
+
+// Bounded wait used while draining: ignores the abort flag.
+__device__ __noinline__ bool drain_bar(uint32_t bar, uint32_t parity, unsigned int* err) {
+  const uint64_t t0 = global_timer();
+  for (uint32_t n = 0;; ++n) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((n & 63u) == 0 && global_timer() - t0 > kDrainNs) {
+      report_error(err, kKernelAttnFwd | (kSiteDrain << 8));
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int c0, int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      : "memory");
+}
+
+// D[tmem] (+)= A[smem] * B[smem]
+__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                       uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// D[tmem] (+)= A[tmem] * B[smem]
+__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                       uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+#define OSS_R8(i) "=r"(r[i]), "=r"(r[i + 1]), "=r"(r[i + 2]), "=r"(r[i + 3]), \
+                  "=r"(r[i + 4]), "=r"(r[i + 5]), "=r"(r[i + 6]), "=r"(r[i + 7])
+#define OSS_W8(i) "r"(r[i]), "r"(r[i + 1]), "r"(r[i + 2]), "r"(r[i + 3]), \
+                  "r"(r[i + 4]), "r"(r[i + 5]), "r"(r[i + 6]), "r"(r[i + 7])
+#define OSS_RW8(i) "+r"(r[i]), "+r"(r[i + 1]), "+r"(r[i + 2]), "+r"(r[i + 3]), \
+                   "+r"(r[i + 4]), "+r"(r[i + 5]), "+r"(r[i + 6]), "+r"(r[i + 7])
+
+// 32 consecutive columns of this warp's 32 lanes: thread i gets lane i.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : OSS_R8(0), OSS_R8(8), OSS_R8(16), OSS_R8(24)
+      : "r"(taddr));
+}
+
+// Completes outstanding tcgen05.ld of this thread; the register operands tie
+// the loaded values to the wait so no use is scheduled before it.
+__device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[32]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+  asm volatile("" : OSS_RW8(0), OSS_RW8(8), OSS_RW8(16), OSS_RW8(24));
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      OSS_W8(0), OSS_W8(8), OSS_W8(16), OSS_W8(24)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_wait() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  uint32_t w;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(w) : "f"(hi), "f"(lo));
+  return w;
+}
+
+// ---------------------------------------------------------------------------
+// Descriptors
+// ---------------------------------------------------------------------------
+
+// Shared-memory matrix descriptor, 128-byte swizzle: start address, leading
+// and stride byte offsets (16-byte units), the fixed 0b001 field at bit 46,
+// swizzle mode 2 at bits 61..63.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) |
+         (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) |
+         (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) |
+         (static_cast<uint64_t>(1) << 46) | (static_cast<uint64_t>(2) << 61);
+}
+
+// Instruction descriptor, kind::f16: fp32 accumulator (bits 4-5 = 1), A and B
+// bf16 (bits 7-9 = 1, 10-12 = 1), A K-major, B K-major (bit 16 = 0) or
+// N-major (bit 16 = 1), N >> 3 at bits 17-22, M >> 4 at bits 24-28.
+constexpr uint32_t make_idesc(uint32_t M, uint32_t N, bool b_mn_major) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) |
+         ((N >> 3) << 17) | ((M >> 4) << 24);
+}
+constexpr uint32_t kIdescQK = make_idesc(kBM, kBN, false);  // S = Q K^T
+constexpr uint32_t kIdescPV = make_idesc(kBM, kD, true);    // O += P V
+
+// K-major operand of 128-byte rows (64 bf16), 8-row groups 1024 bytes apart,
+// the 128-wide contraction split in two 64-wide halves `half_bytes` apart.
+// MMA step kk covers contraction elements [16 kk, 16 kk + 16).
+__device__ __forceinline__ uint64_t kmajor_desc(uint32_t base, uint32_t half_bytes, int kk) {
+  return smem_desc(base + (kk >> 2) * half_bytes + (kk & 3) * 32, 16, 1024);
+}
+
+// V tile [128 keys][128 dims] stored as two [128][64] halves (dims 0-63,
+// 64-127): N-major operand for O += P V. Step kk covers keys [16 kk, 16 kk+16)
+// = two 8-key groups (2048 bytes); the dim halves are kHalfTile apart.
+__device__ __forceinline__ uint64_t v_desc(uint32_t base, int kk) {
+  return smem_desc(base + kk * 2048, kHalfTile, 1024);
+}
+
+// ---------------------------------------------------------------------------
+// The kernel
+// ---------------------------------------------------------------------------
+
+struct AttnParams {
+  uint16_t* o;
+  float* lse;
+  unsigned int* err;
+  int Sq, Sk, BH, n_qblocks;
+  float C;  // scale * log2(e)
+  int causal;
+};
+
+struct Barriers {
+  uint64_t q_full;
+  uint64_t k_full[kStages], v_full[kStages], k_empty[kStages], v_empty[kStages];
+  uint64_t s_full[kTilesPerCta], p_ready[kTilesPerCta], o_done[kTilesPerCta];
+  uint64_t drain;
+};
+
+__global__ void __launch_bounds__(kThreads, 1)
+attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
+                const __grid_constant__ CUtensorMap tmap_k,
+                const __grid_constant__ CUtensorMap tmap_v, const AttnParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ Barriers bars;
+  __shared__ uint32_t tmem_base_slot;
+  __shared__ int abort_flag_s;
+  volatile int* abort_flag = &abort_flag_s;
+
+  const uint32_t raw = smem_addr(smem_raw);
+  const uint32_t sbase = (raw + 1023u) & ~1023u;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  // tile coordinates: heaviest causal query blocks first
+  const int lin = blockIdx.x;
+  const int qb_lin = lin / p.BH;
+  const int bh = lin - qb_lin * p.BH;
+  const int qb = p.causal ? (p.n_qblocks - 1 - qb_lin) : qb_lin;
+  const int q0 = qb * kRowsPerCta;
+  const int kv_end = p.causal ? min(p.Sk, q0 + kRowsPerCta) : p.Sk;
+  const int n_kv = (kv_end + kBN - 1) / kBN;
+  const int diag_first = p.causal ? (q0 / kBN) : n_kv;  // tiles >= this touch the diagonal
+  const int n_diag = n_kv - diag_first;
+  auto kv_tile = [&](int j) { return j < n_diag ? (n_kv - 1 - j) : (j - n_diag); };
+
+  if (threadIdx.x == 0) {
+    mbar_init(smem_addr(&bars.q_full), 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(smem_addr(&bars.k_full[s]), 1);
+      mbar_init(smem_addr(&bars.v_full[s]), 1);
+      mbar_init(smem_addr(&bars.k_empty[s]), 1);
+      mbar_init(smem_addr(&bars.v_empty[s]), 1);
+    }
+    for (int t = 0; t < kTilesPerCta; ++t) {
+      mbar_init(smem_addr(&bars.s_full[t]), 1);
+      mbar_init(smem_addr(&bars.p_ready[t]), kBM);
+      mbar_init(smem_addr(&bars.o_done[t]), 1);
+    }
+    mbar_init(smem_addr(&bars.drain), 1);
+    abort_flag_s = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_addr(&tmem_base_slot)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    tc_fence_before();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = tmem_base_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_k)) : "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_v)) : "memory");
+      const uint32_t qbar = smem_addr(&bars.q_full);
+      mbar_expect_tx(qbar, kTilesPerCta * kTileBytes);
+      for (int t = 0; t < kTilesPerCta; ++t)
+        for (int h = 0; h < 2; ++h)
+          tma_load_3d(sbase + kOffQ + t * kTileBytes + h * kHalfTile, &tmap_q, qbar, h * 64,
+                      q0 + t * kBM, bh);
+      int issued = 0;
+      for (int j = 0; j < n_kv; ++j) {
+        const int s = j % kStages;
+        const int round = j / kStages;
+        const int key0 = kv_tile(j) * kBN;
+        if (round > 0 && !wait_bar(smem_addr(&bars.k_empty[s]), (round - 1) & 1, abort_flag, p.err,
+                                   kSiteKEmpty))
+          break;
+        const uint32_t kb = smem_addr(&bars.k_full[s]);
+        mbar_expect_tx(kb, kTileBytes);
+        for (int h = 0; h < 2; ++h)
+          tma_load_3d(sbase + kOffK + s * kTileBytes + h * kHalfTile, &tmap_k, kb, h * 64, key0, bh);
+        if (round > 0 && !wait_bar(smem_addr(&bars.v_empty[s]), (round - 1) & 1, abort_flag, p.err,
+                                   kSiteVEmpty)) {
+          issued = 2 * j + 1;
+          break;
+        }
+        const uint32_t vb = smem_addr(&bars.v_full[s]);
+        mbar_expect_tx(vb, kTileBytes);
+        for (int h = 0; h < 2; ++h)
+          tma_load_3d(sbase + kOffV + s * kTileBytes + h * kHalfTile, &tmap_v, vb, h * 64, key0, bh);
+        issued = 2 * j + 2;
+      }
+      // drain: every issued copy must land before the CTA may exit
+      drain_bar(qbar, 0, p.err);
+      for (int c = issued - 1; c >= 0 && c >= issued - 2 * kStages; --c) {
+        const int j = c >> 1;
+        const int s = j % kStages;
+        const uint32_t b = (c & 1) ? smem_addr(&bars.v_full[s]) : smem_addr(&bars.k_full[s]);
+        drain_bar(b, (j / kStages) & 1, p.err);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      bool ok = wait_bar(smem_addr(&bars.q_full), 0, abort_flag, p.err, kSiteQFull);
+      for (int j = 0; ok && j < n_kv; ++j) {
+        const int s = j % kStages;
+        const int round = j / kStages;
+        const uint32_t kbase = sbase + kOffK + s * kTileBytes;
+        const uint32_t vbase = sbase + kOffV + s * kTileBytes;
+        if (!(ok = wait_bar(smem_addr(&bars.k_full[s]), round & 1, abort_flag, p.err, kSiteKFull)))
+          break;
+        for (int t = 0; t < kTilesPerCta && ok; ++t) {
+          // S_t aliases P_t: the previous P_t V must have finished reading it
+          if (j > 0 && !(ok = wait_bar(smem_addr(&bars.o_done[t]), (j - 1) & 1, abort_flag, p.err,
+                                       kSiteODone)))
+            break;
+          tc_fence_after();
+          const uint32_t qbase = sbase + kOffQ + t * kTileBytes;
+#pragma unroll
+          for (int kk = 0; kk < kD / 16; ++kk)
+            mma_ss(tbase + col_s(t), kmajor_desc(qbase, kHalfTile, kk),
+                   kmajor_desc(kbase, kHalfTile, kk), kIdescQK, kk > 0 ? 1u : 0u);
+          tc_commit(smem_addr(&bars.s_full[t]));
+        }
+        if (!ok) break;
+        tc_commit(smem_addr(&bars.k_empty[s]));
+        if (!(ok = wait_bar(smem_addr(&bars.v_full[s]), round & 1, abort_flag, p.err, kSiteVFull)))
+          break;
+        for (int t = 0; t < kTilesPerCta && ok; ++t) {
+          if (!(ok = wait_bar(smem_addr(&bars.p_ready[t]), j & 1, abort_flag, p.err, kSitePReady)))
+            break;
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < kBN / 16; ++kk)
+            mma_ts(tbase + col_o(t), tbase + col_s(t) + kk * 8, v_desc(vbase, kk), kIdescPV,
+                   (j > 0 || kk > 0) ? 1u : 0u);
+          tc_commit(smem_addr(&bars.o_done[t]));
+        }
+        if (!ok) break;
+        tc_commit(smem_addr(&bars.v_empty[s]));
+      }
+      // drain: no MMA may still be writing tensor memory when it is freed
+      tc_commit(smem_addr(&bars.drain));
+      drain_bar(smem_addr(&bars.drain), 0, p.err);
+    }
+  } else if (warp >= kSoftmaxWarp0) {
+    // ------------------------------------------------------------ softmax
+    const int t = (warp - kSoftmaxWarp0) >> 2;
+    const int quad = warp & 3;                     // tensor-memory lane quadrant
+    const int r_in_tile = quad * 32 + lane;
+    const int row = q0 + t * kBM + r_in_tile;      // query index
+    const uint32_t tl = tbase + (static_cast<uint32_t>(quad * 32) << 16);
+    const uint32_t colS = col_s(t), colO = col_o(t);
+    const uint32_t s_bar = smem_addr(&bars.s_full[t]);
+    const uint32_t p_bar = smem_addr(&bars.p_ready[t]);
+    const uint32_t o_bar = smem_addr(&bars.o_done[t]);
+    const float C = p.C;
+    const int tile_row0 = q0 + t * kBM;
+    float m = neg_inf();  // running max, base 2
+    float l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < n_kv; ++j) {
+      ok = __all_sync(0xffffffffu, wait_bar(s_bar, j & 1, abort_flag, p.err, kSiteSFull));
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t r0[32], r1[32], r2[32], r3[32];
+      tmem_ld32(tl + colS + 0, r0);
+      tmem_ld32(tl + colS + 32, r1);
+      tmem_ld32(tl + colS + 64, r2);
+      tmem_ld32(tl + colS + 96, r3);
+      tmem_ld_wait(r0);
+      tmem_ld_wait(r1);
+      tmem_ld_wait(r2);
+      tmem_ld_wait(r3);
+      float s[128];
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        s[c] = __uint_as_float(r0[c]);
+        s[32 + c] = __uint_as_float(r1[c]);
+        s[64 + c] = __uint_as_float(r2[c]);
+        s[96 + c] = __uint_as_float(r3[c]);
+      }
+      const int key0 = kv_tile(j) * kBN;
+      const bool ragged = key0 + kBN > p.Sk;
+      const bool diag = p.causal && key0 + kBN - 1 > tile_row0;
+      if (ragged || diag) {
+        const int lim = min(p.Sk, p.causal ? row + 1 : p.Sk) - key0;  // visible keys: c < lim
+#pragma unroll
+        for (int c = 0; c < kBN; ++c)
+          if (c >= lim) s[c] = neg_inf();
+      }
+      float mx = neg_inf();
+#pragma unroll
+      for (int c = 0; c < kBN; ++c) mx = fmaxf(mx, s[c]);
+      const float m_new = fmaxf(m, mx * C);
+      const float m_use = (m_new == neg_inf()) ? 0.f : m_new;  // the -inf guard
+      const float corr = ex2(m - m_use);                        // 0 while m = -inf
+      float rs = 0.f;
+      uint32_t pk[64];
+#pragma unroll
+      for (int c = 0; c < kBN; c += 2) {
+        const float p0 = ex2(fmaf(s[c], C, -m_use));
+        const float p1 = ex2(fmaf(s[c + 1], C, -m_use));
+        rs += p0 + p1;
+        pk[c >> 1] = pack_bf16x2(p0, p1);
+      }
+      l = fmaf(l, corr, rs);
+      m = m_new;
+      {
+        uint32_t w0[32], w1[32];
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          w0[c] = pk[c];
+          w1[c] = pk[32 + c];
+        }
+        tmem_st32(tl + colS + 0, w0);
+        tmem_st32(tl + colS + 32, w1);
+      }
+      if (j > 0) {
+        // O_t still holds the previous tiles' sum: wait for it, then rescale
+        ok = __all_sync(0xffffffffu, wait_bar(o_bar, (j - 1) & 1, abort_flag, p.err, kSiteODone));
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll 1
+        for (int cc = 0; cc < kD; cc += 32) {
+          uint32_t ov[32];
+          tmem_ld32(tl + colO + cc, ov);
+          tmem_ld_wait(ov);
+#pragma unroll
+          for (int c = 0; c < 32; ++c) ov[c] = __float_as_uint(__uint_as_float(ov[c]) * corr);
+          tmem_st32(tl + colO + cc, ov);
+        }
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(p_bar);
+    }
+    // epilogue: O / l and lse for this row
+    if (ok) ok = __all_sync(0xffffffffu, wait_bar(o_bar, (n_kv - 1) & 1, abort_flag, p.err,
+                                                   kSiteODone));
+    if (ok) {
+      tc_fence_after();
+      const float inv = (l > 0.f) ? 1.0f / l : 0.f;
+      const bool live = row < p.Sq;
+      uint4* orow = reinterpret_cast<uint4*>(p.o + (static_cast<size_t>(bh) * p.Sq + row) * kD);
+#pragma unroll 1
+      for (int cc = 0; cc < kD; cc += 32) {
+        uint32_t ov[32];
+        tmem_ld32(tl + colO + cc, ov);
+        tmem_ld_wait(ov);
+        if (live) {
+#pragma unroll
+          for (int c = 0; c < 32; c += 8) {
+            uint4 w;
+            w.x = pack_bf16x2(__uint_as_float(ov[c + 0]) * inv, __uint_as_float(ov[c + 1]) * inv);
+            w.y = pack_bf16x2(__uint_as_float(ov[c + 2]) * inv, __uint_as_float(ov[c + 3]) * inv);
+            w.z = pack_bf16x2(__uint_as_float(ov[c + 4]) * inv, __uint_as_float(ov[c + 5]) * inv);
+            w.w = pack_bf16x2(__uint_as_float(ov[c + 6]) * inv, __uint_as_float(ov[c + 7]) * inv);
+            orow[(cc + c) >> 3] = w;
+          }
+        }
+      }
+      if (live && p.lse) {
+        const float kLn2 = 0.69314718055994530942f;
+        p.lse[static_cast<size_t>(bh) * p.Sq + row] =
+            (l > 0.f) ? (m + __log2f(l)) * kLn2 : neg_inf();
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tbase),
+                 "r"(kTmemCols)
+                 : "memory");
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+// [BH][S][128] bf16 viewed as a 3-D tensor; boxes of 64 dims x 128 rows, 128B swizzle.
+bool make_map(CUtensorMap* map, const uint16_t* base, int S, int BH) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(S),
+                        static_cast<cuuint64_t>(BH)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(kD) * 2,
+                           static_cast<cuuint64_t>(S) * kD * 2};
+  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t estride[3] = {1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t*>(base), dims, strides,
+             box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+cudaError_t launch_attention_fwd(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                                 uint16_t* o, float* lse, int B, int H, int Sq, int Sk, int D,
+                                 float scale, bool causal, unsigned int* err_word,
+                                 cudaStream_t stream) {
+  if (D != kD) return cudaErrorNotSupported;
+  const int BH = B * H;
+  CUtensorMap mq, mk, mv;
+  if (!make_map(&mq, q, Sq, BH) || !make_map(&mk, k, Sk, BH) || !make_map(&mv, v, Sk, BH))
+    return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       kSmemBytes);
+  if (e != cudaSuccess) return e;
+  AttnParams prm;
+  prm.o = o;
+  prm.lse = lse;
+  prm.err = err_word;
+  prm.Sq = Sq;
+  prm.Sk = Sk;
+  prm.BH = BH;
+  prm.n_qblocks = (Sq + kRowsPerCta - 1) / kRowsPerCta;
+  prm.C = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
+  prm.causal = causal ? 1 : 0;
+  const long long grid = static_cast<long long>(prm.n_qblocks) * BH;
+  if (grid > 0x7fffffffLL) return cudaErrorNotSupported;
+  attn_fwd_kernel<<<static_cast<unsigned>(grid), kThreads, kSmemBytes, stream>>>(mq, mk, mv, prm);
+  return cudaGetLastError();
+}
+
+}  // namespace oss

@@ -1,0 +1,37 @@
+// Host-side launchers behind the C ABI in include/oss.h. Arguments are
+// already validated by api.cu when these run.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace oss {
+
+// Kernel ids stored in bits 0..7 of the device error word.
+enum KernelId : unsigned int { kKernelAttnFwd = 1 };
+
+cudaError_t launch_softmax_rows(const float* x, float* y, float* m, float* l,
+                                int64_t rows, int64_t cols, int64_t ld_x, int64_t ld_y,
+                                float scale, cudaStream_t stream);
+
+cudaError_t launch_decode_splitkv(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                                  const int32_t* kv_len, int B, int H, int Lmax, int D,
+                                  int num_splits, float scale, float* part_m, float* part_l,
+                                  float* part_o, cudaStream_t stream);
+
+cudaError_t launch_merge_partials(const float* part_m, const float* part_l, const float* part_o,
+                                  int64_t groups, int num_splits, int D, int finalize,
+                                  void* o_out, float* m_out, float* l_out, float* lse_out,
+                                  cudaStream_t stream);
+
+// Returns cudaErrorNotSupported for shapes the kernel does not cover.
+cudaError_t launch_attention_fwd(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                                 uint16_t* o, float* lse, int B, int H, int Sq, int Sk, int D,
+                                 float scale, bool causal, unsigned int* err_word,
+                                 cudaStream_t stream);
+
+// log2(e) split into a float and the float nearest to the remainder, so that
+// hi + lo carries about 48 bits of it.
+void split_constant(double c, float* hi, float* lo);
+
+}  // namespace oss

@@ -1,0 +1,102 @@
+"""The C ABI without a GPU: the library builds, loads, exports every symbol
+include/oss.h declares, and rejects invalid arguments before touching the
+device. No call here reaches a kernel launch."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import pass_attention_gb300 as oss
+from pass_attention_gb300 import build_lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "oss.h")
+
+INVALID, MISALIGNED, UNSUPPORTED = 1, 2, 3
+A = 4096  # a 16-byte-aligned stand-in address; never dereferenced by these calls
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build_lib.build()
+    return oss.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return re.findall(r"OSS_API\s+[\w\s\*]+?\b(os_\w+)\s*\(", text)
+
+
+def test_header_declares_the_binding_signatures():
+    names = declared_functions()
+    assert sorted(names) == sorted(oss.EXPORTED_SYMBOLS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_abi_version_and_status_strings(lib):
+    assert lib.os_abi_version() == 1
+    for code, name in oss.STATUS_NAMES.items():
+        assert lib.os_status_string(code).decode() == name
+    assert lib.os_status_string(99).decode() == "OS_ERR_UNKNOWN"
+
+
+def test_softmax_rows_rejects_bad_arguments(lib):
+    f = lib.os_softmax_rows
+    assert f(None, A, None, None, 4, 8, 8, 8, 1.0, None) == INVALID
+    assert f(A, None, None, None, 4, 8, 8, 8, 1.0, None) == INVALID
+    assert f(A, A, None, None, 0, 8, 8, 8, 1.0, None) == INVALID
+    assert f(A, A, None, None, 4, 0, 8, 8, 1.0, None) == INVALID
+    assert f(A, A, None, None, 4, 8, 7, 8, 1.0, None) == INVALID   # ld_x < cols
+    assert f(A, A, None, None, 4, 8, 8, 8, 0.0, None) == INVALID   # scale must be > 0
+    assert f(A, A, None, None, 4, 8, 8, 8, -1.0, None) == INVALID
+    assert f(A, A, None, None, 4, 8, 8, 8, float("nan"), None) == INVALID
+    assert f(A, A, None, None, 4, 8, 8, 8, float("inf"), None) == INVALID
+    assert f(A + 2, A, None, None, 4, 8, 8, 8, 1.0, None) == MISALIGNED   # not float-aligned
+    assert f(A, A + 1, None, None, 4, 8, 8, 8, 1.0, None) == MISALIGNED
+
+
+def test_attention_fwd_rejects_bad_arguments(lib):
+    f = lib.os_attention_fwd
+    ok = (1, 2, 64, 64, 128, 0.1, 0, None)
+    assert f(None, A, A, A, None, *ok) == INVALID
+    assert f(A, A, A, None, None, *ok) == INVALID
+    assert f(A, A, A, A, None, 0, 2, 64, 64, 128, 0.1, 0, None) == INVALID
+    assert f(A, A, A, A, None, 1, 2, 0, 64, 128, 0.1, 0, None) == INVALID
+    assert f(A, A, A, A, None, 1, 2, 64, 64, 128, 0.0, 0, None) == INVALID
+    assert f(A + 2, A, A, A, None, *ok) == MISALIGNED
+    assert f(A, A, A, A, None, 1, 2, 64, 64, 64, 0.1, 0, None) == UNSUPPORTED   # D != 128
+    assert f(A, A, A, A, None, 1, 2, 64, 32, 128, 0.1, 1, None) == UNSUPPORTED  # causal, Sq != Sk
+
+
+def test_decode_rejects_bad_arguments(lib):
+    f = lib.os_attention_decode_splitkv
+    assert f(A, A, A, None, 2, 2, 64, 128, 4, 0.1, A, A, A, None) == INVALID
+    assert f(A, A, A, A, 2, 2, 64, 128, 0, 0.1, A, A, A, None) == INVALID
+    assert f(A, A, A, A, 2, 2, 64, 128, 4, -0.1, A, A, A, None) == INVALID
+    assert f(A, A, A, A, 2, 2, 64, 128, 4, 0.1, A, A, A + 4, None) == MISALIGNED
+    assert f(A, A, A, A, 2, 2, 64, 96, 4, 0.1, A, A, A, None) == UNSUPPORTED
+    assert f(A, A, A, A, 2, 2, 64, 128, 65, 0.1, A, A, A, None) == UNSUPPORTED
+
+
+def test_merge_rejects_bad_arguments(lib):
+    f = lib.os_merge_partials
+    assert f(None, A, A, 4, 16, 128, 1, A, None, None, None, None) == INVALID
+    assert f(A, A, A, 4, 16, 128, 1, None, None, None, None, None) == INVALID
+    assert f(A, A, A, 0, 16, 128, 1, A, None, None, None, None) == INVALID
+    assert f(A, A, A + 8, 4, 16, 128, 1, A, None, None, None, None) == MISALIGNED
+    assert f(A, A, A, 4, 65, 128, 1, A, None, None, None, None) == UNSUPPORTED
+    assert f(A, A, A, 4, 16, 130, 1, A, None, None, None, None) == UNSUPPORTED
+
+
+def test_binding_refuses_cpu_tensors(lib):
+    import torch
+    with pytest.raises(ValueError):
+        oss.softmax_rows(torch.zeros(2, 4))
+    with pytest.raises(ValueError):
+        oss.attention_fwd(*(torch.zeros(1, 1, 4, 128, dtype=torch.bfloat16) for _ in range(3)))

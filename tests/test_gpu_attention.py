@@ -1,0 +1,120 @@
+"""os_attention_fwd against the oracle's materialised attention (GPU)."""
+
+import math
+from concurrent.futures import ThreadPoolExecutor
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import pass_attention_gb300 as oss
+from pass_attention_gb300 import workloads
+from parity import check_attn
+
+pytestmark = pytest.mark.gpu
+
+
+def f64(t):
+    return t.detach().cpu().to(torch.float64).numpy()
+
+
+def run(B, H, Sq, Sk, causal, seed, mult=1.0):
+    q, k, v = workloads.qkv(B, H, Sq, Sk, 128, seed, device="cuda")
+    if mult != 1.0:
+        q = (q.float() * mult).to(torch.bfloat16)
+    scale = 1.0 / math.sqrt(128)
+    o, lse = oss.attention_fwd(q, k, v, scale, causal)
+    assert oss.check_device_error() == 0
+    return q, k, v, o, lse, scale
+
+
+def check_all_rows(q, k, v, o, lse, scale, causal, what):
+    qh, kh, vh = f64(q), f64(k), f64(v)
+    B, H = q.shape[:2]
+
+    def one(bh):
+        b, h = divmod(bh, H)
+        O, L = oracle.attention(qh[b:b + 1, h:h + 1], kh[b:b + 1, h:h + 1], vh[b:b + 1, h:h + 1],
+                                scale, causal)
+        return bh, O[0, 0], L[0, 0]
+
+    on, ln = f64(o), f64(lse)
+    with ThreadPoolExecutor(max_workers=4) as ex:
+        for bh, O, L in ex.map(one, range(B * H)):
+            b, h = divmod(bh, H)
+            check_attn(on[b, h], O, f"{what} O b{b} h{h}")
+            check_attn(ln[b, h], L, f"{what} lse b{b} h{h}")
+
+
+@pytest.mark.parametrize("B,H,Sq,Sk", [
+    (1, 1, 128, 128), (1, 2, 256, 256), (2, 3, 300, 200), (1, 1, 1, 1), (1, 1, 5, 700),
+    (1, 2, 513, 1000), (2, 2, 1024, 384),
+])
+def test_noncausal_shapes(B, H, Sq, Sk):
+    q, k, v, o, lse, scale = run(B, H, Sq, Sk, False, seed=Sq * 31 + Sk)
+    check_all_rows(q, k, v, o, lse, scale, False, f"{B}x{H}x{Sq}x{Sk}")
+
+
+@pytest.mark.parametrize("B,H,S", [(1, 1, 1), (1, 1, 129), (1, 2, 256), (1, 1, 300), (2, 2, 1000),
+                                   (1, 2, 2048)])
+def test_causal_shapes(B, H, S):
+    q, k, v, o, lse, scale = run(B, H, S, S, True, seed=S * 17 + B)
+    check_all_rows(q, k, v, o, lse, scale, True, f"causal {B}x{H}x{S}")
+
+
+def test_causal_first_row_is_first_value_and_zero_query_is_mean():
+    q, k, v = workloads.qkv(1, 2, 700, 700, 128, seed=3, device="cuda")
+    o, lse = oss.attention_fwd(q, k, v, 0.1, causal=True)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(f64(o)[:, :, 0], f64(v)[:, :, 0])  # bf16 round trip is exact
+    z = torch.zeros_like(q)
+    o, lse = oss.attention_fwd(z, k, v, 0.1, causal=False)
+    torch.cuda.synchronize()
+    mean = f64(v).mean(axis=2)
+    check_attn(f64(o), np.broadcast_to(mean[:, :, None, :], o.shape), "mean of V")
+    check_attn(f64(lse), np.full(lse.shape, math.log(700)), "lse uniform")
+
+
+def test_large_logits_stay_finite():
+    # |q.k| * scale in the hundreds: exponentials are only ever taken of
+    # non-positive differences, so nothing overflows
+    q, k, v, o, lse, scale = run(1, 2, 384, 640, False, seed=8, mult=30.0)
+    assert torch.isfinite(o.float()).all() and torch.isfinite(lse).all()
+    check_all_rows(q, k, v, o, lse, scale, False, "x30")
+
+
+def test_repeat_calls_identical():
+    q, k, v = workloads.qkv(2, 2, 512, 512, 128, seed=4, device="cuda")
+    o1, l1 = oss.attention_fwd(q, k, v, 0.1, causal=True)
+    o2, l2 = oss.attention_fwd(q, k, v, 0.1, causal=True)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+@pytest.mark.slow
+def test_full_size_attn_4k_every_row():
+    w = workloads.ATTN_4K
+    q, k, v = workloads.qkv(w.B, w.H, w.S, w.S, w.D, w.seed, device="cuda")
+    o, lse = oss.attention_fwd(q, k, v, w.scale, w.causal)
+    assert oss.check_device_error() == 0
+    check_all_rows(q, k, v, o, lse, w.scale, w.causal, "attn_4k")
+
+
+@pytest.mark.slow
+def test_full_size_attn_causal_sampled_rows():
+    w = workloads.ATTN_CAUSAL
+    q, k, v = workloads.qkv(w.B, w.H, w.S, w.S, w.D, w.seed, device="cuda")
+    o, lse = oss.attention_fwd(q, k, v, w.scale, w.causal)
+    assert oss.check_device_error() == 0
+    rng = np.random.default_rng(w.seed)
+    n = 4096
+    rows = list(zip(rng.integers(0, w.B, n), rng.integers(0, w.H, n), rng.integers(0, w.S, n)))
+    rows += [(0, h, i) for h in (0, w.H - 1) for i in (0, 1, 127, 128, 255, 256, w.S - 1)]
+    qh, kh, vh = f64(q), f64(k), f64(v)
+    O, L = oracle.attention(qh, kh, vh, w.scale, True, rows=rows)
+    on, ln = f64(o), f64(lse)
+    got_o = np.stack([on[b, h, i] for b, h, i in rows])
+    got_l = np.array([ln[b, h, i] for b, h, i in rows])
+    check_attn(got_o, O, "attn_causal O")
+    check_attn(got_l, L, "attn_causal lse")

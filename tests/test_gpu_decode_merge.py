@@ -1,0 +1,138 @@
+"""os_attention_decode_splitkv and os_merge_partials against the oracle (GPU)."""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import pass_attention_gb300 as oss
+from pass_attention_gb300 import workloads
+from parity import check_attn
+
+pytestmark = pytest.mark.gpu
+
+
+def f64(t):
+    return t.detach().cpu().to(torch.float64).numpy()
+
+
+def check_partials(pm, pl, po, rm, rl, ro, what):
+    """Compare partials by what they determine: m, lse = m + ln l and O / l;
+    empty splits must be exactly (-inf, 0, 0)."""
+    empty = np.isneginf(rm)
+    assert np.all(np.isneginf(pm[empty])) and np.all(pl[empty] == 0.0), f"{what}: empty splits"
+    assert np.all(po[empty] == 0.0), f"{what}: empty split O"
+    full = ~empty
+    assert np.all(np.isfinite(pm[full])) and np.all(pl[full] > 0), f"{what}: non-empty splits"
+    check_attn(pm[full], rm[full], what + " part m")
+    check_attn(pm[full] + np.log(pl[full]), rm[full] + np.log(rl[full]), what + " part lse")
+    check_attn(po[full] / pl[full][:, None], ro[full] / rl[full][:, None], what + " part O/l")
+
+
+def run_decode(B, H, Lmax, S, seed, kv_len=None):
+    D = 128
+    q, k, v, kv = workloads.decode_inputs(B, H, Lmax, D, seed, device="cuda", kv_len=kv_len)
+    scale = 1.0 / math.sqrt(D)
+    pm, pl, po = oss.attention_decode_splitkv(q, k, v, kv, S, scale)
+    o, m, l, lse = oss.merge_partials(pm, pl, po, finalize=True)
+    torch.cuda.synchronize()
+    qh, kh, vh, kvh = f64(q), f64(k), f64(v), kv.cpu().numpy()
+    rm, rl, ro = oracle.decode_partials(qh, kh, vh, kvh, S, scale)
+    check_partials(f64(pm), f64(pl), f64(po), rm, rl, ro, f"decode {B}x{H}x{Lmax}/{S}")
+    O_ref, lse_ref = oracle.decode(qh, kh, vh, kvh, scale)
+    check_attn(f64(o), O_ref, "decode O")
+    check_attn(f64(lse), lse_ref, "decode lse")
+
+
+@pytest.mark.parametrize("B,H,Lmax,S,kv_len", [
+    (3, 4, 300, 16, [300, 5, 77]),      # ragged; 5 < 16 leaves splits empty
+    (2, 3, 1, 16, [1, 1]),              # one key: O = v_0
+    (2, 2, 1000, 1, [1000, 999]),       # no split at all
+    (1, 2, 4099, 64, [4099]),           # most splits allowed, ragged tail
+    (4, 2, 513, 7, [513, 1, 8, 64]),    # split count that does not divide
+])
+def test_decode_small(B, H, Lmax, S, kv_len):
+    run_decode(B, H, Lmax, S, seed=B * 100 + S, kv_len=torch.tensor(kv_len))
+
+
+def test_decode_random_lengths():
+    run_decode(8, 8, 2048, 16, seed=44)
+
+
+@pytest.mark.slow
+def test_full_size_decode_sampled():
+    w = workloads.DECODE_64X32
+    q, k, v, kv = workloads.decode_inputs(w.B, w.H, w.Lmax, w.D, w.seed, device="cuda")
+    pm, pl, po = oss.attention_decode_splitkv(q, k, v, kv, w.num_splits, w.scale)
+    o, m, l, lse = oss.merge_partials(pm, pl, po, finalize=True)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(w.seed)
+    picks = [(int(b), int(h)) for b, h in zip(rng.integers(0, w.B, 256), rng.integers(0, w.H, 256))]
+    kvh = kv.cpu().numpy()
+    for b, h in picks:
+        L = int(kvh[b])
+        qh = f64(q[b:b + 1, h:h + 1])
+        kh = f64(k[b:b + 1, h:h + 1, :L])
+        vh = f64(v[b:b + 1, h:h + 1, :L])
+        rm, rl, ro = oracle.decode_partials(qh, kh, vh, [L], w.num_splits, w.scale)
+        check_partials(f64(pm[b:b + 1, h:h + 1]), f64(pl[b:b + 1, h:h + 1]),
+                       f64(po[b:b + 1, h:h + 1]), rm, rl, ro, f"decode b{b} h{h}")
+        O_ref, lse_ref = oracle.decode(qh, kh, vh, [L], w.scale)
+        check_attn(f64(o[b, h]), O_ref[0, 0], f"O b{b} h{h}")
+        check_attn(f64(lse[b, h]), lse_ref[0, 0], f"lse b{b} h{h}")
+
+
+# ---------------------------------------------------------------------------
+# merge on its own
+# ---------------------------------------------------------------------------
+
+def random_partials(G, S, D, seed):
+    g = torch.Generator().manual_seed(seed)
+    pm = torch.randn(G, S, generator=g, dtype=torch.float64) * 5
+    pl = torch.rand(G, S, generator=g, dtype=torch.float64) * 49 + 1
+    po = torch.randn(G, S, D, generator=g, dtype=torch.float64) * 10
+    empty = torch.rand(G, S, generator=g) < 0.25
+    pm[empty] = -math.inf
+    pl[empty] = 0.0
+    po[empty] = 0.0
+    pm[0] = -math.inf      # an all-empty group
+    pl[0] = 0.0
+    po[0] = 0.0
+    return pm.float(), pl.float(), po.float()
+
+
+@pytest.mark.parametrize("S", [1, 2, 5, 7, 16, 64])
+@pytest.mark.parametrize("D", [4, 64, 128, 256])
+def test_merge_finalize(S, D):
+    pm, pl, po = random_partials(33, S, D, seed=S * 1000 + D)
+    o, m, l, lse = oss.merge_partials(pm.cuda(), pl.cuda(), po.cuda(), finalize=True)
+    On, rm, rl, rlse = oracle.merge(pm.double().numpy(), pl.double().numpy(), po.double().numpy())
+    torch.cuda.synchronize()
+    check_attn(f64(o), On, "merged O")
+    check_attn(f64(lse), rlse, "merged lse")
+    assert f64(o)[0].max() == 0.0 and f64(o)[0].min() == 0.0 and np.isneginf(f64(lse)[0])
+    assert np.isneginf(f64(m)[0]) and f64(l)[0] == 0.0
+    fin = np.isfinite(rm)
+    np.testing.assert_allclose(f64(m)[fin], rm[fin], rtol=1e-6, atol=1e-6)
+    np.testing.assert_allclose(f64(l)[fin], rl[fin], rtol=1e-5)
+
+
+@pytest.mark.parametrize("S", [3, 16])
+def test_merge_unnormalised_nests(S):
+    # merging in two stages (halves, then the two results) equals one merge
+    pm, pl, po = random_partials(20, 2 * S, 128, seed=77 + S)
+    o1, m1, l1, _ = oss.merge_partials(pm[:, :S].contiguous().cuda(), pl[:, :S].contiguous().cuda(),
+                                       po[:, :S].contiguous().cuda(), finalize=False)
+    o2, m2, l2, _ = oss.merge_partials(pm[:, S:].contiguous().cuda(), pl[:, S:].contiguous().cuda(),
+                                       po[:, S:].contiguous().cuda(), finalize=False)
+    o, m, l, lse = oss.merge_partials(torch.stack([m1, m2], 1), torch.stack([l1, l2], 1),
+                                      torch.stack([o1, o2], 1), finalize=True)
+    On, rm, rl, rlse = oracle.merge(pm.double().numpy(), pl.double().numpy(), po.double().numpy())
+    torch.cuda.synchronize()
+    check_attn(f64(o), On, "nested O")
+    check_attn(f64(lse), rlse, "nested lse")
+    Ou = oracle.merge(pm[:, :S].double().numpy(), pl[:, :S].double().numpy(),
+                      po[:, :S].double().numpy(), finalize=False)[2]
+    np.testing.assert_allclose(f64(o1), Ou, rtol=1e-5, atol=1e-4)
