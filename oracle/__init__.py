@@ -230,22 +230,23 @@ def attention(q, k, v, scale: float, causal: bool = False,
     if causal and Sq != Sk:
         raise ValueError("causal attention is defined here for Sq == Sk")
 
-    def one_row(b, h, i):
-        s = float(scale) * (k[b, h] @ q[b, h, i])
-        if causal:
-            s = s.copy()
-            s[i + 1:] = NEG_INF
-        w, m, l = _softmax_lastdim(s)
-        o = w @ v[b, h]
-        lse = m + math.log(l) if l > 0.0 else NEG_INF
-        return o, lse
-
     if rows is not None:
-        rows = list(rows)
+        rows = [tuple(int(x) for x in r) for r in rows]
         O = np.zeros((len(rows), v.shape[3]), dtype=np.float64)
         lse = np.zeros(len(rows), dtype=np.float64)
+        groups: dict = {}
         for n, (b, h, i) in enumerate(rows):
-            O[n], lse[n] = one_row(b, h, i)
+            groups.setdefault((b, h), []).append((n, i))
+        for (b, h), items in groups.items():
+            idx = np.array([n for n, _ in items])
+            qi = np.array([i for _, i in items])
+            S = float(scale) * (q[b, h, qi] @ k[b, h].T)  # score rows of these queries
+            if causal:
+                S[np.arange(Sk)[None, :] > qi[:, None]] = NEG_INF
+            W, m, l = _softmax_lastdim(S)
+            O[idx] = W @ v[b, h]
+            with np.errstate(divide="ignore"):
+                lse[idx] = np.where(l > 0.0, m + np.log(np.where(l > 0.0, l, 1.0)), NEG_INF)
         return O, lse
 
     O = np.zeros((B, H, Sq, v.shape[3]), dtype=np.float64)
