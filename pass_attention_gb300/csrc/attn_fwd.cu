@@ -4,7 +4,11 @@
 // metalworking page's five-line recurrence states it ("Online Softmax"):
 //   m_new = max(m, rowmax S);  c = 2^(m - m_new);  P = 2^(S - m_new);
 //   l = l*c + rowsum P;        O = O*c + P V;      m = m_new;
-// and after the last tile O /= l. Scores are kept in base 2 with
+// and after the last tile O /= l. The rescale is conditional, in the spirit
+// of the metal-flash-attention guard the page quotes (correction 1 unless
+// the maximum rose): a warp moves its rows' reference maximum only when one
+// of them rose by more than 2^8, so the O round trip through tensor memory
+// is rare; any reference gives the same O / l in exact arithmetic. Scores are kept in base 2 with
 // scale * log2(e) folded in once, and every exponential is exp2, the rescale
 // factor included (roadmapper "Online softmax", "Things that break"). The
 // state starts at m = -inf, l = 0; a row whose keys are all masked so far
@@ -66,6 +70,10 @@ constexpr int kSmemBytes = kOffEnd + 1024;             // + alignment slack
 constexpr uint32_t kTmemCols = 512;
 __device__ __forceinline__ uint32_t col_s(int t) { return 128u * t; }
 __device__ __forceinline__ uint32_t col_o(int t) { return 256u + 128u * t; }
+
+// The reference maximum of a warp's rows moves only when one of them rises
+// by more than this (base-2 units): weights stay below 2^8 = 256.
+constexpr float kRescaleSlack = 8.0f;
 
 constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s per wait
 constexpr uint64_t kDrainNs = 200000000ull;     // 0.2 s to drain own copies
@@ -221,8 +229,23 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
       : "memory");
 }
 
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+      OSS_W8(0), OSS_W8(8)
+      : "memory");
+}
+
 __device__ __forceinline__ void tmem_st_wait() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// max(a, b, c) in one instruction (three-input max.f32, sm_100 and later)
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -480,45 +503,69 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
         for (int c = 0; c < kBN; ++c)
           if (c >= lim) s[c] = neg_inf();
       }
-      float mx = neg_inf();
+      // row maximum: four independent chains of 3-input max
+      float mx0 = neg_inf(), mx1 = neg_inf(), mx2 = neg_inf(), mx3 = neg_inf();
 #pragma unroll
-      for (int c = 0; c < kBN; ++c) mx = fmaxf(mx, s[c]);
-      const float m_new = fmaxf(m, mx * C);
-      const float m_use = (m_new == neg_inf()) ? 0.f : m_new;  // the -inf guard
-      const float corr = ex2(m - m_use);                        // 0 while m = -inf
-      float rs = 0.f;
-      uint32_t pk[64];
-#pragma unroll
-      for (int c = 0; c < kBN; c += 2) {
-        const float p0 = ex2(fmaf(s[c], C, -m_use));
-        const float p1 = ex2(fmaf(s[c + 1], C, -m_use));
-        rs += p0 + p1;
-        pk[c >> 1] = pack_bf16x2(p0, p1);
+      for (int c = 0; c < kBN; c += 8) {
+        mx0 = fmax3(mx0, s[c + 0], s[c + 1]);
+        mx1 = fmax3(mx1, s[c + 2], s[c + 3]);
+        mx2 = fmax3(mx2, s[c + 4], s[c + 5]);
+        mx3 = fmax3(mx3, s[c + 6], s[c + 7]);
       }
-      l = fmaf(l, corr, rs);
-      m = m_new;
-      {
-        uint32_t w0[32], w1[32];
+      const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * C;
+      const float m_new = fmaxf(m, m_tile);
+      // Move the reference maximum only when some row of this warp has risen
+      // by more than kRescaleSlack (base 2). Otherwise keep it: exactly the
+      // same result in exact arithmetic (the reference cancels in O / l),
+      // weights stay <= 2^kRescaleSlack, and the O round trip is skipped.
+      const bool rescale = __any_sync(0xffffffffu, m_new > m + kRescaleSlack);
+      float corr = 1.f;
+      if (rescale) {
+        const float m_use_new = (m_new == neg_inf()) ? 0.f : m_new;
+        corr = ex2(m - m_use_new);  // 0 while m = -inf
+        m = m_new;
+      }
+      const float m_use = (m == neg_inf()) ? 0.f : m;  // the -inf guard
+      const float2 Cv = make_float2(C, C);
+      const float2 mv = make_float2(-m_use, -m_use);
+      float2 acc0 = make_float2(0.f, 0.f), acc1 = acc0;
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          w0[c] = pk[c];
-          w1[c] = pk[32 + c];
+      for (int ch = 0; ch < kBN / 32; ++ch) {
+        // 32 weights -> 16 bf16 pairs, stored over the first half of S_t
+        uint32_t pk[16];
+#pragma unroll
+        for (int c = 0; c < 32; c += 4) {
+          const int cc = ch * 32 + c;
+          const float2 t0 = __ffma2_rn(make_float2(s[cc], s[cc + 1]), Cv, mv);
+          const float2 t1 = __ffma2_rn(make_float2(s[cc + 2], s[cc + 3]), Cv, mv);
+          const float2 e0 = make_float2(ex2(t0.x), ex2(t0.y));
+          const float2 e1 = make_float2(ex2(t1.x), ex2(t1.y));
+          acc0 = __fadd2_rn(acc0, e0);
+          acc1 = __fadd2_rn(acc1, e1);
+          pk[(c >> 1) + 0] = pack_bf16x2(e0.x, e0.y);
+          pk[(c >> 1) + 1] = pack_bf16x2(e1.x, e1.y);
         }
-        tmem_st32(tl + colS + 0, w0);
-        tmem_st32(tl + colS + 32, w1);
+        tmem_st16(tl + colS + ch * 16, pk);
       }
-      if (j > 0) {
+      const float2 acc = __fadd2_rn(acc0, acc1);
+      l = fmaf(l, corr, acc.x + acc.y);
+      if (rescale && j > 0) {
         // O_t still holds the previous tiles' sum: wait for it, then rescale
         ok = __all_sync(0xffffffffu, wait_bar(o_bar, (j - 1) & 1, abort_flag, p.err, kSiteODone));
         if (!ok) break;
         tc_fence_after();
+        const float2 cv = make_float2(corr, corr);
 #pragma unroll 1
         for (int cc = 0; cc < kD; cc += 32) {
           uint32_t ov[32];
           tmem_ld32(tl + colO + cc, ov);
           tmem_ld_wait(ov);
 #pragma unroll
-          for (int c = 0; c < 32; ++c) ov[c] = __float_as_uint(__uint_as_float(ov[c]) * corr);
+          for (int c = 0; c < 32; c += 2) {
+            const float2 o2 = __fmul2_rn(make_float2(__uint_as_float(ov[c]), __uint_as_float(ov[c + 1])), cv);
+            ov[c] = __float_as_uint(o2.x);
+            ov[c + 1] = __float_as_uint(o2.y);
+          }
           tmem_st32(tl + colO + cc, ov);
         }
       }

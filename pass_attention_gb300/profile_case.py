@@ -1,0 +1,62 @@
+"""Run one liboss entry point on one workload a few times, for profilers.
+
+    python -m pass_attention_gb300.profile_case softmax [--rows R --cols C] [--reps N]
+    python -m pass_attention_gb300.profile_case attn [--B --H --S] [--causal] [--reps N]
+    python -m pass_attention_gb300.profile_case decode [--B --H --Lmax --splits] [--reps N]
+
+Inputs are the seeded synthetic ones of ``workloads``; every call is
+followed by a device synchronise, so a profiler filter such as
+``-k regex:attn_fwd -s 1 -c 1`` captures one warm launch.
+"""
+
+from __future__ import annotations
+
+import argparse
+import math
+
+import torch
+
+import pass_attention_gb300 as oss
+from pass_attention_gb300 import workloads
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("case", choices=["softmax", "attn", "decode"])
+    ap.add_argument("--rows", type=int, default=32768)
+    ap.add_argument("--cols", type=int, default=8192)
+    ap.add_argument("--B", type=int, default=None)
+    ap.add_argument("--H", type=int, default=None)
+    ap.add_argument("--S", type=int, default=4096)
+    ap.add_argument("--Lmax", type=int, default=32768)
+    ap.add_argument("--splits", type=int, default=16)
+    ap.add_argument("--causal", action="store_true")
+    ap.add_argument("--reps", type=int, default=3)
+    a = ap.parse_args(argv)
+    oss.load()
+    if a.case == "softmax":
+        x = workloads.logits(a.rows, a.cols, 10.0, seed=1, device="cuda")
+        y = torch.empty_like(x)
+        for _ in range(a.reps):
+            oss.softmax_rows(x, 1.0, y=y)
+            torch.cuda.synchronize()
+    elif a.case == "attn":
+        B, H = a.B or 4, a.H or 16
+        q, k, v = workloads.qkv(B, H, a.S, a.S, 128, seed=2, device="cuda")
+        for _ in range(a.reps):
+            oss.attention_fwd(q, k, v, 1.0 / math.sqrt(128), a.causal)
+            torch.cuda.synchronize()
+        oss.check_device_error()
+    else:
+        B, H = a.B or 8, a.H or 32
+        q, k, v, kv = workloads.decode_inputs(B, H, a.Lmax, 128, seed=4, device="cuda")
+        for _ in range(a.reps):
+            pm, pl, po = oss.attention_decode_splitkv(q, k, v, kv, a.splits)
+            oss.merge_partials(pm, pl, po, finalize=True)
+            torch.cuda.synchronize()
+        print("kv_len sum", int(kv.sum().item()))
+    print("done", a.case)
+
+
+if __name__ == "__main__":
+    main()

@@ -84,6 +84,21 @@ def test_large_logits_stay_finite():
     check_all_rows(q, k, v, o, lse, scale, False, "x30")
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_max_rising_every_tile(causal):
+    # key norms grow along the sequence, so each 128-key tile raises every
+    # row's maximum by far more than the 2^8 slack: the reference maximum and
+    # the output accumulator are rescaled on every tile
+    B, H, S = 1, 2, 1536
+    q, k, v = workloads.qkv(B, H, S, S, 128, seed=12, device="cuda")
+    grow = (1.0 + torch.arange(S, device="cuda", dtype=torch.float32) / 24.0)[None, None, :, None]
+    k = (k.float() * grow).to(torch.bfloat16)
+    scale = 1.0 / math.sqrt(128)
+    o, lse = oss.attention_fwd(q, k, v, scale, causal)
+    assert oss.check_device_error() == 0
+    check_all_rows(q, k, v, o, lse, scale, causal, "rising max")
+
+
 def test_repeat_calls_identical():
     q, k, v = workloads.qkv(2, 2, 512, 512, 128, seed=4, device="cuda")
     o1, l1 = oss.attention_fwd(q, k, v, 0.1, causal=True)
