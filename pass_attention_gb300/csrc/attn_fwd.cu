@@ -16,14 +16,16 @@
 // "Initialise honestly"). No score row is ever written to memory (curionode
 // "The Online Softmax.", "One pass, exactly").
 //
-// CTA layout (384 threads, one CTA per SM):
+// CTA layout (352 threads, one CTA per SM):
 //   * 2 query tiles of 128 rows share every K/V tile of 128 keys.
-//   * warp 0      -- TMA producer: Q once, then K/V tiles into a 2-stage ring.
-//   * warp 1      -- owns tensor memory and issues the MMAs (one thread):
+//   * warps 0..7  -- softmax: warp w serves query tile w / 4 and tensor-
+//                    memory lanes 32 (w % 4) .. +31 (the lane quadrant a warp
+//                    may reach); each thread owns one query row.
+//   * warp 8      -- TMA producer: Q once, then K/V tiles into a 2-stage ring.
+//   * warps 9, 10 -- one thread each issues the MMAs of query tile 0 / 1:
 //                    S_t = Q_t K^T (A, B from shared memory) and
 //                    O_t += P_t V (A = P from tensor memory, B from shared).
-//   * warps 4..7  -- softmax for query tile 0; warps 8..11 for tile 1. Each
-//                    thread owns one query row = one tensor-memory lane.
+//                    Warp 9 also owns the tensor-memory allocation.
 // Tensor memory (512 fp32 columns x 128 lanes): S_0 | S_1 | O_0 | O_1, with
 // P_t (bf16 pairs) written over the first 64 columns of S_t.
 //
@@ -52,9 +54,10 @@ constexpr int kD = 128;           // head dimension
 constexpr int kBM = 128;          // query rows per tile (= tensor-memory lanes)
 constexpr int kTilesPerCta = 2;   // query tiles per CTA
 constexpr int kBN = 128;          // keys per KV tile
-constexpr int kStages = 2;        // K/V ring depth
-constexpr int kThreads = 384;
-constexpr int kSoftmaxWarp0 = 4;
+constexpr int kStages = 2;        // K/V ring depth (the MMA issuer assumes 2)
+constexpr int kThreads = 352;
+constexpr int kProducerWarp = 8;      // warps 0..7: softmax, one thread per query row
+constexpr int kMmaWarp0 = 9;          // warps 9, 10: MMA issuers for query tiles 0, 1
 constexpr int kRowsPerCta = kBM * kTilesPerCta;
 
 // shared memory (bytes from the 1024-aligned base)
@@ -116,6 +119,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Non-blocking test of a phase.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
       : "r"(bar), "r"(parity)
@@ -309,7 +325,7 @@ struct Barriers {
   uint64_t q_full;
   uint64_t k_full[kStages], v_full[kStages], k_empty[kStages], v_empty[kStages];
   uint64_t s_full[kTilesPerCta], p_ready[kTilesPerCta], o_done[kTilesPerCta];
-  uint64_t drain;
+  uint64_t drain[kTilesPerCta];
 };
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -344,20 +360,20 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
     for (int s = 0; s < kStages; ++s) {
       mbar_init(smem_addr(&bars.k_full[s]), 1);
       mbar_init(smem_addr(&bars.v_full[s]), 1);
-      mbar_init(smem_addr(&bars.k_empty[s]), 1);
-      mbar_init(smem_addr(&bars.v_empty[s]), 1);
+      mbar_init(smem_addr(&bars.k_empty[s]), kTilesPerCta);  // one commit per MMA thread
+      mbar_init(smem_addr(&bars.v_empty[s]), kTilesPerCta);
     }
     for (int t = 0; t < kTilesPerCta; ++t) {
       mbar_init(smem_addr(&bars.s_full[t]), 1);
       mbar_init(smem_addr(&bars.p_ready[t]), kBM);
       mbar_init(smem_addr(&bars.o_done[t]), 1);
+      mbar_init(smem_addr(&bars.drain[t]), 1);
     }
-    mbar_init(smem_addr(&bars.drain), 1);
     abort_flag_s = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
-  if (warp == 1) {
+  if (warp == kMmaWarp0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_addr(&tmem_base_slot)),
                  "r"(kTmemCols)
@@ -369,7 +385,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
   tc_fence_after();
   const uint32_t tbase = tmem_base_slot;
 
-  if (warp == 0) {
+  if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_k)) : "memory");
@@ -412,54 +428,65 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
         drain_bar(b, (j / kStages) & 1, p.err);
       }
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == kMmaWarp0 || warp == kMmaWarp0 + 1) {
+    // ------------------------------------------------------------ MMA issuers
+    // One thread per query tile, each running its own chain
+    //   QK_0, PV_0, QK_1, PV_1, ...
+    // Issuing a tcgen05.mma costs its thread tens of cycles, so a single
+    // issuing thread cannot keep the tensor pipe busy; two can, and the
+    // tiles no longer wait on each other's softmax.
     if (lane == 0) {
+      const int t = warp - kMmaWarp0;
       bool ok = wait_bar(smem_addr(&bars.q_full), 0, abort_flag, p.err, kSiteQFull);
+      // operand descriptors per buffer, built once; a 16-element K step only
+      // adds a constant to the start-address field (16-byte units)
+      const uint64_t dq = smem_desc(sbase + kOffQ + t * kTileBytes, 16, 1024);
+      const uint64_t dk0 = smem_desc(sbase + kOffK, 16, 1024);
+      const uint64_t dk1 = smem_desc(sbase + kOffK + kTileBytes, 16, 1024);
+      const uint64_t dv0 = smem_desc(sbase + kOffV, kHalfTile, 1024);
+      const uint64_t dv1 = smem_desc(sbase + kOffV + kTileBytes, kHalfTile, 1024);
+      const uint32_t b_kfull0 = smem_addr(&bars.k_full[0]), b_kfull1 = smem_addr(&bars.k_full[1]);
+      const uint32_t b_vfull0 = smem_addr(&bars.v_full[0]), b_vfull1 = smem_addr(&bars.v_full[1]);
+      const uint32_t b_kempty0 = smem_addr(&bars.k_empty[0]), b_kempty1 = smem_addr(&bars.k_empty[1]);
+      const uint32_t b_vempty0 = smem_addr(&bars.v_empty[0]), b_vempty1 = smem_addr(&bars.v_empty[1]);
+      const uint32_t b_sfull = smem_addr(&bars.s_full[t]);
+      const uint32_t b_pready = smem_addr(&bars.p_ready[t]);
+      const uint32_t b_odone = smem_addr(&bars.o_done[t]);
+      const uint32_t d_s = tbase + col_s(t), d_o = tbase + col_o(t);
       for (int j = 0; ok && j < n_kv; ++j) {
-        const int s = j % kStages;
-        const int round = j / kStages;
-        const uint32_t kbase = sbase + kOffK + s * kTileBytes;
-        const uint32_t vbase = sbase + kOffV + s * kTileBytes;
-        if (!(ok = wait_bar(smem_addr(&bars.k_full[s]), round & 1, abort_flag, p.err, kSiteKFull)))
-          break;
-        for (int t = 0; t < kTilesPerCta && ok; ++t) {
-          // S_t aliases P_t: the previous P_t V must have finished reading it
-          if (j > 0 && !(ok = wait_bar(smem_addr(&bars.o_done[t]), (j - 1) & 1, abort_flag, p.err,
-                                       kSiteODone)))
-            break;
-          tc_fence_after();
-          const uint32_t qbase = sbase + kOffQ + t * kTileBytes;
+        const int s = j & 1;
+        const uint32_t ph = (j >> 1) & 1;
+        // S_t = Q_t K_j^T. S_t aliases P_t: the previous P_t V must be done.
+        if (!(ok = wait_bar(s ? b_kfull1 : b_kfull0, ph, abort_flag, p.err, kSiteKFull))) break;
+        if (j > 0 && !(ok = wait_bar(b_odone, (j - 1) & 1, abort_flag, p.err, kSiteODone))) break;
+        tc_fence_after();
+        const uint64_t dk = s ? dk1 : dk0;
 #pragma unroll
-          for (int kk = 0; kk < kD / 16; ++kk)
-            mma_ss(tbase + col_s(t), kmajor_desc(qbase, kHalfTile, kk),
-                   kmajor_desc(kbase, kHalfTile, kk), kIdescQK, kk > 0 ? 1u : 0u);
-          tc_commit(smem_addr(&bars.s_full[t]));
+        for (int kk = 0; kk < kD / 16; ++kk) {
+          const uint64_t step = static_cast<uint64_t>((kk >> 2) * (kHalfTile >> 4) + (kk & 3) * 2);
+          mma_ss(d_s, dq + step, dk + step, kIdescQK, kk > 0 ? 1u : 0u);
         }
-        if (!ok) break;
-        tc_commit(smem_addr(&bars.k_empty[s]));
-        if (!(ok = wait_bar(smem_addr(&bars.v_full[s]), round & 1, abort_flag, p.err, kSiteVFull)))
-          break;
-        for (int t = 0; t < kTilesPerCta && ok; ++t) {
-          if (!(ok = wait_bar(smem_addr(&bars.p_ready[t]), j & 1, abort_flag, p.err, kSitePReady)))
-            break;
-          tc_fence_after();
+        tc_commit(b_sfull);
+        tc_commit(s ? b_kempty1 : b_kempty0);  // one of the two commits that free K_j
+        // O_t += P_t V_j, once the softmax has written P_t
+        if (!(ok = wait_bar(s ? b_vfull1 : b_vfull0, ph, abort_flag, p.err, kSiteVFull))) break;
+        if (!(ok = wait_bar(b_pready, j & 1, abort_flag, p.err, kSitePReady))) break;
+        tc_fence_after();
+        const uint64_t dv = s ? dv1 : dv0;
 #pragma unroll
-          for (int kk = 0; kk < kBN / 16; ++kk)
-            mma_ts(tbase + col_o(t), tbase + col_s(t) + kk * 8, v_desc(vbase, kk), kIdescPV,
-                   (j > 0 || kk > 0) ? 1u : 0u);
-          tc_commit(smem_addr(&bars.o_done[t]));
-        }
-        if (!ok) break;
-        tc_commit(smem_addr(&bars.v_empty[s]));
+        for (int kk = 0; kk < kBN / 16; ++kk)
+          mma_ts(d_o, d_s + kk * 8, dv + static_cast<uint64_t>(kk * (2048 >> 4)), kIdescPV,
+                 (j > 0 || kk > 0) ? 1u : 0u);
+        tc_commit(b_odone);
+        tc_commit(s ? b_vempty1 : b_vempty0);  // one of the two commits that free V_j
       }
-      // drain: no MMA may still be writing tensor memory when it is freed
-      tc_commit(smem_addr(&bars.drain));
-      drain_bar(smem_addr(&bars.drain), 0, p.err);
+      // drain: no MMA of this thread may still write tensor memory when it is freed
+      tc_commit(smem_addr(&bars.drain[t]));
+      drain_bar(smem_addr(&bars.drain[t]), 0, p.err);
     }
-  } else if (warp >= kSoftmaxWarp0) {
+  } else {
     // ------------------------------------------------------------ softmax
-    const int t = (warp - kSoftmaxWarp0) >> 2;
+    const int t = warp >> 2;
     const int quad = warp & 3;                     // tensor-memory lane quadrant
     const int r_in_tile = quad * 32 + lane;
     const int row = q0 + t * kBM + r_in_tile;      // query index
@@ -608,7 +635,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == kMmaWarp0) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tbase),
                  "r"(kTmemCols)
