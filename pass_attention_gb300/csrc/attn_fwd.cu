@@ -17,17 +17,20 @@
 // "The Online Softmax.", "One pass, exactly").
 //
 // CTA layout (352 threads, one CTA per SM):
-//   * 2 query tiles of 128 rows share every K/V tile of 128 keys.
+//   * 2 query tiles of 128 rows share every K/V tile of 64 keys.
 //   * warps 0..7  -- softmax: warp w serves query tile w / 4 and tensor-
 //                    memory lanes 32 (w % 4) .. +31 (the lane quadrant a warp
 //                    may reach); each thread owns one query row.
-//   * warp 8      -- TMA producer: Q once, then K/V tiles into a 2-stage ring.
+//   * warp 8      -- TMA producer: Q once, then K/V tiles into a 4-stage ring.
 //   * warps 9, 10 -- one thread each issues the MMAs of query tile 0 / 1:
 //                    S_t = Q_t K^T (A, B from shared memory) and
 //                    O_t += P_t V (A = P from tensor memory, B from shared).
 //                    Warp 9 also owns the tensor-memory allocation.
-// Tensor memory (512 fp32 columns x 128 lanes): S_0 | S_1 | O_0 | O_1, with
-// P_t (bf16 pairs) written over the first 64 columns of S_t.
+// Tensor memory (512 fp32 columns x 128 lanes): S_{0,0} S_{0,1} S_{1,0} S_{1,1}
+// (64 columns each: two score buffers per query tile, alternating with the
+// KV step) | O_0 | O_1 (128 each). P_{t,b} (bf16 pairs) is written over the
+// first 32 columns of S_{t,b}. With two score buffers a tile's next QK^T runs
+// while its softmax works on the current one.
 //
 // Causal: query i sees keys 0..i (Sq == Sk). KV tiles wholly above the
 // diagonal are skipped; the diagonal tiles are visited first, from the last
@@ -51,28 +54,33 @@ namespace oss {
 namespace {
 
 constexpr int kD = 128;           // head dimension
-constexpr int kBM = 128;          // query rows per tile (= tensor-memory lanes)
-constexpr int kTilesPerCta = 2;   // query tiles per CTA
+constexpr int kBM = 128;          // query rows per CTA (= tensor-memory lanes)
 constexpr int kBN = 128;          // keys per KV tile
-constexpr int kStages = 2;        // K/V ring depth (the MMA issuer assumes 2)
-constexpr int kThreads = 352;
-constexpr int kProducerWarp = 8;      // warps 0..7: softmax, one thread per query row
-constexpr int kMmaWarp0 = 9;          // warps 9, 10: MMA issuers for query tiles 0, 1
-constexpr int kRowsPerCta = kBM * kTilesPerCta;
+constexpr int kStages = 3;        // depth of the K ring and of the V ring (= score buffers)
+constexpr int kKLead = 2;         // K loads run this many steps ahead of V loads
+constexpr int kThreads = 224;
+constexpr int kProducerWarp = 4;  // warps 0..3: softmax, one thread per query row
+constexpr int kQkWarp = 5;        // warp 5: issues S = Q K^T, owns tensor memory
+constexpr int kPvWarp = 6;        // warp 6: issues O += P V
+constexpr int kCausalShift = 64;  // causal query tiles start 64 rows before a KV tile
 
-// shared memory (bytes from the 1024-aligned base)
-constexpr int kHalfTile = kBM * 64 * 2;            // 128 rows x 64 bf16 = 16 KB
-constexpr int kTileBytes = 2 * kHalfTile;          // 128 x 128 bf16 = 32 KB
-constexpr int kOffQ = 0;                           // Q_0, Q_1
-constexpr int kOffK = kOffQ + kTilesPerCta * kTileBytes;
-constexpr int kOffV = kOffK + kStages * kTileBytes;
-constexpr int kOffEnd = kOffV + kStages * kTileBytes;  // 192 KB
-constexpr int kSmemBytes = kOffEnd + 1024;             // + alignment slack
+// shared memory (bytes from the 1024-aligned base); every operand is stored
+// as two halves of 64 head dims (128-byte rows, 128-byte swizzle)
+constexpr int kHalf = 128 * 128;                   // 128 rows x 64 bf16 = 16 KB
+constexpr int kTile = 2 * kHalf;                   // 32 KB
+constexpr int kOffQ = 0;
+constexpr int kOffK = kOffQ + kTile;
+constexpr int kOffV = kOffK + kStages * kTile;
+constexpr int kOffEnd = kOffV + kStages * kTile;   // 224 KB
+constexpr int kSmemBytes = kOffEnd + 1024;         // + alignment slack
 
-// tensor-memory columns: S_t at 128 t, O_t at 256 + 128 t
+// tensor-memory columns (512 fp32 x 128 lanes): S_0 | S_1 | S_2 | O. KV step j
+// uses score buffer j % 3; P_j (bf16 pairs) is written over its first half.
+constexpr int kSBuf = 3;
+static_assert(kSBuf == kStages, "K/V ring stage and score buffer share one index");
 constexpr uint32_t kTmemCols = 512;
-__device__ __forceinline__ uint32_t col_s(int t) { return 128u * t; }
-__device__ __forceinline__ uint32_t col_o(int t) { return 256u + 128u * t; }
+__device__ __forceinline__ uint32_t col_s(int b) { return 128u * b; }
+constexpr uint32_t kColO = 384;
 
 // The reference maximum of a warp's rows moves only when one of them rises
 // by more than this (base-2 units): weights stay below 2^8 = 256.
@@ -141,9 +149,13 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
 
 // Bounded wait. Returns false on timeout (after raising the abort flag and
 // recording the site) or when another thread has already aborted.
-__device__ __noinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                      unsigned int* err, unsigned int site) {
-  if (mbar_try_wait(bar, parity)) return true;
+// Bounded wait, slow path: polls until the phase completes, another thread
+// aborts, or the time limit passes (then it raises the abort flag and
+// records the site). Kept out of line; the fast path below is inlined
+// because every wait sits on the pipeline's critical path (measured: an
+// out-of-line call costs the caller a few hundred cycles).
+__device__ __noinline__ bool wait_bar_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                           unsigned int* err, unsigned int site) {
   const uint64_t t0 = global_timer();
   for (uint32_t n = 1;; ++n) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -154,6 +166,13 @@ __device__ __noinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile in
       return false;
     }
   }
+}
+
+// Bounded wait. Returns false on timeout or when another thread has aborted.
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                         unsigned int* err, unsigned int site) {
+  if (mbar_test_wait(bar, parity)) return true;
+  return wait_bar_slow(bar, parity, abort_flag, err, site);
 }
 
 // Bounded wait used while draining: ignores the abort flag.
@@ -291,21 +310,13 @@ constexpr uint32_t make_idesc(uint32_t M, uint32_t N, bool b_mn_major) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) |
          ((N >> 3) << 17) | ((M >> 4) << 24);
 }
-constexpr uint32_t kIdescQK = make_idesc(kBM, kBN, false);  // S = Q K^T
-constexpr uint32_t kIdescPV = make_idesc(kBM, kD, true);    // O += P V
+constexpr uint32_t kIdescQK = make_idesc(kBM, kBN, false);  // S = Q K^T (N = 128 keys)
+constexpr uint32_t kIdescPV = make_idesc(kBM, kD, true);    // O += P V (N = 128 dims)
 
-// K-major operand of 128-byte rows (64 bf16), 8-row groups 1024 bytes apart,
-// the 128-wide contraction split in two 64-wide halves `half_bytes` apart.
-// MMA step kk covers contraction elements [16 kk, 16 kk + 16).
-__device__ __forceinline__ uint64_t kmajor_desc(uint32_t base, uint32_t half_bytes, int kk) {
-  return smem_desc(base + (kk >> 2) * half_bytes + (kk & 3) * 32, 16, 1024);
-}
-
-// V tile [128 keys][128 dims] stored as two [128][64] halves (dims 0-63,
-// 64-127): N-major operand for O += P V. Step kk covers keys [16 kk, 16 kk+16)
-// = two 8-key groups (2048 bytes); the dim halves are kHalfTile apart.
-__device__ __forceinline__ uint64_t v_desc(uint32_t base, int kk) {
-  return smem_desc(base + kk * 2048, kHalfTile, 1024);
+// A 16-element step along K of a K-major operand moves 32 bytes inside the
+// 128-byte swizzled row (the first four steps), then to the second half.
+__device__ __forceinline__ uint64_t kstep_kmajor(int kk, int half_bytes) {
+  return static_cast<uint64_t>((kk >> 2) * (half_bytes >> 4) + (kk & 3) * 2);
 }
 
 // ---------------------------------------------------------------------------
@@ -323,9 +334,10 @@ struct AttnParams {
 
 struct Barriers {
   uint64_t q_full;
-  uint64_t k_full[kStages], v_full[kStages], k_empty[kStages], v_empty[kStages];
-  uint64_t s_full[kTilesPerCta], p_ready[kTilesPerCta], o_done[kTilesPerCta];
-  uint64_t drain[kTilesPerCta];
+  uint64_t k_full[kStages], v_full[kStages];
+  uint64_t s_full[kSBuf], p_ready[kSBuf];
+  uint64_t o_done[kSBuf];  // P_j V done, for steps j of each buffer (keeps parity waits exact)
+  uint64_t drain[2];  // one per issuing thread
 };
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -343,15 +355,20 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // tile coordinates: heaviest causal query blocks first
+  // Query tile of this CTA. Causal tiles start kCausalShift rows before a KV
+  // tile boundary (the first tile hangs over row 0; the TMA fills the rows
+  // above with zeros), and the heaviest tiles are launched first.
   const int lin = blockIdx.x;
   const int qb_lin = lin / p.BH;
   const int bh = lin - qb_lin * p.BH;
   const int qb = p.causal ? (p.n_qblocks - 1 - qb_lin) : qb_lin;
-  const int q0 = qb * kRowsPerCta;
-  const int kv_end = p.causal ? min(p.Sk, q0 + kRowsPerCta) : p.Sk;
+  const int q0 = qb * kBM - (p.causal ? kCausalShift : 0);
+  const int kv_end = p.causal ? min(p.Sk, q0 + kBM) : p.Sk;
   const int n_kv = (kv_end + kBN - 1) / kBN;
-  const int diag_first = p.causal ? (q0 / kBN) : n_kv;  // tiles >= this touch the diagonal
+  // KV tiles that reach past the tile's first row touch the diagonal; they
+  // are visited first, from the last one down: for a shifted causal tile the
+  // first one is masked for all of the tile's first kCausalShift rows.
+  const int diag_first = p.causal ? max(0, q0) / kBN : n_kv;
   const int n_diag = n_kv - diag_first;
   auto kv_tile = [&](int j) { return j < n_diag ? (n_kv - 1 - j) : (j - n_diag); };
 
@@ -360,20 +377,19 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
     for (int s = 0; s < kStages; ++s) {
       mbar_init(smem_addr(&bars.k_full[s]), 1);
       mbar_init(smem_addr(&bars.v_full[s]), 1);
-      mbar_init(smem_addr(&bars.k_empty[s]), kTilesPerCta);  // one commit per MMA thread
-      mbar_init(smem_addr(&bars.v_empty[s]), kTilesPerCta);
     }
-    for (int t = 0; t < kTilesPerCta; ++t) {
-      mbar_init(smem_addr(&bars.s_full[t]), 1);
-      mbar_init(smem_addr(&bars.p_ready[t]), kBM);
-      mbar_init(smem_addr(&bars.o_done[t]), 1);
-      mbar_init(smem_addr(&bars.drain[t]), 1);
+    for (int b = 0; b < kSBuf; ++b) {
+      mbar_init(smem_addr(&bars.s_full[b]), 1);
+      mbar_init(smem_addr(&bars.p_ready[b]), kBM);
+      mbar_init(smem_addr(&bars.o_done[b]), 1);
     }
+    mbar_init(smem_addr(&bars.drain[0]), 1);
+    mbar_init(smem_addr(&bars.drain[1]), 1);
     abort_flag_s = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
-  if (warp == kMmaWarp0) {
+  if (warp == kQkWarp) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_addr(&tmem_base_slot)),
                  "r"(kTmemCols)
@@ -391,117 +407,123 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_k)) : "memory");
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_v)) : "memory");
       const uint32_t qbar = smem_addr(&bars.q_full);
-      mbar_expect_tx(qbar, kTilesPerCta * kTileBytes);
-      for (int t = 0; t < kTilesPerCta; ++t)
-        for (int h = 0; h < 2; ++h)
-          tma_load_3d(sbase + kOffQ + t * kTileBytes + h * kHalfTile, &tmap_q, qbar, h * 64,
-                      q0 + t * kBM, bh);
-      int issued = 0;
-      for (int j = 0; j < n_kv; ++j) {
-        const int s = j % kStages;
-        const int round = j / kStages;
-        const int key0 = kv_tile(j) * kBN;
-        if (round > 0 && !wait_bar(smem_addr(&bars.k_empty[s]), (round - 1) & 1, abort_flag, p.err,
-                                   kSiteKEmpty))
-          break;
-        const uint32_t kb = smem_addr(&bars.k_full[s]);
-        mbar_expect_tx(kb, kTileBytes);
-        for (int h = 0; h < 2; ++h)
-          tma_load_3d(sbase + kOffK + s * kTileBytes + h * kHalfTile, &tmap_k, kb, h * 64, key0, bh);
-        if (round > 0 && !wait_bar(smem_addr(&bars.v_empty[s]), (round - 1) & 1, abort_flag, p.err,
-                                   kSiteVEmpty)) {
-          issued = 2 * j + 1;
-          break;
+      mbar_expect_tx(qbar, kTile);
+      for (int h = 0; h < 2; ++h)
+        tma_load_3d(sbase + kOffQ + h * kHalf, &tmap_q, qbar, h * 64, q0, bh);
+      // K_j is consumed by QK_j, which runs up to two steps ahead of P_j V,
+      // the consumer of V_j; so K loads run kKLead steps ahead of V loads,
+      // and each ring is refilled as soon as its own consumer is done: K stage
+      // j % 3 when QK_j has completed (s_full[j % 3]), V stage j % 3 when
+      // P_j V has (o_done[j % 3]) -- ring stage and score buffer coincide.
+      int k_issued = 0, v_issued = 0;
+      for (int i = 0; i < n_kv + kKLead; ++i) {
+        if (i < n_kv) {
+          const int s = i % kStages;
+          const int round = i / kStages;
+          if (round > 0 && !wait_bar(smem_addr(&bars.s_full[s]), (round - 1) & 1, abort_flag,
+                                     p.err, kSiteKEmpty))
+            break;
+          const uint32_t kb = smem_addr(&bars.k_full[s]);
+          mbar_expect_tx(kb, kTile);
+          for (int h = 0; h < 2; ++h)
+            tma_load_3d(sbase + kOffK + s * kTile + h * kHalf, &tmap_k, kb, h * 64,
+                        kv_tile(i) * kBN, bh);
+          k_issued = i + 1;
         }
-        const uint32_t vb = smem_addr(&bars.v_full[s]);
-        mbar_expect_tx(vb, kTileBytes);
-        for (int h = 0; h < 2; ++h)
-          tma_load_3d(sbase + kOffV + s * kTileBytes + h * kHalfTile, &tmap_v, vb, h * 64, key0, bh);
-        issued = 2 * j + 2;
+        const int j = i - kKLead;
+        if (j >= 0 && j < n_kv) {
+          const int s = j % kStages;
+          const int round = j / kStages;
+          if (round > 0 && !wait_bar(smem_addr(&bars.o_done[s]), (round - 1) & 1, abort_flag,
+                                     p.err, kSiteVEmpty))
+            break;
+          const uint32_t vb = smem_addr(&bars.v_full[s]);
+          mbar_expect_tx(vb, kTile);
+          for (int h = 0; h < 2; ++h)
+            tma_load_3d(sbase + kOffV + s * kTile + h * kHalf, &tmap_v, vb, h * 64,
+                        kv_tile(j) * kBN, bh);
+          v_issued = j + 1;
+        }
       }
       // drain: every issued copy must land before the CTA may exit
       drain_bar(qbar, 0, p.err);
-      for (int c = issued - 1; c >= 0 && c >= issued - 2 * kStages; --c) {
-        const int j = c >> 1;
-        const int s = j % kStages;
-        const uint32_t b = (c & 1) ? smem_addr(&bars.v_full[s]) : smem_addr(&bars.k_full[s]);
-        drain_bar(b, (j / kStages) & 1, p.err);
-      }
+      for (int j = k_issued - 1; j >= 0 && j >= k_issued - kStages; --j)
+        drain_bar(smem_addr(&bars.k_full[j % kStages]), (j / kStages) & 1, p.err);
+      for (int j = v_issued - 1; j >= 0 && j >= v_issued - kStages; --j)
+        drain_bar(smem_addr(&bars.v_full[j % kStages]), (j / kStages) & 1, p.err);
     }
-  } else if (warp == kMmaWarp0 || warp == kMmaWarp0 + 1) {
-    // ------------------------------------------------------------ MMA issuers
-    // One thread per query tile, each running its own chain
-    //   QK_0, PV_0, QK_1, PV_1, ...
-    // Issuing a tcgen05.mma costs its thread tens of cycles, so a single
-    // issuing thread cannot keep the tensor pipe busy; two can, and the
-    // tiles no longer wait on each other's softmax.
+  } else if (warp == kQkWarp) {
+    // ------------------------------------------------------------ QK issuer
+    // S_{j % 3} = Q K_j^T for j = 0, 1, ...: the buffer last held P_{j-3},
+    // so P_{j-3} V must be done with it. Issuing a tcgen05.mma costs its
+    // thread tens of cycles, so QK^T and P V are issued by two threads.
     if (lane == 0) {
-      const int t = warp - kMmaWarp0;
       bool ok = wait_bar(smem_addr(&bars.q_full), 0, abort_flag, p.err, kSiteQFull);
-      // operand descriptors per buffer, built once; a 16-element K step only
-      // adds a constant to the start-address field (16-byte units)
-      const uint64_t dq = smem_desc(sbase + kOffQ + t * kTileBytes, 16, 1024);
-      const uint64_t dk0 = smem_desc(sbase + kOffK, 16, 1024);
-      const uint64_t dk1 = smem_desc(sbase + kOffK + kTileBytes, 16, 1024);
-      const uint64_t dv0 = smem_desc(sbase + kOffV, kHalfTile, 1024);
-      const uint64_t dv1 = smem_desc(sbase + kOffV + kTileBytes, kHalfTile, 1024);
-      const uint32_t b_kfull0 = smem_addr(&bars.k_full[0]), b_kfull1 = smem_addr(&bars.k_full[1]);
-      const uint32_t b_vfull0 = smem_addr(&bars.v_full[0]), b_vfull1 = smem_addr(&bars.v_full[1]);
-      const uint32_t b_kempty0 = smem_addr(&bars.k_empty[0]), b_kempty1 = smem_addr(&bars.k_empty[1]);
-      const uint32_t b_vempty0 = smem_addr(&bars.v_empty[0]), b_vempty1 = smem_addr(&bars.v_empty[1]);
-      const uint32_t b_sfull = smem_addr(&bars.s_full[t]);
-      const uint32_t b_pready = smem_addr(&bars.p_ready[t]);
-      const uint32_t b_odone = smem_addr(&bars.o_done[t]);
-      const uint32_t d_s = tbase + col_s(t), d_o = tbase + col_o(t);
+      // operand descriptors built once; a 16-element K step only adds a
+      // constant to the start-address field (16-byte units)
+      const uint64_t dq = smem_desc(sbase + kOffQ, 16, 1024);
       for (int j = 0; ok && j < n_kv; ++j) {
-        const int s = j & 1;
-        const uint32_t ph = (j >> 1) & 1;
-        // S_t = Q_t K_j^T. S_t aliases P_t: the previous P_t V must be done.
-        if (!(ok = wait_bar(s ? b_kfull1 : b_kfull0, ph, abort_flag, p.err, kSiteKFull))) break;
-        if (j > 0 && !(ok = wait_bar(b_odone, (j - 1) & 1, abort_flag, p.err, kSiteODone))) break;
+        const int s = j % kStages;  // K stage = score buffer
+        if (!(ok = wait_bar(smem_addr(&bars.k_full[s]), (j / kStages) & 1, abort_flag, p.err,
+                            kSiteKFull)))
+          break;
+        if (j >= kStages && !(ok = wait_bar(smem_addr(&bars.o_done[s]), (j / kStages - 1) & 1,
+                                            abort_flag, p.err, kSiteODone)))
+          break;
         tc_fence_after();
-        const uint64_t dk = s ? dk1 : dk0;
+        const uint64_t dk = smem_desc(sbase + kOffK + s * kTile, 16, 1024);
+        const uint32_t d_s = tbase + col_s(s);
 #pragma unroll
-        for (int kk = 0; kk < kD / 16; ++kk) {
-          const uint64_t step = static_cast<uint64_t>((kk >> 2) * (kHalfTile >> 4) + (kk & 3) * 2);
-          mma_ss(d_s, dq + step, dk + step, kIdescQK, kk > 0 ? 1u : 0u);
-        }
-        tc_commit(b_sfull);
-        tc_commit(s ? b_kempty1 : b_kempty0);  // one of the two commits that free K_j
-        // O_t += P_t V_j, once the softmax has written P_t
-        if (!(ok = wait_bar(s ? b_vfull1 : b_vfull0, ph, abort_flag, p.err, kSiteVFull))) break;
-        if (!(ok = wait_bar(b_pready, j & 1, abort_flag, p.err, kSitePReady))) break;
-        tc_fence_after();
-        const uint64_t dv = s ? dv1 : dv0;
-#pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk)
-          mma_ts(d_o, d_s + kk * 8, dv + static_cast<uint64_t>(kk * (2048 >> 4)), kIdescPV,
-                 (j > 0 || kk > 0) ? 1u : 0u);
-        tc_commit(b_odone);
-        tc_commit(s ? b_vempty1 : b_vempty0);  // one of the two commits that free V_j
+        for (int kk = 0; kk < kD / 16; ++kk)
+          mma_ss(d_s, dq + kstep_kmajor(kk, kHalf), dk + kstep_kmajor(kk, kHalf), kIdescQK,
+                 kk > 0 ? 1u : 0u);
+        tc_commit(smem_addr(&bars.s_full[s]));  // scores ready; K stage s free
       }
       // drain: no MMA of this thread may still write tensor memory when it is freed
-      tc_commit(smem_addr(&bars.drain[t]));
-      drain_bar(smem_addr(&bars.drain[t]), 0, p.err);
+      tc_commit(smem_addr(&bars.drain[0]));
+      drain_bar(smem_addr(&bars.drain[0]), 0, p.err);
+    }
+  } else if (warp == kPvWarp) {
+    // ------------------------------------------------------------ PV issuer
+    // O += P_j V_j once the softmax has written P_j over S_{j % 3}.
+    if (lane == 0) {
+      bool ok = true;
+      const uint32_t d_o = tbase + kColO;
+      for (int j = 0; ok && j < n_kv; ++j) {
+        const int s = j % kStages;
+        if (!(ok = wait_bar(smem_addr(&bars.v_full[s]), (j / kStages) & 1, abort_flag, p.err,
+                            kSiteVFull)))
+          break;
+        if (!(ok = wait_bar(smem_addr(&bars.p_ready[s]), (j / kStages) & 1, abort_flag, p.err,
+                            kSitePReady)))
+          break;
+        tc_fence_after();
+        const uint64_t dv = smem_desc(sbase + kOffV + s * kTile, kHalf, 1024);
+        const uint32_t a_p = tbase + col_s(s);
+#pragma unroll
+        for (int kk = 0; kk < kBN / 16; ++kk)
+          mma_ts(d_o, a_p + kk * 8, dv + static_cast<uint64_t>(kk * (2048 >> 4)), kIdescPV,
+                 (j > 0 || kk > 0) ? 1u : 0u);
+        tc_commit(smem_addr(&bars.o_done[s]));  // buffer s and V stage s free
+      }
+      tc_commit(smem_addr(&bars.drain[1]));
+      drain_bar(smem_addr(&bars.drain[1]), 0, p.err);
     }
   } else {
     // ------------------------------------------------------------ softmax
-    const int t = warp >> 2;
-    const int quad = warp & 3;                     // tensor-memory lane quadrant
+    const int quad = warp;                         // tensor-memory lane quadrant
     const int r_in_tile = quad * 32 + lane;
-    const int row = q0 + t * kBM + r_in_tile;      // query index
+    const int row = q0 + r_in_tile;                // query index (may be < 0: padding)
     const uint32_t tl = tbase + (static_cast<uint32_t>(quad * 32) << 16);
-    const uint32_t colS = col_s(t), colO = col_o(t);
-    const uint32_t s_bar = smem_addr(&bars.s_full[t]);
-    const uint32_t p_bar = smem_addr(&bars.p_ready[t]);
-    const uint32_t o_bar = smem_addr(&bars.o_done[t]);
     const float C = p.C;
-    const int tile_row0 = q0 + t * kBM;
-    float m = neg_inf();  // running max, base 2
+    float m = neg_inf();  // reference maximum, base 2
     float l = 0.f;
     bool ok = true;
     for (int j = 0; j < n_kv; ++j) {
-      ok = __all_sync(0xffffffffu, wait_bar(s_bar, j & 1, abort_flag, p.err, kSiteSFull));
+      const int b = j % kSBuf;
+      const uint32_t colS = col_s(b);
+      ok = __all_sync(0xffffffffu, wait_bar(smem_addr(&bars.s_full[b]), (j / kSBuf) & 1,
+                                            abort_flag, p.err, kSiteSFull));
       if (!ok) break;
       tc_fence_after();
       uint32_t r0[32], r1[32], r2[32], r3[32];
@@ -513,7 +535,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
       tmem_ld_wait(r1);
       tmem_ld_wait(r2);
       tmem_ld_wait(r3);
-      float s[128];
+      float s[kBN];
 #pragma unroll
       for (int c = 0; c < 32; ++c) {
         s[c] = __uint_as_float(r0[c]);
@@ -523,14 +545,14 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
       }
       const int key0 = kv_tile(j) * kBN;
       const bool ragged = key0 + kBN > p.Sk;
-      const bool diag = p.causal && key0 + kBN - 1 > tile_row0;
+      const bool diag = p.causal && key0 + kBN - 1 > q0;
       if (ragged || diag) {
         const int lim = min(p.Sk, p.causal ? row + 1 : p.Sk) - key0;  // visible keys: c < lim
 #pragma unroll
         for (int c = 0; c < kBN; ++c)
           if (c >= lim) s[c] = neg_inf();
       }
-      // row maximum: four independent chains of 3-input max
+      // row maximum of this tile: four independent chains of 3-input max
       float mx0 = neg_inf(), mx1 = neg_inf(), mx2 = neg_inf(), mx3 = neg_inf();
 #pragma unroll
       for (int c = 0; c < kBN; c += 8) {
@@ -558,7 +580,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
       float2 acc0 = make_float2(0.f, 0.f), acc1 = acc0;
 #pragma unroll
       for (int ch = 0; ch < kBN / 32; ++ch) {
-        // 32 weights -> 16 bf16 pairs, stored over the first half of S_t
+        // 32 weights -> 16 bf16 pairs, stored over the first columns of S_b
         uint32_t pk[16];
 #pragma unroll
         for (int c = 0; c < 32; c += 4) {
@@ -577,15 +599,17 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
       const float2 acc = __fadd2_rn(acc0, acc1);
       l = fmaf(l, corr, acc.x + acc.y);
       if (rescale && j > 0) {
-        // O_t still holds the previous tiles' sum: wait for it, then rescale
-        ok = __all_sync(0xffffffffu, wait_bar(o_bar, (j - 1) & 1, abort_flag, p.err, kSiteODone));
+        // O still holds the previous tiles' sum: wait for P_{j-1} V (whose
+        // completion implies every earlier one), then rescale
+        ok = __all_sync(0xffffffffu, wait_bar(smem_addr(&bars.o_done[(j - 1) % kSBuf]),
+                                              ((j - 1) / kSBuf) & 1, abort_flag, p.err, kSiteODone));
         if (!ok) break;
         tc_fence_after();
         const float2 cv = make_float2(corr, corr);
 #pragma unroll 1
         for (int cc = 0; cc < kD; cc += 32) {
           uint32_t ov[32];
-          tmem_ld32(tl + colO + cc, ov);
+          tmem_ld32(tl + kColO + cc, ov);
           tmem_ld_wait(ov);
 #pragma unroll
           for (int c = 0; c < 32; c += 2) {
@@ -593,25 +617,27 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
             ov[c] = __float_as_uint(o2.x);
             ov[c + 1] = __float_as_uint(o2.y);
           }
-          tmem_st32(tl + colO + cc, ov);
+          tmem_st32(tl + kColO + cc, ov);
         }
       }
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(p_bar);
+      mbar_arrive(smem_addr(&bars.p_ready[b]));
     }
-    // epilogue: O / l and lse for this row
-    if (ok) ok = __all_sync(0xffffffffu, wait_bar(o_bar, (n_kv - 1) & 1, abort_flag, p.err,
-                                                   kSiteODone));
+    // epilogue: O / l and lse for this row, once P_{n-1} V is done (its
+    // completion implies every earlier one)
+    if (ok)
+      ok = __all_sync(0xffffffffu, wait_bar(smem_addr(&bars.o_done[(n_kv - 1) % kSBuf]),
+                                            ((n_kv - 1) / kSBuf) & 1, abort_flag, p.err, kSiteODone));
     if (ok) {
       tc_fence_after();
       const float inv = (l > 0.f) ? 1.0f / l : 0.f;
-      const bool live = row < p.Sq;
+      const bool live = row >= 0 && row < p.Sq;
       uint4* orow = reinterpret_cast<uint4*>(p.o + (static_cast<size_t>(bh) * p.Sq + row) * kD);
 #pragma unroll 1
       for (int cc = 0; cc < kD; cc += 32) {
         uint32_t ov[32];
-        tmem_ld32(tl + colO + cc, ov);
+        tmem_ld32(tl + kColO + cc, ov);
         tmem_ld_wait(ov);
         if (live) {
 #pragma unroll
@@ -635,7 +661,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
 
   tc_fence_before();
   __syncthreads();
-  if (warp == kMmaWarp0) {
+  if (warp == kQkWarp) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tbase),
                  "r"(kTmemCols)
@@ -665,15 +691,15 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// [BH][S][128] bf16 viewed as a 3-D tensor; boxes of 64 dims x 128 rows, 128B swizzle.
-bool make_map(CUtensorMap* map, const uint16_t* base, int S, int BH) {
+// [BH][S][128] bf16 viewed as a 3-D tensor; boxes of 64 dims x box_rows rows, 128B swizzle.
+bool make_map(CUtensorMap* map, const uint16_t* base, int S, int BH, int box_rows) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(S),
                         static_cast<cuuint64_t>(BH)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(kD) * 2,
                            static_cast<cuuint64_t>(S) * kD * 2};
-  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1};
   cuuint32_t estride[3] = {1, 1, 1};
   return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t*>(base), dims, strides,
              box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -689,7 +715,8 @@ cudaError_t launch_attention_fwd(const uint16_t* q, const uint16_t* k, const uin
   if (D != kD) return cudaErrorNotSupported;
   const int BH = B * H;
   CUtensorMap mq, mk, mv;
-  if (!make_map(&mq, q, Sq, BH) || !make_map(&mk, k, Sk, BH) || !make_map(&mv, v, Sk, BH))
+  if (!make_map(&mq, q, Sq, BH, kBM) || !make_map(&mk, k, Sk, BH, kBN) ||
+      !make_map(&mv, v, Sk, BH, kBN))
     return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        kSmemBytes);
@@ -701,7 +728,7 @@ cudaError_t launch_attention_fwd(const uint16_t* q, const uint16_t* k, const uin
   prm.Sq = Sq;
   prm.Sk = Sk;
   prm.BH = BH;
-  prm.n_qblocks = (Sq + kRowsPerCta - 1) / kRowsPerCta;
+  prm.n_qblocks = (Sq + (causal ? kCausalShift : 0) + kBM - 1) / kBM;
   prm.C = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
   prm.causal = causal ? 1 : 0;
   const long long grid = static_cast<long long>(prm.n_qblocks) * BH;
