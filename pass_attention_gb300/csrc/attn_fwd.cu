@@ -4,11 +4,7 @@
 // metalworking page's five-line recurrence states it ("Online Softmax"):
 //   m_new = max(m, rowmax S);  c = 2^(m - m_new);  P = 2^(S - m_new);
 //   l = l*c + rowsum P;        O = O*c + P V;      m = m_new;
-// and after the last tile O /= l. The rescale is conditional, in the spirit
-// of the metal-flash-attention guard the page quotes (correction 1 unless
-// the maximum rose): a warp moves its rows' reference maximum only when one
-// of them rose by more than 2^8, so the O round trip through tensor memory
-// is rare; any reference gives the same O / l in exact arithmetic. Scores are kept in base 2 with
+// and after the last tile O /= l. Scores are kept in base 2 with
 // scale * log2(e) folded in once, and every exponential is exp2, the rescale
 // factor included (roadmapper "Online softmax", "Things that break"). The
 // state starts at m = -inf, l = 0; a row whose keys are all masked so far
@@ -16,26 +12,34 @@
 // "Initialise honestly"). No score row is ever written to memory (curionode
 // "The Online Softmax.", "One pass, exactly").
 //
-// CTA layout (352 threads, one CTA per SM):
-//   * 2 query tiles of 128 rows share every K/V tile of 64 keys.
-//   * warps 0..7  -- softmax: warp w serves query tile w / 4 and tensor-
-//                    memory lanes 32 (w % 4) .. +31 (the lane quadrant a warp
-//                    may reach); each thread owns one query row.
-//   * warp 8      -- TMA producer: Q once, then K/V tiles into a 4-stage ring.
-//   * warps 9, 10 -- one thread each issues the MMAs of query tile 0 / 1:
-//                    S_t = Q_t K^T (A, B from shared memory) and
-//                    O_t += P_t V (A = P from tensor memory, B from shared).
-//                    Warp 9 also owns the tensor-memory allocation.
-// Tensor memory (512 fp32 columns x 128 lanes): S_{0,0} S_{0,1} S_{1,0} S_{1,1}
-// (64 columns each: two score buffers per query tile, alternating with the
-// KV step) | O_0 | O_1 (128 each). P_{t,b} (bf16 pairs) is written over the
-// first 32 columns of S_{t,b}. With two score buffers a tile's next QK^T runs
-// while its softmax works on the current one.
+// The rescale is conditional, in the spirit of the metal-flash-attention
+// guard the metalworking page quotes (correction 1 unless the maximum rose):
+// a warp moves its rows' reference maximum only when one of them rose by
+// more than 2^8, so the O round trip through tensor memory is rare; any
+// reference gives the same O / l in exact arithmetic, and weights stay
+// below 256.
 //
-// Causal: query i sees keys 0..i (Sq == Sk). KV tiles wholly above the
-// diagonal are skipped; the diagonal tiles are visited first, from the last
-// one down, so query tile 0 meets a KV tile in which all of its rows are
-// masked before it meets any visible key -- the case the guard exists for.
+// CTA layout (224 threads, one CTA per SM, one 128-row query tile):
+//   * warps 0..3 -- softmax: warp w reaches tensor-memory lanes 32 w .. +31;
+//                   each thread owns one query row.
+//   * warp 4     -- TMA producer: Q once, then K and V tiles (128 keys) into
+//                   two 3-stage rings, K two steps ahead of V.
+//   * warp 5     -- one thread issues S_b = Q K_j^T (A, B from shared memory);
+//                   the warp owns the tensor-memory allocation.
+//   * warp 6     -- one thread issues O += P_j V_j (A = P from tensor memory,
+//                   B from shared memory).
+//   Issuing a tcgen05.mma costs its thread tens of cycles, so the two MMA
+//   streams have a thread each.
+// Tensor memory (512 fp32 columns x 128 lanes): S_0 | S_1 | S_2 | O. KV step
+// j uses score buffer b = j % 3 (and ring stage j % 3); the softmax writes P_j
+// as bf16 pairs over the first 64 columns of S_b. With three score buffers
+// QK^T runs up to two steps ahead of the softmax.
+//
+// Causal: query i sees keys 0..i (Sq == Sk). Query tiles start 64 rows before
+// a KV-tile boundary; KV tiles wholly above the diagonal are skipped and the
+// two diagonal tiles are visited first, from the last one down, so the first
+// KV tile a causal CTA sees is masked for all of its first 64 rows -- the
+// case the -inf guard exists for.
 //
 // Every wait on an mbarrier is bounded: on timeout the thread raises a
 // CTA-wide abort flag and writes the device error word; all roles then drain
@@ -63,6 +67,7 @@ constexpr int kProducerWarp = 4;  // warps 0..3: softmax, one thread per query r
 constexpr int kQkWarp = 5;        // warp 5: issues S = Q K^T, owns tensor memory
 constexpr int kPvWarp = 6;        // warp 6: issues O += P V
 constexpr int kCausalShift = 64;  // causal query tiles start 64 rows before a KV tile
+constexpr int kCausalGroup = 4;   // heads per causal scheduling group (K/V of 4 heads fit L2)
 
 // shared memory (bytes from the 1024-aligned base); every operand is stored
 // as two halves of 64 head dims (128-byte rows, 128-byte swizzle)
@@ -147,8 +152,6 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Bounded wait. Returns false on timeout (after raising the abort flag and
-// recording the site) or when another thread has already aborted.
 // Bounded wait, slow path: polls until the phase completes, another thread
 // aborts, or the time limit passes (then it raises the abort flag and
 // records the site). Kept out of line; the fast path below is inlined
@@ -358,10 +361,24 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
   // Query tile of this CTA. Causal tiles start kCausalShift rows before a KV
   // tile boundary (the first tile hangs over row 0; the TMA fills the rows
   // above with zeros), and the heaviest tiles are launched first.
+  // CTA order: the ~150 CTAs resident at a time should share (b, h), so
+  // that K and V are read from HBM once and then from L2. Non-causal:
+  // (b, h)-major. Causal: groups of kCausalGroup heads, heaviest query tiles
+  // first within each group.
   const int lin = blockIdx.x;
-  const int qb_lin = lin / p.BH;
-  const int bh = lin - qb_lin * p.BH;
-  const int qb = p.causal ? (p.n_qblocks - 1 - qb_lin) : qb_lin;
+  int bh, qb;
+  if (!p.causal) {
+    bh = lin / p.n_qblocks;
+    qb = lin - bh * p.n_qblocks;
+  } else {
+    const int per_group = kCausalGroup * p.n_qblocks;
+    const int g = lin / per_group;
+    const int gsize = min(kCausalGroup, p.BH - g * kCausalGroup);
+    const int r = lin - g * per_group;
+    const int qb_lin = r / gsize;
+    bh = g * kCausalGroup + (r - qb_lin * gsize);
+    qb = p.n_qblocks - 1 - qb_lin;
+  }
   const int q0 = qb * kBM - (p.causal ? kCausalShift : 0);
   const int kv_end = p.causal ? min(p.Sk, q0 + kBM) : p.Sk;
   const int n_kv = (kv_end + kBN - 1) / kBN;
