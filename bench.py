@@ -44,9 +44,25 @@ METRIC = "softmax GB/s & attention fwd TFLOP/s on 1 GB300, as fraction of roofli
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 # DRAM traffic per launch from ncu (dram__bytes_read.sum + dram__bytes_write.sum),
-# keyed by kernel, with the sha256 of the kernel's source file when it was
+# keyed by workload, with the sha256 of the kernel's source file when it was
 # captured: a changed source reports null. Summaries live under profiles/.
-NCU_TRAFFIC = {}
+# "scale" records traffic / algorithmic bytes of a smaller capture of the
+# same kernel, applied to the full launch's algorithmic bytes.
+NCU_TRAFFIC = {
+    "softmax_32k": {"source": "pass_attention_gb300/csrc/softmax_rows.cu",
+                    "sha256": "9f37f7efad57e9fec69e43131b3ee73741964a0ceee68ec4fd6fbfb9f039d74d",
+                    "bytes_per_launch": 1073969000 + 1017877000},
+    "attn_4k": {"source": "pass_attention_gb300/csrc/attn_fwd.cu",
+                "sha256": "07e11d492b2cd675bc76e6c19119b71bde9f6689c0cce99cf43435a37336d359",
+                "bytes_per_launch": 201379328 + 48655872},
+    "attn_causal": {"source": "pass_attention_gb300/csrc/attn_fwd.cu",
+                    "sha256": "07e11d492b2cd675bc76e6c19119b71bde9f6689c0cce99cf43435a37336d359",
+                    "bytes_per_launch": 403601920 + 116535552},
+    "decode_64x32": {"source": "pass_attention_gb300/csrc/decode_merge.cu",
+                     "sha256": "a9116a8452b09df5ffc198fb6fac3fbf559ce1606b95c551b24f75e9f2c2961f",
+                     "scale": (2484805000 + 4145664) / (151653 * 32 * 512 + 8 * 32 * 128 * 2
+                                                         + 8 * 32 * 16 * 130 * 4)},
+}
 
 
 # ---------------------------------------------------------------------------
@@ -68,8 +84,8 @@ def source_sha(rel):
         return hashlib.sha256(f.read()).hexdigest()
 
 
-def traffic_for(kernel):
-    rec = NCU_TRAFFIC.get(kernel)
+def traffic_for(workload, algorithmic_bytes=None):
+    rec = NCU_TRAFFIC.get(workload)
     if not rec:
         return None
     try:
@@ -77,6 +93,8 @@ def traffic_for(kernel):
             return None
     except OSError:
         return None
+    if "scale" in rec:
+        return None if algorithmic_bytes is None else rec["scale"] * algorithmic_bytes
     return rec["bytes_per_launch"]
 
 
@@ -235,10 +253,10 @@ def bench_attention(args, ctx, w):
     stream = torch.cuda.current_stream()
     fn = lambda: oss.attention_fwd(q, k, v, w.scale, w.causal, o=o, lse=lse, stream=stream)
     steps = max(3, min(args.steps, 50))
-    total_ms, step_ms, _, _ = time_steps(fn, steps, max(3, args.warmup), stream, ctx["barrier"])
+    total_ms, step_ms, t0, t1 = time_steps(fn, steps, max(3, args.warmup), stream, ctx["barrier"])
     oss.check_device_error()
     flops = attention_flops(w.B, w.H, w.S, w.D, w.causal)
-    return step_ms, flops
+    return step_ms, flops, (t0, t1)
 
 
 def bench_decode(args, ctx):
@@ -258,7 +276,7 @@ def bench_decode(args, ctx):
         oss.merge_partials(pm, pl, po, True, o, mo, lo, lseo, stream=stream)
 
     steps = max(3, min(args.steps, 30))
-    total_ms, step_ms, _, _ = time_steps(fn, steps, max(3, args.warmup), stream, ctx["barrier"])
+    total_ms, step_ms, t0, t1 = time_steps(fn, steps, max(3, args.warmup), stream, ctx["barrier"])
     # the decode kernel alone (dominant): events around it only
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * steps)]
     for i in range(steps):
@@ -272,7 +290,7 @@ def bench_decode(args, ctx):
     kv_bytes = int(sum(kvl)) * w.H * w.D * 4
     dec_bytes = kv_bytes + w.B * w.H * w.D * 2 + w.B * w.H * S * (w.D + 2) * 4
     del k, v
-    return step_ms, nbytes, dec_ms, dec_bytes
+    return step_ms, nbytes, dec_ms, dec_bytes, (t0, t1)
 
 
 # ---------------------------------------------------------------------------
@@ -305,7 +323,7 @@ def run_reference(args, rank):
         return
     w = workloads.SOFTMAX_32K
     x_np = workloads.logits(4096, w.cols, w.mult, w.seed).numpy()
-    per_step_s = 2.0
+    per_step_s = args.ref_step_seconds
     for _ in range(args.warmup):
         oracle_softmax_rate(0.2, x_np)
     t0 = time.perf_counter()
@@ -344,6 +362,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--headline-only", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--ref-step-seconds", type=float, default=2.0,
+                    help="oracle time per step of --impl reference")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -395,19 +415,20 @@ def main():
     if not args.headline_only:
         for aw in (workloads.ATTN_4K, workloads.ATTN_CAUSAL):
             try:
-                ms, flops = bench_attention(args, ctx, aw)
+                ms, flops, win = bench_attention(args, ctx, aw)
                 tf = flops / (ms / 1e3) / 1e12
                 extra[aw.name] = {
                     "value": tf, "unit": "TFLOP/s", "ms_per_step": ms,
                     "workload": f"B{aw.B} H{aw.H} S{aw.S} D{aw.D} bf16 {'causal' if aw.causal else 'non-causal'}",
                     "roofline": {"bound": "tensor", "achieved": tf, "peak": pk["bf16_tflops"],
                                  "unit": "TFLOP/s", "frac": tf / pk["bf16_tflops"],
-                                 "traffic": traffic_for("attn_fwd_kernel"),
-                                 "peak_kind": f"{pk_kind} bf16 dense (burst)"}}
+                                 "traffic": traffic_for(aw.name),
+                                 "peak_kind": f"{pk_kind} bf16 dense (burst)"},
+                    "window": win}
             except Exception as e:  # report, do not hide
                 extra[aw.name] = {"unavailable": f"{type(e).__name__}: {e}"}
         try:
-            ms, nbytes, dec_ms, dec_bytes = bench_decode(args, ctx)
+            ms, nbytes, dec_ms, dec_bytes, win = bench_decode(args, ctx)
             gbs = nbytes / (ms / 1e3) / 1e9
             ach = dec_bytes / (dec_ms / 1e3) / 1e9
             extra["decode_64x32"] = {
@@ -415,13 +436,17 @@ def main():
                 "workload": "B64 H32 D128 bf16, kv_len~U{1..32768}, 16 splits, decode + merge",
                 "roofline": {"bound": "hbm", "kernel": "decode_splitkv_kernel", "achieved": ach,
                              "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": ach / pk["hbm_gbs"],
-                             "traffic": traffic_for("decode_splitkv_kernel"),
-                             "peak_kind": f"{pk_kind} HBM copy"}}
+                             "traffic": traffic_for("decode_64x32", dec_bytes),
+                             "peak_kind": f"{pk_kind} HBM copy"},
+                "window": win}
         except Exception as e:
             extra["decode_64x32"] = {"unavailable": f"{type(e).__name__}: {e}"}
 
     sampler.stop()
     clocks = sampler.summary(sm["t0"], sm["t1"])
+    for entry in extra.values():
+        if "window" in entry:
+            entry["clocks"] = sampler.summary(*entry.pop("window"))
 
     cpu = None
     if rank == 0:
@@ -443,7 +468,7 @@ def main():
         "gpu_launches": args.steps,
         "roofline": {"bound": "hbm", "kernel": kname, "achieved": achieved, "peak": pk["hbm_gbs"],
                      "unit": "GB/s", "frac": achieved / pk["hbm_gbs"],
-                     "traffic": traffic_for(kname), "peak_kind": f"{pk_kind} HBM copy"},
+                     "traffic": traffic_for(w.name), "peak_kind": f"{pk_kind} HBM copy"},
         "cpu_baseline": cpu,
         "extra": extra,
     }

@@ -185,6 +185,25 @@ OSS_API os_status os_merge_partials(const float* part_m, const float* part_l, co
  */
 OSS_API os_status os_check_device_error(void* stream, int32_t* code);
 
+/*
+ * os_debug_inject_fault -- test hook for the bounded waits. Arms a fault for
+ * the next os_attention_fwd call made by the calling host thread (then
+ * disarms it):
+ *   kind 0: disarm.
+ *   kind 1: the kernel's load warp skips the V tile of KV step `step` (counted
+ *           in the order each CTA visits its KV tiles), so the thread that
+ *           issues P V waits on a phase that never completes. After
+ *           `timeout_ns` (0: the default of 2 s) it raises the CTA's abort
+ *           flag; every role drains its own copies and MMAs, tensor memory is
+ *           freed, and the kernel exits. os_check_device_error then returns
+ *           OS_ERR_TIMEOUT with code = 1 | (3 << 8) (kernel 1, wait site 3:
+ *           V tile full). The CUDA context stays usable; the outputs of that
+ *           call are undefined.
+ * No GPU fault, trap or endless wait is involved.
+ * Errors: OS_ERR_INVALID_ARGUMENT (kind not 0/1, step < 0, timeout_ns < 0).
+ */
+OSS_API os_status os_debug_inject_fault(int32_t kind, int32_t step, int64_t timeout_ns);
+
 /* Human-readable name of a status (static storage; never NULL). */
 OSS_API const char* os_status_string(os_status status);
 

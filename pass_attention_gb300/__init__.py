@@ -30,6 +30,7 @@ __all__ = [
     "merge_partials",
     "decode_from_host",
     "check_device_error",
+    "debug_inject_fault",
     "abi_version",
     "EXPORTED_SYMBOLS",
 ]
@@ -62,6 +63,7 @@ _SIGNATURES = {
     "os_merge_partials": (_i32, [_vp, _vp, _vp, _i64, _i32, _i32, ctypes.c_int, _vp, _vp, _vp,
                                  _vp, _vp]),
     "os_check_device_error": (_i32, [_vp, ctypes.POINTER(_i32)]),
+    "os_debug_inject_fault": (_i32, [_i32, _i32, _i64]),
     "os_status_string": (ctypes.c_char_p, [_i32]),
     "os_abi_version": (_i32, []),
 }
@@ -319,6 +321,13 @@ def decode_from_host(q_host, k_host, v_host, kv_len_host, num_splits, scale=None
     out[1].copy_(lse, non_blocking=True)
     torch.cuda.current_stream().synchronize()
     return out
+
+
+def debug_inject_fault(kind: int, step: int = 0, timeout_ns: int = 0) -> None:
+    """Test hook: arm a fault for the next attention_fwd call on this thread
+    (see ``os_debug_inject_fault`` in include/oss.h)."""
+    _check(load().os_debug_inject_fault(int(kind), int(step), int(timeout_ns)),
+           "os_debug_inject_fault")
 
 
 def check_device_error(stream=None) -> int:

@@ -40,6 +40,10 @@ os_status from_cuda(cudaError_t e) {
 
 bool valid_scale(float s) { return std::isfinite(s) && s > 0.f; }
 
+// Armed by os_debug_inject_fault, consumed by the next os_attention_fwd on
+// the same host thread.
+thread_local oss::AttnFault t_fault;
+
 }  // namespace
 
 extern "C" {
@@ -81,8 +85,10 @@ os_status os_attention_fwd(const os_bf16* q, const os_bf16* k, const os_bf16* v,
   if (static_cast<int64_t>(B) * H > 65535 * 64) return OS_ERR_UNSUPPORTED;
   unsigned int* err = error_word();
   if (!err) return OS_ERR_CUDA;
+  const oss::AttnFault fault = t_fault;
+  t_fault = oss::AttnFault();
   return from_cuda(oss::launch_attention_fwd(q, k, v, o, lse, B, H, Sq, Sk, D, scale,
-                                             causal != 0, err,
+                                             causal != 0, err, fault,
                                              static_cast<cudaStream_t>(stream)));
 }
 
@@ -112,6 +118,16 @@ os_status os_merge_partials(const float* part_m, const float* part_l, const floa
   return from_cuda(oss::launch_merge_partials(part_m, part_l, part_o, groups, num_splits, D,
                                               finalize, o_out, m_out, l_out, lse_out,
                                               static_cast<cudaStream_t>(stream)));
+}
+
+os_status os_debug_inject_fault(int32_t kind, int32_t step, int64_t timeout_ns) {
+  if (kind < 0 || kind > 1 || step < 0 || timeout_ns < 0) return OS_ERR_INVALID_ARGUMENT;
+  t_fault = oss::AttnFault();
+  if (kind == 1) {
+    t_fault.skip_v_step = step;
+    t_fault.timeout_ns = timeout_ns;
+  }
+  return OS_OK;
 }
 
 os_status os_check_device_error(void* stream, int32_t* code) {

@@ -158,12 +158,13 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
 // because every wait sits on the pipeline's critical path (measured: an
 // out-of-line call costs the caller a few hundred cycles).
 __device__ __noinline__ bool wait_bar_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                           unsigned int* err, unsigned int site) {
+                                           unsigned int* err, unsigned int site,
+                                           uint64_t timeout_ns) {
   const uint64_t t0 = global_timer();
   for (uint32_t n = 1;; ++n) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
-    if ((n & 63u) == 0 && global_timer() - t0 > kTimeoutNs) {
+    if ((n & 63u) == 0 && global_timer() - t0 > timeout_ns) {
       *abort_flag = 1;
       report_error(err, kKernelAttnFwd | (site << 8));
       return false;
@@ -172,11 +173,10 @@ __device__ __noinline__ bool wait_bar_slow(uint32_t bar, uint32_t parity, volati
 }
 
 // Bounded wait. Returns false on timeout or when another thread has aborted.
-__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                         unsigned int* err, unsigned int site) {
-  if (mbar_test_wait(bar, parity)) return true;
-  return wait_bar_slow(bar, parity, abort_flag, err, site);
-}
+// The limit is the kernel's timeout_ns (kTimeoutNs unless a test shortens it).
+#define wait_bar(bar, parity, abort_flag, err, site) \
+  (mbar_test_wait((bar), (parity)) ||                 \
+   wait_bar_slow((bar), (parity), (abort_flag), (err), (site), p.timeout_ns))
 
 // Bounded wait used while draining: ignores the abort flag.
 __device__ __noinline__ bool drain_bar(uint32_t bar, uint32_t parity, unsigned int* err) {
@@ -333,6 +333,8 @@ struct AttnParams {
   int Sq, Sk, BH, n_qblocks;
   float C;  // scale * log2(e)
   int causal;
+  uint64_t timeout_ns;  // limit of every bounded wait
+  int skip_v_step;      // test hook: the producer skips the V load of this step (-1: none)
 };
 
 struct Barriers {
@@ -432,7 +434,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
       // and each ring is refilled as soon as its own consumer is done: K stage
       // j % 3 when QK_j has completed (s_full[j % 3]), V stage j % 3 when
       // P_j V has (o_done[j % 3]) -- ring stage and score buffer coincide.
-      int k_issued = 0, v_issued = 0;
+      int k_issued = 0, v_issued = 0, skipped_v = -1;
       for (int i = 0; i < n_kv + kKLead; ++i) {
         if (i < n_kv) {
           const int s = i % kStages;
@@ -448,7 +450,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
           k_issued = i + 1;
         }
         const int j = i - kKLead;
-        if (j >= 0 && j < n_kv) {
+        if (j >= 0 && j < n_kv && j == p.skip_v_step) {
+          skipped_v = j;  // test hook: this V tile never arrives
+        } else if (j >= 0 && j < n_kv) {
           const int s = j % kStages;
           const int round = j / kStages;
           if (round > 0 && !wait_bar(smem_addr(&bars.o_done[s]), (round - 1) & 1, abort_flag,
@@ -467,7 +471,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
       for (int j = k_issued - 1; j >= 0 && j >= k_issued - kStages; --j)
         drain_bar(smem_addr(&bars.k_full[j % kStages]), (j / kStages) & 1, p.err);
       for (int j = v_issued - 1; j >= 0 && j >= v_issued - kStages; --j)
-        drain_bar(smem_addr(&bars.v_full[j % kStages]), (j / kStages) & 1, p.err);
+        if (j != skipped_v) drain_bar(smem_addr(&bars.v_full[j % kStages]), (j / kStages) & 1, p.err);
     }
   } else if (warp == kQkWarp) {
     // ------------------------------------------------------------ QK issuer
@@ -728,7 +732,7 @@ bool make_map(CUtensorMap* map, const uint16_t* base, int S, int BH, int box_row
 cudaError_t launch_attention_fwd(const uint16_t* q, const uint16_t* k, const uint16_t* v,
                                  uint16_t* o, float* lse, int B, int H, int Sq, int Sk, int D,
                                  float scale, bool causal, unsigned int* err_word,
-                                 cudaStream_t stream) {
+                                 const AttnFault& fault, cudaStream_t stream) {
   if (D != kD) return cudaErrorNotSupported;
   const int BH = B * H;
   CUtensorMap mq, mk, mv;
@@ -748,6 +752,8 @@ cudaError_t launch_attention_fwd(const uint16_t* q, const uint16_t* k, const uin
   prm.n_qblocks = (Sq + (causal ? kCausalShift : 0) + kBM - 1) / kBM;
   prm.C = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
   prm.causal = causal ? 1 : 0;
+  prm.timeout_ns = fault.timeout_ns > 0 ? static_cast<uint64_t>(fault.timeout_ns) : kTimeoutNs;
+  prm.skip_v_step = fault.skip_v_step;
   const long long grid = static_cast<long long>(prm.n_qblocks) * BH;
   if (grid > 0x7fffffffLL) return cudaErrorNotSupported;
   attn_fwd_kernel<<<static_cast<unsigned>(grid), kThreads, kSmemBytes, stream>>>(mq, mk, mv, prm);

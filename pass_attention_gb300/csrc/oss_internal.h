@@ -24,11 +24,19 @@ cudaError_t launch_merge_partials(const float* part_m, const float* part_l, cons
                                   void* o_out, float* m_out, float* l_out, float* lse_out,
                                   cudaStream_t stream);
 
+// Test hook for the bounded waits of the attention kernel (see
+// os_debug_inject_fault): skip_v_step >= 0 makes the producer skip that V
+// load; timeout_ns > 0 replaces the default wait limit.
+struct AttnFault {
+  int skip_v_step = -1;
+  int64_t timeout_ns = 0;
+};
+
 // Returns cudaErrorNotSupported for shapes the kernel does not cover.
 cudaError_t launch_attention_fwd(const uint16_t* q, const uint16_t* k, const uint16_t* v,
                                  uint16_t* o, float* lse, int B, int H, int Sq, int Sk, int D,
                                  float scale, bool causal, unsigned int* err_word,
-                                 cudaStream_t stream);
+                                 const AttnFault& fault, cudaStream_t stream);
 
 // log2(e) split into a float and the float nearest to the remainder, so that
 // hi + lo carries about 48 bits of it.

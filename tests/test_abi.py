@@ -94,6 +94,14 @@ def test_merge_rejects_bad_arguments(lib):
     assert f(A, A, A, 4, 16, 130, 1, A, None, None, None, None) == UNSUPPORTED
 
 
+def test_fault_hook_validates_and_disarms(lib):
+    f = lib.os_debug_inject_fault
+    assert f(2, 0, 0) == INVALID
+    assert f(1, -1, 0) == INVALID
+    assert f(1, 0, -5) == INVALID
+    assert f(0, 0, 0) == 0  # disarm; touches no device
+
+
 def test_binding_refuses_cpu_tensors(lib):
     import torch
     with pytest.raises(ValueError):
