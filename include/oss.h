@@ -118,6 +118,36 @@ OSS_API os_status os_attention_fwd(const os_bf16* q, const os_bf16* k, const os_
                            float scale, int causal, void* stream);
 
 /*
+ * os_attention_fwd_partial -- the attention forward over one shard of the
+ * keys, written as partial softmax states instead of O / l, so that shards of
+ * a long sequence (processed one after another, or on different devices) can
+ * be combined with os_merge_partials -- the use of the pairwise identity the
+ * curionode page names for ring attention ("One pass, exactly").
+ *
+ * For query row r = (b, h, i) over the keys of this call:
+ *     part_m[s] = max_j scale * q_i . k_j              (natural units)
+ *     part_l[s] = sum_j exp(scale * q_i . k_j - part_m[s])
+ *     part_o[s] = sum_j exp(scale * q_i . k_j - part_m[s]) v_j   (fp32, not divided by l)
+ * at slot s = r * part_stride + part_index: part_m, part_l are
+ * [B*H*Sq, part_stride] fp32 and part_o [B*H*Sq, part_stride, D] fp32, the
+ * layout os_merge_partials reads with groups = B*H*Sq, num_splits =
+ * part_stride. A row with no visible key writes (-inf, 0, 0).
+ *
+ *   q [B, H, Sq, D], k, v [B, H, Sk, D] bf16 (the shard's keys), device.
+ *   causal != 0 (Sq == Sk): query i sees keys 0..i of this shard -- the
+ *   diagonal shard of a causally masked sequence; earlier shards use 0.
+ *   B, H, Sq, Sk >= 1; D == 128; 0 <= part_index < part_stride; scale > 0.
+ * Alignment: q, k, v, part_o 16-byte aligned.
+ * Errors: as os_attention_fwd.
+ */
+OSS_API os_status os_attention_fwd_partial(const os_bf16* q, const os_bf16* k, const os_bf16* v,
+                                           int32_t B, int32_t H, int32_t Sq, int32_t Sk,
+                                           int32_t D, float scale, int causal,
+                                           float* part_m, float* part_l, float* part_o,
+                                           int32_t part_stride, int32_t part_index,
+                                           void* stream);
+
+/*
  * os_attention_decode_splitkv -- one query token per (batch, head) against a
  * padded KV cache, cut into num_splits chunks, each chunk written as a
  * partial softmax state (metalworking "Online Softmax", closing note: split-KV

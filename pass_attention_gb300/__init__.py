@@ -26,6 +26,7 @@ __all__ = [
     "softmax_rows_from_host",
     "attention_fwd",
     "attention_fwd_from_host",
+    "attention_fwd_partial",
     "attention_decode_splitkv",
     "merge_partials",
     "decode_from_host",
@@ -58,6 +59,8 @@ _SIGNATURES = {
     "os_softmax_rows": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _f32, _vp]),
     "os_attention_fwd": (_i32, [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _f32,
                                 ctypes.c_int, _vp]),
+    "os_attention_fwd_partial": (_i32, [_vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _f32,
+                                        ctypes.c_int, _vp, _vp, _vp, _i32, _i32, _vp]),
     "os_attention_decode_splitkv": (_i32, [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32,
                                            _f32, _vp, _vp, _vp, _vp]),
     "os_merge_partials": (_i32, [_vp, _vp, _vp, _i64, _i32, _i32, ctypes.c_int, _vp, _vp, _vp,
@@ -215,6 +218,40 @@ def attention_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
                                  _stream_ptr(stream))
     _check(st, "os_attention_fwd")
     return o, lse
+
+
+def attention_fwd_partial(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                          part_m: torch.Tensor, part_l: torch.Tensor, part_o: torch.Tensor,
+                          index: int, scale: Optional[float] = None, causal: bool = False,
+                          stream=None):
+    """Partial softmax states of q against one shard k, v (bf16 [B, H, S, D]).
+
+    part_m, part_l: fp32 [B, H, Sq, S_shards]; part_o: fp32 [B, H, Sq,
+    S_shards, D]; writes slot ``index``. See ``os_attention_fwd_partial``.
+    """
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, n, torch.bfloat16, 4)
+        _dense(t, n)
+    B, H, Sq, D = q.shape
+    Sk = k.shape[2]
+    if tuple(k.shape) != (B, H, Sk, D) or tuple(v.shape) != (B, H, Sk, D):
+        raise ValueError("k and v must be [B, H, Sk, D] matching q")
+    _need(part_m, "part_m", torch.float32, 4)
+    _need(part_l, "part_l", torch.float32, 4)
+    _need(part_o, "part_o", torch.float32, 5)
+    for t, n in ((part_m, "part_m"), (part_l, "part_l"), (part_o, "part_o")):
+        _dense(t, n)
+    stride = part_m.shape[-1]
+    if (tuple(part_m.shape) != (B, H, Sq, stride) or tuple(part_l.shape) != (B, H, Sq, stride)
+            or tuple(part_o.shape) != (B, H, Sq, stride, D)):
+        raise ValueError("partials must be [B, H, Sq, S] and [B, H, Sq, S, D]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    st = load().os_attention_fwd_partial(q.data_ptr(), k.data_ptr(), v.data_ptr(), B, H, Sq, Sk, D,
+                                         float(scale), int(bool(causal)), part_m.data_ptr(),
+                                         part_l.data_ptr(), part_o.data_ptr(), stride, int(index),
+                                         _stream_ptr(stream))
+    _check(st, "os_attention_fwd_partial")
 
 
 def attention_fwd_from_host(q_host, k_host, v_host, scale=None, causal=False, out=None,

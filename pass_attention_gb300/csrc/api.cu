@@ -88,7 +88,29 @@ os_status os_attention_fwd(const os_bf16* q, const os_bf16* k, const os_bf16* v,
   const oss::AttnFault fault = t_fault;
   t_fault = oss::AttnFault();
   return from_cuda(oss::launch_attention_fwd(q, k, v, o, lse, B, H, Sq, Sk, D, scale,
-                                             causal != 0, err, fault,
+                                             causal != 0, err, fault, nullptr,
+                                             static_cast<cudaStream_t>(stream)));
+}
+
+os_status os_attention_fwd_partial(const os_bf16* q, const os_bf16* k, const os_bf16* v,
+                                   int32_t B, int32_t H, int32_t Sq, int32_t Sk, int32_t D,
+                                   float scale, int causal, float* part_m, float* part_l,
+                                   float* part_o, int32_t part_stride, int32_t part_index,
+                                   void* stream) {
+  if (!q || !k || !v || !part_m || !part_l || !part_o) return OS_ERR_INVALID_ARGUMENT;
+  if (B <= 0 || H <= 0 || Sq <= 0 || Sk <= 0 || D <= 0) return OS_ERR_INVALID_ARGUMENT;
+  if (part_stride <= 0 || part_index < 0 || part_index >= part_stride) return OS_ERR_INVALID_ARGUMENT;
+  if (!valid_scale(scale)) return OS_ERR_INVALID_ARGUMENT;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(part_o)) return OS_ERR_MISALIGNED;
+  if (D != 128) return OS_ERR_UNSUPPORTED;
+  if (causal && Sq != Sk) return OS_ERR_UNSUPPORTED;
+  unsigned int* err = error_word();
+  if (!err) return OS_ERR_CUDA;
+  const oss::AttnFault fault = t_fault;
+  t_fault = oss::AttnFault();
+  const oss::AttnPartialOut out{part_m, part_l, part_o, part_stride, part_index};
+  return from_cuda(oss::launch_attention_fwd(q, k, v, nullptr, nullptr, B, H, Sq, Sk, D, scale,
+                                             causal != 0, err, fault, &out,
                                              static_cast<cudaStream_t>(stream)));
 }
 

@@ -335,6 +335,13 @@ struct AttnParams {
   int causal;
   uint64_t timeout_ns;  // limit of every bounded wait
   int skip_v_step;      // test hook: the producer skips the V load of this step (-1: none)
+  // partial-state output (sequence-sharded attention): when part_o != null the
+  // epilogue writes (m, l, O unnormalised) of row r to slot part_index of a
+  // [rows, part_stride] partial array instead of O / l and lse
+  float* part_m;
+  float* part_l;
+  float* part_o;
+  int part_stride, part_index;
 };
 
 struct Barriers {
@@ -537,7 +544,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
     const int row = q0 + r_in_tile;                // query index (may be < 0: padding)
     const uint32_t tl = tbase + (static_cast<uint32_t>(quad * 32) << 16);
     const float C = p.C;
-    float m = neg_inf();  // reference maximum, base 2
+    float m = neg_inf();       // reference maximum, base 2
+    float m_true = neg_inf();  // true row maximum, base 2 (for partial states)
     float l = 0.f;
     bool ok = true;
     for (int j = 0; j < n_kv; ++j) {
@@ -584,6 +592,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
       }
       const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * C;
       const float m_new = fmaxf(m, m_tile);
+      m_true = fmaxf(m_true, m_tile);
       // Move the reference maximum only when some row of this warp has risen
       // by more than kRescaleSlack (base 2). Otherwise keep it: exactly the
       // same result in exact arithmetic (the reference cancels in O / l),
@@ -650,7 +659,33 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
     if (ok)
       ok = __all_sync(0xffffffffu, wait_bar(smem_addr(&bars.o_done[(n_kv - 1) % kSBuf]),
                                             ((n_kv - 1) / kSBuf) & 1, abort_flag, p.err, kSiteODone));
-    if (ok) {
+    if (ok && p.part_o) {
+      // partial state relative to the true row maximum: rescale the sums
+      // taken against the reference by 2^(m_ref - m_true) <= 1
+      tc_fence_after();
+      const bool empty = (m_true == neg_inf()) || !(l > 0.f);
+      const float f = empty ? 0.f : ex2(m - m_true);
+      const bool live = row >= 0 && row < p.Sq;
+      const size_t slot = (static_cast<size_t>(bh) * p.Sq + row) * p.part_stride + p.part_index;
+      float4* orow = reinterpret_cast<float4*>(p.part_o + slot * kD);
+#pragma unroll 1
+      for (int cc = 0; cc < kD; cc += 32) {
+        uint32_t ov[32];
+        tmem_ld32(tl + kColO + cc, ov);
+        tmem_ld_wait(ov);
+        if (live) {
+#pragma unroll
+          for (int c = 0; c < 32; c += 4)
+            orow[(cc + c) >> 2] = make_float4(__uint_as_float(ov[c]) * f, __uint_as_float(ov[c + 1]) * f,
+                                              __uint_as_float(ov[c + 2]) * f, __uint_as_float(ov[c + 3]) * f);
+        }
+      }
+      if (live) {
+        const float kLn2 = 0.69314718055994530942f;
+        p.part_m[slot] = empty ? neg_inf() : m_true * kLn2;
+        p.part_l[slot] = empty ? 0.f : l * f;
+      }
+    } else if (ok) {
       tc_fence_after();
       const float inv = (l > 0.f) ? 1.0f / l : 0.f;
       const bool live = row >= 0 && row < p.Sq;
@@ -732,7 +767,8 @@ bool make_map(CUtensorMap* map, const uint16_t* base, int S, int BH, int box_row
 cudaError_t launch_attention_fwd(const uint16_t* q, const uint16_t* k, const uint16_t* v,
                                  uint16_t* o, float* lse, int B, int H, int Sq, int Sk, int D,
                                  float scale, bool causal, unsigned int* err_word,
-                                 const AttnFault& fault, cudaStream_t stream) {
+                                 const AttnFault& fault, const AttnPartialOut* partial,
+                                 cudaStream_t stream) {
   if (D != kD) return cudaErrorNotSupported;
   const int BH = B * H;
   CUtensorMap mq, mk, mv;
@@ -754,6 +790,11 @@ cudaError_t launch_attention_fwd(const uint16_t* q, const uint16_t* k, const uin
   prm.causal = causal ? 1 : 0;
   prm.timeout_ns = fault.timeout_ns > 0 ? static_cast<uint64_t>(fault.timeout_ns) : kTimeoutNs;
   prm.skip_v_step = fault.skip_v_step;
+  prm.part_m = partial ? partial->m : nullptr;
+  prm.part_l = partial ? partial->l : nullptr;
+  prm.part_o = partial ? partial->o : nullptr;
+  prm.part_stride = partial ? partial->stride : 1;
+  prm.part_index = partial ? partial->index : 0;
   const long long grid = static_cast<long long>(prm.n_qblocks) * BH;
   if (grid > 0x7fffffffLL) return cudaErrorNotSupported;
   attn_fwd_kernel<<<static_cast<unsigned>(grid), kThreads, kSmemBytes, stream>>>(mq, mk, mv, prm);

@@ -32,11 +32,23 @@ struct AttnFault {
   int64_t timeout_ns = 0;
 };
 
-// Returns cudaErrorNotSupported for shapes the kernel does not cover.
+// Partial-state output of the attention forward: row r's (m, l, O) go to
+// slot r * stride + index of m, l [rows * stride] and o [rows * stride, D].
+struct AttnPartialOut {
+  float* m;
+  float* l;
+  float* o;
+  int stride;
+  int index;
+};
+
+// Returns cudaErrorNotSupported for shapes the kernel does not cover. With
+// partial != nullptr the kernel writes partial states instead of o and lse.
 cudaError_t launch_attention_fwd(const uint16_t* q, const uint16_t* k, const uint16_t* v,
                                  uint16_t* o, float* lse, int B, int H, int Sq, int Sk, int D,
                                  float scale, bool causal, unsigned int* err_word,
-                                 const AttnFault& fault, cudaStream_t stream);
+                                 const AttnFault& fault, const AttnPartialOut* partial,
+                                 cudaStream_t stream);
 
 // log2(e) split into a float and the float nearest to the remainder, so that
 // hi + lo carries about 48 bits of it.

@@ -74,6 +74,16 @@ def test_attention_fwd_rejects_bad_arguments(lib):
     assert f(A, A, A, A, None, 1, 2, 64, 32, 128, 0.1, 1, None) == UNSUPPORTED  # causal, Sq != Sk
 
 
+def test_attention_partial_rejects_bad_arguments(lib):
+    f = lib.os_attention_fwd_partial
+    ok = (1, 2, 64, 64, 128, 0.1, 0)
+    assert f(A, A, A, *ok, None, A, A, 2, 0, None) == INVALID
+    assert f(A, A, A, *ok, A, A, A, 2, 2, None) == INVALID    # index past the stride
+    assert f(A, A, A, *ok, A, A, A, 0, 0, None) == INVALID
+    assert f(A, A, A, *ok, A, A, A + 4, 2, 0, None) == MISALIGNED
+    assert f(A, A, A, 1, 2, 64, 32, 128, 0.1, 1, A, A, A, 2, 0, None) == UNSUPPORTED
+
+
 def test_decode_rejects_bad_arguments(lib):
     f = lib.os_attention_decode_splitkv
     assert f(A, A, A, None, 2, 2, 64, 128, 4, 0.1, A, A, A, None) == INVALID
