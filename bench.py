@@ -7,7 +7,9 @@ Headline workload (``config.workload``): softmax_32k -- os_softmax_rows over a
 32768 x 8192 fp32 matrix of N(0,1) * 10 logits (1 GiB in, 1 GiB out). A step
 is one os_softmax_rows call; ``value`` is algorithmic GB/s (bytes read + bytes
 written by the definition) over all ranks. The same JSON line carries, under
-``extra``, the attention forward (attn_4k, non-causal; attn_causal) in
+``extra``, the two- and three-pass comparators on the same matrix (value in
+the same algorithmic GB/s, so the ratio is the saving of the one-pass form),
+the same matrix stored in bf16 (softmax_32k_bf16), the attention forward (attn_4k, non-causal; attn_causal) in
 TFLOP/s and split-KV decode + merge (decode_64x32) in GB/s, each with its own
 roofline.
 
@@ -245,6 +247,41 @@ def bench_softmax(args, ctx):
             "d2h": w.rows * w.cols * 4 + 2 * w.rows * 4}
 
 
+def bench_softmax_multipass(args, ctx, passes):
+    """The comparators of os_softmax_rows on the same matrix: the safe
+    softmax's three sweeps (max, sum, write) or the online normaliser followed
+    by a write sweep. Returns (ms per call, HBM bytes the sweeps move)."""
+    import pass_attention_gb300 as oss
+    w = workloads.SOFTMAX_32K
+    x = workloads.logits(w.rows, w.cols, w.mult, w.seed + ctx["rank"], device="cuda")
+    y = torch.empty_like(x)
+    m = torch.empty(w.rows, device="cuda")
+    l = torch.empty(w.rows, device="cuda")
+    stream = torch.cuda.current_stream()
+    fn = lambda: oss.softmax_rows_multipass(x, passes, w.scale, y=y, m=m, l=l, stream=stream)
+    steps = max(3, min(args.steps, 30))
+    total_ms, step_ms, t0, t1 = time_steps(fn, steps, max(3, args.warmup), stream, ctx["barrier"])
+    moved = w.rows * w.cols * 4 * (passes + 1) + w.rows * 4 * (2 * passes + 2)
+    return step_ms, moved, (t0, t1)
+
+
+def bench_softmax16(args, ctx):
+    """os_softmax_rows_16bit on the softmax_32k matrix stored in bf16."""
+    import pass_attention_gb300 as oss
+    w = workloads.SOFTMAX_32K
+    x = workloads.logits(w.rows, w.cols, w.mult, w.seed + ctx["rank"],
+                         device="cuda").to(torch.bfloat16)
+    y = torch.empty_like(x)
+    m = torch.empty(w.rows, device="cuda")
+    l = torch.empty(w.rows, device="cuda")
+    stream = torch.cuda.current_stream()
+    fn = lambda: oss.softmax_rows_16bit(x, w.scale, y=y, m=m, l=l, stream=stream)
+    steps = max(3, min(args.steps, 50))
+    total_ms, step_ms, t0, t1 = time_steps(fn, steps, max(3, args.warmup), stream, ctx["barrier"])
+    nbytes = w.rows * w.cols * 2 * 2 + w.rows * 4 * 2
+    return step_ms, nbytes, (t0, t1)
+
+
 def bench_attention(args, ctx, w):
     import pass_attention_gb300 as oss
     q, k, v = workloads.qkv(w.B, w.H, w.S, w.S, w.D, w.seed, device="cuda")
@@ -413,6 +450,35 @@ def main():
 
     extra = {}
     if not args.headline_only:
+        for passes in (3, 2):
+            name = f"softmax_32k_{passes}pass"
+            try:
+                ms, moved, win = bench_softmax_multipass(args, ctx, passes)
+                moved_gbs = moved / (ms / 1e3) / 1e9
+                extra[name] = {
+                    "value": sm["nbytes"] / (ms / 1e3) / 1e9, "unit": "GB/s",
+                    "ms_per_step": ms, "one_pass_speedup": ms / sm["step_ms"],
+                    "workload": f"{w.rows}x{w.cols} fp32, os_softmax_rows_multipass passes={passes}",
+                    "hbm_bytes_per_step": moved,
+                    "roofline": {"bound": "hbm", "achieved": moved_gbs, "peak": pk["hbm_gbs"],
+                                 "unit": "GB/s", "frac": moved_gbs / pk["hbm_gbs"],
+                                 "traffic": None, "peak_kind": f"{pk_kind} HBM copy",
+                                 "note": "achieved counts every sweep's bytes"},
+                    "window": win}
+            except Exception as e:
+                extra[name] = {"unavailable": f"{type(e).__name__}: {e}"}
+        try:
+            ms, nbytes, win = bench_softmax16(args, ctx)
+            gbs = nbytes / (ms / 1e3) / 1e9
+            extra["softmax_32k_bf16"] = {
+                "value": gbs, "unit": "GB/s", "ms_per_step": ms,
+                "workload": f"{w.rows}x{w.cols} bf16 rows (y bf16, m and l fp32), os_softmax_rows_16bit",
+                "roofline": {"bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                             "frac": gbs / pk["hbm_gbs"], "traffic": traffic_for("softmax_32k_bf16"),
+                             "peak_kind": f"{pk_kind} HBM copy"},
+                "window": win}
+        except Exception as e:
+            extra["softmax_32k_bf16"] = {"unavailable": f"{type(e).__name__}: {e}"}
         for aw in (workloads.ATTN_4K, workloads.ATTN_CAUSAL):
             try:
                 ms, flops, win = bench_attention(args, ctx, aw)

@@ -73,7 +73,8 @@ typedef enum os_status {
  * x is read from HBM once and each element of y written once.
  *
  *   x     [rows, ld_x] fp32, device. Entries may be -inf (masked); +inf / NaN
- *         inputs are undefined.
+ *         inputs, and finite ones with |scale * x * log2(e)| beyond the fp32
+ *         range, are undefined.
  *   y     [rows, ld_y] fp32, device, written for j < cols.
  *   m, l  [rows] fp32, device, or NULL to skip.
  *   rows  >= 1; cols >= 1; ld_x >= cols, ld_y >= cols (elements).
@@ -87,6 +88,56 @@ typedef enum os_status {
 OSS_API os_status os_softmax_rows(const float* x, float* y, float* m, float* l,
                           int64_t rows, int64_t cols, int64_t ld_x, int64_t ld_y,
                           float scale, void* stream);
+
+/* Element type of a 16-bit row (os_softmax_rows_16bit). */
+typedef enum os_dtype {
+  OS_DTYPE_BF16 = 1, /* bfloat16: the top 16 bits of an IEEE binary32 */
+  OS_DTYPE_F16 = 2   /* IEEE-754 binary16 */
+} os_dtype;
+
+/*
+ * os_softmax_rows_16bit -- os_softmax_rows for rows stored in bf16 or fp16,
+ * the same definition with the same one-pass recurrence (curionode "The
+ * Online Softmax.", "One pass, exactly"). Each element is widened to fp32
+ * exactly; weights, m and l are formed in fp32 as in os_softmax_rows; y is
+ * rounded once to the row's type (round to nearest even), so it carries that
+ * type's rounding error (2^-8 relative for bf16, 2^-11 for fp16, whose
+ * results below 2^-14 are subnormal).
+ *
+ *   x     [rows, ld_x] 16-bit elements of type `dtype`, device. -inf entries
+ *         are masked; +inf / NaN inputs are undefined.
+ *   y     [rows, ld_y] same type, device, written for j < cols.
+ *   m, l  [rows] fp32, device, or NULL to skip (natural units, as
+ *         os_softmax_rows).
+ *   rows >= 1; cols >= 1; ld_x >= cols, ld_y >= cols (elements); scale
+ *   finite and > 0; dtype an os_dtype.
+ * Alignment: x and y 2-byte aligned, m and l 4-byte aligned. With x and y
+ * 16-byte aligned and ld_x, ld_y multiples of 8, rows of up to 16384
+ * elements are held in registers (one read, one write per element); other
+ * rows are streamed twice.
+ * Errors: OS_ERR_INVALID_ARGUMENT, OS_ERR_MISALIGNED, OS_ERR_CUDA.
+ */
+OSS_API os_status os_softmax_rows_16bit(const void* x, void* y, float* m, float* l,
+                                        int64_t rows, int64_t cols, int64_t ld_x, int64_t ld_y,
+                                        float scale, int32_t dtype, void* stream);
+
+/*
+ * os_softmax_rows_multipass -- the same outputs as os_softmax_rows, computed
+ * the way the curionode page describes the methods the online form replaces
+ * (introduction): passes = 3 is the safe softmax -- a maximum pass, a sum pass
+ * and a normalising pass -- and passes = 2 runs the online normaliser over
+ * the row and then a normalising pass. Each pass is a separate sweep over
+ * the whole matrix, so x is read from HBM `passes` times (os_softmax_rows
+ * reads it once). Provided to measure that saving; m and l are required (they
+ * carry the state between passes).
+ *   Arguments and alignment as os_softmax_rows, plus passes in {2, 3}.
+ * Errors: OS_ERR_INVALID_ARGUMENT (also for other passes, null m or l),
+ * OS_ERR_MISALIGNED, OS_ERR_CUDA.
+ */
+OSS_API os_status os_softmax_rows_multipass(const float* x, float* y, float* m, float* l,
+                                            int64_t rows, int64_t cols, int64_t ld_x,
+                                            int64_t ld_y, float scale, int32_t passes,
+                                            void* stream);
 
 /*
  * os_attention_fwd -- fused attention forward that never stores a score row.

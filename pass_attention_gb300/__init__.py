@@ -24,6 +24,8 @@ __all__ = [
     "load",
     "softmax_rows",
     "softmax_rows_from_host",
+    "softmax_rows_multipass",
+    "softmax_rows_16bit",
     "attention_fwd",
     "attention_fwd_from_host",
     "attention_fwd_partial",
@@ -57,6 +59,9 @@ _f32 = ctypes.c_float
 # name -> (restype, argtypes), the signatures of include/oss.h
 _SIGNATURES = {
     "os_softmax_rows": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _f32, _vp]),
+    "os_softmax_rows_16bit": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _f32, _i32, _vp]),
+    "os_softmax_rows_multipass": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _f32, _i32,
+                                         _vp]),
     "os_attention_fwd": (_i32, [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _f32,
                                 ctypes.c_int, _vp]),
     "os_attention_fwd_partial": (_i32, [_vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _f32,
@@ -168,6 +173,64 @@ def softmax_rows(x: torch.Tensor, scale: float = 1.0, y: Optional[torch.Tensor] 
                                 cols, x.stride(0), y.stride(0), float(scale),
                                 _stream_ptr(stream))
     _check(st, "os_softmax_rows")
+    return y, m, l
+
+
+_DTYPE_CODES = {torch.bfloat16: 1, torch.float16: 2}
+
+
+def softmax_rows_16bit(x: torch.Tensor, scale: float = 1.0, y: Optional[torch.Tensor] = None,
+                       m: Optional[torch.Tensor] = None, l: Optional[torch.Tensor] = None,
+                       stream=None):
+    """Row softmax of ``scale * x`` for bf16 or fp16 rows ([rows, cols], unit
+    column stride); y has x's type, m and l are fp32. See
+    ``os_softmax_rows_16bit``."""
+    if not isinstance(x, torch.Tensor) or x.dtype not in _DTYPE_CODES:
+        raise TypeError("x must be a bfloat16 or float16 torch.Tensor")
+    _need(x, "x", x.dtype, 2)
+    if x.stride(1) != 1:
+        raise ValueError("x must have unit column stride")
+    rows, cols = x.shape
+    if y is None:
+        y = torch.empty((rows, cols), dtype=x.dtype, device=x.device)
+    _need(y, "y", x.dtype, 2)
+    if y.stride(1) != 1 or tuple(y.shape) != (rows, cols):
+        raise ValueError("y must be [rows, cols] with unit column stride")
+    if m is None:
+        m = torch.empty(rows, dtype=torch.float32, device=x.device)
+    if l is None:
+        l = torch.empty(rows, dtype=torch.float32, device=x.device)
+    _need(m, "m", torch.float32, 1)
+    _need(l, "l", torch.float32, 1)
+    st = load().os_softmax_rows_16bit(x.data_ptr(), y.data_ptr(), m.data_ptr(), l.data_ptr(),
+                                      rows, cols, x.stride(0), y.stride(0), float(scale),
+                                      _DTYPE_CODES[x.dtype], _stream_ptr(stream))
+    _check(st, "os_softmax_rows_16bit")
+    return y, m, l
+
+
+def softmax_rows_multipass(x: torch.Tensor, passes: int, scale: float = 1.0,
+                           y: Optional[torch.Tensor] = None, m: Optional[torch.Tensor] = None,
+                           l: Optional[torch.Tensor] = None, stream=None):
+    """The 2- or 3-pass comparator of softmax_rows (same outputs; x is read
+    from HBM ``passes`` times). See ``os_softmax_rows_multipass``."""
+    _need(x, "x", torch.float32, 2)
+    if x.stride(1) != 1:
+        raise ValueError("x must have unit column stride")
+    rows, cols = x.shape
+    if y is None:
+        y = torch.empty((rows, cols), dtype=torch.float32, device=x.device)
+    if m is None:
+        m = torch.empty(rows, dtype=torch.float32, device=x.device)
+    if l is None:
+        l = torch.empty(rows, dtype=torch.float32, device=x.device)
+    _need(y, "y", torch.float32, 2)
+    _need(m, "m", torch.float32, 1)
+    _need(l, "l", torch.float32, 1)
+    st = load().os_softmax_rows_multipass(x.data_ptr(), y.data_ptr(), m.data_ptr(), l.data_ptr(),
+                                          rows, cols, x.stride(0), y.stride(0), float(scale),
+                                          int(passes), _stream_ptr(stream))
+    _check(st, "os_softmax_rows_multipass")
     return y, m, l
 
 

@@ -73,6 +73,36 @@ os_status os_softmax_rows(const float* x, float* y, float* m, float* l, int64_t 
                                             static_cast<cudaStream_t>(stream)));
 }
 
+os_status os_softmax_rows_16bit(const void* x, void* y, float* m, float* l, int64_t rows,
+                                int64_t cols, int64_t ld_x, int64_t ld_y, float scale,
+                                int32_t dtype, void* stream) {
+  if (!x || !y) return OS_ERR_INVALID_ARGUMENT;
+  if (rows <= 0 || cols <= 0 || ld_x < cols || ld_y < cols) return OS_ERR_INVALID_ARGUMENT;
+  if (cols > (int64_t(1) << 30) || rows > (int64_t(1) << 40)) return OS_ERR_INVALID_ARGUMENT;
+  if (!valid_scale(scale) || (dtype != OS_DTYPE_BF16 && dtype != OS_DTYPE_F16))
+    return OS_ERR_INVALID_ARGUMENT;
+  if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y)) & 1u) return OS_ERR_MISALIGNED;
+  if ((reinterpret_cast<uintptr_t>(m) | reinterpret_cast<uintptr_t>(l)) & 3u) return OS_ERR_MISALIGNED;
+  return from_cuda(oss::launch_softmax_rows16(static_cast<const uint16_t*>(x),
+                                              static_cast<uint16_t*>(y), m, l, rows, cols, ld_x,
+                                              ld_y, scale, dtype,
+                                              static_cast<cudaStream_t>(stream)));
+}
+
+os_status os_softmax_rows_multipass(const float* x, float* y, float* m, float* l, int64_t rows,
+                                    int64_t cols, int64_t ld_x, int64_t ld_y, float scale,
+                                    int32_t passes, void* stream) {
+  if (!x || !y || !m || !l) return OS_ERR_INVALID_ARGUMENT;
+  if (rows <= 0 || cols <= 0 || ld_x < cols || ld_y < cols) return OS_ERR_INVALID_ARGUMENT;
+  if (cols > (int64_t(1) << 30) || rows > (int64_t(1) << 40)) return OS_ERR_INVALID_ARGUMENT;
+  if (!valid_scale(scale) || (passes != 2 && passes != 3)) return OS_ERR_INVALID_ARGUMENT;
+  if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y) |
+       reinterpret_cast<uintptr_t>(m) | reinterpret_cast<uintptr_t>(l)) & 3u)
+    return OS_ERR_MISALIGNED;
+  return from_cuda(oss::launch_softmax_rows_multipass(x, y, m, l, rows, cols, ld_x, ld_y, scale,
+                                                      passes, static_cast<cudaStream_t>(stream)));
+}
+
 os_status os_attention_fwd(const os_bf16* q, const os_bf16* k, const os_bf16* v, os_bf16* o,
                            float* lse, int32_t B, int32_t H, int32_t Sq, int32_t Sk, int32_t D,
                            float scale, int causal, void* stream) {

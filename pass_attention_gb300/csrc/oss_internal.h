@@ -14,6 +14,17 @@ cudaError_t launch_softmax_rows(const float* x, float* y, float* m, float* l,
                                 int64_t rows, int64_t cols, int64_t ld_x, int64_t ld_y,
                                 float scale, cudaStream_t stream);
 
+// 16-bit rows: dtype 1 = bf16, 2 = fp16 (x and y); m, l fp32 or null.
+cudaError_t launch_softmax_rows16(const uint16_t* x, uint16_t* y, float* m, float* l,
+                                  int64_t rows, int64_t cols, int64_t ld_x, int64_t ld_y,
+                                  float scale, int dtype, cudaStream_t stream);
+
+// Comparators: passes = 2 (online (m, l) pass, then a write pass) or 3 (max
+// pass, sum pass, write pass); each pass re-reads x from HBM. m, l required.
+cudaError_t launch_softmax_rows_multipass(const float* x, float* y, float* m, float* l,
+                                          int64_t rows, int64_t cols, int64_t ld_x, int64_t ld_y,
+                                          float scale, int passes, cudaStream_t stream);
+
 cudaError_t launch_decode_splitkv(const uint16_t* q, const uint16_t* k, const uint16_t* v,
                                   const int32_t* kv_len, int B, int H, int Lmax, int D,
                                   int num_splits, float scale, float* part_m, float* part_l,

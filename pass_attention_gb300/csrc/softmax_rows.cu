@@ -26,8 +26,12 @@
 // rounding matters. ABI outputs are natural: m = fl32(scale * max x) and
 // l = sum exp(scale * x - m).
 
+#include <cuda_fp16.h>
+
 #include <cfloat>
+#include <cmath>
 #include <cstdint>
+#include <limits>
 
 #include "device_common.cuh"
 #include "oss_internal.h"
@@ -56,9 +60,28 @@ __device__ __forceinline__ float base2_of(float xm, const ScaleConsts& k) {
 // cancellation against M happens before any rounding and the result is
 // rounded at its own (small) magnitude; the outer FMA adds x*c_lo. Rounding
 // the other way round (x*c_lo - M first) would cost half an ulp of M, which
-// for large logits (M ~ 5000) is 2.4e-4 in the exponent.
+// for large logits (M ~ 5000) is 2.4e-4 in the exponent. The host splits c
+// so that c_hi and c_lo are both > 0 (make_consts): a masked entry x = -inf
+// then gives -inf in both FMAs and a weight of exactly 0. (With c_lo <= 0,
+// which nearest rounding of c_hi gives for scale 0.1, -inf * c_lo would be
+// +inf or NaN and the weight NaN.)
 __device__ __forceinline__ float weight(float x, float M, const ScaleConsts& k) {
   return ex2(fmaf(x, k.c_lo, fmaf(x, k.c_hi, -M)));
+}
+
+// weight() of two elements with packed (two-lane) FMAs: the same two
+// roundings per element.
+__device__ __forceinline__ float2 weight2(float2 x, float2 negM, const ScaleConsts& k) {
+  const float2 t = __ffma2_rn(x, make_float2(k.c_hi, k.c_hi), negM);
+  const float2 e = __ffma2_rn(x, make_float2(k.c_lo, k.c_lo), t);
+  return make_float2(ex2(e.x), ex2(e.y));
+}
+
+// max(a, b, c) in one instruction (three-input max.f32, sm_100 and later)
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
 }
 
 // Merge partial state (xa, la) with (xb, lb); x* are raw maxima, l* sums of
@@ -244,6 +267,367 @@ softmax_rows_stream_kernel(const float* __restrict__ x, float* __restrict__ y,
   }
 }
 
+// ---------------------------------------------------------------------------
+// Multi-pass comparators. Each pass is its own kernel over the whole matrix,
+// so every pass reads x from HBM again (the curionode page's point: the safe
+// softmax reads the vector three times, the online normaliser twice before
+// the final write, os_softmax_rows once). Between passes m[] holds the raw
+// row maximum and l[] the sum relative to its base-2 image; the write pass
+// converts both to the natural-unit outputs.
+// ---------------------------------------------------------------------------
+
+template <bool kVec>
+__device__ __forceinline__ int load_chunk(const float* xr, int64_t c, int64_t cols, float (&v)[4]) {
+  if (kVec && (c + 1) * 4 <= cols) {
+    const float4 f = __ldcs(reinterpret_cast<const float4*>(xr) + c);
+    v[0] = f.x; v[1] = f.y; v[2] = f.z; v[3] = f.w;
+    return 4;
+  }
+  const int64_t base = c * (kVec ? 4 : 1);
+#pragma unroll
+  for (int e = 0; e < 4; ++e)
+    v[e] = (e < (kVec ? 4 : 1) && base + e < cols) ? xr[base + e] : neg_inf();
+  return kVec ? 4 : 1;
+}
+
+// pass "max": m[r] = max_j x[r, j] (raw)
+template <bool kVec>
+__global__ void __launch_bounds__(kThreads)
+softmax_pass_max(const float* __restrict__ x, float* __restrict__ m_out, int64_t rows,
+                 int64_t cols, int64_t ld_x) {
+  __shared__ float sh[kWarps];
+  const int64_t nchunks = kVec ? (cols + 3) / 4 : cols;
+  for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
+    const float* xr = x + row * ld_x;
+    float xm = neg_inf();
+    for (int64_t c = threadIdx.x; c < nchunks; c += kThreads) {
+      float v[4];
+      load_chunk<kVec>(xr, c, cols, v);
+      xm = fmaxf(xm, fmaxf(fmaxf(v[0], v[1]), fmaxf(v[2], v[3])));
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) xm = fmaxf(xm, __shfl_xor_sync(0xffffffffu, xm, off));
+    if ((threadIdx.x & 31) == 0) sh[threadIdx.x >> 5] = xm;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      float r = sh[0];
+      for (int w = 1; w < kWarps; ++w) r = fmaxf(r, sh[w]);
+      m_out[row] = r;
+    }
+    __syncthreads();
+  }
+}
+
+// pass "sum": l[r] = sum_j 2^(x c - M_r), M_r = base-2 image of m[r]
+template <bool kVec>
+__global__ void __launch_bounds__(kThreads)
+softmax_pass_sum(const float* __restrict__ x, const float* __restrict__ m_in,
+                 float* __restrict__ l_out, int64_t rows, int64_t cols, int64_t ld_x,
+                 ScaleConsts k) {
+  __shared__ float sh[kWarps];
+  const int64_t nchunks = kVec ? (cols + 3) / 4 : cols;
+  for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
+    const float* xr = x + row * ld_x;
+    const float xm = m_in[row];
+    const float M = (xm == neg_inf()) ? 0.f : base2_of(xm, k);
+    float ls = 0.f;
+    for (int64_t c = threadIdx.x; c < nchunks; c += kThreads) {
+      float v[4];
+      load_chunk<kVec>(xr, c, cols, v);
+      ls += (weight(v[0], M, k) + weight(v[1], M, k)) + (weight(v[2], M, k) + weight(v[3], M, k));
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) ls += __shfl_xor_sync(0xffffffffu, ls, off);
+    if ((threadIdx.x & 31) == 0) sh[threadIdx.x >> 5] = ls;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      float r = 0.f;
+      for (int w = 0; w < kWarps; ++w) r += sh[w];
+      l_out[row] = r;
+    }
+    __syncthreads();
+  }
+}
+
+// pass "online": the running (max, sum) pair over the row, then the merge of
+// the threads' pairs: m[r] raw maximum, l[r] relative sum
+template <bool kVec>
+__global__ void __launch_bounds__(kThreads)
+softmax_pass_online(const float* __restrict__ x, float* __restrict__ m_out,
+                    float* __restrict__ l_out, int64_t rows, int64_t cols, int64_t ld_x,
+                    ScaleConsts k) {
+  __shared__ float2 sh[kWarps];
+  const int64_t nchunks = kVec ? (cols + 3) / 4 : cols;
+  for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
+    const float* xr = x + row * ld_x;
+    float xm = neg_inf(), ls = 0.f;
+    for (int64_t c = threadIdx.x; c < nchunks; c += kThreads) {
+      float v[4];
+      load_chunk<kVec>(xr, c, cols, v);
+      const float xn = fmaxf(xm, fmaxf(fmaxf(v[0], v[1]), fmaxf(v[2], v[3])));
+      if (xn == neg_inf()) continue;  // nothing visible yet: no -inf - -inf
+      const float Mn = base2_of(xn, k);
+      const float corr = (xm == neg_inf()) ? 0.f : ex2(base2_of(xm, k) - Mn);
+      ls = ls * corr + ((weight(v[0], Mn, k) + weight(v[1], Mn, k)) +
+                        (weight(v[2], Mn, k) + weight(v[3], Mn, k)));
+      xm = xn;
+    }
+    cta_merge(xm, ls, k, sh);
+    if (threadIdx.x == 0) {
+      m_out[row] = xm;
+      l_out[row] = ls;
+    }
+    __syncthreads();
+  }
+}
+
+// pass "write": y = 2^(x c - M) / l, then m and l converted to natural units
+template <bool kVec>
+__global__ void __launch_bounds__(kThreads)
+softmax_pass_write(const float* __restrict__ x, float* __restrict__ y, float* __restrict__ m_io,
+                   float* __restrict__ l_io, int64_t rows, int64_t cols, int64_t ld_x,
+                   int64_t ld_y, ScaleConsts k) {
+  const int64_t nchunks = kVec ? (cols + 3) / 4 : cols;
+  for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
+    const float* xr = x + row * ld_x;
+    float* yr = y + row * ld_y;
+    const float xm = m_io[row];
+    const float ls = l_io[row];
+    const float M = (xm == neg_inf()) ? 0.f : base2_of(xm, k);
+    const float inv = (ls > 0.f) ? 1.0f / ls : 0.f;
+    for (int64_t c = threadIdx.x; c < nchunks; c += kThreads) {
+      float v[4];
+      const int n = load_chunk<kVec>(xr, c, cols, v);
+      if (kVec && n == 4 && (c + 1) * 4 <= cols) {
+        st_stream(reinterpret_cast<float4*>(yr) + c,
+                  make_float4(weight(v[0], M, k) * inv, weight(v[1], M, k) * inv,
+                              weight(v[2], M, k) * inv, weight(v[3], M, k) * inv));
+      } else {
+        const int64_t base = c * (kVec ? 4 : 1);
+        for (int e = 0; e < (kVec ? 4 : 1); ++e)
+          if (base + e < cols) yr[base + e] = weight(v[e], M, k) * inv;
+      }
+    }
+    __syncthreads();  // every thread has read m_io / l_io of this row
+    if (threadIdx.x == 0) write_ml(xm, ls, k, row, m_io, l_io);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// 16-bit rows (bf16 or fp16 in and out; m, l fp32). The same recurrence and
+// merge; elements are widened to fp32 exactly, every weight is formed in fp32
+// and y is rounded to the row's type once, to nearest even.
+// kType: 1 = bf16, 2 = fp16.
+// ---------------------------------------------------------------------------
+
+template <int kType>
+__device__ __forceinline__ float h16_lo(uint32_t w) {
+  if (kType == 1) return __uint_as_float(w << 16);
+  return __half2float(__ushort_as_half(static_cast<unsigned short>(w & 0xffffu)));
+}
+template <int kType>
+__device__ __forceinline__ float h16_hi(uint32_t w) {
+  if (kType == 1) return __uint_as_float(w & 0xffff0000u);
+  return __half2float(__ushort_as_half(static_cast<unsigned short>(w >> 16)));
+}
+template <int kType>
+__device__ __forceinline__ float h16_one(uint16_t b) {
+  return h16_lo<kType>(b);
+}
+// two fp32 -> one word of two 16-bit values (lo in the low half), RN
+template <int kType>
+__device__ __forceinline__ uint32_t h16_pack(float lo, float hi) {
+  uint32_t w;
+  if (kType == 1)
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(w) : "f"(hi), "f"(lo));
+  else
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(w) : "f"(hi), "f"(lo));
+  return w;
+}
+template <int kType>
+__device__ __forceinline__ uint16_t h16_round(float f) {
+  return static_cast<uint16_t>(h16_pack<kType>(f, 0.f) & 0xffffu);
+}
+// -inf twice, in the type's bits
+template <int kType>
+__device__ __forceinline__ uint32_t h16_neg_inf2() {
+  return kType == 1 ? 0xff80ff80u : 0xfc00fc00u;
+}
+
+template <int kType>
+__device__ __forceinline__ float max8(const uint4& v) {
+  const float a = fmaxf(fmaxf(h16_lo<kType>(v.x), h16_hi<kType>(v.x)),
+                        fmaxf(h16_lo<kType>(v.y), h16_hi<kType>(v.y)));
+  const float b = fmaxf(fmaxf(h16_lo<kType>(v.z), h16_hi<kType>(v.z)),
+                        fmaxf(h16_lo<kType>(v.w), h16_hi<kType>(v.w)));
+  return fmaxf(a, b);
+}
+template <int kType>
+__device__ __forceinline__ float sum8(const uint4& v, float M, const ScaleConsts& k) {
+  const float a = (weight(h16_lo<kType>(v.x), M, k) + weight(h16_hi<kType>(v.x), M, k)) +
+                  (weight(h16_lo<kType>(v.y), M, k) + weight(h16_hi<kType>(v.y), M, k));
+  const float b = (weight(h16_lo<kType>(v.z), M, k) + weight(h16_hi<kType>(v.z), M, k)) +
+                  (weight(h16_lo<kType>(v.w), M, k) + weight(h16_hi<kType>(v.w), M, k));
+  return a + b;
+}
+template <int kType>
+__device__ __forceinline__ uint32_t out2(uint32_t w, float M, float inv, const ScaleConsts& k) {
+  return h16_pack<kType>(weight(h16_lo<kType>(w), M, k) * inv, weight(h16_hi<kType>(w), M, k) * inv);
+}
+template <int kType>
+__device__ __forceinline__ uint4 out8(const uint4& v, float M, float inv, const ScaleConsts& k) {
+  return make_uint4(out2<kType>(v.x, M, inv, k), out2<kType>(v.y, M, inv, k),
+                    out2<kType>(v.z, M, inv, k), out2<kType>(v.w, M, inv, k));
+}
+
+// Register-resident 16-bit rows (cols <= 16384): each thread loads its slice
+// once (NV 16-byte chunks of 8 elements), widens it to fp32 and replaces it
+// by its weights relative to the thread's own maximum (packed FMAs, one ex2
+// per element); the CTA merges the threads' (max, sum) states and each thread
+// scales its weights by 2^(M_t - M_row) / l_row for the single write (2 bytes
+// read and 2 written per element).
+template <int kType, int NV>
+__global__ void __launch_bounds__(kThreads, (NV <= 4) ? 4 : 2)
+softmax_rows16_reg_kernel(const uint16_t* __restrict__ x, uint16_t* __restrict__ y,
+                          float* __restrict__ m_out, float* __restrict__ l_out, int64_t rows,
+                          int cols, int64_t ld_x, int64_t ld_y, ScaleConsts k) {
+  __shared__ float2 sh[kWarps];
+  const int nfull = cols >> 3;
+  const int tail = cols & 7;
+  const int tid = threadIdx.x;
+  for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
+    const uint16_t* xr = x + row * ld_x;
+    uint16_t* yr = y + row * ld_y;
+    float2 w[NV][4];
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+      const int c8 = tid + i * kThreads;
+      uint4 v;
+      if (c8 < nfull) {
+        v = __ldcs(reinterpret_cast<const uint4*>(xr) + c8);
+      } else {
+        uint32_t wd[4];
+#pragma unroll
+        for (int h = 0; h < 4; ++h) wd[h] = h16_neg_inf2<kType>();
+        if (c8 == nfull && tail) {
+          const uint16_t* p = xr + 8 * c8;
+#pragma unroll
+          for (int e = 0; e < 7; ++e)
+            if (e < tail)
+              wd[e >> 1] = (e & 1) ? ((wd[e >> 1] & 0xffffu) | (uint32_t(p[e]) << 16))
+                                   : ((wd[e >> 1] & 0xffff0000u) | uint32_t(p[e]));
+        }
+        v = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+      }
+      w[i][0] = make_float2(h16_lo<kType>(v.x), h16_hi<kType>(v.x));
+      w[i][1] = make_float2(h16_lo<kType>(v.y), h16_hi<kType>(v.y));
+      w[i][2] = make_float2(h16_lo<kType>(v.z), h16_hi<kType>(v.z));
+      w[i][3] = make_float2(h16_lo<kType>(v.w), h16_hi<kType>(v.w));
+    }
+    float xa = neg_inf(), xb = neg_inf();
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+      xa = fmax3(xa, w[i][0].x, w[i][0].y);
+      xb = fmax3(xb, w[i][1].x, w[i][1].y);
+      xa = fmax3(xa, w[i][2].x, w[i][2].y);
+      xb = fmax3(xb, w[i][3].x, w[i][3].y);
+    }
+    float xm = fmaxf(xa, xb);
+    const float Mt = (xm == neg_inf()) ? 0.f : base2_of(xm, k);
+    const float2 negM = make_float2(-Mt, -Mt);
+    float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        w[i][h] = weight2(w[i][h], negM, k);
+        acc = __fadd2_rn(acc, w[i][h]);
+      }
+    }
+    float ls = acc.x + acc.y;
+    const float xm_t = xm;
+    cta_merge(xm, ls, k, sh);
+    float f = 0.f;
+    if (xm_t != neg_inf() && ls > 0.f)
+      f = ex2(base2_of(xm_t, k) - base2_of(xm, k)) * (1.0f / ls);
+    const float2 f2 = make_float2(f, f);
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+      const int c8 = tid + i * kThreads;
+      uint32_t o[4];
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        const float2 q = __fmul2_rn(w[i][h], f2);
+        o[h] = h16_pack<kType>(q.x, q.y);
+      }
+      if (c8 < nfull) {
+        __stcs(reinterpret_cast<uint4*>(yr) + c8, make_uint4(o[0], o[1], o[2], o[3]));
+      } else if (c8 == nfull && tail) {
+        uint16_t* p = yr + 8 * c8;
+#pragma unroll
+        for (int e = 0; e < 7; ++e)
+          if (e < tail) p[e] = static_cast<uint16_t>((e & 1) ? (o[e >> 1] >> 16) : (o[e >> 1] & 0xffffu));
+      }
+    }
+    if (tid == 0) write_ml(xm, ls, k, row, m_out, l_out);
+    __syncthreads();
+  }
+}
+
+// Long or unaligned 16-bit rows: the recurrence over the row as it streams
+// (8-element chunks when aligned, single elements otherwise), the CTA merge,
+// then a second read of the row for the write (2 reads + 1 write).
+template <int kType, bool kVec>
+__global__ void __launch_bounds__(kThreads)
+softmax_rows16_stream_kernel(const uint16_t* __restrict__ x, uint16_t* __restrict__ y,
+                             float* __restrict__ m_out, float* __restrict__ l_out, int64_t rows,
+                             int64_t cols, int64_t ld_x, int64_t ld_y, ScaleConsts k) {
+  __shared__ float2 sh[kWarps];
+  constexpr int W = kVec ? 8 : 1;
+  const int64_t nchunks = (cols + W - 1) / W;
+  const int tid = threadIdx.x;
+  for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
+    const uint16_t* xr = x + row * ld_x;
+    uint16_t* yr = y + row * ld_y;
+    float xm = neg_inf(), ls = 0.f;
+    for (int64_t c = tid; c < nchunks; c += kThreads) {
+      if (kVec && (c + 1) * W <= cols) {
+        const uint4 v = __ldg(reinterpret_cast<const uint4*>(xr) + c);
+        const float xn = fmaxf(xm, max8<kType>(v));
+        if (xn == neg_inf()) continue;  // nothing visible yet: no -inf - -inf
+        const float Mn = base2_of(xn, k);
+        const float corr = (xm == neg_inf()) ? 0.f : ex2(base2_of(xm, k) - Mn);
+        ls = ls * corr + sum8<kType>(v, Mn, k);
+        xm = xn;
+      } else {
+        for (int64_t j = c * W; j < cols && j < (c + 1) * W; ++j) {
+          const float xv = h16_one<kType>(xr[j]);
+          const float xn = fmaxf(xm, xv);
+          if (xn == neg_inf()) continue;
+          const float Mn = base2_of(xn, k);
+          const float corr = (xm == neg_inf()) ? 0.f : ex2(base2_of(xm, k) - Mn);
+          ls = ls * corr + weight(xv, Mn, k);
+          xm = xn;
+        }
+      }
+    }
+    cta_merge(xm, ls, k, sh);
+    const float M = (xm == neg_inf()) ? 0.f : base2_of(xm, k);
+    const float inv = (ls > 0.f) ? 1.0f / ls : 0.f;
+    for (int64_t c = tid; c < nchunks; c += kThreads) {
+      if (kVec && (c + 1) * W <= cols) {
+        const uint4 v = __ldg(reinterpret_cast<const uint4*>(xr) + c);
+        __stcs(reinterpret_cast<uint4*>(yr) + c, out8<kType>(v, M, inv, k));
+      } else {
+        for (int64_t j = c * W; j < cols && j < (c + 1) * W; ++j)
+          yr[j] = h16_round<kType>(weight(h16_one<kType>(xr[j]), M, k) * inv);
+      }
+    }
+    if (tid == 0) write_ml(xm, ls, k, row, m_out, l_out);
+    __syncthreads();
+  }
+}
+
 int grid_for(int64_t rows, int ctas_per_sm) {
   int dev = 0, sms = 148;
   if (cudaGetDevice(&dev) == cudaSuccess)
@@ -254,19 +638,37 @@ int grid_for(int64_t rows, int ctas_per_sm) {
 
 }  // namespace
 
-void split_constant(double c, float* hi, float* lo) {
-  *hi = static_cast<float>(c);
-  *lo = static_cast<float>(c - static_cast<double>(*hi));
+namespace {
+
+// c (> 0) as hi + lo with hi the float below c and lo = c - hi > 0, both
+// positive (the device code relies on it for masked entries, see weight()).
+// Where c is a float itself, hi is the float just below it and lo that
+// spacing; lo is never 0 (for c below the smallest normal it is set to the
+// smallest subnormal, an error of 2^-149 in c).
+void split_positive(double c, float* hi, float* lo) {
+  float h = static_cast<float>(c);
+  if (static_cast<double>(h) >= c) h = std::nextafter(h, 0.0f);
+  float l = static_cast<float>(c - static_cast<double>(h));
+  if (!(l > 0.0f)) l = std::numeric_limits<float>::denorm_min();
+  *hi = h;
+  *lo = l;
 }
+
+ScaleConsts make_consts(float scale) {
+  const double kLog2e = 1.4426950408889634074;
+  ScaleConsts k;
+  k.scale = scale;
+  split_positive(static_cast<double>(scale) * kLog2e, &k.c_hi, &k.c_lo);
+  split_positive(kLog2e, &k.e_hi, &k.e_lo);
+  return k;
+}
+
+}  // namespace
 
 cudaError_t launch_softmax_rows(const float* x, float* y, float* m, float* l, int64_t rows,
                                 int64_t cols, int64_t ld_x, int64_t ld_y, float scale,
                                 cudaStream_t stream) {
-  const double kLog2e = 1.4426950408889634074;
-  ScaleConsts k;
-  k.scale = scale;
-  split_constant(static_cast<double>(scale) * kLog2e, &k.c_hi, &k.c_lo);
-  split_constant(kLog2e, &k.e_hi, &k.e_lo);
+  const ScaleConsts k = make_consts(scale);
 
   const bool vec = ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y)) & 15u) == 0 &&
                    (ld_x & 3) == 0 && (ld_y & 3) == 0;
@@ -289,6 +691,71 @@ cudaError_t launch_softmax_rows(const float* x, float* y, float* m, float* l, in
     softmax_rows_reg_kernel<16><<<grid_for(rows, 2), kThreads, 0, stream>>>(x, y, m, l, rows, c, ld_x, ld_y, k);
   } else {
     softmax_rows_stream_kernel<true><<<grid_for(rows, 4), kThreads, 0, stream>>>(x, y, m, l, rows, cols, ld_x, ld_y, k);
+  }
+  return cudaGetLastError();
+}
+
+template <int kType>
+void dispatch_rows16(const uint16_t* x, uint16_t* y, float* m, float* l, int64_t rows,
+                     int64_t cols, int64_t ld_x, int64_t ld_y, const ScaleConsts& k,
+                     cudaStream_t stream) {
+  const bool vec = ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y)) & 15u) == 0 &&
+                   (ld_x & 7) == 0 && (ld_y & 7) == 0;
+  const int g = grid_for(rows, 4);
+  if (!vec) {
+    softmax_rows16_stream_kernel<kType, false><<<g, kThreads, 0, stream>>>(x, y, m, l, rows, cols, ld_x, ld_y, k);
+    return;
+  }
+  const int64_t chunks = (cols + 7) / 8;
+  const int nv = static_cast<int>((chunks + kThreads - 1) / kThreads);
+  const int c = static_cast<int>(cols);
+  if (nv <= 1) {
+    softmax_rows16_reg_kernel<kType, 1><<<g, kThreads, 0, stream>>>(x, y, m, l, rows, c, ld_x, ld_y, k);
+  } else if (nv <= 2) {
+    softmax_rows16_reg_kernel<kType, 2><<<g, kThreads, 0, stream>>>(x, y, m, l, rows, c, ld_x, ld_y, k);
+  } else if (nv <= 4) {
+    softmax_rows16_reg_kernel<kType, 4><<<g, kThreads, 0, stream>>>(x, y, m, l, rows, c, ld_x, ld_y, k);
+  } else if (nv <= 8) {
+    softmax_rows16_reg_kernel<kType, 8><<<g, kThreads, 0, stream>>>(x, y, m, l, rows, c, ld_x, ld_y, k);
+  } else {
+    softmax_rows16_stream_kernel<kType, true><<<g, kThreads, 0, stream>>>(x, y, m, l, rows, cols, ld_x, ld_y, k);
+  }
+}
+
+cudaError_t launch_softmax_rows16(const uint16_t* x, uint16_t* y, float* m, float* l,
+                                  int64_t rows, int64_t cols, int64_t ld_x, int64_t ld_y,
+                                  float scale, int dtype, cudaStream_t stream) {
+  const ScaleConsts k = make_consts(scale);
+  if (dtype == 1)
+    dispatch_rows16<1>(x, y, m, l, rows, cols, ld_x, ld_y, k, stream);
+  else
+    dispatch_rows16<2>(x, y, m, l, rows, cols, ld_x, ld_y, k, stream);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_softmax_rows_multipass(const float* x, float* y, float* m, float* l,
+                                          int64_t rows, int64_t cols, int64_t ld_x, int64_t ld_y,
+                                          float scale, int passes, cudaStream_t stream) {
+  const ScaleConsts k = make_consts(scale);
+  const bool vec = ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y)) & 15u) == 0 &&
+                   (ld_x & 3) == 0 && (ld_y & 3) == 0;
+  const int g = grid_for(rows, 4);
+  if (vec) {
+    if (passes == 3) {
+      softmax_pass_max<true><<<g, kThreads, 0, stream>>>(x, m, rows, cols, ld_x);
+      softmax_pass_sum<true><<<g, kThreads, 0, stream>>>(x, m, l, rows, cols, ld_x, k);
+    } else {
+      softmax_pass_online<true><<<g, kThreads, 0, stream>>>(x, m, l, rows, cols, ld_x, k);
+    }
+    softmax_pass_write<true><<<g, kThreads, 0, stream>>>(x, y, m, l, rows, cols, ld_x, ld_y, k);
+  } else {
+    if (passes == 3) {
+      softmax_pass_max<false><<<g, kThreads, 0, stream>>>(x, m, rows, cols, ld_x);
+      softmax_pass_sum<false><<<g, kThreads, 0, stream>>>(x, m, l, rows, cols, ld_x, k);
+    } else {
+      softmax_pass_online<false><<<g, kThreads, 0, stream>>>(x, m, l, rows, cols, ld_x, k);
+    }
+    softmax_pass_write<false><<<g, kThreads, 0, stream>>>(x, y, m, l, rows, cols, ld_x, ld_y, k);
   }
   return cudaGetLastError();
 }

@@ -61,6 +61,32 @@ def test_softmax_rows_rejects_bad_arguments(lib):
     assert f(A, A + 1, None, None, 4, 8, 8, 8, 1.0, None) == MISALIGNED
 
 
+def test_softmax_rows_multipass_rejects_bad_arguments(lib):
+    f = lib.os_softmax_rows_multipass
+    for passes in (2, 3):
+        assert f(None, A, A, A, 4, 8, 8, 8, 1.0, passes, None) == INVALID
+        assert f(A, A, None, A, 4, 8, 8, 8, 1.0, passes, None) == INVALID   # m carries state
+        assert f(A, A, A, None, 4, 8, 8, 8, 1.0, passes, None) == INVALID   # so does l
+        assert f(A, A, A, A, 4, 8, 7, 8, 1.0, passes, None) == INVALID
+        assert f(A, A, A, A, 4, 8, 8, 8, 0.0, passes, None) == INVALID
+        assert f(A, A, A, A + 2, 4, 8, 8, 8, 1.0, passes, None) == MISALIGNED
+    for passes in (0, 1, 4, -2):
+        assert f(A, A, A, A, 4, 8, 8, 8, 1.0, passes, None) == INVALID
+
+
+def test_softmax_rows_16bit_rejects_bad_arguments(lib):
+    f = lib.os_softmax_rows_16bit
+    for dt in (1, 2):
+        assert f(None, A, None, None, 4, 8, 8, 8, 1.0, dt, None) == INVALID
+        assert f(A, None, None, None, 4, 8, 8, 8, 1.0, dt, None) == INVALID
+        assert f(A, A, None, None, 4, 8, 7, 8, 1.0, dt, None) == INVALID
+        assert f(A, A, None, None, 4, 8, 8, 8, -1.0, dt, None) == INVALID
+        assert f(A + 1, A, None, None, 4, 8, 8, 8, 1.0, dt, None) == MISALIGNED
+        assert f(A, A, A + 2, None, 4, 8, 8, 8, 1.0, dt, None) == MISALIGNED
+    for dt in (0, 3, -1):
+        assert f(A, A, None, None, 4, 8, 8, 8, 1.0, dt, None) == INVALID
+
+
 def test_attention_fwd_rejects_bad_arguments(lib):
     f = lib.os_attention_fwd
     ok = (1, 2, 64, 64, 128, 0.1, 0, None)

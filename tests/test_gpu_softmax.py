@@ -7,7 +7,7 @@ import torch
 import oracle
 import pass_attention_gb300 as oss
 from pass_attention_gb300 import workloads
-from parity import check_softmax
+from parity import check_softmax, f32
 
 pytestmark = pytest.mark.gpu
 
@@ -22,7 +22,7 @@ def test_worked_example_row64():
     w = workloads.ROW64
     x = workloads.logits(w.rows, w.cols, w.mult, w.seed, device="cuda")
     y, m, l = run(x, w.scale)
-    check_softmax(y, m, l, *oracle.softmax_rows(x.cpu().numpy(), w.scale), what="row64")
+    check_softmax(y, m, l, *oracle.softmax_rows(x.cpu().numpy(), f32(w.scale)), what="row64")
 
 
 SHAPES = [(1, 1), (3, 3), (5, 7), (37, 1000), (64, 1024), (9, 1025), (16, 4096), (8, 8195),
@@ -30,7 +30,9 @@ SHAPES = [(1, 1), (3, 3), (5, 7), (37, 1000), (64, 1024), (9, 1025), (16, 4096),
 
 
 @pytest.mark.parametrize("rows,cols", SHAPES)
-@pytest.mark.parametrize("scale", [1.0, 0.125, 3.0])
+# 0.1 and 10 make the low part of scale*log2(e) negative, the case in which
+# a masked or padding entry must not turn the FMA exponent into NaN
+@pytest.mark.parametrize("scale", [1.0, 0.125, 3.0, 0.1, 10.0])
 def test_shapes_and_scales_aligned(rows, cols, scale):
     # leading dimension rounded up to 4 floats: the 16-byte (register-resident
     # up to 16384 columns) path, with a ragged tail when cols % 4 != 0
@@ -40,7 +42,7 @@ def test_shapes_and_scales_aligned(rows, cols, scale):
     y, m, l = oss.softmax_rows(x, scale, y=y)
     torch.cuda.synchronize()
     check_softmax(y.cpu().numpy(), m.cpu().numpy(), l.cpu().numpy(),
-                  *oracle.softmax_rows(x.cpu().numpy(), scale), what=f"{rows}x{cols}")
+                  *oracle.softmax_rows(x.cpu().numpy(), f32(scale)), what=f"{rows}x{cols}")
 
 
 @pytest.mark.parametrize("rows,cols", [(1, 1), (3, 3), (5, 7), (9, 1025), (8, 8195), (2, 40003)])
@@ -48,12 +50,12 @@ def test_shapes_unaligned(rows, cols):
     # dense rows whose length is not a multiple of 4, and a base offset by one
     # float: the scalar streaming path
     x = workloads.logits(rows, cols, 10.0, seed=rows + cols, device="cuda")
-    y, m, l = run(x, 0.5)
-    check_softmax(y, m, l, *oracle.softmax_rows(x.cpu().numpy(), 0.5), what=f"unaligned {rows}x{cols}")
+    y, m, l = run(x, 0.3)
+    check_softmax(y, m, l, *oracle.softmax_rows(x.cpu().numpy(), f32(0.3)), what=f"unaligned {rows}x{cols}")
     buf = workloads.logits(1, rows * cols + 1, 10.0, seed=3, device="cuda")
     x1 = buf[0, 1:].view(rows, cols)
     y, m, l = run(x1, 1.0)
-    check_softmax(y, m, l, *oracle.softmax_rows(x1.cpu().numpy(), 1.0), what="offset base")
+    check_softmax(y, m, l, *oracle.softmax_rows(x1.cpu().numpy(), f32(1.0)), what="offset base")
 
 
 @pytest.mark.parametrize("cols,pad", [(1000, 8), (8192, 4), (20000, 12)])
@@ -64,19 +66,20 @@ def test_leading_dimension(cols, pad):
     y, m, l = oss.softmax_rows(x, 1.0, y=yb[:, :cols])
     torch.cuda.synchronize()
     check_softmax(y.cpu().numpy(), m.cpu().numpy(), l.cpu().numpy(),
-                  *oracle.softmax_rows(x.cpu().numpy(), 1.0), what="ld")
+                  *oracle.softmax_rows(x.cpu().numpy(), f32(1.0)), what="ld")
     assert torch.all(yb[:, cols:] == 7.0)  # padding untouched
 
 
 @pytest.mark.parametrize("cols", [64, 8192, 20000])
-def test_masked_entries_and_empty_rows(cols):
+@pytest.mark.parametrize("scale", [1.0, 0.1])
+def test_masked_entries_and_empty_rows(cols, scale):
     x = workloads.logits(8, cols, 10.0, seed=cols + 1, device="cuda")
     g = torch.Generator(device="cuda").manual_seed(5)
     x[torch.rand(x.shape, generator=g, device="cuda") < 0.3] = -float("inf")
     x[2] = -float("inf")                  # an entirely masked row
     x[5, : cols // 2] = -float("inf")     # masked first half (first blocks empty)
-    y, m, l = run(x, 1.0)
-    check_softmax(y, m, l, *oracle.softmax_rows(x.cpu().numpy(), 1.0), what="masked")
+    y, m, l = run(x, scale)
+    check_softmax(y, m, l, *oracle.softmax_rows(x.cpu().numpy(), f32(scale)), what="masked")
     assert m[2] == -np.inf and l[2] == 0.0 and np.all(y[2] == 0.0)
     assert not np.any(np.isnan(y))
 
@@ -86,7 +89,7 @@ def test_extreme_logits_stay_finite():
     x = workloads.logits(4, 4096, 1000.0, seed=9, device="cuda")
     y, m, l = run(x, 1.0)
     assert np.all(np.isfinite(y)) and np.all(np.isfinite(l))
-    check_softmax(y, m, l, *oracle.softmax_rows(x.cpu().numpy(), 1.0), what="x1000")
+    check_softmax(y, m, l, *oracle.softmax_rows(x.cpu().numpy(), f32(1.0)), what="x1000")
 
 
 @pytest.mark.slow
@@ -99,7 +102,7 @@ def test_full_size_softmax_32k_every_row():
     step = 2048
     for r0 in range(0, w.rows, step):
         xs = x[r0:r0 + step].cpu().numpy()
-        ref = oracle.softmax_rows(xs, w.scale)
+        ref = oracle.softmax_rows(xs, f32(w.scale))
         worst = max(worst, check_softmax(y[r0:r0 + step].cpu().numpy(), m[r0:r0 + step].cpu().numpy(),
                                          l[r0:r0 + step].cpu().numpy(), *ref, what=f"rows {r0}+"))
     print(f"softmax_32k worst relative error {worst:.3e}")
