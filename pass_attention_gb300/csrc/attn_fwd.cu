@@ -19,21 +19,29 @@
 // reference gives the same O / l in exact arithmetic, and weights stay
 // below 256.
 //
-// CTA layout (224 threads, one CTA per SM, one 128-row query tile):
-//   * warps 0..3 -- softmax: warp w reaches tensor-memory lanes 32 w .. +31;
-//                   each thread owns one query row.
-//   * warp 4     -- TMA producer: Q once, then K and V tiles (128 keys) into
-//                   two 3-stage rings, K two steps ahead of V.
-//   * warp 5     -- one thread issues S_b = Q K_j^T (A, B from shared memory);
+// Persistent: one CTA of 352 threads per SM walks a share of the 128-row
+// query tiles (work_tile); loads and QK^T of the next query tile start while
+// the current one finishes. CTA layout:
+//   * warps 0..7 -- softmax: warp w owns 16 query rows, tensor-memory lanes
+//                   32 (w % 4) + 16 (w / 4) .. + 15; each row's scores are
+//                   spread over four threads (the 16x256b access shape), so
+//                   two softmax warps share each SM sub-partition and a row
+//                   maximum takes two shuffles.
+//   * warp 8     -- TMA producer: the Q tile of each query tile, then K and V
+//                   tiles (128 keys) into two 3-stage rings, K two steps
+//                   ahead of V.
+//   * warp 9     -- one thread issues S_b = Q K_j^T (A, B from shared memory);
 //                   the warp owns the tensor-memory allocation.
-//   * warp 6     -- one thread issues O += P_j V_j (A = P from tensor memory,
+//   * warp 10    -- one thread issues O += P_j V_j (A = P from tensor memory,
 //                   B from shared memory).
 //   Issuing a tcgen05.mma costs its thread tens of cycles, so the two MMA
 //   streams have a thread each.
-// Tensor memory (512 fp32 columns x 128 lanes): S_0 | S_1 | S_2 | O. KV step
-// j uses score buffer b = j % 3 (and ring stage j % 3); the softmax writes P_j
-// as bf16 pairs over the first 64 columns of S_b. With three score buffers
-// QK^T runs up to two steps ahead of the softmax.
+// Tensor memory (512 fp32 columns x 128 lanes): S_0 | S_1 | S_2 | O. KV steps
+// are counted across the CTA's query tiles; step g uses score buffer g % 3
+// (and ring stage g % 3); the softmax writes P_g as bf16 pairs over the first
+// 64 columns of S_{g % 3}. With three score buffers QK^T runs up to two steps
+// ahead of the softmax. The epilogue of a query tile reads O out of tensor
+// memory before the first P V of the next one overwrites it.
 //
 // Causal: query i sees keys 0..i (Sq == Sk). Query tiles start 64 rows before
 // a KV-tile boundary; KV tiles wholly above the diagonal are skipped and the
@@ -62,10 +70,12 @@ constexpr int kBM = 128;          // query rows per CTA (= tensor-memory lanes)
 constexpr int kBN = 128;          // keys per KV tile
 constexpr int kStages = 3;        // depth of the K ring and of the V ring (= score buffers)
 constexpr int kKLead = 2;         // K loads run this many steps ahead of V loads
-constexpr int kThreads = 224;
-constexpr int kProducerWarp = 4;  // warps 0..3: softmax, one thread per query row
-constexpr int kQkWarp = 5;        // warp 5: issues S = Q K^T, owns tensor memory
-constexpr int kPvWarp = 6;        // warp 6: issues O += P V
+constexpr int kSoftWarps = 8;     // warps 0..7: softmax, 16 query rows each
+constexpr int kSoftThreads = kSoftWarps * 32;
+constexpr int kProducerWarp = 8;  // warp 8: TMA producer
+constexpr int kQkWarp = 9;        // warp 9: issues S = Q K^T, owns tensor memory
+constexpr int kPvWarp = 10;       // warp 10: issues O += P V
+constexpr int kThreads = (kPvWarp + 1) * 32;
 constexpr int kCausalShift = 64;  // causal query tiles start 64 rows before a KV tile
 constexpr int kCausalGroup = 4;   // heads per causal scheduling group (K/V of 4 heads fit L2)
 
@@ -97,7 +107,7 @@ constexpr uint64_t kDrainNs = 200000000ull;     // 0.2 s to drain own copies
 // wait sites (error word bits 8..15)
 enum Site : unsigned int {
   kSiteQFull = 1, kSiteKFull, kSiteVFull, kSiteKEmpty, kSiteVEmpty,
-  kSiteSFull, kSitePReady, kSiteODone, kSiteDrain
+  kSiteSFull, kSitePReady, kSiteODone, kSiteDrain, kSiteQEmpty, kSiteOFree
 };
 
 // ---------------------------------------------------------------------------
@@ -241,16 +251,6 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
 #define OSS_RW8(i) "+r"(r[i]), "+r"(r[i + 1]), "+r"(r[i + 2]), "+r"(r[i + 3]), \
                    "+r"(r[i + 4]), "+r"(r[i + 5]), "+r"(r[i + 6]), "+r"(r[i + 7])
 
-// 32 consecutive columns of this warp's 32 lanes: thread i gets lane i.
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-      : OSS_R8(0), OSS_R8(8), OSS_R8(16), OSS_R8(24)
-      : "r"(taddr));
-}
-
 // Completes outstanding tcgen05.ld of this thread; the register operands tie
 // the loaded values to the wait so no use is scheduled before it.
 __device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[32]) {
@@ -258,25 +258,41 @@ __device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[32]) {
   asm volatile("" : OSS_RW8(0), OSS_RW8(8), OSS_RW8(16), OSS_RW8(24));
 }
 
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+__device__ __forceinline__ void tmem_st_wait() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// 16 lanes x 64 columns (shape 16x256b, 8 repetitions). Thread t holds, for
+// repetition k, columns 8k + 2(t%4) and 8k + 2(t%4) + 1 of lane t/4 in
+// r[4k], r[4k+1] and of lane 8 + t/4 in r[4k+2], r[4k+3].
+__device__ __forceinline__ void tmem_ld16x256_x8(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "tcgen05.ld.sync.aligned.16x256b.x8.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : OSS_R8(0), OSS_R8(8), OSS_R8(16), OSS_R8(24)
+      : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_st16x256_x8(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.16x256b.x8.b32 [%0], "
       "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
       "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
       OSS_W8(0), OSS_W8(8), OSS_W8(16), OSS_W8(24)
       : "memory");
 }
 
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+// 16 lanes x 64 columns (shape 16x128b, 16 repetitions). Thread t writes,
+// for repetition k, column 4k + t%4 of lane t/4 from r[2k] and of lane
+// 8 + t/4 from r[2k+1].
+__device__ __forceinline__ void tmem_st16x128_x16(uint32_t taddr, const uint32_t (&r)[32]) {
   asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
-      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
-      OSS_W8(0), OSS_W8(8)
+      "tcgen05.st.sync.aligned.16x128b.x16.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      OSS_W8(0), OSS_W8(8), OSS_W8(16), OSS_W8(24)
       : "memory");
-}
-
-__device__ __forceinline__ void tmem_st_wait() {
-  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
 // max(a, b, c) in one instruction (three-input max.f32, sm_100 and later)
@@ -330,7 +346,7 @@ struct AttnParams {
   uint16_t* o;
   float* lse;
   unsigned int* err;
-  int Sq, Sk, BH, n_qblocks;
+  int Sq, Sk, BH, n_qblocks, n_tiles;
   float C;  // scale * log2(e)
   int causal;
   uint64_t timeout_ns;  // limit of every bounded wait
@@ -345,12 +361,69 @@ struct AttnParams {
 };
 
 struct Barriers {
-  uint64_t q_full;
+  uint64_t q_full;   // Q tile landed
+  uint64_t q_free;   // every QK^T of the tile in the Q buffer is done
   uint64_t k_full[kStages], v_full[kStages];
   uint64_t s_full[kSBuf], p_ready[kSBuf];
-  uint64_t o_done[kSBuf];  // P_j V done, for steps j of each buffer (keeps parity waits exact)
+  uint64_t o_done[kSBuf];  // P V done, for the steps of each buffer (keeps parity waits exact)
+  uint64_t o_free;   // the epilogue has read O out of tensor memory
   uint64_t drain[2];  // one per issuing thread
 };
+
+// A query tile: (b, h), first query row, number of KV tiles and how many of
+// them (the diagonal ones, causal only) are visited first.
+struct TileInfo {
+  int bh, q0, n_kv, n_diag;
+};
+
+// Query tile number lin of the launch. Causal tiles start kCausalShift rows
+// before a KV tile boundary (the first tile hangs over row 0; the TMA fills
+// the rows above with zeros). Numbering: the tiles processed at the same time
+// should share (b, h), so that K and V are read from HBM once and then from
+// L2. Non-causal: (b, h)-major. Causal: groups of kCausalGroup heads,
+// heaviest query tiles first within each group.
+__device__ __forceinline__ TileInfo tile_info(const AttnParams& p, int lin) {
+  int bh, qb;
+  if (!p.causal) {
+    bh = lin / p.n_qblocks;
+    qb = lin - bh * p.n_qblocks;
+  } else {
+    const int per_group = kCausalGroup * p.n_qblocks;
+    const int g = lin / per_group;
+    const int gsize = min(kCausalGroup, p.BH - g * kCausalGroup);
+    const int r = lin - g * per_group;
+    const int qb_lin = r / gsize;
+    bh = g * kCausalGroup + (r - qb_lin * gsize);
+    qb = p.n_qblocks - 1 - qb_lin;
+  }
+  TileInfo t;
+  t.bh = bh;
+  t.q0 = qb * kBM - (p.causal ? kCausalShift : 0);
+  const int kv_end = p.causal ? min(p.Sk, t.q0 + kBM) : p.Sk;
+  t.n_kv = (kv_end + kBN - 1) / kBN;
+  // KV tiles that reach past the tile's first row touch the diagonal; they
+  // are visited first, from the last one down: for a shifted causal tile the
+  // first one is masked for all of the tile's first kCausalShift rows.
+  const int diag_first = p.causal ? max(0, t.q0) / kBN : t.n_kv;
+  t.n_diag = t.n_kv - diag_first;
+  return t;
+}
+
+// KV tile visited at step j of a query tile.
+__device__ __forceinline__ int kv_tile(const TileInfo& t, int j) {
+  return j < t.n_diag ? (t.n_kv - 1 - j) : (j - t.n_diag);
+}
+
+// The k-th query tile of this CTA, or -1. The grid is one CTA per SM; round
+// k hands tiles k*G .. k*G + G - 1 to the G CTAs, in reverse CTA order on odd
+// rounds, so a CTA that drew a heavy causal tile in one round draws a light
+// one in the next.
+__device__ __forceinline__ int work_tile(int k, int n_tiles) {
+  const int G = static_cast<int>(gridDim.x);
+  const int idx = (k & 1) ? (G - 1 - static_cast<int>(blockIdx.x)) : static_cast<int>(blockIdx.x);
+  const long long lin = static_cast<long long>(k) * G + idx;
+  return lin < n_tiles ? static_cast<int>(lin) : -1;
+}
 
 __global__ void __launch_bounds__(kThreads, 1)
 attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
@@ -367,48 +440,19 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // Query tile of this CTA. Causal tiles start kCausalShift rows before a KV
-  // tile boundary (the first tile hangs over row 0; the TMA fills the rows
-  // above with zeros), and the heaviest tiles are launched first.
-  // CTA order: the ~150 CTAs resident at a time should share (b, h), so
-  // that K and V are read from HBM once and then from L2. Non-causal:
-  // (b, h)-major. Causal: groups of kCausalGroup heads, heaviest query tiles
-  // first within each group.
-  const int lin = blockIdx.x;
-  int bh, qb;
-  if (!p.causal) {
-    bh = lin / p.n_qblocks;
-    qb = lin - bh * p.n_qblocks;
-  } else {
-    const int per_group = kCausalGroup * p.n_qblocks;
-    const int g = lin / per_group;
-    const int gsize = min(kCausalGroup, p.BH - g * kCausalGroup);
-    const int r = lin - g * per_group;
-    const int qb_lin = r / gsize;
-    bh = g * kCausalGroup + (r - qb_lin * gsize);
-    qb = p.n_qblocks - 1 - qb_lin;
-  }
-  const int q0 = qb * kBM - (p.causal ? kCausalShift : 0);
-  const int kv_end = p.causal ? min(p.Sk, q0 + kBM) : p.Sk;
-  const int n_kv = (kv_end + kBN - 1) / kBN;
-  // KV tiles that reach past the tile's first row touch the diagonal; they
-  // are visited first, from the last one down: for a shifted causal tile the
-  // first one is masked for all of the tile's first kCausalShift rows.
-  const int diag_first = p.causal ? max(0, q0) / kBN : n_kv;
-  const int n_diag = n_kv - diag_first;
-  auto kv_tile = [&](int j) { return j < n_diag ? (n_kv - 1 - j) : (j - n_diag); };
-
   if (threadIdx.x == 0) {
     mbar_init(smem_addr(&bars.q_full), 1);
+    mbar_init(smem_addr(&bars.q_free), 1);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(smem_addr(&bars.k_full[s]), 1);
       mbar_init(smem_addr(&bars.v_full[s]), 1);
     }
     for (int b = 0; b < kSBuf; ++b) {
       mbar_init(smem_addr(&bars.s_full[b]), 1);
-      mbar_init(smem_addr(&bars.p_ready[b]), kBM);
+      mbar_init(smem_addr(&bars.p_ready[b]), kSoftThreads);
       mbar_init(smem_addr(&bars.o_done[b]), 1);
     }
+    mbar_init(smem_addr(&bars.o_free), kSoftThreads);
     mbar_init(smem_addr(&bars.drain[0]), 1);
     mbar_init(smem_addr(&bars.drain[1]), 1);
     abort_flag_s = 0;
@@ -427,85 +471,124 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
   tc_fence_after();
   const uint32_t tbase = tmem_base_slot;
 
+  // Every role walks the same sequence of query tiles (work_tile) and counts
+  // KV steps g across them: step g uses ring stage and score buffer g % 3, in
+  // round g / 3, so the pipeline runs on from one query tile into the next.
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_q)) : "memory");
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_k)) : "memory");
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_v)) : "memory");
       const uint32_t qbar = smem_addr(&bars.q_full);
-      mbar_expect_tx(qbar, kTile);
-      for (int h = 0; h < 2; ++h)
-        tma_load_3d(sbase + kOffQ + h * kHalf, &tmap_q, qbar, h * 64, q0, bh);
-      // K_j is consumed by QK_j, which runs up to two steps ahead of P_j V,
-      // the consumer of V_j; so K loads run kKLead steps ahead of V loads,
+      // K_g is consumed by QK_g, which runs up to two steps ahead of P_g V,
+      // the consumer of V_g; so K loads run kKLead steps ahead of V loads,
       // and each ring is refilled as soon as its own consumer is done: K stage
-      // j % 3 when QK_j has completed (s_full[j % 3]), V stage j % 3 when
-      // P_j V has (o_done[j % 3]) -- ring stage and score buffer coincide.
-      int k_issued = 0, v_issued = 0, skipped_v = -1;
-      for (int i = 0; i < n_kv + kKLead; ++i) {
-        if (i < n_kv) {
-          const int s = i % kStages;
-          const int round = i / kStages;
-          if (round > 0 && !wait_bar(smem_addr(&bars.s_full[s]), (round - 1) & 1, abort_flag,
-                                     p.err, kSiteKEmpty))
-            break;
-          const uint32_t kb = smem_addr(&bars.k_full[s]);
-          mbar_expect_tx(kb, kTile);
-          for (int h = 0; h < 2; ++h)
-            tma_load_3d(sbase + kOffK + s * kTile + h * kHalf, &tmap_k, kb, h * 64,
-                        kv_tile(i) * kBN, bh);
-          k_issued = i + 1;
+      // g % 3 when QK_g has completed (s_full), V stage g % 3 when P_g V has
+      // (o_done) -- ring stage and score buffer coincide. The KV tile and
+      // (b, h) of each K load are kept for the V load of the same step.
+      int k_issued = 0, v_issued = 0, q_loads = 0, skipped_v = -1;
+      int key_row[kStages] = {0, 0, 0}, key_bh[kStages] = {0, 0, 0};
+      int kt = 0, j = 0;  // K stream: tile ordinal, step within the tile
+      int lin = work_tile(0, p.n_tiles);
+      TileInfo t{};
+      if (lin >= 0) t = tile_info(p, lin);
+      for (int g = 0;; ++g) {
+        // V of step g - kKLead first: it is the load the P V thread waits on
+        // soonest, and the Q wait below may block until this tile's QK^T end
+        const int gv = g - kKLead;
+        if (gv >= 0 && gv < k_issued) {
+          if (gv == p.skip_v_step) {
+            skipped_v = gv;  // test hook: this V tile never arrives
+          } else {
+            const int s = gv % kStages;
+            const int round = gv / kStages;
+            if (round > 0 && !wait_bar(smem_addr(&bars.o_done[s]), (round - 1) & 1, abort_flag,
+                                       p.err, kSiteVEmpty))
+              break;
+            const uint32_t vb = smem_addr(&bars.v_full[s]);
+            mbar_expect_tx(vb, kTile);
+            for (int h = 0; h < 2; ++h)
+              tma_load_3d(sbase + kOffV + s * kTile + h * kHalf, &tmap_v, vb, h * 64, key_row[s],
+                          key_bh[s]);
+            v_issued = gv + 1;
+          }
         }
-        const int j = i - kKLead;
-        if (j >= 0 && j < n_kv && j == p.skip_v_step) {
-          skipped_v = j;  // test hook: this V tile never arrives
-        } else if (j >= 0 && j < n_kv) {
-          const int s = j % kStages;
-          const int round = j / kStages;
-          if (round > 0 && !wait_bar(smem_addr(&bars.o_done[s]), (round - 1) & 1, abort_flag,
-                                     p.err, kSiteVEmpty))
+        if (lin < 0) {
+          if (gv + 1 >= k_issued) break;  // the last V load has been issued
+          continue;
+        }
+        if (j == 0) {
+          // the single Q buffer is free once every QK^T of the previous tile is done
+          if (kt > 0 && !wait_bar(smem_addr(&bars.q_free), (kt - 1) & 1, abort_flag, p.err,
+                                  kSiteQEmpty))
             break;
-          const uint32_t vb = smem_addr(&bars.v_full[s]);
-          mbar_expect_tx(vb, kTile);
+          mbar_expect_tx(qbar, kTile);
           for (int h = 0; h < 2; ++h)
-            tma_load_3d(sbase + kOffV + s * kTile + h * kHalf, &tmap_v, vb, h * 64,
-                        kv_tile(j) * kBN, bh);
-          v_issued = j + 1;
+            tma_load_3d(sbase + kOffQ + h * kHalf, &tmap_q, qbar, h * 64, t.q0, t.bh);
+          ++q_loads;
+        }
+        const int s = g % kStages;
+        const int round = g / kStages;
+        if (round > 0 && !wait_bar(smem_addr(&bars.s_full[s]), (round - 1) & 1, abort_flag,
+                                   p.err, kSiteKEmpty))
+          break;
+        const uint32_t kb = smem_addr(&bars.k_full[s]);
+        mbar_expect_tx(kb, kTile);
+        key_row[s] = kv_tile(t, j) * kBN;
+        key_bh[s] = t.bh;
+        for (int h = 0; h < 2; ++h)
+          tma_load_3d(sbase + kOffK + s * kTile + h * kHalf, &tmap_k, kb, h * 64, key_row[s],
+                      key_bh[s]);
+        k_issued = g + 1;
+        if (++j == t.n_kv) {
+          j = 0;
+          lin = work_tile(++kt, p.n_tiles);
+          if (lin >= 0) t = tile_info(p, lin);
         }
       }
       // drain: every issued copy must land before the CTA may exit
-      drain_bar(qbar, 0, p.err);
-      for (int j = k_issued - 1; j >= 0 && j >= k_issued - kStages; --j)
-        drain_bar(smem_addr(&bars.k_full[j % kStages]), (j / kStages) & 1, p.err);
-      for (int j = v_issued - 1; j >= 0 && j >= v_issued - kStages; --j)
-        if (j != skipped_v) drain_bar(smem_addr(&bars.v_full[j % kStages]), (j / kStages) & 1, p.err);
+      if (q_loads > 0) drain_bar(qbar, (q_loads - 1) & 1, p.err);
+      for (int i = k_issued - 1; i >= 0 && i >= k_issued - kStages; --i)
+        drain_bar(smem_addr(&bars.k_full[i % kStages]), (i / kStages) & 1, p.err);
+      for (int i = v_issued - 1; i >= 0 && i >= v_issued - kStages; --i)
+        if (i != skipped_v) drain_bar(smem_addr(&bars.v_full[i % kStages]), (i / kStages) & 1, p.err);
     }
   } else if (warp == kQkWarp) {
     // ------------------------------------------------------------ QK issuer
-    // S_{j % 3} = Q K_j^T for j = 0, 1, ...: the buffer last held P_{j-3},
-    // so P_{j-3} V must be done with it. Issuing a tcgen05.mma costs its
-    // thread tens of cycles, so QK^T and P V are issued by two threads.
+    // S_{g % 3} = Q K_g^T: the buffer last held P_{g-3}, so P_{g-3} V must be
+    // done with it. Issuing a tcgen05.mma costs its thread tens of cycles, so
+    // QK^T and P V are issued by two threads.
     if (lane == 0) {
-      bool ok = wait_bar(smem_addr(&bars.q_full), 0, abort_flag, p.err, kSiteQFull);
+      bool ok = true;
       // operand descriptors built once; a 16-element K step only adds a
       // constant to the start-address field (16-byte units)
       const uint64_t dq = smem_desc(sbase + kOffQ, 16, 1024);
-      for (int j = 0; ok && j < n_kv; ++j) {
-        const int s = j % kStages;  // K stage = score buffer
-        if (!(ok = wait_bar(smem_addr(&bars.k_full[s]), (j / kStages) & 1, abort_flag, p.err,
-                            kSiteKFull)))
+      int g = 0;
+      for (int kt = 0; ok; ++kt) {
+        const int lin = work_tile(kt, p.n_tiles);
+        if (lin < 0) break;
+        const TileInfo t = tile_info(p, lin);
+        if (!(ok = wait_bar(smem_addr(&bars.q_full), kt & 1, abort_flag, p.err, kSiteQFull)))
           break;
-        if (j >= kStages && !(ok = wait_bar(smem_addr(&bars.o_done[s]), (j / kStages - 1) & 1,
-                                            abort_flag, p.err, kSiteODone)))
-          break;
-        tc_fence_after();
-        const uint64_t dk = smem_desc(sbase + kOffK + s * kTile, 16, 1024);
-        const uint32_t d_s = tbase + col_s(s);
+        for (int j = 0; j < t.n_kv; ++j, ++g) {
+          const int s = g % kStages;  // K stage = score buffer
+          if (!(ok = wait_bar(smem_addr(&bars.k_full[s]), (g / kStages) & 1, abort_flag, p.err,
+                              kSiteKFull)))
+            break;
+          if (g >= kStages && !(ok = wait_bar(smem_addr(&bars.o_done[s]), (g / kStages - 1) & 1,
+                                              abort_flag, p.err, kSiteODone)))
+            break;
+          tc_fence_after();
+          const uint64_t dk = smem_desc(sbase + kOffK + s * kTile, 16, 1024);
+          const uint32_t d_s = tbase + col_s(s);
 #pragma unroll
-        for (int kk = 0; kk < kD / 16; ++kk)
-          mma_ss(d_s, dq + kstep_kmajor(kk, kHalf), dk + kstep_kmajor(kk, kHalf), kIdescQK,
-                 kk > 0 ? 1u : 0u);
-        tc_commit(smem_addr(&bars.s_full[s]));  // scores ready; K stage s free
+          for (int kk = 0; kk < kD / 16; ++kk)
+            mma_ss(d_s, dq + kstep_kmajor(kk, kHalf), dk + kstep_kmajor(kk, kHalf), kIdescQK,
+                   kk > 0 ? 1u : 0u);
+          tc_commit(smem_addr(&bars.s_full[s]));  // scores ready; K stage s free
+        }
+        if (ok) tc_commit(smem_addr(&bars.q_free));  // Q buffer free once these MMAs are done
       }
       // drain: no MMA of this thread may still write tensor memory when it is freed
       tc_commit(smem_addr(&bars.drain[0]));
@@ -513,205 +596,270 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
     }
   } else if (warp == kPvWarp) {
     // ------------------------------------------------------------ PV issuer
-    // O += P_j V_j once the softmax has written P_j over S_{j % 3}.
+    // O += P_g V_g once the softmax has written P_g over S_{g % 3}. The first
+    // step of a query tile overwrites O, so it also waits until the epilogue
+    // of the previous tile has read O out.
     if (lane == 0) {
       bool ok = true;
       const uint32_t d_o = tbase + kColO;
-      for (int j = 0; ok && j < n_kv; ++j) {
-        const int s = j % kStages;
-        if (!(ok = wait_bar(smem_addr(&bars.v_full[s]), (j / kStages) & 1, abort_flag, p.err,
-                            kSiteVFull)))
-          break;
-        if (!(ok = wait_bar(smem_addr(&bars.p_ready[s]), (j / kStages) & 1, abort_flag, p.err,
-                            kSitePReady)))
-          break;
-        tc_fence_after();
-        const uint64_t dv = smem_desc(sbase + kOffV + s * kTile, kHalf, 1024);
-        const uint32_t a_p = tbase + col_s(s);
+      int g = 0;
+      for (int kt = 0; ok; ++kt) {
+        const int lin = work_tile(kt, p.n_tiles);
+        if (lin < 0) break;
+        const TileInfo t = tile_info(p, lin);
+        for (int j = 0; j < t.n_kv; ++j, ++g) {
+          const int s = g % kStages;
+          if (!(ok = wait_bar(smem_addr(&bars.v_full[s]), (g / kStages) & 1, abort_flag, p.err,
+                              kSiteVFull)))
+            break;
+          if (!(ok = wait_bar(smem_addr(&bars.p_ready[s]), (g / kStages) & 1, abort_flag, p.err,
+                              kSitePReady)))
+            break;
+          if (j == 0 && kt > 0 &&
+              !(ok = wait_bar(smem_addr(&bars.o_free), (kt - 1) & 1, abort_flag, p.err,
+                              kSiteOFree)))
+            break;
+          tc_fence_after();
+          const uint64_t dv = smem_desc(sbase + kOffV + s * kTile, kHalf, 1024);
+          const uint32_t a_p = tbase + col_s(s);
 #pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk)
-          mma_ts(d_o, a_p + kk * 8, dv + static_cast<uint64_t>(kk * (2048 >> 4)), kIdescPV,
-                 (j > 0 || kk > 0) ? 1u : 0u);
-        tc_commit(smem_addr(&bars.o_done[s]));  // buffer s and V stage s free
+          for (int kk = 0; kk < kBN / 16; ++kk)
+            mma_ts(d_o, a_p + kk * 8, dv + static_cast<uint64_t>(kk * (2048 >> 4)), kIdescPV,
+                   (j > 0 || kk > 0) ? 1u : 0u);
+          tc_commit(smem_addr(&bars.o_done[s]));  // buffer s and V stage s free
+        }
       }
       tc_commit(smem_addr(&bars.drain[1]));
       drain_bar(smem_addr(&bars.drain[1]), 0, p.err);
     }
   } else {
     // ------------------------------------------------------------ softmax
-    const int quad = warp;                         // tensor-memory lane quadrant
-    const int r_in_tile = quad * 32 + lane;
-    const int row = q0 + r_in_tile;                // query index (may be < 0: padding)
-    const uint32_t tl = tbase + (static_cast<uint32_t>(quad * 32) << 16);
+    // Warp w owns 16 query rows: lanes 32 (w % 4) + 16 (w / 4) .. + 15 of
+    // tensor memory (a warp reaches only its quadrant 32 (w % 4) .. + 31).
+    // In the 16x256b access shape each row's 128 scores are spread over four
+    // consecutive threads, 32 each; thread t holds rows ra = t/4 and rb =
+    // 8 + t/4 of the warp's 16, columns 8k + cq + {0, 1} (cq = 2 (t % 4)).
+    // Row maxima are finished with two shuffles; the row sums stay per
+    // thread (the four threads of a row share its reference maximum) and are
+    // added up once, after the last KV tile.
+    const int lane0 = (warp & 3) * 32 + (warp >> 2) * 16;  // first lane of this warp
+    const int ra = lane0 + (lane >> 2);
+    const int rb = ra + 8;
+    const int cq = 2 * (lane & 3);
+    const uint32_t tl = tbase + (static_cast<uint32_t>(lane0) << 16);
     const float C = p.C;
-    float m = neg_inf();       // reference maximum, base 2
-    float m_true = neg_inf();  // true row maximum, base 2 (for partial states)
-    float l = 0.f;
     bool ok = true;
-    for (int j = 0; j < n_kv; ++j) {
-      const int b = j % kSBuf;
-      const uint32_t colS = col_s(b);
-      ok = __all_sync(0xffffffffu, wait_bar(smem_addr(&bars.s_full[b]), (j / kSBuf) & 1,
-                                            abort_flag, p.err, kSiteSFull));
-      if (!ok) break;
-      tc_fence_after();
-      uint32_t r0[32], r1[32], r2[32], r3[32];
-      tmem_ld32(tl + colS + 0, r0);
-      tmem_ld32(tl + colS + 32, r1);
-      tmem_ld32(tl + colS + 64, r2);
-      tmem_ld32(tl + colS + 96, r3);
-      tmem_ld_wait(r0);
-      tmem_ld_wait(r1);
-      tmem_ld_wait(r2);
-      tmem_ld_wait(r3);
-      float s[kBN];
-#pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        s[c] = __uint_as_float(r0[c]);
-        s[32 + c] = __uint_as_float(r1[c]);
-        s[64 + c] = __uint_as_float(r2[c]);
-        s[96 + c] = __uint_as_float(r3[c]);
-      }
-      const int key0 = kv_tile(j) * kBN;
-      const bool ragged = key0 + kBN > p.Sk;
-      const bool diag = p.causal && key0 + kBN - 1 > q0;
-      if (ragged || diag) {
-        const int lim = min(p.Sk, p.causal ? row + 1 : p.Sk) - key0;  // visible keys: c < lim
-#pragma unroll
-        for (int c = 0; c < kBN; ++c)
-          if (c >= lim) s[c] = neg_inf();
-      }
-      // row maximum of this tile: four independent chains of 3-input max
-      float mx0 = neg_inf(), mx1 = neg_inf(), mx2 = neg_inf(), mx3 = neg_inf();
-#pragma unroll
-      for (int c = 0; c < kBN; c += 8) {
-        mx0 = fmax3(mx0, s[c + 0], s[c + 1]);
-        mx1 = fmax3(mx1, s[c + 2], s[c + 3]);
-        mx2 = fmax3(mx2, s[c + 4], s[c + 5]);
-        mx3 = fmax3(mx3, s[c + 6], s[c + 7]);
-      }
-      const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * C;
-      const float m_new = fmaxf(m, m_tile);
-      m_true = fmaxf(m_true, m_tile);
-      // Move the reference maximum only when some row of this warp has risen
-      // by more than kRescaleSlack (base 2). Otherwise keep it: exactly the
-      // same result in exact arithmetic (the reference cancels in O / l),
-      // weights stay <= 2^kRescaleSlack, and the O round trip is skipped.
-      const bool rescale = __any_sync(0xffffffffu, m_new > m + kRescaleSlack);
-      float corr = 1.f;
-      if (rescale) {
-        const float m_use_new = (m_new == neg_inf()) ? 0.f : m_new;
-        corr = ex2(m - m_use_new);  // 0 while m = -inf
-        m = m_new;
-      }
-      const float m_use = (m == neg_inf()) ? 0.f : m;  // the -inf guard
-      const float2 Cv = make_float2(C, C);
-      const float2 mv = make_float2(-m_use, -m_use);
-      float2 acc0 = make_float2(0.f, 0.f), acc1 = acc0;
-#pragma unroll
-      for (int ch = 0; ch < kBN / 32; ++ch) {
-        // 32 weights -> 16 bf16 pairs, stored over the first columns of S_b
-        uint32_t pk[16];
-#pragma unroll
-        for (int c = 0; c < 32; c += 4) {
-          const int cc = ch * 32 + c;
-          const float2 t0 = __ffma2_rn(make_float2(s[cc], s[cc + 1]), Cv, mv);
-          const float2 t1 = __ffma2_rn(make_float2(s[cc + 2], s[cc + 3]), Cv, mv);
-          const float2 e0 = make_float2(ex2(t0.x), ex2(t0.y));
-          const float2 e1 = make_float2(ex2(t1.x), ex2(t1.y));
-          acc0 = __fadd2_rn(acc0, e0);
-          acc1 = __fadd2_rn(acc1, e1);
-          pk[(c >> 1) + 0] = pack_bf16x2(e0.x, e0.y);
-          pk[(c >> 1) + 1] = pack_bf16x2(e1.x, e1.y);
-        }
-        tmem_st16(tl + colS + ch * 16, pk);
-      }
-      const float2 acc = __fadd2_rn(acc0, acc1);
-      l = fmaf(l, corr, acc.x + acc.y);
-      if (rescale && j > 0) {
-        // O still holds the previous tiles' sum: wait for P_{j-1} V (whose
-        // completion implies every earlier one), then rescale
-        ok = __all_sync(0xffffffffu, wait_bar(smem_addr(&bars.o_done[(j - 1) % kSBuf]),
-                                              ((j - 1) / kSBuf) & 1, abort_flag, p.err, kSiteODone));
+    int g = 0;
+    for (int kt = 0; ok; ++kt) {
+      const int lin = work_tile(kt, p.n_tiles);
+      if (lin < 0) break;
+      const TileInfo t = tile_info(p, lin);
+      const int row_a = t.q0 + ra, row_b = t.q0 + rb;  // query indices (may be < 0: padding)
+      float m_a = neg_inf(), m_b = neg_inf();       // reference maxima, base 2
+      float mt_a = neg_inf(), mt_b = neg_inf();     // true row maxima, base 2 (partial states)
+      float l_a = 0.f, l_b = 0.f;                   // this thread's share of the row sums
+      for (int j = 0; j < t.n_kv; ++j, ++g) {
+        const int b = g % kSBuf;
+        const uint32_t colS = col_s(b);
+        ok = __all_sync(0xffffffffu, wait_bar(smem_addr(&bars.s_full[b]), (g / kSBuf) & 1,
+                                              abort_flag, p.err, kSiteSFull));
         if (!ok) break;
         tc_fence_after();
-        const float2 cv = make_float2(corr, corr);
+        uint32_t r0[32], r1[32];
+        tmem_ld16x256_x8(tl + colS, r0);        // columns 0..63
+        tmem_ld16x256_x8(tl + colS + 64, r1);   // columns 64..127
+        tmem_ld_wait(r0);
+        tmem_ld_wait(r1);
+        // sa[16 h + 2 k + e], sb[...]: column 64 h + 8 k + cq + e of rows ra, rb
+        float sa[32], sb[32];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            sa[2 * k + e] = __uint_as_float(r0[4 * k + e]);
+            sb[2 * k + e] = __uint_as_float(r0[4 * k + 2 + e]);
+            sa[16 + 2 * k + e] = __uint_as_float(r1[4 * k + e]);
+            sb[16 + 2 * k + e] = __uint_as_float(r1[4 * k + 2 + e]);
+          }
+        }
+        const int key0 = kv_tile(t, j) * kBN;
+        const bool ragged = key0 + kBN > p.Sk;
+        const bool diag = p.causal && key0 + kBN - 1 > t.q0;
+        if (ragged || diag) {
+          // visible keys of a row: column < lim
+          const int lim_a = min(p.Sk, p.causal ? row_a + 1 : p.Sk) - key0;
+          const int lim_b = min(p.Sk, p.causal ? row_b + 1 : p.Sk) - key0;
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const int col = (i >> 4) * 64 + ((i >> 1) & 7) * 8 + cq + (i & 1);
+            if (col >= lim_a) sa[i] = neg_inf();
+            if (col >= lim_b) sb[i] = neg_inf();
+          }
+        }
+        // row maxima: this thread's 32 columns, then the row's four threads
+        float xa0 = neg_inf(), xa1 = neg_inf(), xb0 = neg_inf(), xb1 = neg_inf();
+#pragma unroll
+        for (int i = 0; i < 32; i += 4) {
+          xa0 = fmax3(xa0, sa[i], sa[i + 1]);
+          xa1 = fmax3(xa1, sa[i + 2], sa[i + 3]);
+          xb0 = fmax3(xb0, sb[i], sb[i + 1]);
+          xb1 = fmax3(xb1, sb[i + 2], sb[i + 3]);
+        }
+        float xa = fmaxf(xa0, xa1), xb = fmaxf(xb0, xb1);
+        xa = fmaxf(xa, __shfl_xor_sync(0xffffffffu, xa, 1));
+        xb = fmaxf(xb, __shfl_xor_sync(0xffffffffu, xb, 1));
+        xa = fmaxf(xa, __shfl_xor_sync(0xffffffffu, xa, 2));
+        xb = fmaxf(xb, __shfl_xor_sync(0xffffffffu, xb, 2));
+        const float mtile_a = xa * C, mtile_b = xb * C;
+        const float mnew_a = fmaxf(m_a, mtile_a), mnew_b = fmaxf(m_b, mtile_b);
+        mt_a = fmaxf(mt_a, mtile_a);
+        mt_b = fmaxf(mt_b, mtile_b);
+        // Move the reference maxima only when some row of this warp has risen
+        // by more than kRescaleSlack (base 2). Otherwise keep them: the same
+        // O / l in exact arithmetic (the reference cancels), weights stay
+        // <= 2^kRescaleSlack, and the O round trip is skipped.
+        const bool rescale = __any_sync(0xffffffffu, (mnew_a > m_a + kRescaleSlack) ||
+                                                         (mnew_b > m_b + kRescaleSlack));
+        float corr_a = 1.f, corr_b = 1.f;
+        if (rescale) {
+          corr_a = ex2(m_a - ((mnew_a == neg_inf()) ? 0.f : mnew_a));  // 0 while m = -inf
+          corr_b = ex2(m_b - ((mnew_b == neg_inf()) ? 0.f : mnew_b));
+          m_a = mnew_a;
+          m_b = mnew_b;
+        }
+        // P = 2^(S C - m), the -inf guard subtracting 0 for an empty row; bf16
+        // pairs (keys c, c + 1) go to packed column c / 2 = 4 (8 h + k) + t % 4,
+        // which is where the 16x128b shape puts repetition 8 h + k of thread t
+        const float2 Cv = make_float2(C, C);
+        const float2 mva = make_float2(-((m_a == neg_inf()) ? 0.f : m_a), -((m_a == neg_inf()) ? 0.f : m_a));
+        const float2 mvb = make_float2(-((m_b == neg_inf()) ? 0.f : m_b), -((m_b == neg_inf()) ? 0.f : m_b));
+        float2 acc_a = make_float2(0.f, 0.f), acc_b = acc_a;
+        uint32_t pk[32];
+#pragma unroll
+        for (int kk = 0; kk < 16; ++kk) {
+          const float2 ta = __ffma2_rn(make_float2(sa[2 * kk], sa[2 * kk + 1]), Cv, mva);
+          const float2 tb = __ffma2_rn(make_float2(sb[2 * kk], sb[2 * kk + 1]), Cv, mvb);
+          const float2 ea = make_float2(ex2(ta.x), ex2(ta.y));
+          const float2 eb = make_float2(ex2(tb.x), ex2(tb.y));
+          acc_a = __fadd2_rn(acc_a, ea);
+          acc_b = __fadd2_rn(acc_b, eb);
+          pk[2 * kk] = pack_bf16x2(ea.x, ea.y);
+          pk[2 * kk + 1] = pack_bf16x2(eb.x, eb.y);
+        }
+        tmem_st16x128_x16(tl + colS, pk);
+        l_a = fmaf(l_a, corr_a, acc_a.x + acc_a.y);
+        l_b = fmaf(l_b, corr_b, acc_b.x + acc_b.y);
+        if (rescale && j > 0) {
+          // O still holds the previous tiles' sum: wait for P_{j-1} V (whose
+          // completion implies every earlier one), then rescale this warp's rows
+          ok = __all_sync(0xffffffffu, wait_bar(smem_addr(&bars.o_done[(g - 1) % kSBuf]),
+                                                ((g - 1) / kSBuf) & 1, abort_flag, p.err, kSiteODone));
+          if (!ok) break;
+          tc_fence_after();
 #pragma unroll 1
-        for (int cc = 0; cc < kD; cc += 32) {
+          for (int h = 0; h < 2; ++h) {
+            uint32_t ov[32];
+            tmem_ld16x256_x8(tl + kColO + 64 * h, ov);
+            tmem_ld_wait(ov);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              const float2 oa = __fmul2_rn(make_float2(__uint_as_float(ov[4 * k]), __uint_as_float(ov[4 * k + 1])),
+                                           make_float2(corr_a, corr_a));
+              const float2 ob = __fmul2_rn(make_float2(__uint_as_float(ov[4 * k + 2]), __uint_as_float(ov[4 * k + 3])),
+                                           make_float2(corr_b, corr_b));
+              ov[4 * k] = __float_as_uint(oa.x);
+              ov[4 * k + 1] = __float_as_uint(oa.y);
+              ov[4 * k + 2] = __float_as_uint(ob.x);
+              ov[4 * k + 3] = __float_as_uint(ob.y);
+            }
+            tmem_st16x256_x8(tl + kColO + 64 * h, ov);
+          }
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(smem_addr(&bars.p_ready[b]));
+      }
+      // the row sums: the four threads of a row add their shares
+      l_a += __shfl_xor_sync(0xffffffffu, l_a, 1);
+      l_b += __shfl_xor_sync(0xffffffffu, l_b, 1);
+      l_a += __shfl_xor_sync(0xffffffffu, l_a, 2);
+      l_b += __shfl_xor_sync(0xffffffffu, l_b, 2);
+      // epilogue: O / l and lse for these rows, once the tile's last P V is
+      // done (its completion implies every earlier one)
+      if (ok)
+        ok = __all_sync(0xffffffffu, wait_bar(smem_addr(&bars.o_done[(g - 1) % kSBuf]),
+                                              ((g - 1) / kSBuf) & 1, abort_flag, p.err, kSiteODone));
+      const bool live_a = row_a >= 0 && row_a < p.Sq;
+      const bool live_b = row_b >= 0 && row_b < p.Sq;
+      const bool writes_row = (lane & 3) == 0;  // one thread per row writes m, l, lse
+      if (ok && p.part_o) {
+        // partial state relative to the true row maximum: rescale the sums
+        // taken against the reference by 2^(m_ref - m_true) <= 1
+        tc_fence_after();
+        const bool empty_a = (mt_a == neg_inf()) || !(l_a > 0.f);
+        const bool empty_b = (mt_b == neg_inf()) || !(l_b > 0.f);
+        const float f_a = empty_a ? 0.f : ex2(m_a - mt_a);
+        const float f_b = empty_b ? 0.f : ex2(m_b - mt_b);
+        const size_t slot_a = (static_cast<size_t>(t.bh) * p.Sq + row_a) * p.part_stride + p.part_index;
+        const size_t slot_b = (static_cast<size_t>(t.bh) * p.Sq + row_b) * p.part_stride + p.part_index;
+        float2* oa = reinterpret_cast<float2*>(p.part_o + slot_a * kD);
+        float2* ob = reinterpret_cast<float2*>(p.part_o + slot_b * kD);
+#pragma unroll 1
+        for (int h = 0; h < 2; ++h) {
           uint32_t ov[32];
-          tmem_ld32(tl + kColO + cc, ov);
+          tmem_ld16x256_x8(tl + kColO + 64 * h, ov);
           tmem_ld_wait(ov);
 #pragma unroll
-          for (int c = 0; c < 32; c += 2) {
-            const float2 o2 = __fmul2_rn(make_float2(__uint_as_float(ov[c]), __uint_as_float(ov[c + 1])), cv);
-            ov[c] = __float_as_uint(o2.x);
-            ov[c + 1] = __float_as_uint(o2.y);
+          for (int k = 0; k < 8; ++k) {
+            const int col = 64 * h + 8 * k + cq;
+            if (live_a)
+              oa[col >> 1] = make_float2(__uint_as_float(ov[4 * k]) * f_a, __uint_as_float(ov[4 * k + 1]) * f_a);
+            if (live_b)
+              ob[col >> 1] = make_float2(__uint_as_float(ov[4 * k + 2]) * f_b, __uint_as_float(ov[4 * k + 3]) * f_b);
           }
-          tmem_st32(tl + kColO + cc, ov);
+        }
+        if (writes_row) {
+          const float kLn2 = 0.69314718055994530942f;
+          if (live_a) {
+            p.part_m[slot_a] = empty_a ? neg_inf() : mt_a * kLn2;
+            p.part_l[slot_a] = empty_a ? 0.f : l_a * f_a;
+          }
+          if (live_b) {
+            p.part_m[slot_b] = empty_b ? neg_inf() : mt_b * kLn2;
+            p.part_l[slot_b] = empty_b ? 0.f : l_b * f_b;
+          }
+        }
+      } else if (ok) {
+        tc_fence_after();
+        const float inv_a = (l_a > 0.f) ? 1.0f / l_a : 0.f;
+        const float inv_b = (l_b > 0.f) ? 1.0f / l_b : 0.f;
+        uint32_t* oa = reinterpret_cast<uint32_t*>(p.o + (static_cast<size_t>(t.bh) * p.Sq + row_a) * kD);
+        uint32_t* ob = reinterpret_cast<uint32_t*>(p.o + (static_cast<size_t>(t.bh) * p.Sq + row_b) * kD);
+#pragma unroll 1
+        for (int h = 0; h < 2; ++h) {
+          uint32_t ov[32];
+          tmem_ld16x256_x8(tl + kColO + 64 * h, ov);
+          tmem_ld_wait(ov);
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const int col = 64 * h + 8 * k + cq;
+            if (live_a)
+              oa[col >> 1] = pack_bf16x2(__uint_as_float(ov[4 * k]) * inv_a, __uint_as_float(ov[4 * k + 1]) * inv_a);
+            if (live_b)
+              ob[col >> 1] = pack_bf16x2(__uint_as_float(ov[4 * k + 2]) * inv_b, __uint_as_float(ov[4 * k + 3]) * inv_b);
+          }
+        }
+        if (writes_row && p.lse) {
+          const float kLn2 = 0.69314718055994530942f;
+          if (live_a)
+            p.lse[static_cast<size_t>(t.bh) * p.Sq + row_a] = (l_a > 0.f) ? (m_a + __log2f(l_a)) * kLn2 : neg_inf();
+          if (live_b)
+            p.lse[static_cast<size_t>(t.bh) * p.Sq + row_b] = (l_b > 0.f) ? (m_b + __log2f(l_b)) * kLn2 : neg_inf();
         }
       }
-      tmem_st_wait();
+      // O has been read: the next tile's first P V may overwrite it
       tc_fence_before();
-      mbar_arrive(smem_addr(&bars.p_ready[b]));
-    }
-    // epilogue: O / l and lse for this row, once P_{n-1} V is done (its
-    // completion implies every earlier one)
-    if (ok)
-      ok = __all_sync(0xffffffffu, wait_bar(smem_addr(&bars.o_done[(n_kv - 1) % kSBuf]),
-                                            ((n_kv - 1) / kSBuf) & 1, abort_flag, p.err, kSiteODone));
-    if (ok && p.part_o) {
-      // partial state relative to the true row maximum: rescale the sums
-      // taken against the reference by 2^(m_ref - m_true) <= 1
-      tc_fence_after();
-      const bool empty = (m_true == neg_inf()) || !(l > 0.f);
-      const float f = empty ? 0.f : ex2(m - m_true);
-      const bool live = row >= 0 && row < p.Sq;
-      const size_t slot = (static_cast<size_t>(bh) * p.Sq + row) * p.part_stride + p.part_index;
-      float4* orow = reinterpret_cast<float4*>(p.part_o + slot * kD);
-#pragma unroll 1
-      for (int cc = 0; cc < kD; cc += 32) {
-        uint32_t ov[32];
-        tmem_ld32(tl + kColO + cc, ov);
-        tmem_ld_wait(ov);
-        if (live) {
-#pragma unroll
-          for (int c = 0; c < 32; c += 4)
-            orow[(cc + c) >> 2] = make_float4(__uint_as_float(ov[c]) * f, __uint_as_float(ov[c + 1]) * f,
-                                              __uint_as_float(ov[c + 2]) * f, __uint_as_float(ov[c + 3]) * f);
-        }
-      }
-      if (live) {
-        const float kLn2 = 0.69314718055994530942f;
-        p.part_m[slot] = empty ? neg_inf() : m_true * kLn2;
-        p.part_l[slot] = empty ? 0.f : l * f;
-      }
-    } else if (ok) {
-      tc_fence_after();
-      const float inv = (l > 0.f) ? 1.0f / l : 0.f;
-      const bool live = row >= 0 && row < p.Sq;
-      uint4* orow = reinterpret_cast<uint4*>(p.o + (static_cast<size_t>(bh) * p.Sq + row) * kD);
-#pragma unroll 1
-      for (int cc = 0; cc < kD; cc += 32) {
-        uint32_t ov[32];
-        tmem_ld32(tl + kColO + cc, ov);
-        tmem_ld_wait(ov);
-        if (live) {
-#pragma unroll
-          for (int c = 0; c < 32; c += 8) {
-            uint4 w;
-            w.x = pack_bf16x2(__uint_as_float(ov[c + 0]) * inv, __uint_as_float(ov[c + 1]) * inv);
-            w.y = pack_bf16x2(__uint_as_float(ov[c + 2]) * inv, __uint_as_float(ov[c + 3]) * inv);
-            w.z = pack_bf16x2(__uint_as_float(ov[c + 4]) * inv, __uint_as_float(ov[c + 5]) * inv);
-            w.w = pack_bf16x2(__uint_as_float(ov[c + 6]) * inv, __uint_as_float(ov[c + 7]) * inv);
-            orow[(cc + c) >> 3] = w;
-          }
-        }
-      }
-      if (live && p.lse) {
-        const float kLn2 = 0.69314718055994530942f;
-        p.lse[static_cast<size_t>(bh) * p.Sq + row] =
-            (l > 0.f) ? (m + __log2f(l)) * kLn2 : neg_inf();
-      }
+      mbar_arrive(smem_addr(&bars.o_free));
     }
   }
 
@@ -795,8 +943,15 @@ cudaError_t launch_attention_fwd(const uint16_t* q, const uint16_t* k, const uin
   prm.part_o = partial ? partial->o : nullptr;
   prm.part_stride = partial ? partial->stride : 1;
   prm.part_index = partial ? partial->index : 0;
-  const long long grid = static_cast<long long>(prm.n_qblocks) * BH;
-  if (grid > 0x7fffffffLL) return cudaErrorNotSupported;
+  const long long tiles = static_cast<long long>(prm.n_qblocks) * BH;
+  if (tiles > 0x7fffffffLL) return cudaErrorNotSupported;
+  prm.n_tiles = static_cast<int>(tiles);
+  // persistent: one CTA per SM, each walking its share of the query tiles
+  int dev = 0, sms = 0;
+  e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const int grid = static_cast<int>(tiles < sms ? tiles : sms);
   attn_fwd_kernel<<<static_cast<unsigned>(grid), kThreads, kSmemBytes, stream>>>(mq, mk, mv, prm);
   return cudaGetLastError();
 }
