@@ -52,14 +52,17 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # same kernel, applied to the full launch's algorithmic bytes.
 NCU_TRAFFIC = {
     "softmax_32k": {"source": "pass_attention_gb300/csrc/softmax_rows.cu",
-                    "sha256": "9f37f7efad57e9fec69e43131b3ee73741964a0ceee68ec4fd6fbfb9f039d74d",
-                    "bytes_per_launch": 1073969000 + 1017877000},
+                    "sha256": "0e9f96cd9cc10f643ffb690e7b7d73b654d106e637c003e62039271cf0e9bec7",
+                    "bytes_per_launch": 1073803008 + 1018858752},
+    "softmax_32k_bf16": {"source": "pass_attention_gb300/csrc/softmax_rows.cu",
+                         "sha256": "0e9f96cd9cc10f643ffb690e7b7d73b654d106e637c003e62039271cf0e9bec7",
+                         "bytes_per_launch": 536955392 + 485213440},
     "attn_4k": {"source": "pass_attention_gb300/csrc/attn_fwd.cu",
-                "sha256": "07e11d492b2cd675bc76e6c19119b71bde9f6689c0cce99cf43435a37336d359",
-                "bytes_per_launch": 201379328 + 48655872},
+                "sha256": "f918c254f1c632c15d9052607c3b5f973949364ff1fff49bc4c9a9ef2257bc75",
+                "bytes_per_launch": 201510400 + 46380288},
     "attn_causal": {"source": "pass_attention_gb300/csrc/attn_fwd.cu",
-                    "sha256": "07e11d492b2cd675bc76e6c19119b71bde9f6689c0cce99cf43435a37336d359",
-                    "bytes_per_launch": 403601920 + 116535552},
+                    "sha256": "f918c254f1c632c15d9052607c3b5f973949364ff1fff49bc4c9a9ef2257bc75",
+                    "bytes_per_launch": 403565568 + 117761024},
     "decode_64x32": {"source": "pass_attention_gb300/csrc/decode_merge.cu",
                      "sha256": "a9116a8452b09df5ffc198fb6fac3fbf559ce1606b95c551b24f75e9f2c2961f",
                      "scale": (2484805000 + 4145664) / (151653 * 32 * 512 + 8 * 32 * 128 * 2
@@ -473,7 +476,8 @@ def main():
             extra["softmax_32k_bf16"] = {
                 "value": gbs, "unit": "GB/s", "ms_per_step": ms,
                 "workload": f"{w.rows}x{w.cols} bf16 rows (y bf16, m and l fp32), os_softmax_rows_16bit",
-                "roofline": {"bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "roofline": {"bound": "hbm", "kernel": "softmax_rows16_reg_kernel<bf16,4>",
+                             "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
                              "frac": gbs / pk["hbm_gbs"], "traffic": traffic_for("softmax_32k_bf16"),
                              "peak_kind": f"{pk_kind} HBM copy"},
                 "window": win}

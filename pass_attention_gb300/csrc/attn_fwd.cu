@@ -19,9 +19,11 @@
 // reference gives the same O / l in exact arithmetic, and weights stay
 // below 256.
 //
-// Persistent: one CTA of 352 threads per SM walks a share of the 128-row
-// query tiles (work_tile); loads and QK^T of the next query tile start while
-// the current one finishes. CTA layout:
+// Non-causal launches are persistent: one CTA of 352 threads per SM walks a
+// share of the 128-row query tiles (work_tile), and loads and QK^T of the
+// next query tile start while the current one finishes. Causal launches use
+// one CTA per query tile (their costs differ; the block scheduler balances
+// them). CTA layout:
 //   * warps 0..7 -- softmax: warp w owns 16 query rows, tensor-memory lanes
 //                   32 (w % 4) + 16 (w / 4) .. + 15; each row's scores are
 //                   spread over four threads (the 16x256b access shape), so
@@ -414,10 +416,10 @@ __device__ __forceinline__ int kv_tile(const TileInfo& t, int j) {
   return j < t.n_diag ? (t.n_kv - 1 - j) : (j - t.n_diag);
 }
 
-// The k-th query tile of this CTA, or -1. The grid is one CTA per SM; round
-// k hands tiles k*G .. k*G + G - 1 to the G CTAs, in reverse CTA order on odd
-// rounds, so a CTA that drew a heavy causal tile in one round draws a light
-// one in the next.
+// The k-th query tile of this CTA, or -1. With G CTAs, round k hands tiles
+// k*G .. k*G + G - 1 to them, in reverse CTA order on odd rounds (a CTA that
+// drew a heavier tile in one round draws a lighter one in the next). With
+// one CTA per tile (G = number of tiles) CTA i takes tile i only.
 __device__ __forceinline__ int work_tile(int k, int n_tiles) {
   const int G = static_cast<int>(gridDim.x);
   const int idx = (k & 1) ? (G - 1 - static_cast<int>(blockIdx.x)) : static_cast<int>(blockIdx.x);
@@ -946,12 +948,15 @@ cudaError_t launch_attention_fwd(const uint16_t* q, const uint16_t* k, const uin
   const long long tiles = static_cast<long long>(prm.n_qblocks) * BH;
   if (tiles > 0x7fffffffLL) return cudaErrorNotSupported;
   prm.n_tiles = static_cast<int>(tiles);
-  // persistent: one CTA per SM, each walking its share of the query tiles
+  // Non-causal query tiles all cost the same: persistent, one CTA per SM
+  // walking its share. Causal tiles range from 1 to Sk / 128 KV steps; one
+  // CTA per tile, launched heaviest first, lets the block scheduler hand
+  // each freed SM the next tile (measured faster than any static split).
   int dev = 0, sms = 0;
   e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
-  const int grid = static_cast<int>(tiles < sms ? tiles : sms);
+  const int grid = static_cast<int>((causal || tiles < sms) ? tiles : sms);
   attn_fwd_kernel<<<static_cast<unsigned>(grid), kThreads, kSmemBytes, stream>>>(mq, mk, mv, prm);
   return cudaGetLastError();
 }

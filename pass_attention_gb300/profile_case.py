@@ -1,6 +1,8 @@
 """Run one liboss entry point on one workload a few times, for profilers.
 
     python -m pass_attention_gb300.profile_case softmax [--rows R --cols C] [--reps N]
+    python -m pass_attention_gb300.profile_case softmax16 [--rows R --cols C] [--reps N]
+    python -m pass_attention_gb300.profile_case multipass --passes 2|3 [--rows R --cols C]
     python -m pass_attention_gb300.profile_case attn [--B --H --S] [--causal] [--reps N]
     python -m pass_attention_gb300.profile_case decode [--B --H --Lmax --splits] [--reps N]
 
@@ -22,7 +24,8 @@ from pass_attention_gb300 import workloads
 
 def main(argv=None):
     ap = argparse.ArgumentParser()
-    ap.add_argument("case", choices=["softmax", "attn", "decode"])
+    ap.add_argument("case", choices=["softmax", "softmax16", "multipass", "attn", "decode"])
+    ap.add_argument("--passes", type=int, default=3)
     ap.add_argument("--rows", type=int, default=32768)
     ap.add_argument("--cols", type=int, default=8192)
     ap.add_argument("--B", type=int, default=None)
@@ -39,6 +42,18 @@ def main(argv=None):
         y = torch.empty_like(x)
         for _ in range(a.reps):
             oss.softmax_rows(x, 1.0, y=y)
+            torch.cuda.synchronize()
+    elif a.case == "softmax16":
+        x = workloads.logits(a.rows, a.cols, 10.0, seed=1, device="cuda").to(torch.bfloat16)
+        y = torch.empty_like(x)
+        for _ in range(a.reps):
+            oss.softmax_rows_16bit(x, 1.0, y=y)
+            torch.cuda.synchronize()
+    elif a.case == "multipass":
+        x = workloads.logits(a.rows, a.cols, 10.0, seed=1, device="cuda")
+        y = torch.empty_like(x)
+        for _ in range(a.reps):
+            oss.softmax_rows_multipass(x, a.passes, 1.0, y=y)
             torch.cuda.synchronize()
     elif a.case == "attn":
         B, H = a.B or 4, a.H or 16
