@@ -276,10 +276,12 @@ OSS_API os_status os_check_device_error(void* stream, int32_t* code);
  *           issues P V waits on a phase that never completes. After
  *           `timeout_ns` (0: the default of 2 s) it raises the CTA's abort
  *           flag; every role drains its own copies and MMAs, tensor memory is
- *           freed, and the kernel exits. os_check_device_error then returns
- *           OS_ERR_TIMEOUT with code = 1 | (3 << 8) (kernel 1, wait site 3:
- *           V tile full). The CUDA context stays usable; the outputs of that
- *           call are undefined.
+ *           freed, and the kernel exits (the other CTAs of the launch see
+ *           the recorded error and stop too). os_check_device_error then
+ *           returns OS_ERR_TIMEOUT with code & 0xFFFF = 1 | (3 << 8) (kernel
+ *           1, wait site 3: V tile full); bits 16..31 hold the launch's tag.
+ *           The CUDA context stays usable; the outputs of that call are
+ *           undefined.
  * No GPU fault, trap or endless wait is involved.
  * Errors: OS_ERR_INVALID_ARGUMENT (kind not 0/1, step < 0, timeout_ns < 0).
  */

@@ -59,6 +59,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 
 #include "device_common.cuh"
@@ -169,17 +170,28 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
 // records the site). Kept out of line; the fast path below is inlined
 // because every wait sits on the pipeline's critical path (measured: an
 // out-of-line call costs the caller a few hundred cycles).
+// A give-up is recorded in the device error word together with the launch's
+// tag (bits 16..31); the other CTAs of the same launch see the tag on their
+// next slow-path poll and give up too, so a failed launch ends after one
+// timeout instead of one per wave of CTAs.
 __device__ __noinline__ bool wait_bar_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                            unsigned int* err, unsigned int site,
-                                           uint64_t timeout_ns) {
+                                           uint64_t timeout_ns, unsigned int tag) {
   const uint64_t t0 = global_timer();
   for (uint32_t n = 1;; ++n) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
-    if ((n & 63u) == 0 && global_timer() - t0 > timeout_ns) {
-      *abort_flag = 1;
-      report_error(err, kKernelAttnFwd | (site << 8));
-      return false;
+    if ((n & 63u) == 0) {
+      const unsigned int e = *reinterpret_cast<volatile unsigned int*>(err);
+      if (e != 0 && (e >> 16) == tag) {
+        *abort_flag = 1;
+        return false;
+      }
+      if (global_timer() - t0 > timeout_ns) {
+        *abort_flag = 1;
+        report_error(err, kKernelAttnFwd | (site << 8) | (tag << 16));
+        return false;
+      }
     }
   }
 }
@@ -188,7 +200,7 @@ __device__ __noinline__ bool wait_bar_slow(uint32_t bar, uint32_t parity, volati
 // The limit is the kernel's timeout_ns (kTimeoutNs unless a test shortens it).
 #define wait_bar(bar, parity, abort_flag, err, site) \
   (mbar_test_wait((bar), (parity)) ||                 \
-   wait_bar_slow((bar), (parity), (abort_flag), (err), (site), p.timeout_ns))
+   wait_bar_slow((bar), (parity), (abort_flag), (err), (site), p.timeout_ns, p.tag))
 
 // Bounded wait used while draining: ignores the abort flag.
 __device__ __noinline__ bool drain_bar(uint32_t bar, uint32_t parity, unsigned int* err) {
@@ -352,6 +364,7 @@ struct AttnParams {
   float C;  // scale * log2(e)
   int causal;
   uint64_t timeout_ns;  // limit of every bounded wait
+  unsigned int tag;     // launch tag, 1..65535, in bits 16..31 of a reported error
   int skip_v_step;      // test hook: the producer skips the V load of this step (-1: none)
   // partial-state output (sequence-sharded attention): when part_o != null the
   // epilogue writes (m, l, O unnormalised) of row r to slot part_index of a
@@ -939,6 +952,8 @@ cudaError_t launch_attention_fwd(const uint16_t* q, const uint16_t* k, const uin
   prm.C = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
   prm.causal = causal ? 1 : 0;
   prm.timeout_ns = fault.timeout_ns > 0 ? static_cast<uint64_t>(fault.timeout_ns) : kTimeoutNs;
+  static std::atomic<unsigned int> launches{0};
+  prm.tag = launches.fetch_add(1, std::memory_order_relaxed) % 65535u + 1u;
   prm.skip_v_step = fault.skip_v_step;
   prm.part_m = partial ? partial->m : nullptr;
   prm.part_l = partial ? partial->l : nullptr;

@@ -51,3 +51,31 @@ def test_fault_is_consumed_by_one_call():
     oss.debug_inject_fault(0)  # disarmed again
     oss.attention_fwd(q, k, v)
     assert oss.check_device_error() == 0
+
+
+def test_timeout_stops_the_whole_launch():
+    # a causal launch has one CTA per query tile, 27 waves of CTAs on 152
+    # SMs here; every CTA skips the V tile of its second KV step. The first
+    # timeout is recorded with the launch's tag and the remaining CTAs give
+    # up on their next poll, so the launch ends after about one timeout
+    # (20 ms), not one per wave
+    import time
+    q, k, v = workloads.qkv(1, 32, 16384, 16384, 128, seed=23, device="cuda")
+    assert oss.check_device_error() == 0
+    torch.cuda.synchronize()
+    oss.debug_inject_fault(1, step=1, timeout_ns=20_000_000)
+    t0 = time.perf_counter()
+    oss.attention_fwd(q, k, v, 1 / math.sqrt(128), True)
+    torch.cuda.synchronize()
+    elapsed = time.perf_counter() - t0
+    with pytest.raises(oss.OssError) as info:
+        oss.check_device_error()
+    code = int(str(info.value).split("code ")[1].split(")")[0], 16)
+    assert code & 0xFF == KERNEL_ATTN
+    assert (code >> 8) & 0xFF == SITE_V_FULL
+    assert 1 <= (code >> 16) <= 65535  # the launch tag
+    assert elapsed < 0.3, f"launch took {elapsed:.3f} s after the first timeout"
+    # the context still works
+    o, _ = oss.attention_fwd(q[:, :1, :256].contiguous(), k[:, :1, :256].contiguous(),
+                             v[:, :1, :256].contiguous(), 1 / math.sqrt(128), True)
+    assert oss.check_device_error() == 0
