@@ -63,6 +63,15 @@ def test_causal_shapes(B, H, S):
     check_all_rows(q, k, v, o, lse, scale, True, f"causal {B}x{H}x{S}")
 
 
+@pytest.mark.parametrize("B,H,Sq,Sk", [(3, 40, 300, 300), (2, 90, 130, 77)])
+def test_noncausal_persistent_ragged_tiles(B, H, Sq, Sk):
+    # more query tiles than SMs (360 and 360): each persistent CTA walks
+    # several tiles, most with a ragged last query block and KV tile, so the
+    # hand-over of Q, O and the step counters between tiles is exercised
+    q, k, v, o, lse, scale = run(B, H, Sq, Sk, False, seed=B * 1000 + H + Sk)
+    check_all_rows(q, k, v, o, lse, scale, False, f"persistent {B}x{H}x{Sq}x{Sk}")
+
+
 def test_causal_first_row_is_first_value_and_zero_query_is_mean():
     q, k, v = workloads.qkv(1, 2, 700, 700, 128, seed=3, device="cuda")
     o, lse = oss.attention_fwd(q, k, v, 0.1, causal=True)
