@@ -52,17 +52,17 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # same kernel, applied to the full launch's algorithmic bytes.
 NCU_TRAFFIC = {
     "softmax_32k": {"source": "pass_attention_gb300/csrc/softmax_rows.cu",
-                    "sha256": "0e9f96cd9cc10f643ffb690e7b7d73b654d106e637c003e62039271cf0e9bec7",
-                    "bytes_per_launch": 1073803008 + 1018858752},
+                    "sha256": "e4d707c17a2875b83424d91d3de7b53592a83e4f005016ae395564ca6cb2ad67",
+                    "bytes_per_launch": 1073796096 + 1018313216},
     "softmax_32k_bf16": {"source": "pass_attention_gb300/csrc/softmax_rows.cu",
-                         "sha256": "0e9f96cd9cc10f643ffb690e7b7d73b654d106e637c003e62039271cf0e9bec7",
-                         "bytes_per_launch": 536955392 + 485213440},
+                         "sha256": "e4d707c17a2875b83424d91d3de7b53592a83e4f005016ae395564ca6cb2ad67",
+                         "bytes_per_launch": 536889344 + 484662528},
     "attn_4k": {"source": "pass_attention_gb300/csrc/attn_fwd.cu",
-                "sha256": "f918c254f1c632c15d9052607c3b5f973949364ff1fff49bc4c9a9ef2257bc75",
-                "bytes_per_launch": 201510400 + 46380288},
+                "sha256": "6a7fae67c1b59de4d249a2fb5211a9151cee804edb781aedb26d83e7961897d1",
+                "bytes_per_launch": 201506560 + 46065664},
     "attn_causal": {"source": "pass_attention_gb300/csrc/attn_fwd.cu",
-                    "sha256": "f918c254f1c632c15d9052607c3b5f973949364ff1fff49bc4c9a9ef2257bc75",
-                    "bytes_per_launch": 403565568 + 117761024},
+                    "sha256": "6a7fae67c1b59de4d249a2fb5211a9151cee804edb781aedb26d83e7961897d1",
+                    "bytes_per_launch": 403265280 + 117748992},
     "decode_64x32": {"source": "pass_attention_gb300/csrc/decode_merge.cu",
                      "sha256": "a9116a8452b09df5ffc198fb6fac3fbf559ce1606b95c551b24f75e9f2c2961f",
                      "scale": (2484805000 + 4145664) / (151653 * 32 * 512 + 8 * 32 * 128 * 2
