@@ -316,6 +316,24 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   return d;
 }
 
+// 4 x 4 transpose of 32-bit words among the four lanes 4q .. 4q + 3 of a
+// warp (j = lane % 4): lane j gives a[i] = element (j, i) and gets back
+// a[i] = element (i, j). Two exchange rounds, at lane distance 1 and 2.
+__device__ __forceinline__ void lane_transpose4(uint32_t (&a)[4], int j) {
+  const bool o1 = (j & 1) != 0;
+  uint32_t x = o1 ? a[0] : a[1];
+  uint32_t y = o1 ? a[2] : a[3];
+  x = __shfl_xor_sync(0xffffffffu, x, 1);
+  y = __shfl_xor_sync(0xffffffffu, y, 1);
+  if (o1) { a[0] = x; a[2] = y; } else { a[1] = x; a[3] = y; }
+  const bool o2 = (j & 2) != 0;
+  x = o2 ? a[0] : a[2];
+  y = o2 ? a[1] : a[3];
+  x = __shfl_xor_sync(0xffffffffu, x, 2);
+  y = __shfl_xor_sync(0xffffffffu, y, 2);
+  if (o2) { a[0] = x; a[1] = y; } else { a[2] = x; a[3] = y; }
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t w;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(w) : "f"(hi), "f"(lo));
@@ -586,6 +604,14 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
         const TileInfo t = tile_info(p, lin);
         if (!(ok = wait_bar(smem_addr(&bars.q_full), kt & 1, abort_flag, p.err, kSiteQFull)))
           break;
+        // The previous tile's last P V goes through the tensor pipe before this
+        // tile's first QK^T: its epilogue waits on it, while the softmax has
+        // nothing to do with the new scores until that epilogue is over. (The
+        // wait is exact: the next phase of that o_done needs a QK^T this thread
+        // has not issued.)
+        if (kt > 0 && !(ok = wait_bar(smem_addr(&bars.o_done[(g - 1) % kStages]),
+                                      ((g - 1) / kStages) & 1, abort_flag, p.err, kSiteODone)))
+          break;
         for (int j = 0; j < t.n_kv; ++j, ++g) {
           const int s = g % kStages;  // K stage = score buffer
           if (!(ok = wait_bar(smem_addr(&bars.k_full[s]), (g / kStages) & 1, abort_flag, p.err,
@@ -848,20 +874,32 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
         tc_fence_after();
         const float inv_a = (l_a > 0.f) ? 1.0f / l_a : 0.f;
         const float inv_b = (l_b > 0.f) ? 1.0f / l_b : 0.f;
-        uint32_t* oa = reinterpret_cast<uint32_t*>(p.o + (static_cast<size_t>(t.bh) * p.Sq + row_a) * kD);
-        uint32_t* ob = reinterpret_cast<uint32_t*>(p.o + (static_cast<size_t>(t.bh) * p.Sq + row_b) * kD);
+        // Each 8-column chunk of a row is spread over the row's four threads
+        // (2 columns each); a 4 x 4 transpose among them hands every thread
+        // whole chunks, written with 16-byte stores (whole sectors for each
+        // pair of threads instead of 16-byte pieces).
+        uint4* oa = reinterpret_cast<uint4*>(p.o + (static_cast<size_t>(t.bh) * p.Sq + row_a) * kD);
+        uint4* ob = reinterpret_cast<uint4*>(p.o + (static_cast<size_t>(t.bh) * p.Sq + row_b) * kD);
+        const int jj = lane & 3;
 #pragma unroll 1
         for (int h = 0; h < 2; ++h) {
           uint32_t ov[32];
           tmem_ld16x256_x8(tl + kColO + 64 * h, ov);
           tmem_ld_wait(ov);
 #pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const int col = 64 * h + 8 * k + cq;
-            if (live_a)
-              oa[col >> 1] = pack_bf16x2(__uint_as_float(ov[4 * k]) * inv_a, __uint_as_float(ov[4 * k + 1]) * inv_a);
-            if (live_b)
-              ob[col >> 1] = pack_bf16x2(__uint_as_float(ov[4 * k + 2]) * inv_b, __uint_as_float(ov[4 * k + 3]) * inv_b);
+          for (int mb = 0; mb < 2; ++mb) {
+            uint32_t wa[4], wb[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int k = 4 * mb + i;  // chunk 8 h + k of the row
+              wa[i] = pack_bf16x2(__uint_as_float(ov[4 * k]) * inv_a, __uint_as_float(ov[4 * k + 1]) * inv_a);
+              wb[i] = pack_bf16x2(__uint_as_float(ov[4 * k + 2]) * inv_b, __uint_as_float(ov[4 * k + 3]) * inv_b);
+            }
+            lane_transpose4(wa, jj);
+            lane_transpose4(wb, jj);
+            const int chunk = 8 * h + 4 * mb + jj;
+            if (live_a) oa[chunk] = make_uint4(wa[0], wa[1], wa[2], wa[3]);
+            if (live_b) ob[chunk] = make_uint4(wb[0], wb[1], wb[2], wb[3]);
           }
         }
         if (writes_row && p.lse) {
