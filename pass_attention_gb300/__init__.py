@@ -234,18 +234,55 @@ def softmax_rows_multipass(x: torch.Tensor, passes: int, scale: float = 1.0,
     return y, m, l
 
 
-def softmax_rows_from_host(x_host: torch.Tensor, scale: float = 1.0, out=None, device="cuda"):
+def softmax_rows_from_host(x_host: torch.Tensor, scale: float = 1.0, out=None, device="cuda",
+                           chunk_rows: Optional[int] = None, x_dev: Optional[torch.Tensor] = None,
+                           y_dev: Optional[torch.Tensor] = None):
     """End-to-end call on host memory: copy x to the GPU, run os_softmax_rows,
-    copy y, m and l back into (pinned) host tensors. Returns host (y, m, l)."""
-    x_dev = x_host.to(device, non_blocking=True)
-    y, m, l = softmax_rows(x_dev, scale)
+    copy y, m and l back into (pinned) host tensors. Returns host (y, m, l).
+
+    The rows are processed in blocks of ``chunk_rows`` (default: about 64 MiB
+    of x per block) on three streams: the upload of block i + 1, the kernel
+    on block i and the download of block i - 1 overlap, so the host link
+    carries both directions at once. ``x_dev`` / ``y_dev`` are optional
+    device buffers of x's shape to reuse across calls."""
+    if x_host.dim() != 2 or x_host.dtype != torch.float32 or x_host.is_cuda:
+        raise ValueError("x_host must be a 2-D float32 host tensor")
+    rows, cols = x_host.shape
     if out is None:
-        out = (torch.empty(y.shape, dtype=y.dtype, pin_memory=True),
-               torch.empty(m.shape, dtype=m.dtype, pin_memory=True),
-               torch.empty(l.shape, dtype=l.dtype, pin_memory=True))
-    for dst, src in zip(out, (y, m, l)):
-        dst.copy_(src, non_blocking=True)
-    torch.cuda.current_stream().synchronize()
+        out = (torch.empty((rows, cols), dtype=torch.float32, pin_memory=True),
+               torch.empty(rows, dtype=torch.float32, pin_memory=True),
+               torch.empty(rows, dtype=torch.float32, pin_memory=True))
+    y_host, m_host, l_host = out
+    if x_dev is None:
+        x_dev = torch.empty((rows, cols), dtype=torch.float32, device=device)
+    if y_dev is None:
+        y_dev = torch.empty((rows, cols), dtype=torch.float32, device=device)
+    m_dev = torch.empty(rows, dtype=torch.float32, device=device)
+    l_dev = torch.empty(rows, dtype=torch.float32, device=device)
+    if chunk_rows is None:
+        chunk_rows = max(1, (64 << 20) // max(1, cols * 4))
+    main = torch.cuda.current_stream(x_dev.device)
+    s_in = torch.cuda.Stream(device=x_dev.device)
+    s_out = torch.cuda.Stream(device=x_dev.device)
+    s_in.wait_stream(main)   # buffers may still be in use by earlier work on main
+    s_out.wait_stream(main)
+    for r0 in range(0, rows, chunk_rows):
+        r1 = min(rows, r0 + chunk_rows)
+        with torch.cuda.stream(s_in):
+            x_dev[r0:r1].copy_(x_host[r0:r1], non_blocking=True)
+        main.wait_stream(s_in)
+        softmax_rows(x_dev[r0:r1], scale, y=y_dev[r0:r1], m=m_dev[r0:r1], l=l_dev[r0:r1],
+                     stream=main)
+        s_out.wait_stream(main)
+        with torch.cuda.stream(s_out):
+            y_host[r0:r1].copy_(y_dev[r0:r1], non_blocking=True)
+            m_host[r0:r1].copy_(m_dev[r0:r1], non_blocking=True)
+            l_host[r0:r1].copy_(l_dev[r0:r1], non_blocking=True)
+    main.wait_stream(s_out)
+    for t in (x_dev, y_dev, m_dev, l_dev):
+        t.record_stream(s_in)
+        t.record_stream(s_out)
+    s_out.synchronize()
     return out
 
 

@@ -106,3 +106,14 @@ def test_full_size_softmax_32k_every_row():
         worst = max(worst, check_softmax(y[r0:r0 + step].cpu().numpy(), m[r0:r0 + step].cpu().numpy(),
                                          l[r0:r0 + step].cpu().numpy(), *ref, what=f"rows {r0}+"))
     print(f"softmax_32k worst relative error {worst:.3e}")
+
+
+@pytest.mark.parametrize("rows,cols,chunk", [(1000, 4096, 300), (37, 1000, None), (5, 7, 2)])
+def test_from_host_pipelined_matches_device_call(rows, cols, chunk):
+    # the host-buffer path copies and computes in row blocks on three streams;
+    # every row sees the same kernel, so the results are identical
+    x = workloads.logits(rows, cols, 10.0, seed=rows + cols, device="cuda")
+    y_ref, m_ref, l_ref = oss.softmax_rows(x, 0.5)
+    torch.cuda.synchronize()
+    yh, mh, lh = oss.softmax_rows_from_host(x.cpu().pin_memory(), 0.5, chunk_rows=chunk)
+    assert torch.equal(yh, y_ref.cpu()) and torch.equal(mh, m_ref.cpu()) and torch.equal(lh, l_ref.cpu())
