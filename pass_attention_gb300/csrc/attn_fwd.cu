@@ -19,11 +19,11 @@
 // reference gives the same O / l in exact arithmetic, and weights stay
 // below 256.
 //
-// Non-causal launches are persistent: one CTA of 352 threads per SM walks a
-// share of the 128-row query tiles (work_tile), and loads and QK^T of the
-// next query tile start while the current one finishes. Causal launches use
-// one CTA per query tile (their costs differ; the block scheduler balances
-// them). CTA layout:
+// Launches are persistent: one CTA of 352 threads per SM walks a share of the
+// 128-row query tiles, and loads and QK^T of the next query tile start while
+// the current one finishes. Non-causal tiles follow a round rule (work_tile);
+// causal tiles, whose costs differ, follow a greedy schedule built on the
+// host (tile_of). CTA layout:
 //   * warps 0..7 -- softmax: warp w owns 16 query rows, tensor-memory lanes
 //                   32 (w % 4) + 16 (w / 4) .. + 15; each row's scores are
 //                   spread over four threads (the 16x256b access shape), so
@@ -61,6 +61,10 @@
 
 #include <atomic>
 #include <cstdint>
+#include <functional>
+#include <queue>
+#include <utility>
+#include <vector>
 
 #include "device_common.cuh"
 #include "oss_internal.h"
@@ -415,7 +419,10 @@ struct TileInfo {
 // should share (b, h), so that K and V are read from HBM once and then from
 // L2. Non-causal: (b, h)-major. Causal: groups of kCausalGroup heads,
 // heaviest query tiles first within each group.
-__device__ __forceinline__ TileInfo tile_info(const AttnParams& p, int lin) {
+__host__ __device__ __forceinline__ int imin(int a, int b) { return a < b ? a : b; }
+__host__ __device__ __forceinline__ int imax(int a, int b) { return a > b ? a : b; }
+
+__host__ __device__ __forceinline__ TileInfo tile_info(const AttnParams& p, int lin) {
   int bh, qb;
   if (!p.causal) {
     bh = lin / p.n_qblocks;
@@ -423,7 +430,7 @@ __device__ __forceinline__ TileInfo tile_info(const AttnParams& p, int lin) {
   } else {
     const int per_group = kCausalGroup * p.n_qblocks;
     const int g = lin / per_group;
-    const int gsize = min(kCausalGroup, p.BH - g * kCausalGroup);
+    const int gsize = imin(kCausalGroup, p.BH - g * kCausalGroup);
     const int r = lin - g * per_group;
     const int qb_lin = r / gsize;
     bh = g * kCausalGroup + (r - qb_lin * gsize);
@@ -432,12 +439,12 @@ __device__ __forceinline__ TileInfo tile_info(const AttnParams& p, int lin) {
   TileInfo t;
   t.bh = bh;
   t.q0 = qb * kBM - (p.causal ? kCausalShift : 0);
-  const int kv_end = p.causal ? min(p.Sk, t.q0 + kBM) : p.Sk;
+  const int kv_end = p.causal ? imin(p.Sk, t.q0 + kBM) : p.Sk;
   t.n_kv = (kv_end + kBN - 1) / kBN;
   // KV tiles that reach past the tile's first row touch the diagonal; they
   // are visited first, from the last one down: for a shifted causal tile the
   // first one is masked for all of the tile's first kCausalShift rows.
-  const int diag_first = p.causal ? max(0, t.q0) / kBN : t.n_kv;
+  const int diag_first = p.causal ? imax(0, t.q0) / kBN : t.n_kv;
   t.n_diag = t.n_kv - diag_first;
   return t;
 }
@@ -458,10 +465,39 @@ __device__ __forceinline__ int work_tile(int k, int n_tiles) {
   return lin < n_tiles ? static_cast<int>(lin) : -1;
 }
 
+// Per-CTA lists of query tiles, for causal launches: computed on the host
+// (greedy, heaviest first: the tiles in their launch order, each to the CTA
+// with the least work so far) and passed as a kernel parameter.
+constexpr int kSchedMaxCtas = 160;
+constexpr int kSchedMaxTiles = 15000;
+template <bool kSched>
+struct TileSched {
+  unsigned char unused;
+};
+template <>
+struct TileSched<true> {
+  uint16_t off[kSchedMaxCtas + 1];  // CTA c walks list[off[c] .. off[c + 1])
+  uint16_t list[kSchedMaxTiles];
+};
+
+// The k-th query tile of this CTA, or -1: from the host's lists, or by the
+// round rule of work_tile.
+template <bool kSched>
+__device__ __forceinline__ int tile_of(int k, const AttnParams& p, const TileSched<kSched>& sc) {
+  if constexpr (kSched) {
+    const int b = sc.off[blockIdx.x];
+    return (b + k < static_cast<int>(sc.off[blockIdx.x + 1])) ? static_cast<int>(sc.list[b + k]) : -1;
+  } else {
+    return work_tile(k, p.n_tiles);
+  }
+}
+
+template <bool kSched>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
                 const __grid_constant__ CUtensorMap tmap_k,
-                const __grid_constant__ CUtensorMap tmap_v, const AttnParams p) {
+                const __grid_constant__ CUtensorMap tmap_v, const AttnParams p,
+                const __grid_constant__ TileSched<kSched> sched) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ Barriers bars;
   __shared__ uint32_t tmem_base_slot;
@@ -523,7 +559,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
       int k_issued = 0, v_issued = 0, q_loads = 0, skipped_v = -1;
       int key_row[kStages] = {0, 0, 0}, key_bh[kStages] = {0, 0, 0};
       int kt = 0, j = 0;  // K stream: tile ordinal, step within the tile
-      int lin = work_tile(0, p.n_tiles);
+      int lin = tile_of(0, p, sched);
       TileInfo t{};
       if (lin >= 0) t = tile_info(p, lin);
       for (int g = 0;; ++g) {
@@ -576,7 +612,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
         k_issued = g + 1;
         if (++j == t.n_kv) {
           j = 0;
-          lin = work_tile(++kt, p.n_tiles);
+          lin = tile_of(++kt, p, sched);
           if (lin >= 0) t = tile_info(p, lin);
         }
       }
@@ -599,7 +635,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
       const uint64_t dq = smem_desc(sbase + kOffQ, 16, 1024);
       int g = 0;
       for (int kt = 0; ok; ++kt) {
-        const int lin = work_tile(kt, p.n_tiles);
+        const int lin = tile_of(kt, p, sched);
         if (lin < 0) break;
         const TileInfo t = tile_info(p, lin);
         if (!(ok = wait_bar(smem_addr(&bars.q_full), kt & 1, abort_flag, p.err, kSiteQFull)))
@@ -645,7 +681,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
       const uint32_t d_o = tbase + kColO;
       int g = 0;
       for (int kt = 0; ok; ++kt) {
-        const int lin = work_tile(kt, p.n_tiles);
+        const int lin = tile_of(kt, p, sched);
         if (lin < 0) break;
         const TileInfo t = tile_info(p, lin);
         for (int j = 0; j < t.n_kv; ++j, ++g) {
@@ -692,7 +728,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
     bool ok = true;
     int g = 0;
     for (int kt = 0; ok; ++kt) {
-      const int lin = work_tile(kt, p.n_tiles);
+      const int lin = tile_of(kt, p, sched);
       if (lin < 0) break;
       const TileInfo t = tile_info(p, lin);
       const int row_a = t.q0 + ra, row_b = t.q0 + rb;  // query indices (may be < 0: padding)
@@ -963,6 +999,42 @@ bool make_map(CUtensorMap* map, const uint16_t* base, int S, int BH, int box_row
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Greedy schedule of the causal query tiles over G CTAs: tiles are taken in
+// launch order (groups of heads, heaviest first within a group) and each
+// goes to the CTA with the least work so far, a tile's work being its KV
+// steps plus a fixed fill / drain overhead. Each CTA's list keeps launch
+// order, so the CTAs move through the head groups together (L2 reuse).
+constexpr int kTileOverheadSteps = 3;
+
+bool build_schedule(const AttnParams& prm, int G, TileSched<true>* sc) {
+  const int T = prm.n_tiles;
+  if (T > kSchedMaxTiles || G > kSchedMaxCtas || G < 1) return false;
+  std::vector<int> owner(T);
+  std::vector<int> count(G, 0);
+  using Load = std::pair<long long, int>;  // (work so far, CTA)
+  std::priority_queue<Load, std::vector<Load>, std::greater<Load>> heap;
+  for (int c = 0; c < G; ++c) heap.push({0, c});
+  for (int lin = 0; lin < T; ++lin) {
+    const Load l = heap.top();
+    heap.pop();
+    owner[lin] = l.second;
+    ++count[l.second];
+    heap.push({l.first + tile_info(prm, lin).n_kv + kTileOverheadSteps, l.second});
+  }
+  sc->off[0] = 0;
+  for (int c = 0; c < G; ++c) sc->off[c + 1] = static_cast<uint16_t>(sc->off[c] + count[c]);
+  for (int c = G; c < kSchedMaxCtas; ++c) sc->off[c + 1] = sc->off[G];
+  std::vector<int> pos(sc->off, sc->off + G);
+  for (int lin = 0; lin < T; ++lin) sc->list[pos[owner[lin]]++] = static_cast<uint16_t>(lin);
+  return true;
+}
+
+// The last schedule built by this host thread, reused while the shape stays.
+struct SchedCache {
+  int bh = -1, n_qblocks = -1, sk = -1, grid = -1;
+  TileSched<true> sched;
+};
+
 }  // namespace
 
 cudaError_t launch_attention_fwd(const uint16_t* q, const uint16_t* k, const uint16_t* v,
@@ -976,8 +1048,11 @@ cudaError_t launch_attention_fwd(const uint16_t* q, const uint16_t* k, const uin
   if (!make_map(&mq, q, Sq, BH, kBM) || !make_map(&mk, k, Sk, BH, kBN) ||
       !make_map(&mv, v, Sk, BH, kBN))
     return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       kSmemBytes);
+  cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<false>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(attn_fwd_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kSmemBytes);
   if (e != cudaSuccess) return e;
   AttnParams prm;
   prm.o = o;
@@ -1001,16 +1076,38 @@ cudaError_t launch_attention_fwd(const uint16_t* q, const uint16_t* k, const uin
   const long long tiles = static_cast<long long>(prm.n_qblocks) * BH;
   if (tiles > 0x7fffffffLL) return cudaErrorNotSupported;
   prm.n_tiles = static_cast<int>(tiles);
-  // Non-causal query tiles all cost the same: persistent, one CTA per SM
-  // walking its share. Causal tiles range from 1 to Sk / 128 KV steps; one
-  // CTA per tile, launched heaviest first, lets the block scheduler hand
-  // each freed SM the next tile (measured faster than any static split).
+  // Persistent: one CTA per SM walking its share of the query tiles.
+  // Non-causal tiles all cost the same and follow the round rule; causal
+  // tiles range from 1 to Sk / 128 KV steps and follow a greedy schedule
+  // built here. A causal launch with more tiles than the schedule holds
+  // uses one CTA per tile, and the block scheduler balances them.
   int dev = 0, sms = 0;
   e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
-  const int grid = static_cast<int>((causal || tiles < sms) ? tiles : sms);
-  attn_fwd_kernel<<<static_cast<unsigned>(grid), kThreads, kSmemBytes, stream>>>(mq, mk, mv, prm);
+  const int G = static_cast<int>(tiles < sms ? tiles : sms);
+  if (causal) {
+    thread_local SchedCache cache;
+    const bool hit = cache.bh == BH && cache.n_qblocks == prm.n_qblocks && cache.sk == Sk &&
+                     cache.grid == G;
+    if (hit || build_schedule(prm, G, &cache.sched)) {
+      cache.bh = BH;
+      cache.n_qblocks = prm.n_qblocks;
+      cache.sk = Sk;
+      cache.grid = G;
+      attn_fwd_kernel<true><<<static_cast<unsigned>(G), kThreads, kSmemBytes, stream>>>(
+          mq, mk, mv, prm, cache.sched);
+      return cudaGetLastError();
+    }
+    cache.bh = -1;  // not schedulable: one CTA per tile
+    TileSched<false> none{};
+    attn_fwd_kernel<false><<<static_cast<unsigned>(tiles), kThreads, kSmemBytes, stream>>>(
+        mq, mk, mv, prm, none);
+    return cudaGetLastError();
+  }
+  TileSched<false> none{};
+  attn_fwd_kernel<false><<<static_cast<unsigned>(G), kThreads, kSmemBytes, stream>>>(mq, mk, mv,
+                                                                                     prm, none);
   return cudaGetLastError();
 }
 
