@@ -142,3 +142,22 @@ def test_full_size_attn_causal_sampled_rows():
     got_l = np.array([ln[b, h, i] for b, h, i in rows])
     check_attn(got_o, O, "attn_causal O")
     check_attn(got_l, L, "attn_causal lse")
+
+
+def test_causal_beyond_the_schedule_size():
+    # 8 x 950 heads of 128 queries: 2 causal query tiles per head, 15200 tiles,
+    # more than the host-built schedule holds, so this launch takes one CTA per
+    # tile; the other causal tests run on the schedule
+    B, H, S = 8, 950, 128
+    q, k, v = workloads.qkv(B, H, S, S, 128, seed=29, device="cuda")
+    scale = 1.0 / math.sqrt(128)
+    o, lse = oss.attention_fwd(q, k, v, scale, True)
+    assert oss.check_device_error() == 0
+    rng = np.random.default_rng(29)
+    n = 2048
+    rows = list(zip(rng.integers(0, B, n), rng.integers(0, H, n), rng.integers(0, S, n)))
+    rows += [(b, h, i) for b, h in ((0, 0), (B - 1, H - 1)) for i in (0, 63, 64, 127)]
+    O, L = oracle.attention(f64(q), f64(k), f64(v), scale, True, rows=rows)
+    on, ln = f64(o), f64(lse)
+    check_attn(np.stack([on[b, h, i] for b, h, i in rows]), O, "15200 tiles O")
+    check_attn(np.array([ln[b, h, i] for b, h, i in rows]), L, "15200 tiles lse")

@@ -54,13 +54,14 @@ def test_fault_is_consumed_by_one_call():
 
 
 def test_timeout_stops_the_whole_launch():
-    # a causal launch has one CTA per query tile, 27 waves of CTAs on 152
-    # SMs here; every CTA skips the V tile of its second KV step. The first
-    # timeout is recorded with the launch's tag and the remaining CTAs give
-    # up on their next poll, so the launch ends after about one timeout
+    # a causal launch with more query tiles than the host-built schedule holds
+    # (8 x 950 heads x 3 tiles = 22800) runs one CTA per tile, ~150 waves of
+    # CTAs on 152 SMs; every CTA skips the V tile of its second KV step. The
+    # first timeout is recorded with the launch's tag and the remaining CTAs
+    # give up on their next poll, so the launch ends after about one timeout
     # (20 ms), not one per wave
     import time
-    q, k, v = workloads.qkv(1, 32, 16384, 16384, 128, seed=23, device="cuda")
+    q, k, v = workloads.qkv(8, 950, 256, 256, 128, seed=23, device="cuda")
     assert oss.check_device_error() == 0
     torch.cuda.synchronize()
     oss.debug_inject_fault(1, step=1, timeout_ns=20_000_000)
