@@ -79,7 +79,7 @@ typedef enum os_status {
  *   m, l  [rows] fp32, device, or NULL to skip.
  *   rows  >= 1; cols >= 1; ld_x >= cols, ld_y >= cols (elements).
  *   scale finite and > 0.
- * Alignment: x and y 4-byte aligned. When x and y are 16-byte aligned and
+ * Alignment: x, y, m and l 4-byte aligned. When x and y are 16-byte aligned and
  * ld_x, ld_y are multiples of 4 the kernel uses 16-byte loads and stores and,
  * for cols <= 16384, holds each row in registers (one read, one write per
  * element); otherwise it streams the row twice (two reads, one write).

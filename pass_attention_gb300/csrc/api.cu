@@ -68,7 +68,9 @@ os_status os_softmax_rows(const float* x, float* y, float* m, float* l, int64_t 
   if (rows <= 0 || cols <= 0 || ld_x < cols || ld_y < cols) return OS_ERR_INVALID_ARGUMENT;
   if (cols > (int64_t(1) << 30) || rows > (int64_t(1) << 40)) return OS_ERR_INVALID_ARGUMENT;
   if (!valid_scale(scale)) return OS_ERR_INVALID_ARGUMENT;
-  if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y)) & 3u) return OS_ERR_MISALIGNED;
+  if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y) |
+       reinterpret_cast<uintptr_t>(m) | reinterpret_cast<uintptr_t>(l)) & 3u)
+    return OS_ERR_MISALIGNED;
   return from_cuda(oss::launch_softmax_rows(x, y, m, l, rows, cols, ld_x, ld_y, scale,
                                             static_cast<cudaStream_t>(stream)));
 }

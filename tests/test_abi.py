@@ -59,6 +59,8 @@ def test_softmax_rows_rejects_bad_arguments(lib):
     assert f(A, A, None, None, 4, 8, 8, 8, float("inf"), None) == INVALID
     assert f(A + 2, A, None, None, 4, 8, 8, 8, 1.0, None) == MISALIGNED   # not float-aligned
     assert f(A, A + 1, None, None, 4, 8, 8, 8, 1.0, None) == MISALIGNED
+    assert f(A, A, A + 2, None, 4, 8, 8, 8, 1.0, None) == MISALIGNED   # m not float-aligned
+    assert f(A, A, None, A + 1, 4, 8, 8, 8, 1.0, None) == MISALIGNED   # l
 
 
 def test_softmax_rows_multipass_rejects_bad_arguments(lib):
