@@ -58,11 +58,11 @@ NCU_TRAFFIC = {
                          "sha256": "e4d707c17a2875b83424d91d3de7b53592a83e4f005016ae395564ca6cb2ad67",
                          "bytes_per_launch": 536889344 + 484662528},
     "attn_4k": {"source": "pass_attention_gb300/csrc/attn_fwd.cu",
-                "sha256": "6a7fae67c1b59de4d249a2fb5211a9151cee804edb781aedb26d83e7961897d1",
-                "bytes_per_launch": 201506560 + 46065664},
+                "sha256": "a9a4a0cdd6f6c45ad7f4f5202c481ab685350fa206192746fb71c39f07ed4ca1",
+                "bytes_per_launch": 201511424 + 48596992},
     "attn_causal": {"source": "pass_attention_gb300/csrc/attn_fwd.cu",
-                    "sha256": "6a7fae67c1b59de4d249a2fb5211a9151cee804edb781aedb26d83e7961897d1",
-                    "bytes_per_launch": 403265280 + 117748992},
+                    "sha256": "a9a4a0cdd6f6c45ad7f4f5202c481ab685350fa206192746fb71c39f07ed4ca1",
+                    "bytes_per_launch": 406867712 + 120198400},
     "decode_64x32": {"source": "pass_attention_gb300/csrc/decode_merge.cu",
                      "sha256": "a9116a8452b09df5ffc198fb6fac3fbf559ce1606b95c551b24f75e9f2c2961f",
                      "scale": (2484805000 + 4145664) / (151653 * 32 * 512 + 8 * 32 * 128 * 2
