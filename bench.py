@@ -44,6 +44,8 @@ from pass_attention_gb300 import workloads  # noqa: E402
 
 METRIC = "softmax GB/s & attention fwd TFLOP/s on 1 GB300, as fraction of roofline"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# the GB300's nominal figures, reported beside the measured-peak fractions
+NOMINAL = {"hbm_gbs": 7900.0, "bf16_tflops": 2250.0}
 
 # DRAM traffic per launch from ncu (dram__bytes_read.sum + dram__bytes_write.sum),
 # keyed by workload, with the sha256 of the kernel's source file when it was
@@ -296,7 +298,14 @@ def bench_attention(args, ctx, w):
     total_ms, step_ms, t0, t1 = time_steps(fn, steps, max(3, args.warmup), stream, ctx["barrier"])
     oss.check_device_error()
     flops = attention_flops(w.B, w.H, w.S, w.D, w.causal)
-    return step_ms, flops, (t0, t1)
+    cpu = None
+    if ctx["rank"] == 0 and args.extra_cpu_seconds > 0:
+        rate, cores, rows, full_s = oracle_attention_rate(q, k, v, w, args.extra_cpu_seconds)
+        cpu = {"value": rate, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+               "sample": f"{rows} seeded query rows of 4 heads, 64 at a time, "
+                         f"~{args.extra_cpu_seconds:g} s on {cores} host threads",
+               "extrapolated_full_s": full_s}
+    return step_ms, flops, (t0, t1), cpu
 
 
 def bench_decode(args, ctx):
@@ -329,8 +338,14 @@ def bench_decode(args, ctx):
     nbytes = decode_bytes(kvl, w.H, w.D, S)
     kv_bytes = int(sum(kvl)) * w.H * w.D * 4
     dec_bytes = kv_bytes + w.B * w.H * w.D * 2 + w.B * w.H * S * (w.D + 2) * 4
+    cpu = None
+    if ctx["rank"] == 0 and args.extra_cpu_seconds > 0:
+        rate, cores, rows = oracle_decode_rate(q, k, v, kv, w, args.extra_cpu_seconds)
+        cpu = {"value": rate, "unit": "GB/s (K and V read)", "cores": cores, "kind": "oracle",
+               "sample": f"{rows} seeded (b, h) query rows over their whole kv_len, "
+                         f"~{args.extra_cpu_seconds:g} s on {cores} host threads"}
     del k, v
-    return step_ms, nbytes, dec_ms, dec_bytes, (t0, t1)
+    return step_ms, nbytes, dec_ms, dec_bytes, (t0, t1), cpu
 
 
 # ---------------------------------------------------------------------------
@@ -356,6 +371,66 @@ def oracle_softmax_rate(seconds, x_np=None):
             done_rows += chunk * cores
     dt = time.perf_counter() - t0
     return softmax_bytes(done_rows, w.cols) / dt / 1e9, cores, done_rows
+
+
+def oracle_attention_rate(q, k, v, w, seconds):
+    """Time the fp64 oracle's attention on seeded sample rows of an attention
+    workload (64 query rows at a time, from four heads) on the host cores for
+    about ``seconds``. Returns (TFLOP/s, cores, rows, extrapolated seconds for
+    the whole workload)."""
+    import oracle
+    rng = np.random.default_rng(w.seed)
+    heads = [(int(rng.integers(w.B)), int(rng.integers(w.H))) for _ in range(4)]
+    host = {bh: tuple(t[bh[0]:bh[0] + 1, bh[1]:bh[1] + 1].float().cpu().numpy().astype(np.float64)
+                      for t in (q, k, v)) for bh in heads}
+    cores = os.cpu_count() or 1
+
+    def job(i):
+        qh, kh, vh = host[heads[i % len(heads)]]
+        rows = [(0, 0, (i * 977 + j * 61) % w.S) for j in range(64)]
+        oracle.attention(qh, kh, vh, w.scale, w.causal, rows=rows)
+        return sum(4 * w.D * ((r[2] + 1) if w.causal else w.S) for r in rows)
+
+    flops, n = 0, 0
+    t0 = time.perf_counter()
+    with ThreadPoolExecutor(max_workers=cores) as ex:
+        while time.perf_counter() - t0 < seconds:
+            flops += sum(ex.map(job, range(n, n + cores)))
+            n += cores
+    dt = time.perf_counter() - t0
+    rate = flops / dt / 1e12
+    return rate, cores, n * 64, attention_flops(w.B, w.H, w.S, w.D, w.causal) / (rate * 1e12)
+
+
+def oracle_decode_rate(q, k, v, kv, w, seconds):
+    """Time the fp64 oracle's decode on seeded (b, h) rows of the decode
+    workload on the host cores for about ``seconds``. Returns (GB/s of K and V
+    read, cores, rows)."""
+    import oracle
+    rng = np.random.default_rng(w.seed)
+    kvl = kv.cpu().numpy()
+    pairs = [(int(rng.integers(w.B)), int(rng.integers(w.H))) for _ in range(8)]
+    host = {}
+    for b, h in pairs:
+        L = int(kvl[b])
+        host[(b, h)] = (q[b:b + 1, h:h + 1].float().cpu().numpy().astype(np.float64),
+                        k[b:b + 1, h:h + 1, :L].float().cpu().numpy().astype(np.float64),
+                        v[b:b + 1, h:h + 1, :L].float().cpu().numpy().astype(np.float64), L)
+    cores = os.cpu_count() or 1
+
+    def job(i):
+        qh, kh, vh, L = host[pairs[i % len(pairs)]]
+        oracle.decode(qh, kh, vh, np.array([L]), w.scale)
+        return L * w.D * 2 * 2
+
+    nbytes, n = 0, 0
+    t0 = time.perf_counter()
+    with ThreadPoolExecutor(max_workers=cores) as ex:
+        while time.perf_counter() - t0 < seconds:
+            nbytes += sum(ex.map(job, range(n, n + cores)))
+            n += cores
+    dt = time.perf_counter() - t0
+    return nbytes / dt / 1e9, cores, n
 
 
 def run_reference(args, rank):
@@ -402,6 +477,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--headline-only", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--extra-cpu-seconds", type=float, default=3.0,
+                    help="oracle time beside each attention / decode extra (rank 0)")
     ap.add_argument("--ref-step-seconds", type=float, default=2.0,
                     help="oracle time per step of --impl reference")
     args = ap.parse_args()
@@ -466,6 +543,8 @@ def main():
                     "roofline": {"bound": "hbm", "achieved": moved_gbs, "peak": pk["hbm_gbs"],
                                  "unit": "GB/s", "frac": moved_gbs / pk["hbm_gbs"],
                                  "traffic": None, "peak_kind": f"{pk_kind} HBM copy",
+                                 "nominal_peak": NOMINAL["hbm_gbs"],
+                                 "frac_nominal": moved_gbs / NOMINAL["hbm_gbs"],
                                  "note": "achieved counts every sweep's bytes"},
                     "window": win}
             except Exception as e:
@@ -479,13 +558,14 @@ def main():
                 "roofline": {"bound": "hbm", "kernel": "softmax_rows16_reg_kernel<bf16,4>",
                              "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
                              "frac": gbs / pk["hbm_gbs"], "traffic": traffic_for("softmax_32k_bf16"),
-                             "peak_kind": f"{pk_kind} HBM copy"},
+                             "peak_kind": f"{pk_kind} HBM copy", "nominal_peak": NOMINAL["hbm_gbs"],
+                             "frac_nominal": gbs / NOMINAL["hbm_gbs"]},
                 "window": win}
         except Exception as e:
             extra["softmax_32k_bf16"] = {"unavailable": f"{type(e).__name__}: {e}"}
         for aw in (workloads.ATTN_4K, workloads.ATTN_CAUSAL):
             try:
-                ms, flops, win = bench_attention(args, ctx, aw)
+                ms, flops, win, cpu_a = bench_attention(args, ctx, aw)
                 tf = flops / (ms / 1e3) / 1e12
                 extra[aw.name] = {
                     "value": tf, "unit": "TFLOP/s", "ms_per_step": ms,
@@ -493,12 +573,15 @@ def main():
                     "roofline": {"bound": "tensor", "achieved": tf, "peak": pk["bf16_tflops"],
                                  "unit": "TFLOP/s", "frac": tf / pk["bf16_tflops"],
                                  "traffic": traffic_for(aw.name),
-                                 "peak_kind": f"{pk_kind} bf16 dense (burst)"},
+                                 "peak_kind": f"{pk_kind} bf16 dense (burst)",
+                                 "nominal_peak": NOMINAL["bf16_tflops"],
+                                 "frac_nominal": tf / NOMINAL["bf16_tflops"]},
+                    "cpu_baseline": cpu_a,
                     "window": win}
             except Exception as e:  # report, do not hide
                 extra[aw.name] = {"unavailable": f"{type(e).__name__}: {e}"}
         try:
-            ms, nbytes, dec_ms, dec_bytes, win = bench_decode(args, ctx)
+            ms, nbytes, dec_ms, dec_bytes, win, cpu_d = bench_decode(args, ctx)
             gbs = nbytes / (ms / 1e3) / 1e9
             ach = dec_bytes / (dec_ms / 1e3) / 1e9
             extra["decode_64x32"] = {
@@ -507,7 +590,10 @@ def main():
                 "roofline": {"bound": "hbm", "kernel": "decode_splitkv_kernel", "achieved": ach,
                              "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": ach / pk["hbm_gbs"],
                              "traffic": traffic_for("decode_64x32", dec_bytes),
-                             "peak_kind": f"{pk_kind} HBM copy"},
+                             "peak_kind": f"{pk_kind} HBM copy",
+                             "nominal_peak": NOMINAL["hbm_gbs"],
+                             "frac_nominal": ach / NOMINAL["hbm_gbs"]},
+                "cpu_baseline": cpu_d,
                 "window": win}
         except Exception as e:
             extra["decode_64x32"] = {"unavailable": f"{type(e).__name__}: {e}"}
@@ -538,7 +624,9 @@ def main():
         "gpu_launches": args.steps,
         "roofline": {"bound": "hbm", "kernel": kname, "achieved": achieved, "peak": pk["hbm_gbs"],
                      "unit": "GB/s", "frac": achieved / pk["hbm_gbs"],
-                     "traffic": traffic_for(w.name), "peak_kind": f"{pk_kind} HBM copy"},
+                     "traffic": traffic_for(w.name), "peak_kind": f"{pk_kind} HBM copy",
+                     "nominal_peak": NOMINAL["hbm_gbs"],
+                     "frac_nominal": achieved / NOMINAL["hbm_gbs"]},
         "cpu_baseline": cpu,
         "extra": extra,
     }
