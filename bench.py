@@ -59,6 +59,14 @@ NCU_TRAFFIC = {
     "softmax_32k_bf16": {"source": "pass_attention_gb300/csrc/softmax_rows.cu",
                          "sha256": "e4d707c17a2875b83424d91d3de7b53592a83e4f005016ae395564ca6cb2ad67",
                          "bytes_per_launch": 536889344 + 484662528},
+    # the comparators: all sweeps of one call (each reads x from DRAM again)
+    "softmax_32k_3pass": {"source": "pass_attention_gb300/csrc/softmax_rows.cu",
+                          "sha256": "e4d707c17a2875b83424d91d3de7b53592a83e4f005016ae395564ca6cb2ad67",
+                          "bytes_per_launch": (1073840896 + 2963968) + (1073957376 + 169216)
+                          + (1074188288 + 1024787968)},
+    "softmax_32k_2pass": {"source": "pass_attention_gb300/csrc/softmax_rows.cu",
+                          "sha256": "e4d707c17a2875b83424d91d3de7b53592a83e4f005016ae395564ca6cb2ad67",
+                          "bytes_per_launch": (1073760512 + 2718208) + (1074039808 + 1024710912)},
     "attn_4k": {"source": "pass_attention_gb300/csrc/attn_fwd.cu",
                 "sha256": "a9a4a0cdd6f6c45ad7f4f5202c481ab685350fa206192746fb71c39f07ed4ca1",
                 "bytes_per_launch": 201511424 + 48596992},
@@ -542,7 +550,7 @@ def main():
                     "hbm_bytes_per_step": moved,
                     "roofline": {"bound": "hbm", "achieved": moved_gbs, "peak": pk["hbm_gbs"],
                                  "unit": "GB/s", "frac": moved_gbs / pk["hbm_gbs"],
-                                 "traffic": None, "peak_kind": f"{pk_kind} HBM copy",
+                                 "traffic": traffic_for(name), "peak_kind": f"{pk_kind} HBM copy",
                                  "nominal_peak": NOMINAL["hbm_gbs"],
                                  "frac_nominal": moved_gbs / NOMINAL["hbm_gbs"],
                                  "note": "achieved counts every sweep's bytes"},
