@@ -301,15 +301,14 @@ __device__ __forceinline__ void tmem_st16x256_x8(uint32_t taddr, const uint32_t 
       : "memory");
 }
 
-// 16 lanes x 64 columns (shape 16x128b, 16 repetitions). Thread t writes,
+// 16 lanes x 32 columns (shape 16x128b, 8 repetitions). Thread t writes,
 // for repetition k, column 4k + t%4 of lane t/4 from r[2k] and of lane
 // 8 + t/4 from r[2k+1].
-__device__ __forceinline__ void tmem_st16x128_x16(uint32_t taddr, const uint32_t (&r)[32]) {
+__device__ __forceinline__ void tmem_st16x128_x8(uint32_t taddr, const uint32_t (&r)[16]) {
   asm volatile(
-      "tcgen05.st.sync.aligned.16x128b.x16.b32 [%0], "
-      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
-      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
-      OSS_W8(0), OSS_W8(8), OSS_W8(16), OSS_W8(24)
+      "tcgen05.st.sync.aligned.16x128b.x8.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+      OSS_W8(0), OSS_W8(8)
       : "memory");
 }
 
@@ -401,7 +400,8 @@ struct Barriers {
   uint64_t q_full;   // Q tile landed
   uint64_t q_free;   // every QK^T of the tile in the Q buffer is done
   uint64_t k_full[kStages], v_full[kStages];
-  uint64_t s_full[kSBuf], p_ready[kSBuf];
+  uint64_t s_full[kSBuf];
+  uint64_t p_ready[2][kSBuf];  // P of keys 0..63 / 64..127 written (the two halves of P V)
   uint64_t o_done[kSBuf];  // P V done, for the steps of each buffer (keeps parity waits exact)
   uint64_t o_free;   // the epilogue has read O out of tensor memory
   uint64_t drain[2];  // one per issuing thread
@@ -518,7 +518,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
     }
     for (int b = 0; b < kSBuf; ++b) {
       mbar_init(smem_addr(&bars.s_full[b]), 1);
-      mbar_init(smem_addr(&bars.p_ready[b]), kSoftThreads);
+      mbar_init(smem_addr(&bars.p_ready[0][b]), kSoftThreads);
+      mbar_init(smem_addr(&bars.p_ready[1][b]), kSoftThreads);
       mbar_init(smem_addr(&bars.o_done[b]), 1);
     }
     mbar_init(smem_addr(&bars.o_free), kSoftThreads);
@@ -689,20 +690,26 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
           if (!(ok = wait_bar(smem_addr(&bars.v_full[s]), (g / kStages) & 1, abort_flag, p.err,
                               kSiteVFull)))
             break;
-          if (!(ok = wait_bar(smem_addr(&bars.p_ready[s]), (g / kStages) & 1, abort_flag, p.err,
-                              kSitePReady)))
-            break;
           if (j == 0 && kt > 0 &&
               !(ok = wait_bar(smem_addr(&bars.o_free), (kt - 1) & 1, abort_flag, p.err,
                               kSiteOFree)))
             break;
-          tc_fence_after();
+          // the two halves of P V (keys 0..63, 64..127) start as soon as the
+          // softmax has written the matching half of P
           const uint64_t dv = smem_desc(sbase + kOffV + s * kTile, kHalf, 1024);
           const uint32_t a_p = tbase + col_s(s);
 #pragma unroll
-          for (int kk = 0; kk < kBN / 16; ++kk)
-            mma_ts(d_o, a_p + kk * 8, dv + static_cast<uint64_t>(kk * (2048 >> 4)), kIdescPV,
-                   (j > 0 || kk > 0) ? 1u : 0u);
+          for (int hp = 0; hp < 2; ++hp) {
+            if (!(ok = wait_bar(smem_addr(&bars.p_ready[hp][s]), (g / kStages) & 1, abort_flag,
+                                p.err, kSitePReady)))
+              break;
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 4 * hp; kk < 4 * hp + 4; ++kk)
+              mma_ts(d_o, a_p + kk * 8, dv + static_cast<uint64_t>(kk * (2048 >> 4)), kIdescPV,
+                     (j > 0 || kk > 0) ? 1u : 0u);
+          }
+          if (!ok) break;
           tc_commit(smem_addr(&bars.o_done[s]));  // buffer s and V stage s free
         }
       }
@@ -804,28 +811,6 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
           m_a = mnew_a;
           m_b = mnew_b;
         }
-        // P = 2^(S C - m), the -inf guard subtracting 0 for an empty row; bf16
-        // pairs (keys c, c + 1) go to packed column c / 2 = 4 (8 h + k) + t % 4,
-        // which is where the 16x128b shape puts repetition 8 h + k of thread t
-        const float2 Cv = make_float2(C, C);
-        const float2 mva = make_float2(-((m_a == neg_inf()) ? 0.f : m_a), -((m_a == neg_inf()) ? 0.f : m_a));
-        const float2 mvb = make_float2(-((m_b == neg_inf()) ? 0.f : m_b), -((m_b == neg_inf()) ? 0.f : m_b));
-        float2 acc_a = make_float2(0.f, 0.f), acc_b = acc_a;
-        uint32_t pk[32];
-#pragma unroll
-        for (int kk = 0; kk < 16; ++kk) {
-          const float2 ta = __ffma2_rn(make_float2(sa[2 * kk], sa[2 * kk + 1]), Cv, mva);
-          const float2 tb = __ffma2_rn(make_float2(sb[2 * kk], sb[2 * kk + 1]), Cv, mvb);
-          const float2 ea = make_float2(ex2(ta.x), ex2(ta.y));
-          const float2 eb = make_float2(ex2(tb.x), ex2(tb.y));
-          acc_a = __fadd2_rn(acc_a, ea);
-          acc_b = __fadd2_rn(acc_b, eb);
-          pk[2 * kk] = pack_bf16x2(ea.x, ea.y);
-          pk[2 * kk + 1] = pack_bf16x2(eb.x, eb.y);
-        }
-        tmem_st16x128_x16(tl + colS, pk);
-        l_a = fmaf(l_a, corr_a, acc_a.x + acc_a.y);
-        l_b = fmaf(l_b, corr_b, acc_b.x + acc_b.y);
         if (rescale && j > 0) {
           // O still holds the previous tiles' sum: wait for P_{j-1} V (whose
           // completion implies every earlier one), then rescale this warp's rows
@@ -852,9 +837,38 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
             tmem_st16x256_x8(tl + kColO + 64 * h, ov);
           }
         }
-        tmem_st_wait();
-        tc_fence_before();
-        mbar_arrive(smem_addr(&bars.p_ready[b]));
+        // P = 2^(S C - m), the -inf guard subtracting 0 for an empty row, in two
+        // halves of 64 keys; each half is released to P V as soon as it is in
+        // tensor memory (the O rescale above is complete by then: the first
+        // tcgen05.wait::st covers it). bf16 pairs (keys c, c + 1) go to packed
+        // column c / 2 = 32 h + 4 k + t % 4, where the 16x128b shape puts
+        // repetition k of thread t when it writes packed columns 32 h .. + 31.
+        const float2 Cv = make_float2(C, C);
+        const float2 mva = make_float2(-((m_a == neg_inf()) ? 0.f : m_a), -((m_a == neg_inf()) ? 0.f : m_a));
+        const float2 mvb = make_float2(-((m_b == neg_inf()) ? 0.f : m_b), -((m_b == neg_inf()) ? 0.f : m_b));
+        float2 acc_a = make_float2(0.f, 0.f), acc_b = acc_a;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const int kk = 8 * h + k;
+            const float2 ta = __ffma2_rn(make_float2(sa[2 * kk], sa[2 * kk + 1]), Cv, mva);
+            const float2 tb = __ffma2_rn(make_float2(sb[2 * kk], sb[2 * kk + 1]), Cv, mvb);
+            const float2 ea = make_float2(ex2(ta.x), ex2(ta.y));
+            const float2 eb = make_float2(ex2(tb.x), ex2(tb.y));
+            acc_a = __fadd2_rn(acc_a, ea);
+            acc_b = __fadd2_rn(acc_b, eb);
+            pk[2 * k] = pack_bf16x2(ea.x, ea.y);
+            pk[2 * k + 1] = pack_bf16x2(eb.x, eb.y);
+          }
+          tmem_st16x128_x8(tl + colS + 32 * h, pk);
+          tmem_st_wait();
+          tc_fence_before();
+          mbar_arrive(smem_addr(&bars.p_ready[h][b]));
+        }
+        l_a = fmaf(l_a, corr_a, acc_a.x + acc_a.y);
+        l_b = fmaf(l_b, corr_b, acc_b.x + acc_b.y);
       }
       // the row sums: the four threads of a row add their shares
       l_a += __shfl_xor_sync(0xffffffffu, l_a, 1);
