@@ -254,9 +254,32 @@ def bench_softmax(args, ctx):
     e.record()
     torch.cuda.synchronize()
     e2e_ms = s.elapsed_time(e) / e2e_steps
+    # the host link on this machine: plain pinned copies of the same buffers, both
+    # directions at once (the e2e step cannot beat this)
+    s_up, s_dn = torch.cuda.Stream(), torch.cuda.Stream()
+
+    def both():
+        with torch.cuda.stream(s_up):
+            x.copy_(xh, non_blocking=True)
+        with torch.cuda.stream(s_dn):
+            outs[0].copy_(y, non_blocking=True)
+
+    both()
+    torch.cuda.synchronize()
+    cur = torch.cuda.current_stream()
+    s.record()
+    for _ in range(5):
+        s_up.wait_stream(cur)
+        s_dn.wait_stream(cur)
+        both()
+        cur.wait_stream(s_up)
+        cur.wait_stream(s_dn)
+    e.record()
+    torch.cuda.synchronize()
+    link_gbs = 2 * w.rows * w.cols * 4 * 5 / (s.elapsed_time(e) / 1e3) / 1e9
     del xh, outs
     return {"workload": w, "total_ms": total_ms, "step_ms": step_ms, "t0": t0, "t1": t1,
-            "nbytes": nbytes, "e2e_ms": e2e_ms, "h2d": w.rows * w.cols * 4,
+            "nbytes": nbytes, "e2e_ms": e2e_ms, "link_gbs": link_gbs, "h2d": w.rows * w.cols * 4,
             "d2h": w.rows * w.cols * 4 + 2 * w.rows * 4}
 
 
@@ -628,7 +651,10 @@ def main():
                    "l2": "inputs larger than L2 (1 GiB per step), no flush"},
         "clocks": clocks,
         "e2e": {"value": sm["nbytes"] * n / (e2e_ms / 1e3) / 1e9, "unit": "GB/s",
-                "h2d_bytes_per_step": sm["h2d"], "d2h_bytes_per_step": sm["d2h"]},
+                "h2d_bytes_per_step": sm["h2d"], "d2h_bytes_per_step": sm["d2h"],
+                "host_link_gbs": sm["link_gbs"],
+                "frac_of_host_link": (sm["nbytes"] / (e2e_ms / 1e3) / 1e9) / sm["link_gbs"],
+                "note": "host_link_gbs: pinned H2D + D2H copies of the same buffers, both at once"},
         "gpu_launches": args.steps,
         "roofline": {"bound": "hbm", "kernel": kname, "achieved": achieved, "peak": pk["hbm_gbs"],
                      "unit": "GB/s", "frac": achieved / pk["hbm_gbs"],
