@@ -68,11 +68,11 @@ NCU_TRAFFIC = {
                           "sha256": "e4d707c17a2875b83424d91d3de7b53592a83e4f005016ae395564ca6cb2ad67",
                           "bytes_per_launch": (1073760512 + 2718208) + (1074039808 + 1024710912)},
     "attn_4k": {"source": "pass_attention_gb300/csrc/attn_fwd.cu",
-                "sha256": "a9a4a0cdd6f6c45ad7f4f5202c481ab685350fa206192746fb71c39f07ed4ca1",
-                "bytes_per_launch": 201511424 + 48596992},
+                "sha256": "45466cc319abf9067313e3aa1e97fe5f82a53b78ab4ce5482765f5e8b634de2a",
+                "bytes_per_launch": 201508608 + 47728896},
     "attn_causal": {"source": "pass_attention_gb300/csrc/attn_fwd.cu",
-                    "sha256": "a9a4a0cdd6f6c45ad7f4f5202c481ab685350fa206192746fb71c39f07ed4ca1",
-                    "bytes_per_launch": 406867712 + 120198400},
+                    "sha256": "45466cc319abf9067313e3aa1e97fe5f82a53b78ab4ce5482765f5e8b634de2a",
+                    "bytes_per_launch": 405676288 + 119841024},
     "decode_64x32": {"source": "pass_attention_gb300/csrc/decode_merge.cu",
                      "sha256": "a9116a8452b09df5ffc198fb6fac3fbf559ce1606b95c551b24f75e9f2c2961f",
                      "scale": (2484805000 + 4145664) / (151653 * 32 * 512 + 8 * 32 * 128 * 2
