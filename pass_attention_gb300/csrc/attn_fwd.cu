@@ -52,9 +52,10 @@
 // case the -inf guard exists for.
 //
 // Every wait on an mbarrier is bounded: on timeout the thread raises a
-// CTA-wide abort flag and writes the device error word; all roles then drain
-// their own in-flight copies and MMAs (again with a bound), and tensor memory
-// is released before the CTA exits.
+// CTA-wide abort flag and writes the device error word (tagged with the
+// launch, so the launch's other CTAs stop too); all roles then drain their
+// own in-flight copies and MMAs (again with a bound), and tensor memory is
+// released before the CTA exits.
 
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -96,8 +97,9 @@ constexpr int kOffV = kOffK + kStages * kTile;
 constexpr int kOffEnd = kOffV + kStages * kTile;   // 224 KB
 constexpr int kSmemBytes = kOffEnd + 1024;         // + alignment slack
 
-// tensor-memory columns (512 fp32 x 128 lanes): S_0 | S_1 | S_2 | O. KV step j
-// uses score buffer j % 3; P_j (bf16 pairs) is written over its first half.
+// tensor-memory columns (512 fp32 x 128 lanes): S_0 | S_1 | S_2 | O. KV step g
+// (counted across the CTA's query tiles) uses score buffer g % 3; P_g (bf16
+// pairs) is written over its first half.
 constexpr int kSBuf = 3;
 static_assert(kSBuf == kStages, "K/V ring stage and score buffer share one index");
 constexpr uint32_t kTmemCols = 512;
