@@ -48,33 +48,33 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 NOMINAL = {"hbm_gbs": 7900.0, "bf16_tflops": 2250.0}
 
 # DRAM traffic per launch from ncu (dram__bytes_read.sum + dram__bytes_write.sum),
-# keyed by workload, with the sha256 of the kernel's source file when it was
-# captured: a changed source reports null. Summaries live under profiles/.
+# keyed by workload, with the sha256 of the kernel source's code (comments and
+# blank lines removed) when it was captured: changed code reports null. Summaries live under profiles/.
 # "scale" records traffic / algorithmic bytes of a smaller capture of the
 # same kernel, applied to the full launch's algorithmic bytes.
 NCU_TRAFFIC = {
     "softmax_32k": {"source": "pass_attention_gb300/csrc/softmax_rows.cu",
-                    "sha256": "e4d707c17a2875b83424d91d3de7b53592a83e4f005016ae395564ca6cb2ad67",
+                    "sha256": "71a29c1c352470f7b735a5b444e9ec7bc2c8ccc530c3d5f0deb9d33cb16f0ecd",
                     "bytes_per_launch": 1073796096 + 1018313216},
     "softmax_32k_bf16": {"source": "pass_attention_gb300/csrc/softmax_rows.cu",
-                         "sha256": "e4d707c17a2875b83424d91d3de7b53592a83e4f005016ae395564ca6cb2ad67",
+                         "sha256": "71a29c1c352470f7b735a5b444e9ec7bc2c8ccc530c3d5f0deb9d33cb16f0ecd",
                          "bytes_per_launch": 536889344 + 484662528},
     # the comparators: all sweeps of one call (each reads x from DRAM again)
     "softmax_32k_3pass": {"source": "pass_attention_gb300/csrc/softmax_rows.cu",
-                          "sha256": "e4d707c17a2875b83424d91d3de7b53592a83e4f005016ae395564ca6cb2ad67",
+                          "sha256": "71a29c1c352470f7b735a5b444e9ec7bc2c8ccc530c3d5f0deb9d33cb16f0ecd",
                           "bytes_per_launch": (1073840896 + 2963968) + (1073957376 + 169216)
                           + (1074188288 + 1024787968)},
     "softmax_32k_2pass": {"source": "pass_attention_gb300/csrc/softmax_rows.cu",
-                          "sha256": "e4d707c17a2875b83424d91d3de7b53592a83e4f005016ae395564ca6cb2ad67",
+                          "sha256": "71a29c1c352470f7b735a5b444e9ec7bc2c8ccc530c3d5f0deb9d33cb16f0ecd",
                           "bytes_per_launch": (1073760512 + 2718208) + (1074039808 + 1024710912)},
     "attn_4k": {"source": "pass_attention_gb300/csrc/attn_fwd.cu",
-                "sha256": "45466cc319abf9067313e3aa1e97fe5f82a53b78ab4ce5482765f5e8b634de2a",
+                "sha256": "8a240dd167034436ed1d94b177e2ad0232747422fbe14a93e6eb75a0438a9488",
                 "bytes_per_launch": 201508608 + 47728896},
     "attn_causal": {"source": "pass_attention_gb300/csrc/attn_fwd.cu",
-                    "sha256": "45466cc319abf9067313e3aa1e97fe5f82a53b78ab4ce5482765f5e8b634de2a",
+                    "sha256": "8a240dd167034436ed1d94b177e2ad0232747422fbe14a93e6eb75a0438a9488",
                     "bytes_per_launch": 405676288 + 119841024},
     "decode_64x32": {"source": "pass_attention_gb300/csrc/decode_merge.cu",
-                     "sha256": "a9116a8452b09df5ffc198fb6fac3fbf559ce1606b95c551b24f75e9f2c2961f",
+                     "sha256": "0d345bb183c174c3248d68638b3899f9499e35b1a5ceb04884c68dbc28755393",
                      "scale": (2484805000 + 4145664) / (151653 * 32 * 512 + 8 * 32 * 128 * 2
                                                          + 8 * 32 * 16 * 130 * 4)},
 }
@@ -95,8 +95,15 @@ def peaks():
 
 
 def source_sha(rel):
-    with open(os.path.join(ROOT, rel), "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()
+    """sha256 of a kernel source with its comments and blank lines removed,
+    so that a comment edit keeps the ncu figures taken of the same code."""
+    import re
+    with open(os.path.join(ROOT, rel)) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    lines = [re.sub(r"//.*$", "", ln).rstrip() for ln in text.splitlines()]
+    code = "\n".join(ln for ln in lines if ln.strip())
+    return hashlib.sha256(code.encode()).hexdigest()
 
 
 def traffic_for(workload, algorithmic_bytes=None):
