@@ -68,11 +68,11 @@ NCU_TRAFFIC = {
                           "sha256": "71a29c1c352470f7b735a5b444e9ec7bc2c8ccc530c3d5f0deb9d33cb16f0ecd",
                           "bytes_per_launch": (1073760512 + 2718208) + (1074039808 + 1024710912)},
     "attn_4k": {"source": "pass_attention_gb300/csrc/attn_fwd.cu",
-                "sha256": "8a240dd167034436ed1d94b177e2ad0232747422fbe14a93e6eb75a0438a9488",
-                "bytes_per_launch": 201508608 + 47728896},
+                "sha256": "1de91f1a14f7b69059f99bd37628b4126df733c28a5f205b034826a15235ccec",
+                "bytes_per_launch": 201502976 + 47736320},
     "attn_causal": {"source": "pass_attention_gb300/csrc/attn_fwd.cu",
-                    "sha256": "8a240dd167034436ed1d94b177e2ad0232747422fbe14a93e6eb75a0438a9488",
-                    "bytes_per_launch": 405676288 + 119841024},
+                    "sha256": "1de91f1a14f7b69059f99bd37628b4126df733c28a5f205b034826a15235ccec",
+                    "bytes_per_launch": 406748672 + 119554048},
     "decode_64x32": {"source": "pass_attention_gb300/csrc/decode_merge.cu",
                      "sha256": "0d345bb183c174c3248d68638b3899f9499e35b1a5ceb04884c68dbc28755393",
                      "scale": (2484805000 + 4145664) / (151653 * 32 * 512 + 8 * 32 * 128 * 2

@@ -1064,12 +1064,21 @@ cudaError_t launch_attention_fwd(const uint16_t* q, const uint16_t* k, const uin
   if (!make_map(&mq, q, Sq, BH, kBM) || !make_map(&mk, k, Sk, BH, kBN) ||
       !make_map(&mv, v, Sk, BH, kBN))
     return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<false>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(attn_fwd_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kSmemBytes);
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
+  // the kernels' shared-memory limit, raised once per device
+  constexpr int kMaxDevices = 64;
+  static std::atomic<bool> smem_set[kMaxDevices];
+  if (dev < 0 || dev >= kMaxDevices || !smem_set[dev].load(std::memory_order_acquire)) {
+    e = cudaFuncSetAttribute(attn_fwd_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kSmemBytes);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(attn_fwd_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               kSmemBytes);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < kMaxDevices) smem_set[dev].store(true, std::memory_order_release);
+  }
   AttnParams prm;
   prm.o = o;
   prm.lse = lse;
@@ -1097,9 +1106,8 @@ cudaError_t launch_attention_fwd(const uint16_t* q, const uint16_t* k, const uin
   // tiles range from 1 to Sk / 128 KV steps and follow a greedy schedule
   // built here. A causal launch with more tiles than the schedule holds
   // uses one CTA per tile, and the block scheduler balances them.
-  int dev = 0, sms = 0;
-  e = cudaGetDevice(&dev);
-  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  int sms = 0;
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
   const int G = static_cast<int>(tiles < sms ? tiles : sms);
   if (causal) {
