@@ -23,6 +23,7 @@ oracle on the host cores on bounded samples of the same workload.
 from __future__ import annotations
 
 import argparse
+import collections
 import hashlib
 import json
 import math
@@ -190,9 +191,13 @@ def device_index_for_smi(local_rank):
     return local_rank
 
 
+Timing = collections.namedtuple("Timing", "total_ms mean_ms median_ms t0 t1")
+
+
 def time_steps(fn, steps, warmup, stream, barrier):
-    """W untimed calls, then K timed calls with per-step events. Returns
-    (total_ms, mean_step_ms, t_wall0, t_wall1)."""
+    """W untimed calls, then K timed calls with per-step events. Returns a
+    Timing: the K-step total, the mean and median step (ms), and the wall
+    clock at both ends."""
     for _ in range(warmup):
         fn()
     torch.cuda.synchronize()
@@ -209,7 +214,7 @@ def time_steps(fn, steps, warmup, stream, barrier):
     t1 = time.time()
     barrier()
     per = [ev[i].elapsed_time(ev[i + 1]) for i in range(steps)]
-    return ev[0].elapsed_time(ev[steps]), sum(per) / len(per), t0, t1
+    return Timing(ev[0].elapsed_time(ev[steps]), sum(per) / len(per), statistics.median(per), t0, t1)
 
 
 # ---------------------------------------------------------------------------
@@ -244,7 +249,8 @@ def bench_softmax(args, ctx):
     l = torch.empty(w.rows, device="cuda")
     stream = torch.cuda.current_stream()
     fn = lambda: oss.softmax_rows(x, w.scale, y=y, m=m, l=l, stream=stream)
-    total_ms, step_ms, t0, t1 = time_steps(fn, args.steps, args.warmup, stream, ctx["barrier"])
+    total_ms, step_ms, median_ms, t0, t1 = time_steps(fn, args.steps, args.warmup, stream,
+                                                      ctx["barrier"])
     nbytes = softmax_bytes(w.rows, w.cols)
     # end to end: pinned host input -> device -> kernel -> pinned host outputs
     xh = x.cpu().pin_memory()
@@ -285,7 +291,8 @@ def bench_softmax(args, ctx):
     torch.cuda.synchronize()
     link_gbs = 2 * w.rows * w.cols * 4 * 5 / (s.elapsed_time(e) / 1e3) / 1e9
     del xh, outs
-    return {"workload": w, "total_ms": total_ms, "step_ms": step_ms, "t0": t0, "t1": t1,
+    return {"workload": w, "total_ms": total_ms, "step_ms": step_ms, "median_ms": median_ms,
+            "t0": t0, "t1": t1,
             "nbytes": nbytes, "e2e_ms": e2e_ms, "link_gbs": link_gbs, "h2d": w.rows * w.cols * 4,
             "d2h": w.rows * w.cols * 4 + 2 * w.rows * 4}
 
@@ -303,9 +310,9 @@ def bench_softmax_multipass(args, ctx, passes):
     stream = torch.cuda.current_stream()
     fn = lambda: oss.softmax_rows_multipass(x, passes, w.scale, y=y, m=m, l=l, stream=stream)
     steps = max(3, min(args.steps, 30))
-    total_ms, step_ms, t0, t1 = time_steps(fn, steps, max(3, args.warmup), stream, ctx["barrier"])
+    tm = time_steps(fn, steps, max(3, args.warmup), stream, ctx["barrier"])
     moved = w.rows * w.cols * 4 * (passes + 1) + w.rows * 4 * (2 * passes + 2)
-    return step_ms, moved, (t0, t1)
+    return tm, moved
 
 
 def bench_softmax16(args, ctx):
@@ -320,9 +327,9 @@ def bench_softmax16(args, ctx):
     stream = torch.cuda.current_stream()
     fn = lambda: oss.softmax_rows_16bit(x, w.scale, y=y, m=m, l=l, stream=stream)
     steps = max(3, min(args.steps, 50))
-    total_ms, step_ms, t0, t1 = time_steps(fn, steps, max(3, args.warmup), stream, ctx["barrier"])
+    tm = time_steps(fn, steps, max(3, args.warmup), stream, ctx["barrier"])
     nbytes = w.rows * w.cols * 2 * 2 + w.rows * 4 * 2
-    return step_ms, nbytes, (t0, t1)
+    return tm, nbytes
 
 
 def bench_attention(args, ctx, w):
@@ -333,7 +340,7 @@ def bench_attention(args, ctx, w):
     stream = torch.cuda.current_stream()
     fn = lambda: oss.attention_fwd(q, k, v, w.scale, w.causal, o=o, lse=lse, stream=stream)
     steps = max(3, min(args.steps, 50))
-    total_ms, step_ms, t0, t1 = time_steps(fn, steps, max(3, args.warmup), stream, ctx["barrier"])
+    tm = time_steps(fn, steps, max(3, args.warmup), stream, ctx["barrier"])
     oss.check_device_error()
     flops = attention_flops(w.B, w.H, w.S, w.D, w.causal)
     cpu = None
@@ -343,7 +350,7 @@ def bench_attention(args, ctx, w):
                "sample": f"{rows} seeded query rows of 4 heads, 64 at a time, "
                          f"~{args.extra_cpu_seconds:g} s on {cores} host threads",
                "extrapolated_full_s": full_s}
-    return step_ms, flops, (t0, t1), cpu
+    return tm, flops, cpu
 
 
 def bench_decode(args, ctx):
@@ -363,7 +370,7 @@ def bench_decode(args, ctx):
         oss.merge_partials(pm, pl, po, True, o, mo, lo, lseo, stream=stream)
 
     steps = max(3, min(args.steps, 30))
-    total_ms, step_ms, t0, t1 = time_steps(fn, steps, max(3, args.warmup), stream, ctx["barrier"])
+    tm = time_steps(fn, steps, max(3, args.warmup), stream, ctx["barrier"])
     # the decode kernel alone (dominant): events around it only
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * steps)]
     for i in range(steps):
@@ -383,7 +390,7 @@ def bench_decode(args, ctx):
                "sample": f"{rows} seeded (b, h) query rows over their whole kv_len, "
                          f"~{args.extra_cpu_seconds:g} s on {cores} host threads"}
     del k, v
-    return step_ms, nbytes, dec_ms, dec_bytes, (t0, t1), cpu
+    return tm, nbytes, dec_ms, dec_bytes, cpu
 
 
 # ---------------------------------------------------------------------------
@@ -571,11 +578,13 @@ def main():
         for passes in (3, 2):
             name = f"softmax_32k_{passes}pass"
             try:
-                ms, moved, win = bench_softmax_multipass(args, ctx, passes)
+                tm, moved = bench_softmax_multipass(args, ctx, passes)
+                ms = tm.mean_ms
                 moved_gbs = moved / (ms / 1e3) / 1e9
                 extra[name] = {
                     "value": sm["nbytes"] / (ms / 1e3) / 1e9, "unit": "GB/s",
-                    "ms_per_step": ms, "one_pass_speedup": ms / sm["step_ms"],
+                    "ms_per_step": ms, "ms_per_step_median": tm.median_ms,
+                    "one_pass_speedup": ms / sm["step_ms"],
                     "workload": f"{w.rows}x{w.cols} fp32, os_softmax_rows_multipass passes={passes}",
                     "hbm_bytes_per_step": moved,
                     "roofline": {"bound": "hbm", "achieved": moved_gbs, "peak": pk["hbm_gbs"],
@@ -584,29 +593,32 @@ def main():
                                  "nominal_peak": NOMINAL["hbm_gbs"],
                                  "frac_nominal": moved_gbs / NOMINAL["hbm_gbs"],
                                  "note": "achieved counts every sweep's bytes"},
-                    "window": win}
+                    "window": (tm.t0, tm.t1)}
             except Exception as e:
                 extra[name] = {"unavailable": f"{type(e).__name__}: {e}"}
         try:
-            ms, nbytes, win = bench_softmax16(args, ctx)
+            tm, nbytes = bench_softmax16(args, ctx)
+            ms = tm.mean_ms
             gbs = nbytes / (ms / 1e3) / 1e9
             extra["softmax_32k_bf16"] = {
-                "value": gbs, "unit": "GB/s", "ms_per_step": ms,
+                "value": gbs, "unit": "GB/s", "ms_per_step": ms, "ms_per_step_median": tm.median_ms,
                 "workload": f"{w.rows}x{w.cols} bf16 rows (y bf16, m and l fp32), os_softmax_rows_16bit",
                 "roofline": {"bound": "hbm", "kernel": "softmax_rows16_reg_kernel<bf16,4>",
                              "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
                              "frac": gbs / pk["hbm_gbs"], "traffic": traffic_for("softmax_32k_bf16"),
                              "peak_kind": f"{pk_kind} HBM copy", "nominal_peak": NOMINAL["hbm_gbs"],
                              "frac_nominal": gbs / NOMINAL["hbm_gbs"]},
-                "window": win}
+                "window": (tm.t0, tm.t1)}
         except Exception as e:
             extra["softmax_32k_bf16"] = {"unavailable": f"{type(e).__name__}: {e}"}
         for aw in (workloads.ATTN_4K, workloads.ATTN_CAUSAL):
             try:
-                ms, flops, win, cpu_a = bench_attention(args, ctx, aw)
+                tm, flops, cpu_a = bench_attention(args, ctx, aw)
+                ms = tm.mean_ms
                 tf = flops / (ms / 1e3) / 1e12
                 extra[aw.name] = {
                     "value": tf, "unit": "TFLOP/s", "ms_per_step": ms,
+                    "ms_per_step_median": tm.median_ms,
                     "workload": f"B{aw.B} H{aw.H} S{aw.S} D{aw.D} bf16 {'causal' if aw.causal else 'non-causal'}",
                     "roofline": {"bound": "tensor", "achieved": tf, "peak": pk["bf16_tflops"],
                                  "unit": "TFLOP/s", "frac": tf / pk["bf16_tflops"],
@@ -615,15 +627,16 @@ def main():
                                  "nominal_peak": NOMINAL["bf16_tflops"],
                                  "frac_nominal": tf / NOMINAL["bf16_tflops"]},
                     "cpu_baseline": cpu_a,
-                    "window": win}
+                    "window": (tm.t0, tm.t1)}
             except Exception as e:  # report, do not hide
                 extra[aw.name] = {"unavailable": f"{type(e).__name__}: {e}"}
         try:
-            ms, nbytes, dec_ms, dec_bytes, win, cpu_d = bench_decode(args, ctx)
+            tm, nbytes, dec_ms, dec_bytes, cpu_d = bench_decode(args, ctx)
+            ms = tm.mean_ms
             gbs = nbytes / (ms / 1e3) / 1e9
             ach = dec_bytes / (dec_ms / 1e3) / 1e9
             extra["decode_64x32"] = {
-                "value": gbs, "unit": "GB/s", "ms_per_step": ms,
+                "value": gbs, "unit": "GB/s", "ms_per_step": ms, "ms_per_step_median": tm.median_ms,
                 "workload": "B64 H32 D128 bf16, kv_len~U{1..32768}, 16 splits, decode + merge",
                 "roofline": {"bound": "hbm", "kernel": "decode_splitkv_kernel", "achieved": ach,
                              "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": ach / pk["hbm_gbs"],
@@ -632,7 +645,7 @@ def main():
                              "nominal_peak": NOMINAL["hbm_gbs"],
                              "frac_nominal": ach / NOMINAL["hbm_gbs"]},
                 "cpu_baseline": cpu_d,
-                "window": win}
+                "window": (tm.t0, tm.t1)}
         except Exception as e:
             extra["decode_64x32"] = {"unavailable": f"{type(e).__name__}: {e}"}
 
@@ -651,7 +664,8 @@ def main():
 
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": n, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+        "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
+        "ms_per_step_median": sm["median_ms"], "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": f"{w.name} {w.rows}x{w.cols} fp32 N(0,1)*{w.mult:g}, scale {w.scale:g}",
                    "rows": w.rows, "cols": w.cols, "per_rank": "one full matrix per rank",
