@@ -55,19 +55,19 @@ NOMINAL = {"hbm_gbs": 7900.0, "bf16_tflops": 2250.0}
 # same kernel, applied to the full launch's algorithmic bytes.
 NCU_TRAFFIC = {
     "softmax_32k": {"source": "pass_attention_gb300/csrc/softmax_rows.cu",
-                    "sha256": "71a29c1c352470f7b735a5b444e9ec7bc2c8ccc530c3d5f0deb9d33cb16f0ecd",
-                    "bytes_per_launch": 1073796096 + 1018313216},
+                    "sha256": "299978f16ab23a3f0d44622f16f84ae3a1b0cc1fa0874d6777bf815033f0bf85",
+                    "bytes_per_launch": 1073781248 + 1017929472},
     "softmax_32k_bf16": {"source": "pass_attention_gb300/csrc/softmax_rows.cu",
-                         "sha256": "71a29c1c352470f7b735a5b444e9ec7bc2c8ccc530c3d5f0deb9d33cb16f0ecd",
-                         "bytes_per_launch": 536889344 + 484662528},
+                         "sha256": "299978f16ab23a3f0d44622f16f84ae3a1b0cc1fa0874d6777bf815033f0bf85",
+                         "bytes_per_launch": 536906752 + 482694656},
     # the comparators: all sweeps of one call (each reads x from DRAM again)
     "softmax_32k_3pass": {"source": "pass_attention_gb300/csrc/softmax_rows.cu",
-                          "sha256": "71a29c1c352470f7b735a5b444e9ec7bc2c8ccc530c3d5f0deb9d33cb16f0ecd",
-                          "bytes_per_launch": (1073840896 + 2963968) + (1073957376 + 169216)
-                          + (1074188288 + 1024787968)},
+                          "sha256": "299978f16ab23a3f0d44622f16f84ae3a1b0cc1fa0874d6777bf815033f0bf85",
+                          "bytes_per_launch": (1073762048 + 2868224) + (1073899264 + 177664)
+                          + (1074052352 + 1024664832)},
     "softmax_32k_2pass": {"source": "pass_attention_gb300/csrc/softmax_rows.cu",
-                          "sha256": "71a29c1c352470f7b735a5b444e9ec7bc2c8ccc530c3d5f0deb9d33cb16f0ecd",
-                          "bytes_per_launch": (1073760512 + 2718208) + (1074039808 + 1024710912)},
+                          "sha256": "299978f16ab23a3f0d44622f16f84ae3a1b0cc1fa0874d6777bf815033f0bf85",
+                          "bytes_per_launch": (1073761280 + 2997504) + (1074095360 + 1024706048)},
     "attn_4k": {"source": "pass_attention_gb300/csrc/attn_fwd.cu",
                 "sha256": "1de91f1a14f7b69059f99bd37628b4126df733c28a5f205b034826a15235ccec",
                 "bytes_per_launch": 201502976 + 47736320},
@@ -330,6 +330,31 @@ def bench_softmax16(args, ctx):
     tm = time_steps(fn, steps, max(3, args.warmup), stream, ctx["barrier"])
     nbytes = w.rows * w.cols * 2 * 2 + w.rows * 4 * 2
     return tm, nbytes
+
+
+def bench_softmax_lengths(args, ctx):
+    """os_softmax_rows / os_softmax_rows_16bit over row lengths from 128 to
+    16384 at 2^28 elements per matrix (1 GiB fp32, 512 MiB 16-bit: larger
+    than L2). Returns {dtype: {cols: (ms per call, algorithmic bytes)}}."""
+    import pass_attention_gb300 as oss
+    out = {}
+    stream = torch.cuda.current_stream()
+    for name, dtype in (("fp32", torch.float32), ("bf16", torch.bfloat16), ("fp16", torch.float16)):
+        out[name] = {}
+        for cols in (128, 512, 1024, 2048, 4096, 8192, 16384):
+            rows = (1 << 28) // cols
+            x = workloads.logits(rows, cols, 10.0, 7 + ctx["rank"], device="cuda").to(dtype)
+            y = torch.empty_like(x)
+            m = torch.empty(rows, device="cuda")
+            l = torch.empty(rows, device="cuda")
+            if dtype == torch.float32:
+                fn = lambda: oss.softmax_rows(x, 1.0, y=y, m=m, l=l, stream=stream)
+            else:
+                fn = lambda: oss.softmax_rows_16bit(x, 1.0, y=y, m=m, l=l, stream=stream)
+            tm = time_steps(fn, 10, 3, stream, ctx["barrier"])
+            out[name][cols] = (tm.mean_ms, rows * cols * 2 * x.element_size() + rows * 8)
+            del x, y
+    return out
 
 
 def bench_attention(args, ctx, w):
@@ -603,7 +628,8 @@ def main():
             extra["softmax_32k_bf16"] = {
                 "value": gbs, "unit": "GB/s", "ms_per_step": ms, "ms_per_step_median": tm.median_ms,
                 "workload": f"{w.rows}x{w.cols} bf16 rows (y bf16, m and l fp32), os_softmax_rows_16bit",
-                "roofline": {"bound": "hbm", "kernel": "softmax_rows16_reg_kernel<bf16,4>",
+                "roofline": {"bound": "hbm",
+                             "kernel": "softmax_rows_grouped_kernel<bf16, 256 threads a row, 4 chunks, prefetch>",
                              "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
                              "frac": gbs / pk["hbm_gbs"], "traffic": traffic_for("softmax_32k_bf16"),
                              "peak_kind": f"{pk_kind} HBM copy", "nominal_peak": NOMINAL["hbm_gbs"],
@@ -611,6 +637,19 @@ def main():
                 "window": (tm.t0, tm.t1)}
         except Exception as e:
             extra["softmax_32k_bf16"] = {"unavailable": f"{type(e).__name__}: {e}"}
+        try:
+            lens = bench_softmax_lengths(args, ctx)
+            extra["softmax_row_lengths"] = {
+                "unit": "GB/s",
+                "workload": "2^28 elements per matrix, N(0,1)*10 logits, scale 1; cols 128..16384",
+                "peak": pk["hbm_gbs"], "peak_kind": f"{pk_kind} HBM copy",
+                "value": {d: {str(c): nb / (ms / 1e3) / 1e9 for c, (ms, nb) in v.items()}
+                          for d, v in lens.items()},
+                "frac": {d: {str(c): nb / (ms / 1e3) / 1e9 / pk["hbm_gbs"] for c, (ms, nb) in v.items()}
+                         for d, v in lens.items()},
+            }
+        except Exception as e:
+            extra["softmax_row_lengths"] = {"unavailable": f"{type(e).__name__}: {e}"}
         for aw in (workloads.ATTN_4K, workloads.ATTN_CAUSAL):
             try:
                 tm, flops, cpu_a = bench_attention(args, ctx, aw)

@@ -6,10 +6,13 @@
 // every exponential, the rescale factor included (roadmapper "Things that
 // break": mixing bases is one of the listed failures).
 //
-// Register-resident path (cols <= 16384): one CTA of 256 threads per row.
-// Each thread loads its slice of the row once with 16-byte streaming loads,
+// Register-resident path: rows of up to 2048 fp32 (16384 16-bit) elements go
+// to the grouped kernel below, where a group of 32-256 threads owns a row and
+// a CTA works on several rows at once; longer fp32 rows of up to 16384
+// elements take one CTA of 256 threads per row. In both, each thread loads
+// its slice of the row once with 16-byte streaming loads,
 // keeps it in registers, forms its own partial state (m_t, l_t, p_t) and the
-// CTA merges the 256 partial states with the merge identity (warp shuffles,
+// row's threads merge their partial states with the merge identity (warp shuffles,
 // then one shared-memory round) -- the merge the curionode page calls
 // associative, used here in place of a second pass over HBM. The weights p
 // are then rescaled in registers and written once: 4 bytes read and 4 bytes
@@ -480,97 +483,237 @@ __device__ __forceinline__ uint4 out8(const uint4& v, float M, float inv, const 
                     out2<kType>(v.z, M, inv, k), out2<kType>(v.w, M, inv, k));
 }
 
-// Register-resident 16-bit rows (cols <= 16384): each thread loads its slice
-// once (NV 16-byte chunks of 8 elements), widens it to fp32 and replaces it
-// by its weights relative to the thread's own maximum (packed FMAs, one ex2
-// per element); the CTA merges the threads' (max, sum) states and each thread
-// scales its weights by 2^(M_t - M_row) / l_row for the single write (2 bytes
-// read and 2 written per element).
-template <int kType, int NV>
-__global__ void __launch_bounds__(kThreads, (NV <= 4) ? 4 : 2)
-softmax_rows16_reg_kernel(const uint16_t* __restrict__ x, uint16_t* __restrict__ y,
-                          float* __restrict__ m_out, float* __restrict__ l_out, int64_t rows,
-                          int cols, int64_t ld_x, int64_t ld_y, ScaleConsts k) {
-  __shared__ float2 sh[kWarps];
-  const int nfull = cols >> 3;
-  const int tail = cols & 7;
+// ---------------------------------------------------------------------------
+// Grouped rows: one kernel for fp32, bf16 and fp16 rows that are 16-byte
+// aligned and fit in registers. A group of TPR threads (32, 64, 128 or 256)
+// owns one row at a time, so a CTA of 256 threads works on 256 / TPR rows
+// and short rows keep as many bytes in flight per SM as long ones. A chunk is
+// 16 bytes: 4 fp32 or 8 16-bit elements; each thread holds NV chunks.
+//
+// Per row: the thread's maximum, its weights 2^(x*c - M_t) (packed FMAs, one
+// ex2 per element), the merge of the group's (max, sum) states in n-ary form
+// (warp shuffles, then shared memory between the group's warps), then each
+// weight scaled by 2^(M_t - M_row) / l_row and written once. With kPrefetch
+// the grid is persistent and the next row's chunks are loaded into registers
+// before the current row is reduced, so a group's loads overlap its own
+// arithmetic and stores.
+// kKind: 0 = fp32, 1 = bf16, 2 = fp16.
+// ---------------------------------------------------------------------------
+
+template <int kKind>
+struct RowElem {
+  static constexpr int kEpc = (kKind == 0) ? 4 : 8;  // elements per 16-byte chunk
+  static constexpr int kSize = (kKind == 0) ? 4 : 2;  // bytes per element
+};
+
+template <int kKind>
+__device__ __forceinline__ uint32_t neg_inf_word() {
+  return (kKind == 0) ? 0xff800000u : h16_neg_inf2<kKind>();
+}
+
+// Chunk c of a row: 16 bytes when complete, else the row's last elements
+// padded with -inf (and -inf beyond the row).
+template <int kKind>
+__device__ __forceinline__ uint4 load_chunk16(const char* xr, int c, int nfull, int tail) {
+  if (c < nfull) return __ldcs(reinterpret_cast<const uint4*>(xr) + c);
+  uint32_t wd[4];
+#pragma unroll
+  for (int h = 0; h < 4; ++h) wd[h] = neg_inf_word<kKind>();
+  if (c == nfull && tail) {
+    if (kKind == 0) {
+      const uint32_t* p = reinterpret_cast<const uint32_t*>(xr) + 4 * c;
+#pragma unroll
+      for (int e = 0; e < 3; ++e)
+        if (e < tail) wd[e] = p[e];
+    } else {
+      const uint16_t* p = reinterpret_cast<const uint16_t*>(xr) + 8 * c;
+#pragma unroll
+      for (int e = 0; e < 7; ++e)
+        if (e < tail)
+          wd[e >> 1] = (e & 1) ? ((wd[e >> 1] & 0xffffu) | (uint32_t(p[e]) << 16))
+                               : ((wd[e >> 1] & 0xffff0000u) | uint32_t(p[e]));
+    }
+  }
+  return make_uint4(wd[0], wd[1], wd[2], wd[3]);
+}
+
+template <int kKind>
+__device__ __forceinline__ void store_chunk16(char* yr, int c, int nfull, int tail, const uint4& o) {
+  if (c < nfull) {
+    __stcs(reinterpret_cast<uint4*>(yr) + c, o);
+  } else if (c == nfull && tail) {
+    const uint32_t wd[4] = {o.x, o.y, o.z, o.w};
+    if (kKind == 0) {
+      uint32_t* p = reinterpret_cast<uint32_t*>(yr) + 4 * c;
+#pragma unroll
+      for (int e = 0; e < 3; ++e)
+        if (e < tail) p[e] = wd[e];
+    } else {
+      uint16_t* p = reinterpret_cast<uint16_t*>(yr) + 8 * c;
+#pragma unroll
+      for (int e = 0; e < 7; ++e)
+        if (e < tail) p[e] = static_cast<uint16_t>((e & 1) ? (wd[e >> 1] >> 16) : (wd[e >> 1] & 0xffffu));
+    }
+  }
+}
+
+// the chunk's elements widened to fp32 (exact), as pairs
+template <int kKind>
+__device__ __forceinline__ void unpack_chunk16(const uint4& v, float2* w /* [kEpc / 2] */) {
+  if (kKind == 0) {
+    w[0] = make_float2(__uint_as_float(v.x), __uint_as_float(v.y));
+    w[1] = make_float2(__uint_as_float(v.z), __uint_as_float(v.w));
+  } else {
+    w[0] = make_float2(h16_lo<kKind>(v.x), h16_hi<kKind>(v.x));
+    w[1] = make_float2(h16_lo<kKind>(v.y), h16_hi<kKind>(v.y));
+    w[2] = make_float2(h16_lo<kKind>(v.z), h16_hi<kKind>(v.z));
+    w[3] = make_float2(h16_lo<kKind>(v.w), h16_hi<kKind>(v.w));
+  }
+}
+
+// the chunk's weights times f, in the row's type (one rounding for 16-bit)
+template <int kKind>
+__device__ __forceinline__ uint4 pack_chunk16(const float2* w, float2 f) {
+  if (kKind == 0) {
+    const float2 a = __fmul2_rn(w[0], f);
+    const float2 b = __fmul2_rn(w[1], f);
+    return make_uint4(__float_as_uint(a.x), __float_as_uint(a.y), __float_as_uint(b.x),
+                      __float_as_uint(b.y));
+  } else {
+    uint32_t o[4];
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+      const float2 q = __fmul2_rn(w[h], f);
+      o[h] = h16_pack<kKind>(q.x, q.y);
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
+__device__ __forceinline__ void group_barrier(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Merge of the (xm, ls) states of the TPR threads that own one row; returns
+// the row state in all of them. The n-ary form of cta_merge, over TPR / 32
+// warps whose states meet in sh[] (one entry per warp of the CTA) behind a
+// barrier of the group's own threads.
+template <int TPR>
+__device__ __forceinline__ void group_merge(float& xm, float& ls, const ScaleConsts& k,
+                                            float2* sh, int g) {
+  float xw = xm;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) xw = fmaxf(xw, __shfl_xor_sync(0xffffffffu, xw, off));
+  float lw = (xm == neg_inf()) ? 0.f : ls * ex2(base2_of(xm, k) - base2_of(xw, k));
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) lw += __shfl_xor_sync(0xffffffffu, lw, off);
+  if (TPR == 32) {
+    xm = xw;
+    ls = lw;
+    return;
+  }
+  constexpr int kW = TPR / 32;
+  if ((threadIdx.x & 31) == 0) sh[threadIdx.x >> 5] = make_float2(xw, lw);
+  if (TPR == kThreads)
+    __syncthreads();
+  else
+    group_barrier(1 + g, TPR);
+  const float2* s = sh + g * kW;
+  float x = s[0].x;
+#pragma unroll
+  for (int w = 1; w < kW; ++w) x = fmaxf(x, s[w].x);
+  float l = 0.f;
+  if (x != neg_inf()) {
+    const float M = base2_of(x, k);
+#pragma unroll
+    for (int w = 0; w < kW; ++w) {
+      const float2 e = s[w];
+      if (e.x != neg_inf()) l += e.y * ex2(base2_of(e.x, k) - M);
+    }
+  }
+  xm = x;
+  ls = l;
+}
+
+template <int kKind, int TPR, int NV, bool kPrefetch, int kMinBlocks>
+__global__ void __launch_bounds__(kThreads, kMinBlocks)
+softmax_rows_grouped_kernel(const void* __restrict__ x, void* __restrict__ y,
+                            float* __restrict__ m_out, float* __restrict__ l_out, int64_t rows,
+                            int cols, int64_t ld_x, int64_t ld_y, ScaleConsts k) {
+  constexpr int kEpc = RowElem<kKind>::kEpc;
+  constexpr int kEsz = RowElem<kKind>::kSize;
+  constexpr int kGroups = kThreads / TPR;
+  // two sets of per-warp states: a warp may start the next row's merge
+  // while the group's slower warps still read this row's, and a set is not
+  // written again until every warp of the group has passed the barrier
+  // of the row in between
+  __shared__ float2 sh[2][kWarps];
   const int tid = threadIdx.x;
-  for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
-    const uint16_t* xr = x + row * ld_x;
-    uint16_t* yr = y + row * ld_y;
-    float2 w[NV][4];
+  const int g = tid / TPR;
+  const int t = tid % TPR;
+  const int nfull = cols / kEpc;
+  const int tail = cols % kEpc;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * kGroups;
+  int64_t row = static_cast<int64_t>(blockIdx.x) * kGroups + g;
+  const char* xb = static_cast<const char*>(x);
+  char* yb = static_cast<char*>(y);
+
+  uint4 nx[NV];
+  if (kPrefetch && row < rows) {
+    const char* xr = xb + row * ld_x * kEsz;
 #pragma unroll
-    for (int i = 0; i < NV; ++i) {
-      const int c8 = tid + i * kThreads;
-      uint4 v;
-      if (c8 < nfull) {
-        v = __ldcs(reinterpret_cast<const uint4*>(xr) + c8);
-      } else {
-        uint32_t wd[4];
+    for (int i = 0; i < NV; ++i) nx[i] = load_chunk16<kKind>(xr, t + i * TPR, nfull, tail);
+  }
+  int buf = 0;
+  for (; row < rows; row += stride) {
+    float2 w[NV][kEpc / 2];
+    if (kPrefetch) {
 #pragma unroll
-        for (int h = 0; h < 4; ++h) wd[h] = h16_neg_inf2<kType>();
-        if (c8 == nfull && tail) {
-          const uint16_t* p = xr + 8 * c8;
+      for (int i = 0; i < NV; ++i) unpack_chunk16<kKind>(nx[i], w[i]);
+      const int64_t next = row + stride;
+      if (next < rows) {
+        const char* xr = xb + next * ld_x * kEsz;
 #pragma unroll
-          for (int e = 0; e < 7; ++e)
-            if (e < tail)
-              wd[e >> 1] = (e & 1) ? ((wd[e >> 1] & 0xffffu) | (uint32_t(p[e]) << 16))
-                                   : ((wd[e >> 1] & 0xffff0000u) | uint32_t(p[e]));
-        }
-        v = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+        for (int i = 0; i < NV; ++i) nx[i] = load_chunk16<kKind>(xr, t + i * TPR, nfull, tail);
       }
-      w[i][0] = make_float2(h16_lo<kType>(v.x), h16_hi<kType>(v.x));
-      w[i][1] = make_float2(h16_lo<kType>(v.y), h16_hi<kType>(v.y));
-      w[i][2] = make_float2(h16_lo<kType>(v.z), h16_hi<kType>(v.z));
-      w[i][3] = make_float2(h16_lo<kType>(v.w), h16_hi<kType>(v.w));
+    } else {
+      const char* xr = xb + row * ld_x * kEsz;
+#pragma unroll
+      for (int i = 0; i < NV; ++i) unpack_chunk16<kKind>(load_chunk16<kKind>(xr, t + i * TPR, nfull, tail), w[i]);
     }
-    float xa = neg_inf(), xb = neg_inf();
+    float xa = neg_inf(), xc = neg_inf();
 #pragma unroll
     for (int i = 0; i < NV; ++i) {
-      xa = fmax3(xa, w[i][0].x, w[i][0].y);
-      xb = fmax3(xb, w[i][1].x, w[i][1].y);
-      xa = fmax3(xa, w[i][2].x, w[i][2].y);
-      xb = fmax3(xb, w[i][3].x, w[i][3].y);
+#pragma unroll
+      for (int h = 0; h < kEpc / 2; h += 2) {
+        xa = fmax3(xa, w[i][h].x, w[i][h].y);
+        if (h + 1 < kEpc / 2) xc = fmax3(xc, w[i][h + 1].x, w[i][h + 1].y);
+      }
     }
-    float xm = fmaxf(xa, xb);
+    float xm = fmaxf(xa, xc);
     const float Mt = (xm == neg_inf()) ? 0.f : base2_of(xm, k);
     const float2 negM = make_float2(-Mt, -Mt);
     float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
     for (int i = 0; i < NV; ++i) {
 #pragma unroll
-      for (int h = 0; h < 4; ++h) {
+      for (int h = 0; h < kEpc / 2; ++h) {
         w[i][h] = weight2(w[i][h], negM, k);
         acc = __fadd2_rn(acc, w[i][h]);
       }
     }
     float ls = acc.x + acc.y;
     const float xm_t = xm;
-    cta_merge(xm, ls, k, sh);
+    group_merge<TPR>(xm, ls, k, sh[buf], g);
     float f = 0.f;
     if (xm_t != neg_inf() && ls > 0.f)
       f = ex2(base2_of(xm_t, k) - base2_of(xm, k)) * (1.0f / ls);
     const float2 f2 = make_float2(f, f);
+    char* yr = yb + row * ld_y * kEsz;
 #pragma unroll
-    for (int i = 0; i < NV; ++i) {
-      const int c8 = tid + i * kThreads;
-      uint32_t o[4];
-#pragma unroll
-      for (int h = 0; h < 4; ++h) {
-        const float2 q = __fmul2_rn(w[i][h], f2);
-        o[h] = h16_pack<kType>(q.x, q.y);
-      }
-      if (c8 < nfull) {
-        __stcs(reinterpret_cast<uint4*>(yr) + c8, make_uint4(o[0], o[1], o[2], o[3]));
-      } else if (c8 == nfull && tail) {
-        uint16_t* p = yr + 8 * c8;
-#pragma unroll
-        for (int e = 0; e < 7; ++e)
-          if (e < tail) p[e] = static_cast<uint16_t>((e & 1) ? (o[e >> 1] >> 16) : (o[e >> 1] & 0xffffu));
-      }
-    }
-    if (tid == 0) write_ml(xm, ls, k, row, m_out, l_out);
-    __syncthreads();
+    for (int i = 0; i < NV; ++i) store_chunk16<kKind>(yr, t + i * TPR, nfull, tail, pack_chunk16<kKind>(w[i], f2));
+    if (t == 0) write_ml(xm, ls, k, row, m_out, l_out);
+    buf ^= 1;
   }
 }
 
@@ -628,11 +771,15 @@ softmax_rows16_stream_kernel(const uint16_t* __restrict__ x, uint16_t* __restric
   }
 }
 
-int grid_for(int64_t rows, int ctas_per_sm) {
+int sm_count() {
   int dev = 0, sms = 148;
   if (cudaGetDevice(&dev) == cudaSuccess)
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const int64_t cap = static_cast<int64_t>(sms) * ctas_per_sm * 64;
+  return sms;
+}
+
+int grid_for(int64_t rows, int ctas_per_sm) {
+  const int64_t cap = static_cast<int64_t>(sm_count()) * ctas_per_sm * 64;
   return static_cast<int>(rows < cap ? rows : cap);
 }
 
@@ -665,6 +812,19 @@ ScaleConsts make_consts(float scale) {
 
 }  // namespace
 
+// Launch of softmax_rows_grouped_kernel: persistent (one wave of kMinBlocks
+// CTAs per SM) when it prefetches, else up to 64 waves of a grid-stride loop.
+template <int kKind, int TPR, int NV, bool kPrefetch, int kMinBlocks>
+void launch_grouped(const void* x, void* y, float* m, float* l, int64_t rows, int cols,
+                    int64_t ld_x, int64_t ld_y, const ScaleConsts& k, cudaStream_t stream) {
+  constexpr int kGroups = kThreads / TPR;
+  const int64_t need = (rows + kGroups - 1) / kGroups;
+  const int64_t cap = static_cast<int64_t>(sm_count()) * kMinBlocks * (kPrefetch ? 1 : 64);
+  const int g = static_cast<int>(need < cap ? need : cap);
+  softmax_rows_grouped_kernel<kKind, TPR, NV, kPrefetch, kMinBlocks>
+      <<<g, kThreads, 0, stream>>>(x, y, m, l, rows, cols, ld_x, ld_y, k);
+}
+
 cudaError_t launch_softmax_rows(const float* x, float* y, float* m, float* l, int64_t rows,
                                 int64_t cols, int64_t ld_x, int64_t ld_y, float scale,
                                 cudaStream_t stream) {
@@ -679,10 +839,19 @@ cudaError_t launch_softmax_rows(const float* x, float* y, float* m, float* l, in
   const int64_t chunks = (cols + 3) / 4;
   const int nv = static_cast<int>((chunks + kThreads - 1) / kThreads);
   const int c = static_cast<int>(cols);
-  if (nv <= 1) {
-    softmax_rows_reg_kernel<1><<<grid_for(rows, 4), kThreads, 0, stream>>>(x, y, m, l, rows, c, ld_x, ld_y, k);
-  } else if (nv <= 2) {
-    softmax_rows_reg_kernel<2><<<grid_for(rows, 4), kThreads, 0, stream>>>(x, y, m, l, rows, c, ld_x, ld_y, k);
+  // Rows of up to 2048 elements: several rows per CTA, each thread holding
+  // up to four 16-byte chunks (configurations measured on the GB300 at
+  // 2^28 elements per matrix; prefetching helped only the shortest rows).
+  if (chunks <= 32) {
+    launch_grouped<0, 32, 1, true, 8>(x, y, m, l, rows, c, ld_x, ld_y, k, stream);
+  } else if (chunks <= 64) {
+    launch_grouped<0, 32, 2, false, 6>(x, y, m, l, rows, c, ld_x, ld_y, k, stream);
+  } else if (chunks <= 128) {
+    launch_grouped<0, 32, 4, false, 6>(x, y, m, l, rows, c, ld_x, ld_y, k, stream);
+  } else if (chunks <= 256) {
+    launch_grouped<0, 64, 4, false, 6>(x, y, m, l, rows, c, ld_x, ld_y, k, stream);
+  } else if (chunks <= 512) {
+    launch_grouped<0, 128, 4, false, 5>(x, y, m, l, rows, c, ld_x, ld_y, k, stream);
   } else if (nv <= 4) {
     softmax_rows_reg_kernel<4><<<grid_for(rows, 4), kThreads, 0, stream>>>(x, y, m, l, rows, c, ld_x, ld_y, k);
   } else if (nv <= 8) {
@@ -707,16 +876,25 @@ void dispatch_rows16(const uint16_t* x, uint16_t* y, float* m, float* l, int64_t
     return;
   }
   const int64_t chunks = (cols + 7) / 8;
-  const int nv = static_cast<int>((chunks + kThreads - 1) / kThreads);
   const int c = static_cast<int>(cols);
-  if (nv <= 1) {
-    softmax_rows16_reg_kernel<kType, 1><<<g, kThreads, 0, stream>>>(x, y, m, l, rows, c, ld_x, ld_y, k);
-  } else if (nv <= 2) {
-    softmax_rows16_reg_kernel<kType, 2><<<g, kThreads, 0, stream>>>(x, y, m, l, rows, c, ld_x, ld_y, k);
-  } else if (nv <= 4) {
-    softmax_rows16_reg_kernel<kType, 4><<<g, kThreads, 0, stream>>>(x, y, m, l, rows, c, ld_x, ld_y, k);
-  } else if (nv <= 8) {
-    softmax_rows16_reg_kernel<kType, 8><<<g, kThreads, 0, stream>>>(x, y, m, l, rows, c, ld_x, ld_y, k);
+  // Rows of up to 16384 elements: persistent CTAs with the next row's chunks
+  // prefetched into registers (the widening of fp16 costs a conversion per
+  // element, and without the prefetch that arithmetic stalled the loads);
+  // 256 / TPR rows per CTA for rows of up to 4096 elements.
+  if (chunks <= 32) {
+    launch_grouped<kType, 32, 1, true, 6>(x, y, m, l, rows, c, ld_x, ld_y, k, stream);
+  } else if (chunks <= 64) {
+    launch_grouped<kType, 32, 2, true, 5>(x, y, m, l, rows, c, ld_x, ld_y, k, stream);
+  } else if (chunks <= 128) {
+    launch_grouped<kType, 32, 4, true, 3>(x, y, m, l, rows, c, ld_x, ld_y, k, stream);
+  } else if (chunks <= 256) {
+    launch_grouped<kType, 64, 4, true, 3>(x, y, m, l, rows, c, ld_x, ld_y, k, stream);
+  } else if (chunks <= 512) {
+    launch_grouped<kType, 128, 4, true, 3>(x, y, m, l, rows, c, ld_x, ld_y, k, stream);
+  } else if (chunks <= 1024) {
+    launch_grouped<kType, 256, 4, true, 3>(x, y, m, l, rows, c, ld_x, ld_y, k, stream);
+  } else if (chunks <= 2048) {
+    launch_grouped<kType, 256, 8, true, 2>(x, y, m, l, rows, c, ld_x, ld_y, k, stream);
   } else {
     softmax_rows16_stream_kernel<kType, true><<<g, kThreads, 0, stream>>>(x, y, m, l, rows, cols, ld_x, ld_y, k);
   }

@@ -1,7 +1,7 @@
 """Run one liboss entry point on one workload a few times, for profilers.
 
     python -m pass_attention_gb300.profile_case softmax [--rows R --cols C] [--reps N]
-    python -m pass_attention_gb300.profile_case softmax16 [--rows R --cols C] [--reps N]
+    python -m pass_attention_gb300.profile_case softmax16 [--dtype bf16|f16] [--rows R --cols C]
     python -m pass_attention_gb300.profile_case multipass --passes 2|3 [--rows R --cols C]
     python -m pass_attention_gb300.profile_case attn [--B --H --S] [--causal] [--reps N]
     python -m pass_attention_gb300.profile_case decode [--B --H --Lmax --splits] [--reps N]
@@ -35,6 +35,7 @@ def main(argv=None):
     ap.add_argument("--splits", type=int, default=16)
     ap.add_argument("--causal", action="store_true")
     ap.add_argument("--reps", type=int, default=3)
+    ap.add_argument("--dtype", choices=["bf16", "f16"], default="bf16")
     a = ap.parse_args(argv)
     oss.load()
     if a.case == "softmax":
@@ -44,7 +45,8 @@ def main(argv=None):
             oss.softmax_rows(x, 1.0, y=y)
             torch.cuda.synchronize()
     elif a.case == "softmax16":
-        x = workloads.logits(a.rows, a.cols, 10.0, seed=1, device="cuda").to(torch.bfloat16)
+        dtype = torch.bfloat16 if a.dtype == "bf16" else torch.float16
+        x = workloads.logits(a.rows, a.cols, 10.0, seed=1, device="cuda").to(dtype)
         y = torch.empty_like(x)
         for _ in range(a.reps):
             oss.softmax_rows_16bit(x, 1.0, y=y)
