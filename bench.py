@@ -55,19 +55,19 @@ NOMINAL = {"hbm_gbs": 7900.0, "bf16_tflops": 2250.0}
 # same kernel, applied to the full launch's algorithmic bytes.
 NCU_TRAFFIC = {
     "softmax_32k": {"source": "pass_attention_gb300/csrc/softmax_rows.cu",
-                    "sha256": "299978f16ab23a3f0d44622f16f84ae3a1b0cc1fa0874d6777bf815033f0bf85",
-                    "bytes_per_launch": 1073781248 + 1017929472},
+                    "sha256": "00c835c523616da637c5ba8ecb09d112ff43c6a0c71b6d7a4a33cee3f8760a59",
+                    "bytes_per_launch": 1073935872 + 1017135616},
     "softmax_32k_bf16": {"source": "pass_attention_gb300/csrc/softmax_rows.cu",
-                         "sha256": "299978f16ab23a3f0d44622f16f84ae3a1b0cc1fa0874d6777bf815033f0bf85",
-                         "bytes_per_launch": 536906752 + 482694656},
+                         "sha256": "00c835c523616da637c5ba8ecb09d112ff43c6a0c71b6d7a4a33cee3f8760a59",
+                         "bytes_per_launch": 536966400 + 482791680},
     # the comparators: all sweeps of one call (each reads x from DRAM again)
     "softmax_32k_3pass": {"source": "pass_attention_gb300/csrc/softmax_rows.cu",
-                          "sha256": "299978f16ab23a3f0d44622f16f84ae3a1b0cc1fa0874d6777bf815033f0bf85",
-                          "bytes_per_launch": (1073762048 + 2868224) + (1073899264 + 177664)
-                          + (1074052352 + 1024664832)},
+                          "sha256": "00c835c523616da637c5ba8ecb09d112ff43c6a0c71b6d7a4a33cee3f8760a59",
+                          "bytes_per_launch": (1073761280 + 2887936) + (1073905920 + 154624)
+                          + (1074054912 + 1024637952)},
     "softmax_32k_2pass": {"source": "pass_attention_gb300/csrc/softmax_rows.cu",
-                          "sha256": "299978f16ab23a3f0d44622f16f84ae3a1b0cc1fa0874d6777bf815033f0bf85",
-                          "bytes_per_launch": (1073761280 + 2997504) + (1074095360 + 1024706048)},
+                          "sha256": "00c835c523616da637c5ba8ecb09d112ff43c6a0c71b6d7a4a33cee3f8760a59",
+                          "bytes_per_launch": (1073771264 + 3108864) + (1074049536 + 1024851712)},
     "attn_4k": {"source": "pass_attention_gb300/csrc/attn_fwd.cu",
                 "sha256": "1de91f1a14f7b69059f99bd37628b4126df733c28a5f205b034826a15235ccec",
                 "bytes_per_launch": 201502976 + 47736320},
@@ -334,14 +334,14 @@ def bench_softmax16(args, ctx):
 
 def bench_softmax_lengths(args, ctx):
     """os_softmax_rows / os_softmax_rows_16bit over row lengths from 128 to
-    16384 at 2^28 elements per matrix (1 GiB fp32, 512 MiB 16-bit: larger
+    131072 at 2^28 elements per matrix (1 GiB fp32, 512 MiB 16-bit: larger
     than L2). Returns {dtype: {cols: (ms per call, algorithmic bytes)}}."""
     import pass_attention_gb300 as oss
     out = {}
     stream = torch.cuda.current_stream()
     for name, dtype in (("fp32", torch.float32), ("bf16", torch.bfloat16), ("fp16", torch.float16)):
         out[name] = {}
-        for cols in (128, 512, 1024, 2048, 4096, 8192, 16384):
+        for cols in (128, 512, 1024, 2048, 4096, 8192, 16384, 32768, 131072):
             rows = (1 << 28) // cols
             x = workloads.logits(rows, cols, 10.0, 7 + ctx["rank"], device="cuda").to(dtype)
             y = torch.empty_like(x)
@@ -641,7 +641,7 @@ def main():
             lens = bench_softmax_lengths(args, ctx)
             extra["softmax_row_lengths"] = {
                 "unit": "GB/s",
-                "workload": "2^28 elements per matrix, N(0,1)*10 logits, scale 1; cols 128..16384",
+                "workload": "2^28 elements per matrix, N(0,1)*10 logits, scale 1; cols 128..131072",
                 "peak": pk["hbm_gbs"], "peak_kind": f"{pk_kind} HBM copy",
                 "value": {d: {str(c): nb / (ms / 1e3) / 1e9 for c, (ms, nb) in v.items()}
                           for d, v in lens.items()},

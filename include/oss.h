@@ -80,9 +80,13 @@ typedef enum os_status {
  *   rows  >= 1; cols >= 1; ld_x >= cols, ld_y >= cols (elements).
  *   scale finite and > 0.
  * Alignment: x, y, m and l 4-byte aligned. When x and y are 16-byte aligned and
- * ld_x, ld_y are multiples of 4 the kernel uses 16-byte loads and stores and,
- * for cols <= 16384, holds each row in registers (one read, one write per
- * element); otherwise it streams the row twice (two reads, one write).
+ * ld_x, ld_y are multiples of 4 the kernel uses 16-byte loads and stores and
+ * reads each element once and writes it once: rows of up to 16384 elements
+ * are held in registers (several rows per CTA up to 2048 elements); longer
+ * rows of up to 1.6 MB in the shared memory of a thread-block cluster of up
+ * to eight CTAs, whose slices' (max, sum) states are merged through
+ * distributed shared memory. Other rows are streamed twice (two reads, one
+ * write).
  * Errors: OS_ERR_INVALID_ARGUMENT, OS_ERR_MISALIGNED, OS_ERR_CUDA.
  */
 OSS_API os_status os_softmax_rows(const float* x, float* y, float* m, float* l,
@@ -113,8 +117,9 @@ typedef enum os_dtype {
  *   finite and > 0; dtype an os_dtype.
  * Alignment: x and y 2-byte aligned, m and l 4-byte aligned. With x and y
  * 16-byte aligned and ld_x, ld_y multiples of 8, rows of up to 16384
- * elements are held in registers (one read, one write per element); other
- * rows are streamed twice.
+ * elements are held in registers and longer rows of up to 1.6 MB in a
+ * cluster's shared memory, as for os_softmax_rows (one read, one write per
+ * element); other rows are streamed twice.
  * Errors: OS_ERR_INVALID_ARGUMENT, OS_ERR_MISALIGNED, OS_ERR_CUDA.
  */
 OSS_API os_status os_softmax_rows_16bit(const void* x, void* y, float* m, float* l,
@@ -260,8 +265,11 @@ OSS_API os_status os_merge_partials(const float* part_m, const float* part_l, co
  * os_check_device_error -- synchronise `stream`, then read and clear the
  * current device's error word. *code receives 0 when no kernel gave up on a
  * wait since the last check, otherwise an OS_ERR_TIMEOUT detail code
- * (bits 0..7 = kernel id, bits 8..15 = wait site). Returns OS_ERR_TIMEOUT
- * when the word was set, OS_ERR_CUDA when a CUDA call failed, OS_OK otherwise.
+ * (bits 0..7 = kernel id, bits 8..15 = wait site): kernel 1 is the attention
+ * forward (see os_debug_inject_fault); 2 | (1 << 8) is a row softmax whose
+ * wait for its row's bulk copies into shared memory gave up. Returns
+ * OS_ERR_TIMEOUT when the word was set, OS_ERR_CUDA when a CUDA call failed,
+ * OS_OK otherwise.
  * `code` may be NULL.
  */
 OSS_API os_status os_check_device_error(void* stream, int32_t* code);

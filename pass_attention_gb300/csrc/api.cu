@@ -72,7 +72,7 @@ os_status os_softmax_rows(const float* x, float* y, float* m, float* l, int64_t 
        reinterpret_cast<uintptr_t>(m) | reinterpret_cast<uintptr_t>(l)) & 3u)
     return OS_ERR_MISALIGNED;
   return from_cuda(oss::launch_softmax_rows(x, y, m, l, rows, cols, ld_x, ld_y, scale,
-                                            static_cast<cudaStream_t>(stream)));
+                                            error_word(), static_cast<cudaStream_t>(stream)));
 }
 
 os_status os_softmax_rows_16bit(const void* x, void* y, float* m, float* l, int64_t rows,
@@ -87,7 +87,7 @@ os_status os_softmax_rows_16bit(const void* x, void* y, float* m, float* l, int6
   if ((reinterpret_cast<uintptr_t>(m) | reinterpret_cast<uintptr_t>(l)) & 3u) return OS_ERR_MISALIGNED;
   return from_cuda(oss::launch_softmax_rows16(static_cast<const uint16_t*>(x),
                                               static_cast<uint16_t*>(y), m, l, rows, cols, ld_x,
-                                              ld_y, scale, dtype,
+                                              ld_y, scale, dtype, error_word(),
                                               static_cast<cudaStream_t>(stream)));
 }
 

@@ -31,6 +31,7 @@
 
 #include <cuda_fp16.h>
 
+#include <atomic>
 #include <cfloat>
 #include <cmath>
 #include <cstdint>
@@ -717,6 +718,287 @@ softmax_rows_grouped_kernel(const void* __restrict__ x, void* __restrict__ y,
   }
 }
 
+// ---------------------------------------------------------------------------
+// Cluster-resident rows: rows too long for registers (more than 16384
+// elements) but short enough to fit in the shared memory of a thread-block
+// cluster of C <= 8 CTAs. CTA r of a cluster holds slice r of the row, copied
+// in by bulk asynchronous copies; each CTA reduces its slice to a (max, sum)
+// state, the CTAs exchange their states through distributed shared memory and
+// merge them (the merge identity of partial results), and each CTA then
+// writes its slice once. One HBM read and one write per element, where the
+// streaming kernel reads the row twice.
+// ---------------------------------------------------------------------------
+
+constexpr int kClThreads = 512;
+constexpr int kClUnroll = 4;  // chunks each thread loads before using them
+constexpr int kClWarps = kClThreads / 32;
+constexpr int kClMaxCtas = 8;
+constexpr int kClPiece = 16384;                       // bytes per bulk copy
+constexpr unsigned long long kClTimeoutNs = 2000000000ull;  // bounded wait on the copies
+constexpr int64_t kClDoubleCap = int64_t(48) << 10;   // rows this short: one CTA, two buffers
+constexpr int64_t kClSingleCap = int64_t(200) << 10;  // longer rows: one buffer per CTA
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ uint64_t timer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_size() {
+  uint32_t n;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(n));
+  return n;
+}
+__device__ __forceinline__ uint32_t cluster_id() {
+  uint32_t c;
+  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(c));
+  return c;
+}
+__device__ __forceinline__ uint32_t cluster_count() {
+  uint32_t c;
+  asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(c));
+  return c;
+}
+// every thread of every CTA of the cluster; orders shared-memory writes
+// (local and remote) before the barrier with reads after it
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
+// The same barrier when only warp 0 has written anything the cluster reads
+// after it: the other warps arrive without a release fence.
+__device__ __forceinline__ void cluster_sync_warp0_wrote() {
+  if (threadIdx.x < 32)
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+  else
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// (a, b) into the same shared-memory slot of CTA `rank` of the cluster
+__device__ __forceinline__ void st_peer_f2(const void* slot, uint32_t rank, float a, float b) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(slot)), "r"(rank));
+  asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(remote), "f"(a), "f"(b) : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Wait for the phase with the given parity, for at most kClTimeoutNs; a
+// give-up is recorded in the error word and the caller carries on (every CTA
+// of the cluster must still reach the same cluster barriers).
+__device__ __forceinline__ void mbar_wait_bounded(uint32_t bar, uint32_t parity, unsigned int* err) {
+  if (mbar_try(bar, parity)) return;
+  const uint64_t t0 = timer_ns();
+  for (uint32_t n = 1;; ++n) {
+    if (mbar_try(bar, parity)) return;
+    if ((n & 63u) == 0 && timer_ns() - t0 > kClTimeoutNs) {
+      report_error(err, kKernelSoftmaxRows | (1u << 8));
+      return;
+    }
+  }
+}
+
+// n-ary merge of the n <= 32 (max, sum) states s[0..n), by one warp: lane w
+// takes state w, the lanes' maximum by shuffles, then each sum scaled to it
+// (one ex2) and the scaled sums added by shuffles. Every warp that calls it
+// gets the same result.
+__device__ __forceinline__ float2 merge_states_warp(const float2* s, int n, const ScaleConsts& k) {
+  const int lane = threadIdx.x & 31;
+  const float2 e = (lane < n) ? s[lane] : make_float2(neg_inf(), 0.f);
+  float x = e.x;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, off));
+  float l = (e.x == neg_inf()) ? 0.f : e.y * ex2(base2_of(e.x, k) - base2_of(x, k));
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
+  return make_float2(x, l);
+}
+
+// Issue the copies of one row's slice into `buf_a` (thread 0 only): the
+// whole 16-byte chunks by bulk copies that complete on `bar_a`, the last
+// partial chunk (if any) by plain loads, padded with -inf.
+template <int kKind>
+__device__ __forceinline__ void issue_slice(const char* xr, uint4* buf, uint32_t buf_a, uint32_t bar_a,
+                                            uint32_t bulk, int nfull, int tail) {
+  // the buffer's previous contents were last touched through the generic
+  // proxy; order that before the copies' asynchronous writes
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  if (bulk > 0) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar_a), "r"(bulk)
+                 : "memory");
+    for (uint32_t off = 0; off < bulk; off += kClPiece) {
+      const uint32_t size = (bulk - off < kClPiece) ? (bulk - off) : kClPiece;
+      asm volatile(
+          "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+              "r"(buf_a + off), "l"(xr + off), "r"(size), "r"(bar_a)
+          : "memory");
+    }
+  } else {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar_a) : "memory");
+  }
+  if (tail) buf[nfull] = load_chunk16<kKind>(xr, nfull, nfull, tail);
+}
+
+// kDouble: two slice buffers; the next row's copies are issued as soon as
+// the current row's have landed, so they are in flight while the current row
+// is reduced and written.
+template <int kKind, bool kDouble>
+__global__ void __launch_bounds__(kClThreads, 2)
+softmax_rows_cluster_kernel(const void* __restrict__ x, void* __restrict__ y,
+                            float* __restrict__ m_out, float* __restrict__ l_out, int64_t rows,
+                            int64_t cols, int64_t ld_x, int64_t ld_y, ScaleConsts k,
+                            int slice_elems, unsigned int* err) {
+  constexpr int kEpc = RowElem<kKind>::kEpc;
+  constexpr int kEsz = RowElem<kKind>::kSize;
+  extern __shared__ __align__(128) uint4 slices[];  // this CTA's slice buffer(s), 16-byte chunks
+  __shared__ float2 wstate[kClWarps];
+  __shared__ float2 cstate[2][kClMaxCtas];         // the cluster's CTA states, by row parity
+  __shared__ __align__(8) uint64_t bars[2];
+
+  const int tid = threadIdx.x;
+  const uint32_t C = cluster_size();
+  const uint32_t rank = cluster_rank();
+  const int64_t lo = static_cast<int64_t>(rank) * slice_elems;
+  const int64_t left = cols - lo;
+  const int n = static_cast<int>(left <= 0 ? 0 : (left < slice_elems ? left : slice_elems));
+  const int nfull = n / kEpc;
+  const int tail = n % kEpc;
+  const int nch = nfull + (tail ? 1 : 0);
+  const uint32_t bulk = static_cast<uint32_t>(nfull) * 16u;
+  const int stride_chunks = (slice_elems / kEpc + 7) / 8 * 8;  // second buffer 128-byte aligned
+  const int64_t row0 = cluster_id();
+  const int64_t rstep = cluster_count();
+  const char* xb = static_cast<const char*>(x);
+
+  if (tid == 0) {
+    for (int b = 0; b < (kDouble ? 2 : 1); ++b)
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&bars[b])) : "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  // every CTA of the cluster has started (its shared memory may be written
+  // by peers from here on) and the barriers' initialisation is visible
+  cluster_sync_all();
+  if (kDouble && tid == 0 && row0 < rows)
+    issue_slice<kKind>(xb + (row0 * ld_x + lo) * kEsz, slices, smem_u32(slices), smem_u32(&bars[0]),
+                       bulk, nfull, tail);
+
+  uint32_t parity = 0u;  // bit b: the phase parity to wait for on buffer b
+  int sbuf = 0;  // cstate set
+  int it = 0;
+  for (int64_t row = row0; row < rows; row += rstep, ++it) {
+    const int b = kDouble ? (it & 1) : 0;
+    uint4* slice = slices + b * stride_chunks;
+    const uint32_t bar_a = smem_u32(&bars[b]);
+    char* yr = static_cast<char*>(y) + (row * ld_y + lo) * kEsz;
+    if (!kDouble && tid == 0)
+      issue_slice<kKind>(xb + (row * ld_x + lo) * kEsz, slice, smem_u32(slice), bar_a, bulk, nfull, tail);
+    mbar_wait_bounded(bar_a, (parity >> b) & 1u, err);
+    parity ^= 1u << b;
+    __syncthreads();  // the tail chunk, written by thread 0
+    if (kDouble && tid == 0 && row + rstep < rows) {
+      // the other buffer was read out before the end of the previous row
+      uint4* other = slices + (b ^ 1) * stride_chunks;
+      issue_slice<kKind>(xb + ((row + rstep) * ld_x + lo) * kEsz, other, smem_u32(other),
+                         smem_u32(&bars[b ^ 1]), bulk, nfull, tail);
+    }
+
+    // The thread's (max, sum) over its chunks, by the online recurrence:
+    // each step loads kClUnroll chunks (tid, tid + T, ...), takes their
+    // maximum, rescales the running sum once if it rose, then adds the
+    // step's weights relative to the running maximum.
+    const uint4 pad = make_uint4(neg_inf_word<kKind>(), neg_inf_word<kKind>(), neg_inf_word<kKind>(),
+                                 neg_inf_word<kKind>());
+    float xm = neg_inf();
+    float2 negM = make_float2(0.f, 0.f);
+    float2 acc = make_float2(0.f, 0.f);
+    for (int c0 = tid; c0 < nch; c0 += kClThreads * kClUnroll) {
+      float2 w[kClUnroll][kEpc / 2];
+#pragma unroll
+      for (int u = 0; u < kClUnroll; ++u)
+        unpack_chunk16<kKind>((c0 + u * kClThreads < nch) ? slice[c0 + u * kClThreads] : pad, w[u]);
+      float cm = xm;
+#pragma unroll
+      for (int u = 0; u < kClUnroll; ++u)
+#pragma unroll
+        for (int h = 0; h < kEpc / 2; ++h) cm = fmax3(cm, w[u][h].x, w[u][h].y);
+      if (cm != xm) {  // a larger (finite) maximum: rescale what is summed so far
+        const float Mn = base2_of(cm, k);
+        if (xm != neg_inf()) {
+          const float r = ex2(-negM.x - Mn);
+          acc = __fmul2_rn(acc, make_float2(r, r));
+        }
+        xm = cm;
+        negM = make_float2(-Mn, -Mn);
+      }
+#pragma unroll
+      for (int u = 0; u < kClUnroll; ++u)
+#pragma unroll
+        for (int h = 0; h < kEpc / 2; ++h) acc = __fadd2_rn(acc, weight2(w[u][h], negM, k));
+    }
+    float ls = acc.x + acc.y;
+
+    // the CTA's state: warp maxima and scaled sums by shuffles, then the
+    // warp states through shared memory
+    float xw = xm;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) xw = fmaxf(xw, __shfl_xor_sync(0xffffffffu, xw, off));
+    float lw = (xm == neg_inf()) ? 0.f : ls * ex2(base2_of(xm, k) - base2_of(xw, k));
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) lw += __shfl_xor_sync(0xffffffffu, lw, off);
+    if ((tid & 31) == 0) wstate[tid >> 5] = make_float2(xw, lw);
+    __syncthreads();
+    float2 st = merge_states_warp(wstate, kClWarps, k);
+    if (C > 1) {
+      if (tid == 0)
+        for (uint32_t r = 0; r < C; ++r) st_peer_f2(&cstate[sbuf][rank], r, st.x, st.y);
+      cluster_sync_warp0_wrote();
+      st = merge_states_warp(cstate[sbuf], static_cast<int>(C), k);
+      sbuf ^= 1;
+    }
+    xm = st.x;
+    ls = st.y;
+
+    // y = 2^(x*c - M_row) / l, formed again from x (an empty row gives 0)
+    const bool live = (xm != neg_inf()) && ls > 0.f;
+    const float Mr = live ? base2_of(xm, k) : 0.f;
+    const float2 negMr = make_float2(-Mr, -Mr);
+    const float inv = live ? 1.0f / ls : 0.f;
+    const float2 f2 = make_float2(inv, inv);
+    for (int c0 = tid; c0 < nch; c0 += kClThreads * kClUnroll) {
+      uint4 v[kClUnroll];
+#pragma unroll
+      for (int u = 0; u < kClUnroll; ++u) v[u] = (c0 + u * kClThreads < nch) ? slice[c0 + u * kClThreads] : pad;
+#pragma unroll
+      for (int u = 0; u < kClUnroll; ++u) {
+        if (c0 + u * kClThreads < nch) {
+          float2 w[kEpc / 2];
+          unpack_chunk16<kKind>(v[u], w);
+#pragma unroll
+          for (int h = 0; h < kEpc / 2; ++h) w[h] = weight2(w[h], negMr, k);
+          store_chunk16<kKind>(yr, c0 + u * kClThreads, nfull, tail, pack_chunk16<kKind>(w, f2));
+        }
+      }
+    }
+    if (rank == 0 && tid == 0) write_ml(xm, ls, k, row, m_out, l_out);
+    __syncthreads();  // the slice is read out before its buffer is refilled
+  }
+}
+
 // Long or unaligned 16-bit rows: the recurrence over the row as it streams
 // (8-element chunks when aligned, single elements otherwise), the CTA merge,
 // then a second read of the row for the write (2 reads + 1 write).
@@ -825,9 +1107,132 @@ void launch_grouped(const void* x, void* y, float* m, float* l, int64_t rows, in
       <<<g, kThreads, 0, stream>>>(x, y, m, l, rows, cols, ld_x, ld_y, k);
 }
 
+struct ClusterCfg {
+  int ctas;
+  int slice_elems;
+  size_t smem;
+};
+
+template <int kKind, bool kDouble>
+cudaLaunchConfig_t cluster_launch_cfg(const ClusterCfg& cc, cudaLaunchAttribute* attr,
+                                      cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = cc.ctas;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(kClThreads, 1, 1);
+  cfg.gridDim = dim3(cc.ctas, 1, 1);
+  cfg.dynamicSmemBytes = cc.smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cfg;
+}
+
+// Clusters of `ctas` CTAs that can be resident at once (0 when none can),
+// cached per device, cluster size and shared-memory size in 8 KB steps.
+template <int kKind, bool kDouble>
+int resident_clusters(const ClusterCfg& cc) {
+  static std::atomic<int> cache[64][kClMaxCtas + 1][32];  // resident + 1; 0 = not asked yet
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const size_t kb8 = (cc.smem + 8191) >> 13;
+  const bool cached = dev >= 0 && dev < 64 && kb8 < 32;
+  if (cached) {
+    const int v = cache[dev][cc.ctas][kb8].load();
+    if (v > 0) return v - 1;
+  }
+  auto kernel = softmax_rows_cluster_kernel<kKind, kDouble>;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 210 << 10) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = cluster_launch_cfg<kKind, kDouble>(cc, attr, nullptr);
+  int resident = 0;
+  if (cudaOccupancyMaxActiveClusters(&resident, kernel, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    resident = 0;
+  }
+  if (cached) cache[dev][cc.ctas][kb8].store(resident + 1);
+  return resident;
+}
+
+// The cluster for a row of `cols` elements: slices of at most `cap` bytes
+// (in each of two buffers when kDouble), at most kClMaxCtas of them, and
+// among the cluster sizes that hold the row the one that keeps the most SMs
+// busy (clusters resident at once x CTAs per cluster; a GPC's SMs need not
+// divide into clusters evenly), the smallest on a tie.
+template <int kKind, bool kDouble>
+bool pick_cluster(int64_t cols, int64_t cap, int max_ctas, ClusterCfg* out) {
+  constexpr int kEpc = RowElem<kKind>::kEpc;
+  constexpr int kEsz = RowElem<kKind>::kSize;
+  if (cap <= 0) return false;
+  const int64_t cmin = (cols * kEsz + cap - 1) / cap;
+  int best_used = 0;
+  for (int64_t c = cmin < 1 ? 1 : cmin; c <= max_ctas; ++c) {
+    int64_t per = (cols + c - 1) / c;
+    per = (per + kEpc - 1) / kEpc * kEpc;
+    if (per * kEsz > cap) continue;
+    const int64_t chunks = per / kEpc;
+    const int64_t stride = (chunks + 7) / 8 * 8;
+    ClusterCfg cc{static_cast<int>(c), static_cast<int>(per),
+                  static_cast<size_t>((kDouble ? stride + chunks : chunks) * 16)};
+    const int used = resident_clusters<kKind, kDouble>(cc) * cc.ctas;
+    if (used > best_used) {
+      best_used = used;
+      *out = cc;
+    }
+  }
+  return best_used > 0;
+}
+
+// Launch of softmax_rows_cluster_kernel, as many clusters as can be resident
+// at once (each loops over its rows).
+template <int kKind, bool kDouble>
+bool launch_cluster_rows_as(const void* x, void* y, float* m, float* l, int64_t rows, int64_t cols,
+                            int64_t ld_x, int64_t ld_y, const ScaleConsts& k, const ClusterCfg& cc,
+                            unsigned int* err, cudaStream_t stream) {
+  // the bulk copies need 16-byte aligned rows: x and y aligned, and both
+  // leading dimensions whole chunks
+  constexpr int kEpc = RowElem<kKind>::kEpc;
+  if (((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y)) & 15u) != 0 ||
+      ld_x % kEpc != 0 || ld_y % kEpc != 0 || cc.slice_elems % kEpc != 0)
+    return false;
+  const int resident = resident_clusters<kKind, kDouble>(cc);
+  if (resident < 1) return false;
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = cluster_launch_cfg<kKind, kDouble>(cc, attr, stream);
+  const int64_t nclusters = rows < resident ? rows : resident;
+  cfg.gridDim = dim3(static_cast<unsigned int>(nclusters * cc.ctas), 1, 1);
+  const int64_t c64 = cols;
+  return cudaLaunchKernelEx(&cfg, softmax_rows_cluster_kernel<kKind, kDouble>, x, y, m, l, rows, c64,
+                            ld_x, ld_y, k, cc.slice_elems, err) == cudaSuccess;
+}
+
+// Rows held in a cluster's shared memory. A row of at most kClDoubleCap
+// bytes takes one CTA with two buffers (its next row's copies in flight
+// while it reduces the current one); a longer row takes one buffer of at
+// most 200 KB in each of up to eight CTAs. False, launching nothing, when the
+// row is longer. (Measured on the GB300 with 2^28-element matrices: two
+// buffers won only when the row fit one CTA; for longer rows the extra CTAs
+// they need cost more than the overlap gained.)
+template <int kKind>
+bool launch_cluster_rows(const void* x, void* y, float* m, float* l, int64_t rows, int64_t cols,
+                         int64_t ld_x, int64_t ld_y, const ScaleConsts& k, unsigned int* err,
+                         cudaStream_t stream) {
+  ClusterCfg cc;
+  if (pick_cluster<kKind, true>(cols, kClDoubleCap, 1, &cc))
+    return launch_cluster_rows_as<kKind, true>(x, y, m, l, rows, cols, ld_x, ld_y, k, cc, err, stream);
+  if (pick_cluster<kKind, false>(cols, kClSingleCap, kClMaxCtas, &cc))
+    return launch_cluster_rows_as<kKind, false>(x, y, m, l, rows, cols, ld_x, ld_y, k, cc, err, stream);
+  return false;
+}
+
 cudaError_t launch_softmax_rows(const float* x, float* y, float* m, float* l, int64_t rows,
                                 int64_t cols, int64_t ld_x, int64_t ld_y, float scale,
-                                cudaStream_t stream) {
+                                unsigned int* err_word, cudaStream_t stream) {
   const ScaleConsts k = make_consts(scale);
 
   const bool vec = ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y)) & 15u) == 0 &&
@@ -859,7 +1264,8 @@ cudaError_t launch_softmax_rows(const float* x, float* y, float* m, float* l, in
   } else if (nv <= 16) {
     softmax_rows_reg_kernel<16><<<grid_for(rows, 2), kThreads, 0, stream>>>(x, y, m, l, rows, c, ld_x, ld_y, k);
   } else {
-    softmax_rows_stream_kernel<true><<<grid_for(rows, 4), kThreads, 0, stream>>>(x, y, m, l, rows, cols, ld_x, ld_y, k);
+    if (!launch_cluster_rows<0>(x, y, m, l, rows, cols, ld_x, ld_y, k, err_word, stream))
+      softmax_rows_stream_kernel<true><<<grid_for(rows, 4), kThreads, 0, stream>>>(x, y, m, l, rows, cols, ld_x, ld_y, k);
   }
   return cudaGetLastError();
 }
@@ -867,7 +1273,7 @@ cudaError_t launch_softmax_rows(const float* x, float* y, float* m, float* l, in
 template <int kType>
 void dispatch_rows16(const uint16_t* x, uint16_t* y, float* m, float* l, int64_t rows,
                      int64_t cols, int64_t ld_x, int64_t ld_y, const ScaleConsts& k,
-                     cudaStream_t stream) {
+                     unsigned int* err_word, cudaStream_t stream) {
   const bool vec = ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y)) & 15u) == 0 &&
                    (ld_x & 7) == 0 && (ld_y & 7) == 0;
   const int g = grid_for(rows, 4);
@@ -896,18 +1302,20 @@ void dispatch_rows16(const uint16_t* x, uint16_t* y, float* m, float* l, int64_t
   } else if (chunks <= 2048) {
     launch_grouped<kType, 256, 8, true, 2>(x, y, m, l, rows, c, ld_x, ld_y, k, stream);
   } else {
-    softmax_rows16_stream_kernel<kType, true><<<g, kThreads, 0, stream>>>(x, y, m, l, rows, cols, ld_x, ld_y, k);
+    if (!launch_cluster_rows<kType>(x, y, m, l, rows, cols, ld_x, ld_y, k, err_word, stream))
+      softmax_rows16_stream_kernel<kType, true><<<g, kThreads, 0, stream>>>(x, y, m, l, rows, cols, ld_x, ld_y, k);
   }
 }
 
 cudaError_t launch_softmax_rows16(const uint16_t* x, uint16_t* y, float* m, float* l,
                                   int64_t rows, int64_t cols, int64_t ld_x, int64_t ld_y,
-                                  float scale, int dtype, cudaStream_t stream) {
+                                  float scale, int dtype, unsigned int* err_word,
+                                  cudaStream_t stream) {
   const ScaleConsts k = make_consts(scale);
   if (dtype == 1)
-    dispatch_rows16<1>(x, y, m, l, rows, cols, ld_x, ld_y, k, stream);
+    dispatch_rows16<1>(x, y, m, l, rows, cols, ld_x, ld_y, k, err_word, stream);
   else
-    dispatch_rows16<2>(x, y, m, l, rows, cols, ld_x, ld_y, k, stream);
+    dispatch_rows16<2>(x, y, m, l, rows, cols, ld_x, ld_y, k, err_word, stream);
   return cudaGetLastError();
 }
 

@@ -1,0 +1,96 @@
+"""Rows longer than 16384 elements against the oracle (GPU).
+
+Aligned rows of up to 8 x 200 KB are held in the shared memory of a
+thread-block cluster: CTA r of a cluster of C CTAs holds slice r, the CTAs
+merge their (max, sum) states through distributed shared memory, and each
+writes its slice once. A row of at most 48 KB takes one CTA with two slice
+buffers (the next row's copies overlap the current row). Longer rows fall back
+to the streaming kernel. The lengths below take one CTA with two buffers, one
+with one buffer, and clusters of up to eight, with ragged last slices and
+slices that are empty; the row counts exceed the clusters resident at once,
+so each cluster walks several rows."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import pass_attention_gb300 as oss
+from pass_attention_gb300 import workloads
+from parity import check_softmax, check_softmax16, f32
+
+pytestmark = pytest.mark.gpu
+
+# (cols, rows); the row's size and the fewest 200 KB slices that hold it
+F32_CASES = [
+    (16385, 301),    # 64 KB, one CTA, ragged tail
+    (20000, 401),    # 80 KB; more rows than resident CTAs
+    (25601, 160),    # 100 KB, one element past a 16-byte chunk
+    (32768, 160),    # 128 KB
+    (65536, 130),    # 256 KB: two or more CTAs
+    (100003, 41),    # 391 KB, ragged
+    (204800, 21),    # 800 KB: four or more
+    (204801, 21),    # one element more: five or more
+    (409600, 9),     # 1.6 MB: eight, the longest held row
+    (409601, 9),     # beyond: the streaming kernel
+]
+H16_CASES = [
+    (16385, 301),    # 32 KB: one CTA, two buffers
+    (20000, 401),    # 40 KB: one CTA, two buffers
+    (51201, 160),    # 100 KB: one buffer
+    (131072, 64),    # 256 KB
+    (409600, 12), (409601, 12),
+    (819200, 6),     # 1.6 MB: eight
+    (819201, 6),     # beyond: the streaming kernel
+]
+
+
+def masked(x, seed):
+    g = torch.Generator(device="cuda").manual_seed(seed)
+    x[torch.rand(x.shape, generator=g, device="cuda") < 0.2] = -float("inf")
+    x[1::5] = -float("inf")   # whole rows
+    cols = x.shape[1]
+    x[2, : cols // 2] = -float("inf")   # first half masked: leading slices empty
+    return x
+
+
+@pytest.mark.parametrize("cols,rows", F32_CASES)
+@pytest.mark.parametrize("mask", [False, True])
+def test_fp32_long_rows(cols, rows, mask):
+    ld = (cols + 3) // 4 * 4
+    x = workloads.logits(rows, ld, 10.0, seed=cols + mask, device="cuda")[:, :cols]
+    if mask:
+        x = masked(x, cols)
+    y = torch.empty((rows, ld), device="cuda")[:, :cols]
+    y, m, l = oss.softmax_rows(x, 0.9, y=y)
+    torch.cuda.synchronize()
+    assert oss.check_device_error() == 0
+    check_softmax(y.cpu().numpy(), m.cpu().numpy(), l.cpu().numpy(),
+                  *oracle.softmax_rows(x.cpu().numpy(), f32(0.9)), what=f"fp32 {rows}x{cols}")
+
+
+@pytest.mark.parametrize("kind", ["bf16", "f16"])
+@pytest.mark.parametrize("cols,rows", H16_CASES)
+@pytest.mark.parametrize("mask", [False, True])
+def test_16bit_long_rows(kind, cols, rows, mask):
+    ld = (cols + 7) // 8 * 8
+    dtype = torch.bfloat16 if kind == "bf16" else torch.float16
+    x = workloads.logits(rows, ld, 10.0, seed=cols * 3 + mask, device="cuda").to(dtype)[:, :cols]
+    if mask:
+        x = masked(x, cols + 1)
+    y = torch.empty((rows, ld), dtype=dtype, device="cuda")[:, :cols]
+    y, m, l = oss.softmax_rows_16bit(x, 0.9, y=y)
+    torch.cuda.synchronize()
+    assert oss.check_device_error() == 0
+    xr = x.float().cpu().numpy().astype(np.float64)
+    check_softmax16(y.float().cpu().numpy(), m.cpu().numpy(), l.cpu().numpy(),
+                    *oracle.softmax_rows(xr, f32(0.9)), kind=kind, what=f"{kind} {rows}x{cols}")
+
+
+def test_long_rows_repeat_identical():
+    # the cluster merge runs in a fixed order: results repeat bit for bit
+    x = workloads.logits(50, 100000, 10.0, seed=5, device="cuda")
+    y1, m1, l1 = oss.softmax_rows(x, 1.0)
+    y2, m2, l2 = oss.softmax_rows(x, 1.0)
+    torch.cuda.synchronize()
+    assert torch.equal(y1, y2) and torch.equal(m1, m2) and torch.equal(l1, l2)
