@@ -55,19 +55,19 @@ NOMINAL = {"hbm_gbs": 7900.0, "bf16_tflops": 2250.0}
 # same kernel, applied to the full launch's algorithmic bytes.
 NCU_TRAFFIC = {
     "softmax_32k": {"source": "pass_attention_gb300/csrc/softmax_rows.cu",
-                    "sha256": "00c835c523616da637c5ba8ecb09d112ff43c6a0c71b6d7a4a33cee3f8760a59",
-                    "bytes_per_launch": 1073935872 + 1017135616},
+                    "sha256": "821ba7b1d176258ad6a976c863ebf32a3bea1ce5793057cd4b863b837b265c5f",
+                    "bytes_per_launch": 1073795584 + 1017249792},
     "softmax_32k_bf16": {"source": "pass_attention_gb300/csrc/softmax_rows.cu",
-                         "sha256": "00c835c523616da637c5ba8ecb09d112ff43c6a0c71b6d7a4a33cee3f8760a59",
-                         "bytes_per_launch": 536966400 + 482791680},
+                         "sha256": "821ba7b1d176258ad6a976c863ebf32a3bea1ce5793057cd4b863b837b265c5f",
+                         "bytes_per_launch": 536905472 + 482804736},
     # the comparators: all sweeps of one call (each reads x from DRAM again)
     "softmax_32k_3pass": {"source": "pass_attention_gb300/csrc/softmax_rows.cu",
-                          "sha256": "00c835c523616da637c5ba8ecb09d112ff43c6a0c71b6d7a4a33cee3f8760a59",
-                          "bytes_per_launch": (1073761280 + 2887936) + (1073905920 + 154624)
-                          + (1074054912 + 1024637952)},
+                          "sha256": "821ba7b1d176258ad6a976c863ebf32a3bea1ce5793057cd4b863b837b265c5f",
+                          "bytes_per_launch": (1073761536 + 2903552) + (1073906944 + 164096)
+                          + (1074059776 + 1025022464)},
     "softmax_32k_2pass": {"source": "pass_attention_gb300/csrc/softmax_rows.cu",
-                          "sha256": "00c835c523616da637c5ba8ecb09d112ff43c6a0c71b6d7a4a33cee3f8760a59",
-                          "bytes_per_launch": (1073771264 + 3108864) + (1074049536 + 1024851712)},
+                          "sha256": "821ba7b1d176258ad6a976c863ebf32a3bea1ce5793057cd4b863b837b265c5f",
+                          "bytes_per_launch": (1073761024 + 3028480) + (1074143232 + 1024922880)},
     "attn_4k": {"source": "pass_attention_gb300/csrc/attn_fwd.cu",
                 "sha256": "1de91f1a14f7b69059f99bd37628b4126df733c28a5f205b034826a15235ccec",
                 "bytes_per_launch": 201502976 + 47736320},

@@ -486,9 +486,9 @@ __device__ __forceinline__ uint4 out8(const uint4& v, float M, float inv, const 
 
 // ---------------------------------------------------------------------------
 // Grouped rows: one kernel for fp32, bf16 and fp16 rows that are 16-byte
-// aligned and fit in registers. A group of TPR threads (32, 64, 128 or 256)
-// owns one row at a time, so a CTA of 256 threads works on 256 / TPR rows
-// and short rows keep as many bytes in flight per SM as long ones. A chunk is
+// aligned and fit in registers. A group of TPR threads (8, 16, 32, 64, 128 or
+// 256) owns one row at a time, so a CTA of 256 threads works on 256 / TPR
+// rows and short rows keep as many bytes in flight per SM as long ones. A chunk is
 // 16 bytes: 4 fp32 or 8 16-bit elements; each thread holds NV chunks.
 //
 // Per row: the thread's maximum, its weights 2^(x*c - M_t) (packed FMAs, one
@@ -596,19 +596,22 @@ __device__ __forceinline__ void group_barrier(int id, int nthreads) {
 }
 
 // Merge of the (xm, ls) states of the TPR threads that own one row; returns
-// the row state in all of them. The n-ary form of cta_merge, over TPR / 32
-// warps whose states meet in sh[] (one entry per warp of the CTA) behind a
-// barrier of the group's own threads.
+// the row state in all of them. The n-ary form of cta_merge: shuffles within
+// the group, then (TPR > 32) the TPR / 32 warp states through sh[] (one entry
+// per warp of the CTA) behind a barrier of the group's own threads. Every
+// lane of a warp must call it (all shuffles use the full mask).
 template <int TPR>
 __device__ __forceinline__ void group_merge(float& xm, float& ls, const ScaleConsts& k,
                                             float2* sh, int g) {
+  // a group narrower than a warp shuffles within its own aligned lanes
+  constexpr int kTop = (TPR < 32 ? TPR : 32) / 2;
   float xw = xm;
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) xw = fmaxf(xw, __shfl_xor_sync(0xffffffffu, xw, off));
+  for (int off = kTop; off > 0; off >>= 1) xw = fmaxf(xw, __shfl_xor_sync(0xffffffffu, xw, off));
   float lw = (xm == neg_inf()) ? 0.f : ls * ex2(base2_of(xm, k) - base2_of(xw, k));
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) lw += __shfl_xor_sync(0xffffffffu, lw, off);
-  if (TPR == 32) {
+  for (int off = kTop; off > 0; off >>= 1) lw += __shfl_xor_sync(0xffffffffu, lw, off);
+  if (TPR <= 32) {
     xm = xw;
     ls = lw;
     return;
@@ -655,22 +658,32 @@ softmax_rows_grouped_kernel(const void* __restrict__ x, void* __restrict__ y,
   const int nfull = cols / kEpc;
   const int tail = cols % kEpc;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * kGroups;
-  int64_t row = static_cast<int64_t>(blockIdx.x) * kGroups + g;
+  // Groups narrower than a warp share their warp's shuffles, so the warp
+  // walks its rows together: the loop runs on the row of the warp's first
+  // group, and a group whose own row is past the end takes part as an empty
+  // row (no loads or stores).
+  constexpr int kPerWarp = (TPR < 32) ? 32 / TPR : 1;
+  const int lead = g % kPerWarp;
+  const uint4 pad = make_uint4(neg_inf_word<kKind>(), neg_inf_word<kKind>(), neg_inf_word<kKind>(),
+                               neg_inf_word<kKind>());
+  int64_t wrow = static_cast<int64_t>(blockIdx.x) * kGroups + g - lead;
   const char* xb = static_cast<const char*>(x);
   char* yb = static_cast<char*>(y);
 
   uint4 nx[NV];
-  if (kPrefetch && row < rows) {
-    const char* xr = xb + row * ld_x * kEsz;
+  if (kPrefetch && wrow + lead < rows) {
+    const char* xr = xb + (wrow + lead) * ld_x * kEsz;
 #pragma unroll
     for (int i = 0; i < NV; ++i) nx[i] = load_chunk16<kKind>(xr, t + i * TPR, nfull, tail);
   }
   int buf = 0;
-  for (; row < rows; row += stride) {
+  for (; wrow < rows; wrow += stride) {
+    const int64_t row = wrow + lead;
+    const bool active = row < rows;
     float2 w[NV][kEpc / 2];
     if (kPrefetch) {
 #pragma unroll
-      for (int i = 0; i < NV; ++i) unpack_chunk16<kKind>(nx[i], w[i]);
+      for (int i = 0; i < NV; ++i) unpack_chunk16<kKind>(active ? nx[i] : pad, w[i]);
       const int64_t next = row + stride;
       if (next < rows) {
         const char* xr = xb + next * ld_x * kEsz;
@@ -680,7 +693,8 @@ softmax_rows_grouped_kernel(const void* __restrict__ x, void* __restrict__ y,
     } else {
       const char* xr = xb + row * ld_x * kEsz;
 #pragma unroll
-      for (int i = 0; i < NV; ++i) unpack_chunk16<kKind>(load_chunk16<kKind>(xr, t + i * TPR, nfull, tail), w[i]);
+      for (int i = 0; i < NV; ++i)
+        unpack_chunk16<kKind>(active ? load_chunk16<kKind>(xr, t + i * TPR, nfull, tail) : pad, w[i]);
     }
     float xa = neg_inf(), xc = neg_inf();
 #pragma unroll
@@ -710,10 +724,12 @@ softmax_rows_grouped_kernel(const void* __restrict__ x, void* __restrict__ y,
     if (xm_t != neg_inf() && ls > 0.f)
       f = ex2(base2_of(xm_t, k) - base2_of(xm, k)) * (1.0f / ls);
     const float2 f2 = make_float2(f, f);
-    char* yr = yb + row * ld_y * kEsz;
+    if (active) {
+      char* yr = yb + row * ld_y * kEsz;
 #pragma unroll
-    for (int i = 0; i < NV; ++i) store_chunk16<kKind>(yr, t + i * TPR, nfull, tail, pack_chunk16<kKind>(w[i], f2));
-    if (t == 0) write_ml(xm, ls, k, row, m_out, l_out);
+      for (int i = 0; i < NV; ++i) store_chunk16<kKind>(yr, t + i * TPR, nfull, tail, pack_chunk16<kKind>(w[i], f2));
+      if (t == 0) write_ml(xm, ls, k, row, m_out, l_out);
+    }
     buf ^= 1;
   }
 }
@@ -1247,7 +1263,11 @@ cudaError_t launch_softmax_rows(const float* x, float* y, float* m, float* l, in
   // Rows of up to 2048 elements: several rows per CTA, each thread holding
   // up to four 16-byte chunks (configurations measured on the GB300 at
   // 2^28 elements per matrix; prefetching helped only the shortest rows).
-  if (chunks <= 32) {
+  if (chunks <= 8) {
+    launch_grouped<0, 8, 1, true, 8>(x, y, m, l, rows, c, ld_x, ld_y, k, stream);
+  } else if (chunks <= 16) {
+    launch_grouped<0, 16, 1, true, 8>(x, y, m, l, rows, c, ld_x, ld_y, k, stream);
+  } else if (chunks <= 32) {
     launch_grouped<0, 32, 1, true, 8>(x, y, m, l, rows, c, ld_x, ld_y, k, stream);
   } else if (chunks <= 64) {
     launch_grouped<0, 32, 2, false, 6>(x, y, m, l, rows, c, ld_x, ld_y, k, stream);
@@ -1286,8 +1306,13 @@ void dispatch_rows16(const uint16_t* x, uint16_t* y, float* m, float* l, int64_t
   // Rows of up to 16384 elements: persistent CTAs with the next row's chunks
   // prefetched into registers (the widening of fp16 costs a conversion per
   // element, and without the prefetch that arithmetic stalled the loads);
-  // 256 / TPR rows per CTA for rows of up to 4096 elements.
-  if (chunks <= 32) {
+  // 256 / TPR rows per CTA for rows of up to 4096 elements (groups of 8 and
+  // 16 threads, without the prefetch, for rows of up to 128).
+  if (chunks <= 8) {
+    launch_grouped<kType, 8, 1, false, 8>(x, y, m, l, rows, c, ld_x, ld_y, k, stream);
+  } else if (chunks <= 16) {
+    launch_grouped<kType, 16, 1, false, 8>(x, y, m, l, rows, c, ld_x, ld_y, k, stream);
+  } else if (chunks <= 32) {
     launch_grouped<kType, 32, 1, true, 6>(x, y, m, l, rows, c, ld_x, ld_y, k, stream);
   } else if (chunks <= 64) {
     launch_grouped<kType, 32, 2, true, 5>(x, y, m, l, rows, c, ld_x, ld_y, k, stream);
