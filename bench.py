@@ -55,19 +55,19 @@ NOMINAL = {"hbm_gbs": 7900.0, "bf16_tflops": 2250.0}
 # same kernel, applied to the full launch's algorithmic bytes.
 NCU_TRAFFIC = {
     "softmax_32k": {"source": "pass_attention_gb300/csrc/softmax_rows.cu",
-                    "sha256": "821ba7b1d176258ad6a976c863ebf32a3bea1ce5793057cd4b863b837b265c5f",
-                    "bytes_per_launch": 1073795584 + 1017249792},
+                    "sha256": "3707cb03171d8e73906b9ddeebaf2326b15efb121e82c4a44d70131e637db429",
+                    "bytes_per_launch": 1073794816 + 1017689856},
     "softmax_32k_bf16": {"source": "pass_attention_gb300/csrc/softmax_rows.cu",
-                         "sha256": "821ba7b1d176258ad6a976c863ebf32a3bea1ce5793057cd4b863b837b265c5f",
-                         "bytes_per_launch": 536905472 + 482804736},
+                         "sha256": "3707cb03171d8e73906b9ddeebaf2326b15efb121e82c4a44d70131e637db429",
+                         "bytes_per_launch": 536906240 + 482423296},
     # the comparators: all sweeps of one call (each reads x from DRAM again)
     "softmax_32k_3pass": {"source": "pass_attention_gb300/csrc/softmax_rows.cu",
-                          "sha256": "821ba7b1d176258ad6a976c863ebf32a3bea1ce5793057cd4b863b837b265c5f",
-                          "bytes_per_launch": (1073761536 + 2903552) + (1073906944 + 164096)
-                          + (1074059776 + 1025022464)},
+                          "sha256": "3707cb03171d8e73906b9ddeebaf2326b15efb121e82c4a44d70131e637db429",
+                          "bytes_per_launch": (1073779456 + 2790400) + (1073906432 + 194304)
+                          + (1074053120 + 1024722944)},
     "softmax_32k_2pass": {"source": "pass_attention_gb300/csrc/softmax_rows.cu",
-                          "sha256": "821ba7b1d176258ad6a976c863ebf32a3bea1ce5793057cd4b863b837b265c5f",
-                          "bytes_per_launch": (1073761024 + 3028480) + (1074143232 + 1024922880)},
+                          "sha256": "3707cb03171d8e73906b9ddeebaf2326b15efb121e82c4a44d70131e637db429",
+                          "bytes_per_launch": (1073800704 + 3015680) + (1074044672 + 1024711936)},
     "attn_4k": {"source": "pass_attention_gb300/csrc/attn_fwd.cu",
                 "sha256": "1de91f1a14f7b69059f99bd37628b4126df733c28a5f205b034826a15235ccec",
                 "bytes_per_launch": 201502976 + 47736320},

@@ -142,6 +142,112 @@ __device__ __forceinline__ void write_ml(float xm, float ls, const ScaleConsts& 
   if (l_out) l_out[row] = ls * ex2(delta);
 }
 
+// ---------------------------------------------------------------------------
+// Thread-block clusters: the launch constants of the cluster-resident kernel
+// and the helpers every cluster-aware kernel uses. A kernel launched without
+// a cluster sees each CTA as a cluster of one.
+// ---------------------------------------------------------------------------
+
+constexpr int kClThreads = 512;
+constexpr int kClUnroll = 4;  // chunks each thread loads before using them
+constexpr int kClWarps = kClThreads / 32;
+constexpr int kClMaxCtas = 8;
+constexpr int kClPiece = 16384;                       // bytes per bulk copy
+constexpr unsigned long long kClTimeoutNs = 2000000000ull;  // bounded wait on the copies
+constexpr int64_t kClDoubleCap = int64_t(48) << 10;   // rows this short: one CTA, two buffers
+constexpr int64_t kClSingleCap = int64_t(200) << 10;  // longer rows: one buffer per CTA
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ uint64_t timer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_size() {
+  uint32_t n;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(n));
+  return n;
+}
+__device__ __forceinline__ uint32_t cluster_id() {
+  uint32_t c;
+  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(c));
+  return c;
+}
+__device__ __forceinline__ uint32_t cluster_count() {
+  uint32_t c;
+  asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(c));
+  return c;
+}
+// every thread of every CTA of the cluster; orders shared-memory writes
+// (local and remote) before the barrier with reads after it
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
+// The same barrier when only warp 0 has written anything the cluster reads
+// after it: the other warps arrive without a release fence.
+__device__ __forceinline__ void cluster_sync_warp0_wrote() {
+  if (threadIdx.x < 32)
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+  else
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// (a, b) into the same shared-memory slot of CTA `rank` of the cluster
+__device__ __forceinline__ void st_peer_f2(const void* slot, uint32_t rank, float a, float b) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(slot)), "r"(rank));
+  asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(remote), "f"(a), "f"(b) : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Wait for the phase with the given parity, for at most kClTimeoutNs; a
+// give-up is recorded in the error word and the caller carries on (every CTA
+// of the cluster must still reach the same cluster barriers).
+__device__ __forceinline__ void mbar_wait_bounded(uint32_t bar, uint32_t parity, unsigned int* err) {
+  if (mbar_try(bar, parity)) return;
+  const uint64_t t0 = timer_ns();
+  for (uint32_t n = 1;; ++n) {
+    if (mbar_try(bar, parity)) return;
+    if ((n & 63u) == 0 && timer_ns() - t0 > kClTimeoutNs) {
+      report_error(err, kKernelSoftmaxRows | (1u << 8));
+      return;
+    }
+  }
+}
+
+// n-ary merge of the n <= 32 (max, sum) states s[0..n), by one warp: lane w
+// takes state w, the lanes' maximum by shuffles, then each sum scaled to it
+// (one ex2) and the scaled sums added by shuffles. Every warp that calls it
+// gets the same result.
+__device__ __forceinline__ float2 merge_states_warp(const float2* s, int n, const ScaleConsts& k) {
+  const int lane = threadIdx.x & 31;
+  const float2 e = (lane < n) ? s[lane] : make_float2(neg_inf(), 0.f);
+  float x = e.x;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, off));
+  float l = (e.x == neg_inf()) ? 0.f : e.y * ex2(base2_of(e.x, k) - base2_of(x, k));
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
+  return make_float2(x, l);
+}
+
 template <int NV>
 __global__ void __launch_bounds__(kThreads, (NV <= 8) ? 4 : 2)
 softmax_rows_reg_kernel(const float* __restrict__ x, float* __restrict__ y,
@@ -220,16 +326,24 @@ __global__ void __launch_bounds__(kThreads)
 softmax_rows_stream_kernel(const float* __restrict__ x, float* __restrict__ y,
                            float* __restrict__ m_out, float* __restrict__ l_out,
                            int64_t rows, int64_t cols, int64_t ld_x, int64_t ld_y,
-                           ScaleConsts k) {
+                           ScaleConsts k, int64_t slice_chunks) {
   __shared__ float2 sh[kWarps];
+  __shared__ float2 cstate[2][kClMaxCtas];
   constexpr int W = kVec ? 4 : 1;
   const int64_t nchunks = (cols + W - 1) / W;
   const int tid = threadIdx.x;
-  for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
+  // in a cluster of C CTAs, CTA r streams chunks [r * slice, (r + 1) * slice)
+  const uint32_t C = cluster_size();
+  const uint32_t rank = cluster_rank();
+  const int64_t c_lo = static_cast<int64_t>(rank) * slice_chunks;
+  const int64_t c_hi = (c_lo + slice_chunks < nchunks) ? c_lo + slice_chunks : nchunks;
+  if (C > 1) cluster_sync_all();  // every peer has started before any writes to it
+  int sbuf = 0;
+  for (int64_t row = cluster_id(); row < rows; row += cluster_count()) {
     const float* xr = x + row * ld_x;
     float* yr = y + row * ld_y;
     float xm = neg_inf(), ls = 0.f;
-    for (int64_t c = tid; c < nchunks; c += kThreads) {
+    for (int64_t c = c_lo + tid; c < c_hi; c += kThreads) {
       float v[W];
       if (kVec && (c + 1) * W <= cols) {
         const float4 f = __ldg(reinterpret_cast<const float4*>(xr) + c);
@@ -253,9 +367,18 @@ softmax_rows_stream_kernel(const float* __restrict__ x, float* __restrict__ y,
       xm = xn;
     }
     cta_merge(xm, ls, k, sh);
+    if (C > 1) {  // the cluster's CTA states, through distributed shared memory
+      if (tid == 0)
+        for (uint32_t r = 0; r < C; ++r) st_peer_f2(&cstate[sbuf][rank], r, xm, ls);
+      cluster_sync_warp0_wrote();
+      const float2 st = merge_states_warp(cstate[sbuf], static_cast<int>(C), k);
+      xm = st.x;
+      ls = st.y;
+      sbuf ^= 1;
+    }
     const float M = (xm == neg_inf()) ? 0.f : base2_of(xm, k);
     const float inv = (ls > 0.f) ? 1.0f / ls : 0.f;
-    for (int64_t c = tid; c < nchunks; c += kThreads) {
+    for (int64_t c = c_lo + tid; c < c_hi; c += kThreads) {
       if (kVec && (c + 1) * W <= cols) {
         const float4 f = __ldg(reinterpret_cast<const float4*>(xr) + c);
         const float4 o = make_float4(weight(f.x, M, k) * inv, weight(f.y, M, k) * inv,
@@ -266,7 +389,7 @@ softmax_rows_stream_kernel(const float* __restrict__ x, float* __restrict__ y,
           if (c * W + e < cols) yr[c * W + e] = weight(xr[c * W + e], M, k) * inv;
       }
     }
-    if (tid == 0) write_ml(xm, ls, k, row, m_out, l_out);
+    if (rank == 0 && tid == 0) write_ml(xm, ls, k, row, m_out, l_out);
     __syncthreads();
   }
 }
@@ -745,106 +868,6 @@ softmax_rows_grouped_kernel(const void* __restrict__ x, void* __restrict__ y,
 // streaming kernel reads the row twice.
 // ---------------------------------------------------------------------------
 
-constexpr int kClThreads = 512;
-constexpr int kClUnroll = 4;  // chunks each thread loads before using them
-constexpr int kClWarps = kClThreads / 32;
-constexpr int kClMaxCtas = 8;
-constexpr int kClPiece = 16384;                       // bytes per bulk copy
-constexpr unsigned long long kClTimeoutNs = 2000000000ull;  // bounded wait on the copies
-constexpr int64_t kClDoubleCap = int64_t(48) << 10;   // rows this short: one CTA, two buffers
-constexpr int64_t kClSingleCap = int64_t(200) << 10;  // longer rows: one buffer per CTA
-
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-__device__ __forceinline__ uint64_t timer_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-__device__ __forceinline__ uint32_t cluster_size() {
-  uint32_t n;
-  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(n));
-  return n;
-}
-__device__ __forceinline__ uint32_t cluster_id() {
-  uint32_t c;
-  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(c));
-  return c;
-}
-__device__ __forceinline__ uint32_t cluster_count() {
-  uint32_t c;
-  asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(c));
-  return c;
-}
-// every thread of every CTA of the cluster; orders shared-memory writes
-// (local and remote) before the barrier with reads after it
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
-                   : "memory");
-}
-// The same barrier when only warp 0 has written anything the cluster reads
-// after it: the other warps arrive without a release fence.
-__device__ __forceinline__ void cluster_sync_warp0_wrote() {
-  if (threadIdx.x < 32)
-    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
-  else
-    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
-  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-// (a, b) into the same shared-memory slot of CTA `rank` of the cluster
-__device__ __forceinline__ void st_peer_f2(const void* slot, uint32_t rank, float a, float b) {
-  uint32_t remote;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(slot)), "r"(rank));
-  asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(remote), "f"(a), "f"(b) : "memory");
-}
-__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-// Wait for the phase with the given parity, for at most kClTimeoutNs; a
-// give-up is recorded in the error word and the caller carries on (every CTA
-// of the cluster must still reach the same cluster barriers).
-__device__ __forceinline__ void mbar_wait_bounded(uint32_t bar, uint32_t parity, unsigned int* err) {
-  if (mbar_try(bar, parity)) return;
-  const uint64_t t0 = timer_ns();
-  for (uint32_t n = 1;; ++n) {
-    if (mbar_try(bar, parity)) return;
-    if ((n & 63u) == 0 && timer_ns() - t0 > kClTimeoutNs) {
-      report_error(err, kKernelSoftmaxRows | (1u << 8));
-      return;
-    }
-  }
-}
-
-// n-ary merge of the n <= 32 (max, sum) states s[0..n), by one warp: lane w
-// takes state w, the lanes' maximum by shuffles, then each sum scaled to it
-// (one ex2) and the scaled sums added by shuffles. Every warp that calls it
-// gets the same result.
-__device__ __forceinline__ float2 merge_states_warp(const float2* s, int n, const ScaleConsts& k) {
-  const int lane = threadIdx.x & 31;
-  const float2 e = (lane < n) ? s[lane] : make_float2(neg_inf(), 0.f);
-  float x = e.x;
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, off));
-  float l = (e.x == neg_inf()) ? 0.f : e.y * ex2(base2_of(e.x, k) - base2_of(x, k));
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
-  return make_float2(x, l);
-}
-
 // Issue the copies of one row's slice into `buf_a` (thread 0 only): the
 // whole 16-byte chunks by bulk copies that complete on `bar_a`, the last
 // partial chunk (if any) by plain loads, padded with -inf.
@@ -1022,16 +1045,25 @@ template <int kType, bool kVec>
 __global__ void __launch_bounds__(kThreads)
 softmax_rows16_stream_kernel(const uint16_t* __restrict__ x, uint16_t* __restrict__ y,
                              float* __restrict__ m_out, float* __restrict__ l_out, int64_t rows,
-                             int64_t cols, int64_t ld_x, int64_t ld_y, ScaleConsts k) {
+                             int64_t cols, int64_t ld_x, int64_t ld_y, ScaleConsts k,
+                             int64_t slice_chunks) {
   __shared__ float2 sh[kWarps];
+  __shared__ float2 cstate[2][kClMaxCtas];
   constexpr int W = kVec ? 8 : 1;
   const int64_t nchunks = (cols + W - 1) / W;
   const int tid = threadIdx.x;
-  for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
+  // in a cluster of C CTAs, CTA r streams chunks [r * slice, (r + 1) * slice)
+  const uint32_t C = cluster_size();
+  const uint32_t rank = cluster_rank();
+  const int64_t c_lo = static_cast<int64_t>(rank) * slice_chunks;
+  const int64_t c_hi = (c_lo + slice_chunks < nchunks) ? c_lo + slice_chunks : nchunks;
+  if (C > 1) cluster_sync_all();  // every peer has started before any writes to it
+  int sbuf = 0;
+  for (int64_t row = cluster_id(); row < rows; row += cluster_count()) {
     const uint16_t* xr = x + row * ld_x;
     uint16_t* yr = y + row * ld_y;
     float xm = neg_inf(), ls = 0.f;
-    for (int64_t c = tid; c < nchunks; c += kThreads) {
+    for (int64_t c = c_lo + tid; c < c_hi; c += kThreads) {
       if (kVec && (c + 1) * W <= cols) {
         const uint4 v = __ldg(reinterpret_cast<const uint4*>(xr) + c);
         const float xn = fmaxf(xm, max8<kType>(v));
@@ -1053,9 +1085,18 @@ softmax_rows16_stream_kernel(const uint16_t* __restrict__ x, uint16_t* __restric
       }
     }
     cta_merge(xm, ls, k, sh);
+    if (C > 1) {  // the cluster's CTA states, through distributed shared memory
+      if (tid == 0)
+        for (uint32_t r = 0; r < C; ++r) st_peer_f2(&cstate[sbuf][rank], r, xm, ls);
+      cluster_sync_warp0_wrote();
+      const float2 st = merge_states_warp(cstate[sbuf], static_cast<int>(C), k);
+      xm = st.x;
+      ls = st.y;
+      sbuf ^= 1;
+    }
     const float M = (xm == neg_inf()) ? 0.f : base2_of(xm, k);
     const float inv = (ls > 0.f) ? 1.0f / ls : 0.f;
-    for (int64_t c = tid; c < nchunks; c += kThreads) {
+    for (int64_t c = c_lo + tid; c < c_hi; c += kThreads) {
       if (kVec && (c + 1) * W <= cols) {
         const uint4 v = __ldg(reinterpret_cast<const uint4*>(xr) + c);
         __stcs(reinterpret_cast<uint4*>(yr) + c, out8<kType>(v, M, inv, k));
@@ -1064,7 +1105,7 @@ softmax_rows16_stream_kernel(const uint16_t* __restrict__ x, uint16_t* __restric
           yr[j] = h16_round<kType>(weight(h16_one<kType>(xr[j]), M, k) * inv);
       }
     }
-    if (tid == 0) write_ml(xm, ls, k, row, m_out, l_out);
+    if (rank == 0 && tid == 0) write_ml(xm, ls, k, row, m_out, l_out);
     __syncthreads();
   }
 }
@@ -1109,6 +1150,45 @@ ScaleConsts make_consts(float scale) {
 }
 
 }  // namespace
+
+// Launch of a streaming kernel (`width` elements per chunk): a CTA per row
+// while the rows fill the GPU (eight CTAs per SM); with fewer rows each row is
+// cut into C contiguous slices, one per CTA of a cluster of C <= 8, as long
+// as every CTA keeps at least 16 chunks per thread. The slices' states meet
+// through distributed shared memory. A failed cluster launch falls back to a
+// CTA per row.
+template <typename T, typename Kernel>
+void launch_stream(Kernel kernel, const T* x, T* y, float* m, float* l, int64_t rows, int64_t cols,
+                   int64_t ld_x, int64_t ld_y, const ScaleConsts& k, int width, cudaStream_t stream) {
+  const int64_t nchunks = (cols + width - 1) / width;
+  const int64_t resident = static_cast<int64_t>(sm_count()) * 8;
+  int64_t c = 1;
+  if (rows < resident) {
+    c = resident / rows;
+    const int64_t by_work = nchunks / (int64_t(kThreads) * 16);
+    if (c > by_work) c = by_work;
+    if (c > kClMaxCtas) c = kClMaxCtas;
+    if (c < 1) c = 1;
+  }
+  if (c > 1) {
+    const int64_t slice = (nchunks + c - 1) / c;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned int>(c);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.gridDim = dim3(static_cast<unsigned int>(rows * c), 1, 1);
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, kernel, x, y, m, l, rows, cols, ld_x, ld_y, k, slice) == cudaSuccess)
+      return;
+    cudaGetLastError();
+  }
+  kernel<<<grid_for(rows, 4), kThreads, 0, stream>>>(x, y, m, l, rows, cols, ld_x, ld_y, k, nchunks);
+}
 
 // Launch of softmax_rows_grouped_kernel: persistent (one wave of kMinBlocks
 // CTAs per SM) when it prefetches, else up to 64 waves of a grid-stride loop.
@@ -1254,7 +1334,7 @@ cudaError_t launch_softmax_rows(const float* x, float* y, float* m, float* l, in
   const bool vec = ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y)) & 15u) == 0 &&
                    (ld_x & 3) == 0 && (ld_y & 3) == 0;
   if (!vec) {
-    softmax_rows_stream_kernel<false><<<grid_for(rows, 4), kThreads, 0, stream>>>(x, y, m, l, rows, cols, ld_x, ld_y, k);
+    launch_stream(softmax_rows_stream_kernel<false>, x, y, m, l, rows, cols, ld_x, ld_y, k, 1, stream);
     return cudaGetLastError();
   }
   const int64_t chunks = (cols + 3) / 4;
@@ -1285,7 +1365,7 @@ cudaError_t launch_softmax_rows(const float* x, float* y, float* m, float* l, in
     softmax_rows_reg_kernel<16><<<grid_for(rows, 2), kThreads, 0, stream>>>(x, y, m, l, rows, c, ld_x, ld_y, k);
   } else {
     if (!launch_cluster_rows<0>(x, y, m, l, rows, cols, ld_x, ld_y, k, err_word, stream))
-      softmax_rows_stream_kernel<true><<<grid_for(rows, 4), kThreads, 0, stream>>>(x, y, m, l, rows, cols, ld_x, ld_y, k);
+      launch_stream(softmax_rows_stream_kernel<true>, x, y, m, l, rows, cols, ld_x, ld_y, k, 4, stream);
   }
   return cudaGetLastError();
 }
@@ -1296,9 +1376,8 @@ void dispatch_rows16(const uint16_t* x, uint16_t* y, float* m, float* l, int64_t
                      unsigned int* err_word, cudaStream_t stream) {
   const bool vec = ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y)) & 15u) == 0 &&
                    (ld_x & 7) == 0 && (ld_y & 7) == 0;
-  const int g = grid_for(rows, 4);
   if (!vec) {
-    softmax_rows16_stream_kernel<kType, false><<<g, kThreads, 0, stream>>>(x, y, m, l, rows, cols, ld_x, ld_y, k);
+    launch_stream(softmax_rows16_stream_kernel<kType, false>, x, y, m, l, rows, cols, ld_x, ld_y, k, 1, stream);
     return;
   }
   const int64_t chunks = (cols + 7) / 8;
@@ -1328,7 +1407,7 @@ void dispatch_rows16(const uint16_t* x, uint16_t* y, float* m, float* l, int64_t
     launch_grouped<kType, 256, 8, true, 2>(x, y, m, l, rows, c, ld_x, ld_y, k, stream);
   } else {
     if (!launch_cluster_rows<kType>(x, y, m, l, rows, cols, ld_x, ld_y, k, err_word, stream))
-      softmax_rows16_stream_kernel<kType, true><<<g, kThreads, 0, stream>>>(x, y, m, l, rows, cols, ld_x, ld_y, k);
+      launch_stream(softmax_rows16_stream_kernel<kType, true>, x, y, m, l, rows, cols, ld_x, ld_y, k, 8, stream);
   }
 }
 

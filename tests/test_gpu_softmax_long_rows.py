@@ -94,3 +94,47 @@ def test_long_rows_repeat_identical():
     y2, m2, l2 = oss.softmax_rows(x, 1.0)
     torch.cuda.synchronize()
     assert torch.equal(y1, y2) and torch.equal(m1, m2) and torch.equal(l1, l2)
+
+
+@pytest.mark.parametrize("rows,cols,ld,offset", [
+    (2, 40003, 40003, 0),      # unaligned rows, too few to fill the GPU: a cluster per row
+    (3, 300001, 300002, 1),    # unaligned base and leading dimension
+    (1, 2000000, 2000000, 0),  # aligned but beyond a cluster's shared memory (8 MB)
+    (5, 600000, 600000, 0),
+])
+@pytest.mark.parametrize("mask", [False, True])
+def test_fp32_streamed_rows_split_across_a_cluster(rows, cols, ld, offset, mask):
+    # rows that take the streaming kernel, with fewer rows than the GPU holds
+    # CTAs: each row is cut into slices streamed by the CTAs of a cluster,
+    # whose states merge through distributed shared memory
+    buf = workloads.logits(1, rows * ld + offset, 10.0, seed=cols + offset + mask, device="cuda")
+    x = buf[0, offset:].view(rows, ld)[:, :cols]
+    if mask:
+        g = torch.Generator(device="cuda").manual_seed(cols)
+        x[torch.rand(x.shape, generator=g, device="cuda") < 0.2] = -float("inf")
+        x[0, : cols - 10] = -float("inf")  # only the last slice has live entries
+    ybuf = torch.empty(rows * ld + offset, device="cuda")
+    y = ybuf[offset:].view(rows, ld)[:, :cols]
+    y, m, l = oss.softmax_rows(x, 0.6, y=y)
+    torch.cuda.synchronize()
+    check_softmax(y.cpu().numpy(), m.cpu().numpy(), l.cpu().numpy(),
+                  *oracle.softmax_rows(x.cpu().numpy(), f32(0.6)), what=f"fp32 {rows}x{cols}")
+
+
+@pytest.mark.parametrize("kind", ["bf16", "f16"])
+@pytest.mark.parametrize("rows,cols,ld,offset", [
+    (2, 40003, 40003, 0), (3, 300001, 300003, 1), (1, 4000000, 4000000, 0),
+])
+def test_16bit_streamed_rows_split_across_a_cluster(kind, rows, cols, ld, offset):
+    dtype = torch.bfloat16 if kind == "bf16" else torch.float16
+    buf = workloads.logits(1, rows * ld + offset, 10.0, seed=cols * 7 + offset, device="cuda").to(dtype)
+    x = buf[0, offset:].view(rows, ld)[:, :cols]
+    g = torch.Generator(device="cuda").manual_seed(cols + 1)
+    x[torch.rand(x.shape, generator=g, device="cuda") < 0.2] = -float("inf")
+    ybuf = torch.empty(rows * ld + offset, dtype=dtype, device="cuda")
+    y = ybuf[offset:].view(rows, ld)[:, :cols]
+    y, m, l = oss.softmax_rows_16bit(x, 0.6, y=y)
+    torch.cuda.synchronize()
+    xr = x.float().cpu().numpy().astype(np.float64)
+    check_softmax16(y.float().cpu().numpy(), m.cpu().numpy(), l.cpu().numpy(),
+                    *oracle.softmax_rows(xr, f32(0.6)), kind=kind, what=f"{kind} {rows}x{cols}")
