@@ -276,8 +276,8 @@ OSS_API os_status os_check_device_error(void* stream, int32_t* code);
 
 /*
  * os_debug_inject_fault -- test hook for the bounded waits. Arms a fault for
- * the next os_attention_fwd call made by the calling host thread (then
- * disarms it):
+ * the next call of the kind's entry point made by the calling host thread
+ * (that call disarms it):
  *   kind 0: disarm.
  *   kind 1: the kernel's load warp skips the V tile of KV step `step` (counted
  *           in the order each CTA visits its KV tiles), so the thread that
@@ -290,8 +290,18 @@ OSS_API os_status os_check_device_error(void* stream, int32_t* code);
  *           1, wait site 3: V tile full); bits 16..31 hold the launch's tag.
  *           The CUDA context stays usable; the outputs of that call are
  *           undefined.
+ *   kind 2: the next os_softmax_rows or os_softmax_rows_16bit call. If it
+ *           holds its rows in a cluster's shared memory (aligned rows longer
+ *           than 16384 elements and at most 1.6 MB), every CTA's barrier for
+ *           the bulk copies of its first row is told to expect 16 bytes more
+ *           than are copied. The wait gives up after `timeout_ns` (0: 2 s);
+ *           from then on each CTA waits and copies no more but still meets
+ *           its cluster's barriers, so the launch ends. os_check_device_error
+ *           then returns OS_ERR_TIMEOUT with code 2 | (1 << 8). The outputs of
+ *           that call are undefined; other paths ignore the hook. `step` is
+ *           unused.
  * No GPU fault, trap or endless wait is involved.
- * Errors: OS_ERR_INVALID_ARGUMENT (kind not 0/1, step < 0, timeout_ns < 0).
+ * Errors: OS_ERR_INVALID_ARGUMENT (kind not 0/1/2, step < 0, timeout_ns < 0).
  */
 OSS_API os_status os_debug_inject_fault(int32_t kind, int32_t step, int64_t timeout_ns);
 

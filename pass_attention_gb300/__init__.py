@@ -461,8 +461,9 @@ def decode_from_host(q_host, k_host, v_host, kv_len_host, num_splits, scale=None
 
 
 def debug_inject_fault(kind: int, step: int = 0, timeout_ns: int = 0) -> None:
-    """Test hook: arm a fault for the next attention_fwd call on this thread
-    (see ``os_debug_inject_fault`` in include/oss.h)."""
+    """Test hook: arm a fault for the next attention_fwd call (kind 1) or
+    row softmax call (kind 2) on this thread; kind 0 disarms (see
+    ``os_debug_inject_fault`` in include/oss.h)."""
     _check(load().os_debug_inject_fault(int(kind), int(step), int(timeout_ns)),
            "os_debug_inject_fault")
 

@@ -43,6 +43,9 @@ bool valid_scale(float s) { return std::isfinite(s) && s > 0.f; }
 // Armed by os_debug_inject_fault, consumed by the next os_attention_fwd on
 // the same host thread.
 thread_local oss::AttnFault t_fault;
+// Armed by os_debug_inject_fault (kind 2), consumed by the next
+// os_softmax_rows or os_softmax_rows_16bit on the same host thread.
+thread_local oss::RowsFault t_rows_fault;
 
 }  // namespace
 
@@ -71,8 +74,10 @@ os_status os_softmax_rows(const float* x, float* y, float* m, float* l, int64_t 
   if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y) |
        reinterpret_cast<uintptr_t>(m) | reinterpret_cast<uintptr_t>(l)) & 3u)
     return OS_ERR_MISALIGNED;
+  const oss::RowsFault fault = t_rows_fault;
+  t_rows_fault = oss::RowsFault();
   return from_cuda(oss::launch_softmax_rows(x, y, m, l, rows, cols, ld_x, ld_y, scale,
-                                            error_word(), static_cast<cudaStream_t>(stream)));
+                                            error_word(), fault, static_cast<cudaStream_t>(stream)));
 }
 
 os_status os_softmax_rows_16bit(const void* x, void* y, float* m, float* l, int64_t rows,
@@ -85,9 +90,11 @@ os_status os_softmax_rows_16bit(const void* x, void* y, float* m, float* l, int6
     return OS_ERR_INVALID_ARGUMENT;
   if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y)) & 1u) return OS_ERR_MISALIGNED;
   if ((reinterpret_cast<uintptr_t>(m) | reinterpret_cast<uintptr_t>(l)) & 3u) return OS_ERR_MISALIGNED;
+  const oss::RowsFault fault = t_rows_fault;
+  t_rows_fault = oss::RowsFault();
   return from_cuda(oss::launch_softmax_rows16(static_cast<const uint16_t*>(x),
                                               static_cast<uint16_t*>(y), m, l, rows, cols, ld_x,
-                                              ld_y, scale, dtype, error_word(),
+                                              ld_y, scale, dtype, error_word(), fault,
                                               static_cast<cudaStream_t>(stream)));
 }
 
@@ -175,11 +182,15 @@ os_status os_merge_partials(const float* part_m, const float* part_l, const floa
 }
 
 os_status os_debug_inject_fault(int32_t kind, int32_t step, int64_t timeout_ns) {
-  if (kind < 0 || kind > 1 || step < 0 || timeout_ns < 0) return OS_ERR_INVALID_ARGUMENT;
+  if (kind < 0 || kind > 2 || step < 0 || timeout_ns < 0) return OS_ERR_INVALID_ARGUMENT;
   t_fault = oss::AttnFault();
+  t_rows_fault = oss::RowsFault();
   if (kind == 1) {
     t_fault.skip_v_step = step;
     t_fault.timeout_ns = timeout_ns;
+  } else if (kind == 2) {
+    t_rows_fault.extra_tx = 16;
+    t_rows_fault.timeout_ns = timeout_ns;
   }
   return OS_OK;
 }

@@ -10,17 +10,27 @@ namespace oss {
 // Kernel ids stored in bits 0..7 of the device error word.
 enum KernelId : unsigned int { kKernelAttnFwd = 1, kKernelSoftmaxRows = 2 };
 
+// Test hook for the bounded wait of the cluster-resident row kernel (see
+// os_debug_inject_fault): extra_tx > 0 makes each CTA expect that many bytes
+// more than its first row's copies deliver; timeout_ns > 0 replaces the
+// default wait limit.
+struct RowsFault {
+  uint32_t extra_tx = 0;
+  int64_t timeout_ns = 0;
+};
+
 // err_word: the device error word (the cluster-resident kernel records a
 // give-up on its bounded wait there); may be null.
 cudaError_t launch_softmax_rows(const float* x, float* y, float* m, float* l,
                                 int64_t rows, int64_t cols, int64_t ld_x, int64_t ld_y,
-                                float scale, unsigned int* err_word, cudaStream_t stream);
+                                float scale, unsigned int* err_word, const RowsFault& fault,
+                                cudaStream_t stream);
 
 // 16-bit rows: dtype 1 = bf16, 2 = fp16 (x and y); m, l fp32 or null.
 cudaError_t launch_softmax_rows16(const uint16_t* x, uint16_t* y, float* m, float* l,
                                   int64_t rows, int64_t cols, int64_t ld_x, int64_t ld_y,
                                   float scale, int dtype, unsigned int* err_word,
-                                  cudaStream_t stream);
+                                  const RowsFault& fault, cudaStream_t stream);
 
 // Comparators: passes = 2 (online (m, l) pass, then a write pass) or 3 (max
 // pass, sum pass, write pass); each pass re-reads x from HBM. m, l required.

@@ -217,17 +217,20 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Wait for the phase with the given parity, for at most kClTimeoutNs; a
-// give-up is recorded in the error word and the caller carries on (every CTA
-// of the cluster must still reach the same cluster barriers).
-__device__ __forceinline__ void mbar_wait_bounded(uint32_t bar, uint32_t parity, unsigned int* err) {
-  if (mbar_try(bar, parity)) return;
+// Wait for the phase with the given parity, for at most timeout_ns.
+// Returns false on a give-up, which is recorded in the error word; the caller
+// carries on (every CTA of the cluster must still reach the same cluster
+// barriers) but waits and copies no more, so a failed launch ends after
+// about one timeout rather than one per row.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, unsigned int* err,
+                                                  uint64_t timeout_ns) {
+  if (mbar_try(bar, parity)) return true;
   const uint64_t t0 = timer_ns();
   for (uint32_t n = 1;; ++n) {
-    if (mbar_try(bar, parity)) return;
-    if ((n & 63u) == 0 && timer_ns() - t0 > kClTimeoutNs) {
+    if (mbar_try(bar, parity)) return true;
+    if ((n & 63u) == 0 && timer_ns() - t0 > timeout_ns) {
       report_error(err, kKernelSoftmaxRows | (1u << 8));
-      return;
+      return false;
     }
   }
 }
@@ -870,15 +873,18 @@ softmax_rows_grouped_kernel(const void* __restrict__ x, void* __restrict__ y,
 
 // Issue the copies of one row's slice into `buf_a` (thread 0 only): the
 // whole 16-byte chunks by bulk copies that complete on `bar_a`, the last
-// partial chunk (if any) by plain loads, padded with -inf.
+// partial chunk (if any) by plain loads, padded with -inf. The barrier is
+// told to expect `extra` bytes more than are copied (0 but in the test hook,
+// which makes the wait run out).
 template <int kKind>
 __device__ __forceinline__ void issue_slice(const char* xr, uint4* buf, uint32_t buf_a, uint32_t bar_a,
-                                            uint32_t bulk, int nfull, int tail) {
+                                            uint32_t bulk, int nfull, int tail, uint32_t extra) {
   // the buffer's previous contents were last touched through the generic
   // proxy; order that before the copies' asynchronous writes
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-  if (bulk > 0) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar_a), "r"(bulk)
+  if (bulk + extra > 0) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar_a),
+                 "r"(bulk + extra)
                  : "memory");
     for (uint32_t off = 0; off < bulk; off += kClPiece) {
       const uint32_t size = (bulk - off < kClPiece) ? (bulk - off) : kClPiece;
@@ -901,7 +907,8 @@ __global__ void __launch_bounds__(kClThreads, 2)
 softmax_rows_cluster_kernel(const void* __restrict__ x, void* __restrict__ y,
                             float* __restrict__ m_out, float* __restrict__ l_out, int64_t rows,
                             int64_t cols, int64_t ld_x, int64_t ld_y, ScaleConsts k,
-                            int slice_elems, unsigned int* err) {
+                            int slice_elems, unsigned int* err, uint32_t fault_tx,
+                            uint64_t timeout_ns) {
   constexpr int kEpc = RowElem<kKind>::kEpc;
   constexpr int kEsz = RowElem<kKind>::kSize;
   extern __shared__ __align__(128) uint4 slices[];  // this CTA's slice buffer(s), 16-byte chunks
@@ -934,26 +941,28 @@ softmax_rows_cluster_kernel(const void* __restrict__ x, void* __restrict__ y,
   cluster_sync_all();
   if (kDouble && tid == 0 && row0 < rows)
     issue_slice<kKind>(xb + (row0 * ld_x + lo) * kEsz, slices, smem_u32(slices), smem_u32(&bars[0]),
-                       bulk, nfull, tail);
+                       bulk, nfull, tail, fault_tx);
 
   uint32_t parity = 0u;  // bit b: the phase parity to wait for on buffer b
   int sbuf = 0;  // cstate set
   int it = 0;
+  bool live = true;  // false once this thread gave up on a wait: no more waits or copies
   for (int64_t row = row0; row < rows; row += rstep, ++it) {
     const int b = kDouble ? (it & 1) : 0;
     uint4* slice = slices + b * stride_chunks;
     const uint32_t bar_a = smem_u32(&bars[b]);
     char* yr = static_cast<char*>(y) + (row * ld_y + lo) * kEsz;
-    if (!kDouble && tid == 0)
-      issue_slice<kKind>(xb + (row * ld_x + lo) * kEsz, slice, smem_u32(slice), bar_a, bulk, nfull, tail);
-    mbar_wait_bounded(bar_a, (parity >> b) & 1u, err);
+    if (!kDouble && tid == 0 && live)
+      issue_slice<kKind>(xb + (row * ld_x + lo) * kEsz, slice, smem_u32(slice), bar_a, bulk, nfull, tail,
+                         it == 0 ? fault_tx : 0u);
+    if (live) live = mbar_wait_bounded(bar_a, (parity >> b) & 1u, err, timeout_ns);
     parity ^= 1u << b;
     __syncthreads();  // the tail chunk, written by thread 0
-    if (kDouble && tid == 0 && row + rstep < rows) {
+    if (kDouble && tid == 0 && live && row + rstep < rows) {
       // the other buffer was read out before the end of the previous row
       uint4* other = slices + (b ^ 1) * stride_chunks;
       issue_slice<kKind>(xb + ((row + rstep) * ld_x + lo) * kEsz, other, smem_u32(other),
-                         smem_u32(&bars[b ^ 1]), bulk, nfull, tail);
+                         smem_u32(&bars[b ^ 1]), bulk, nfull, tail, 0u);
     }
 
     // The thread's (max, sum) over its chunks, by the online recurrence:
@@ -1013,10 +1022,10 @@ softmax_rows_cluster_kernel(const void* __restrict__ x, void* __restrict__ y,
     ls = st.y;
 
     // y = 2^(x*c - M_row) / l, formed again from x (an empty row gives 0)
-    const bool live = (xm != neg_inf()) && ls > 0.f;
-    const float Mr = live ? base2_of(xm, k) : 0.f;
+    const bool nonempty = (xm != neg_inf()) && ls > 0.f;
+    const float Mr = nonempty ? base2_of(xm, k) : 0.f;
     const float2 negMr = make_float2(-Mr, -Mr);
-    const float inv = live ? 1.0f / ls : 0.f;
+    const float inv = nonempty ? 1.0f / ls : 0.f;
     const float2 f2 = make_float2(inv, inv);
     for (int c0 = tid; c0 < nch; c0 += kClThreads * kClUnroll) {
       uint4 v[kClUnroll];
@@ -1289,7 +1298,7 @@ bool pick_cluster(int64_t cols, int64_t cap, int max_ctas, ClusterCfg* out) {
 template <int kKind, bool kDouble>
 bool launch_cluster_rows_as(const void* x, void* y, float* m, float* l, int64_t rows, int64_t cols,
                             int64_t ld_x, int64_t ld_y, const ScaleConsts& k, const ClusterCfg& cc,
-                            unsigned int* err, cudaStream_t stream) {
+                            unsigned int* err, const RowsFault& fault, cudaStream_t stream) {
   // the bulk copies need 16-byte aligned rows: x and y aligned, and both
   // leading dimensions whole chunks
   constexpr int kEpc = RowElem<kKind>::kEpc;
@@ -1303,8 +1312,9 @@ bool launch_cluster_rows_as(const void* x, void* y, float* m, float* l, int64_t 
   const int64_t nclusters = rows < resident ? rows : resident;
   cfg.gridDim = dim3(static_cast<unsigned int>(nclusters * cc.ctas), 1, 1);
   const int64_t c64 = cols;
+  const uint64_t timeout = fault.timeout_ns > 0 ? static_cast<uint64_t>(fault.timeout_ns) : kClTimeoutNs;
   return cudaLaunchKernelEx(&cfg, softmax_rows_cluster_kernel<kKind, kDouble>, x, y, m, l, rows, c64,
-                            ld_x, ld_y, k, cc.slice_elems, err) == cudaSuccess;
+                            ld_x, ld_y, k, cc.slice_elems, err, fault.extra_tx, timeout) == cudaSuccess;
 }
 
 // Rows held in a cluster's shared memory. A row of at most kClDoubleCap
@@ -1317,18 +1327,20 @@ bool launch_cluster_rows_as(const void* x, void* y, float* m, float* l, int64_t 
 template <int kKind>
 bool launch_cluster_rows(const void* x, void* y, float* m, float* l, int64_t rows, int64_t cols,
                          int64_t ld_x, int64_t ld_y, const ScaleConsts& k, unsigned int* err,
-                         cudaStream_t stream) {
+                         const RowsFault& fault, cudaStream_t stream) {
   ClusterCfg cc;
   if (pick_cluster<kKind, true>(cols, kClDoubleCap, 1, &cc))
-    return launch_cluster_rows_as<kKind, true>(x, y, m, l, rows, cols, ld_x, ld_y, k, cc, err, stream);
+    return launch_cluster_rows_as<kKind, true>(x, y, m, l, rows, cols, ld_x, ld_y, k, cc, err, fault,
+                                               stream);
   if (pick_cluster<kKind, false>(cols, kClSingleCap, kClMaxCtas, &cc))
-    return launch_cluster_rows_as<kKind, false>(x, y, m, l, rows, cols, ld_x, ld_y, k, cc, err, stream);
+    return launch_cluster_rows_as<kKind, false>(x, y, m, l, rows, cols, ld_x, ld_y, k, cc, err, fault,
+                                                stream);
   return false;
 }
 
 cudaError_t launch_softmax_rows(const float* x, float* y, float* m, float* l, int64_t rows,
                                 int64_t cols, int64_t ld_x, int64_t ld_y, float scale,
-                                unsigned int* err_word, cudaStream_t stream) {
+                                unsigned int* err_word, const RowsFault& fault, cudaStream_t stream) {
   const ScaleConsts k = make_consts(scale);
 
   const bool vec = ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y)) & 15u) == 0 &&
@@ -1364,7 +1376,7 @@ cudaError_t launch_softmax_rows(const float* x, float* y, float* m, float* l, in
   } else if (nv <= 16) {
     softmax_rows_reg_kernel<16><<<grid_for(rows, 2), kThreads, 0, stream>>>(x, y, m, l, rows, c, ld_x, ld_y, k);
   } else {
-    if (!launch_cluster_rows<0>(x, y, m, l, rows, cols, ld_x, ld_y, k, err_word, stream))
+    if (!launch_cluster_rows<0>(x, y, m, l, rows, cols, ld_x, ld_y, k, err_word, fault, stream))
       launch_stream(softmax_rows_stream_kernel<true>, x, y, m, l, rows, cols, ld_x, ld_y, k, 4, stream);
   }
   return cudaGetLastError();
@@ -1373,7 +1385,7 @@ cudaError_t launch_softmax_rows(const float* x, float* y, float* m, float* l, in
 template <int kType>
 void dispatch_rows16(const uint16_t* x, uint16_t* y, float* m, float* l, int64_t rows,
                      int64_t cols, int64_t ld_x, int64_t ld_y, const ScaleConsts& k,
-                     unsigned int* err_word, cudaStream_t stream) {
+                     unsigned int* err_word, const RowsFault& fault, cudaStream_t stream) {
   const bool vec = ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y)) & 15u) == 0 &&
                    (ld_x & 7) == 0 && (ld_y & 7) == 0;
   if (!vec) {
@@ -1406,7 +1418,7 @@ void dispatch_rows16(const uint16_t* x, uint16_t* y, float* m, float* l, int64_t
   } else if (chunks <= 2048) {
     launch_grouped<kType, 256, 8, true, 2>(x, y, m, l, rows, c, ld_x, ld_y, k, stream);
   } else {
-    if (!launch_cluster_rows<kType>(x, y, m, l, rows, cols, ld_x, ld_y, k, err_word, stream))
+    if (!launch_cluster_rows<kType>(x, y, m, l, rows, cols, ld_x, ld_y, k, err_word, fault, stream))
       launch_stream(softmax_rows16_stream_kernel<kType, true>, x, y, m, l, rows, cols, ld_x, ld_y, k, 8, stream);
   }
 }
@@ -1414,12 +1426,12 @@ void dispatch_rows16(const uint16_t* x, uint16_t* y, float* m, float* l, int64_t
 cudaError_t launch_softmax_rows16(const uint16_t* x, uint16_t* y, float* m, float* l,
                                   int64_t rows, int64_t cols, int64_t ld_x, int64_t ld_y,
                                   float scale, int dtype, unsigned int* err_word,
-                                  cudaStream_t stream) {
+                                  const RowsFault& fault, cudaStream_t stream) {
   const ScaleConsts k = make_consts(scale);
   if (dtype == 1)
-    dispatch_rows16<1>(x, y, m, l, rows, cols, ld_x, ld_y, k, err_word, stream);
+    dispatch_rows16<1>(x, y, m, l, rows, cols, ld_x, ld_y, k, err_word, fault, stream);
   else
-    dispatch_rows16<2>(x, y, m, l, rows, cols, ld_x, ld_y, k, err_word, stream);
+    dispatch_rows16<2>(x, y, m, l, rows, cols, ld_x, ld_y, k, err_word, fault, stream);
   return cudaGetLastError();
 }
 

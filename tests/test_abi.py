@@ -134,9 +134,12 @@ def test_merge_rejects_bad_arguments(lib):
 
 def test_fault_hook_validates_and_disarms(lib):
     f = lib.os_debug_inject_fault
-    assert f(2, 0, 0) == INVALID
+    assert f(3, 0, 0) == INVALID
+    assert f(-1, 0, 0) == INVALID
     assert f(1, -1, 0) == INVALID
     assert f(1, 0, -5) == INVALID
+    assert f(2, 0, -5) == INVALID
+    assert f(2, 0, 1000) == 0  # armed for the next row softmax of this thread
     assert f(0, 0, 0) == 0  # disarm; touches no device
 
 

@@ -1,7 +1,8 @@
 """Failure detection without a GPU fault: a bounded wait inside the
-attention kernel is made to run out (one V tile is never loaded), and the
-host reads the timeout through os_check_device_error. No trap, no bad
-address, no endless wait; the context must stay usable (GPU)."""
+attention kernel (one V tile is never loaded) or inside the cluster-resident
+row softmax (a copy barrier expects 16 bytes that never come) is made to run
+out, and the host reads the timeout through os_check_device_error. No trap,
+no bad address, no endless wait; the context must stay usable (GPU)."""
 
 import math
 
@@ -79,4 +80,58 @@ def test_timeout_stops_the_whole_launch():
     # the context still works
     o, _ = oss.attention_fwd(q[:, :1, :256].contiguous(), k[:, :1, :256].contiguous(),
                              v[:, :1, :256].contiguous(), 1 / math.sqrt(128), True)
+    assert oss.check_device_error() == 0
+
+
+KERNEL_SOFTMAX_ROWS = 2
+SITE_COPIES = 1
+
+
+def timeout_code():
+    with pytest.raises(oss.OssError) as info:
+        oss.check_device_error()
+    assert info.value.status == OS_ERR_TIMEOUT
+    return int(str(info.value).split("code ")[1].split(")")[0], 16)
+
+
+@pytest.mark.parametrize("kind,cols,rows", [
+    ("fp32", 65536, 200),   # 256 KB rows: a cluster of several CTAs, one buffer each
+    ("bf16", 20000, 700),   # 40 KB rows: one CTA with two buffers
+])
+def test_row_softmax_copy_wait_times_out_and_context_survives(kind, cols, rows):
+    # every CTA's first row expects 16 bytes that never arrive: its wait gives
+    # up after 20 ms, it copies and waits no more but still meets its
+    # cluster's barriers, and the launch ends
+    import time
+    dtype = torch.float32 if kind == "fp32" else torch.bfloat16
+    x = workloads.logits(rows, cols, 10.0, seed=cols, device="cuda").to(dtype)
+    call = oss.softmax_rows if kind == "fp32" else oss.softmax_rows_16bit
+    call(x, 1.0)
+    assert oss.check_device_error() == 0
+    oss.debug_inject_fault(2, timeout_ns=20_000_000)
+    t0 = time.perf_counter()
+    call(x, 1.0)
+    code = timeout_code()
+    assert time.perf_counter() - t0 < 1.0
+    assert code & 0xFF == KERNEL_SOFTMAX_ROWS
+    assert (code >> 8) & 0xFF == SITE_COPIES
+    # the word was cleared, the hook consumed, and the context computes correctly
+    assert oss.check_device_error() == 0
+    y, m, l = call(x, 1.0)
+    assert oss.check_device_error() == 0
+    xr = x.float().cpu().numpy().astype(np.float64)
+    ry, rm, rl = oracle.softmax_rows(xr, 1.0)
+    assert np.array_equal(m.cpu().numpy(), rm.astype(np.float32))
+    bar = 1e-5 if kind == "fp32" else 2.0 ** -8 + 1e-5
+    assert np.all(np.abs(y.float().cpu().numpy() - ry) <= bar * ry + 2.0 ** -126)
+
+
+def test_row_softmax_hook_ignored_off_the_cluster_path():
+    # rows short enough for registers never wait on copies: the armed hook is
+    # consumed without effect
+    x = workloads.logits(64, 4096, 10.0, seed=3, device="cuda")
+    oss.debug_inject_fault(2, timeout_ns=20_000_000)
+    oss.softmax_rows(x, 1.0)
+    assert oss.check_device_error() == 0
+    oss.softmax_rows(workloads.logits(8, 100000, 10.0, seed=4, device="cuda"), 1.0)
     assert oss.check_device_error() == 0
