@@ -55,19 +55,19 @@ NOMINAL = {"hbm_gbs": 7900.0, "bf16_tflops": 2250.0}
 # same kernel, applied to the full launch's algorithmic bytes.
 NCU_TRAFFIC = {
     "softmax_32k": {"source": "pass_attention_gb300/csrc/softmax_rows.cu",
-                    "sha256": "dcac2e4eed59138b6812062b3a3d8f4e9298b85d2c307464aa629e97a03dce96",
-                    "bytes_per_launch": 1073781504 + 1017767936},
+                    "sha256": "f2c3cf6a2e23c2a370e6bc8fbb098f0a92b625935b51c26be50756722b76e40b",
+                    "bytes_per_launch": 1073785344 + 1017656064},
     "softmax_32k_bf16": {"source": "pass_attention_gb300/csrc/softmax_rows.cu",
-                         "sha256": "dcac2e4eed59138b6812062b3a3d8f4e9298b85d2c307464aa629e97a03dce96",
-                         "bytes_per_launch": 536907776 + 482675712},
+                         "sha256": "f2c3cf6a2e23c2a370e6bc8fbb098f0a92b625935b51c26be50756722b76e40b",
+                         "bytes_per_launch": 536911872 + 482367488},
     # the comparators: all sweeps of one call (each reads x from DRAM again)
     "softmax_32k_3pass": {"source": "pass_attention_gb300/csrc/softmax_rows.cu",
-                          "sha256": "dcac2e4eed59138b6812062b3a3d8f4e9298b85d2c307464aa629e97a03dce96",
-                          "bytes_per_launch": (1073760256 + 2599168) + (1073882368 + 266752)
-                          + (1074030848 + 1024722944)},
+                          "sha256": "f2c3cf6a2e23c2a370e6bc8fbb098f0a92b625935b51c26be50756722b76e40b",
+                          "bytes_per_launch": (1073818624 + 2815488) + (1073973760 + 166144)
+                          + (1074052352 + 1024768000)},
     "softmax_32k_2pass": {"source": "pass_attention_gb300/csrc/softmax_rows.cu",
-                          "sha256": "dcac2e4eed59138b6812062b3a3d8f4e9298b85d2c307464aa629e97a03dce96",
-                          "bytes_per_launch": (1073761024 + 3053824) + (1074085888 + 1024695808)},
+                          "sha256": "f2c3cf6a2e23c2a370e6bc8fbb098f0a92b625935b51c26be50756722b76e40b",
+                          "bytes_per_launch": (1073793024 + 3014400) + (1074185472 + 1025043456)},
     "attn_4k": {"source": "pass_attention_gb300/csrc/attn_fwd.cu",
                 "sha256": "1de91f1a14f7b69059f99bd37628b4126df733c28a5f205b034826a15235ccec",
                 "bytes_per_launch": 201502976 + 47736320},

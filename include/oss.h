@@ -79,14 +79,18 @@ typedef enum os_status {
  *   m, l  [rows] fp32, device, or NULL to skip.
  *   rows  >= 1; cols >= 1; ld_x >= cols, ld_y >= cols (elements).
  *   scale finite and > 0.
- * Alignment: x, y, m and l 4-byte aligned. When x and y are 16-byte aligned and
- * ld_x, ld_y are multiples of 4 the kernel uses 16-byte loads and stores and
- * reads each element once and writes it once: rows of up to 16384 elements
- * are held in registers (several rows per CTA up to 2048 elements); longer
- * rows of up to 1.6 MB in the shared memory of a thread-block cluster of up
- * to eight CTAs, whose slices' (max, sum) states are merged through
- * distributed shared memory. Other rows are streamed twice (two reads, one
- * write).
+ * Alignment: x, y, m and l 4-byte aligned. When each row of x starts at the
+ * same offset from a 16-byte boundary as the same row of y (x and y 16-byte
+ * aligned with ld_x, ld_y multiples of 4; or, say, y laid out like x), the
+ * kernel moves the row in 16-byte chunks on that grid and reads each element
+ * once and writes it once: rows of up to 16384 elements are held in
+ * registers (several rows per CTA up to 2048 elements); longer rows of up to
+ * 1.6 MB in the shared memory of a thread-block cluster of up to eight CTAs,
+ * whose slices' (max, sum) states are merged through distributed shared
+ * memory. For a row off the 16-byte grid, the loads of its first and last
+ * chunks may read (never write) bytes of the same 16-byte granules outside
+ * the row. Rows whose x and y offsets differ, and rows longer than 1.6 MB,
+ * are streamed twice (two reads, one write).
  * Errors: OS_ERR_INVALID_ARGUMENT, OS_ERR_MISALIGNED, OS_ERR_CUDA.
  */
 OSS_API os_status os_softmax_rows(const float* x, float* y, float* m, float* l,
@@ -115,11 +119,12 @@ typedef enum os_dtype {
  *         os_softmax_rows).
  *   rows >= 1; cols >= 1; ld_x >= cols, ld_y >= cols (elements); scale
  *   finite and > 0; dtype an os_dtype.
- * Alignment: x and y 2-byte aligned, m and l 4-byte aligned. With x and y
- * 16-byte aligned and ld_x, ld_y multiples of 8, rows of up to 16384
- * elements are held in registers and longer rows of up to 1.6 MB in a
+ * Alignment: x and y 2-byte aligned, m and l 4-byte aligned. When x's and
+ * y's rows start at the same offsets from a 16-byte boundary, rows of up to
+ * 16384 elements are held in registers and longer rows of up to 1.6 MB in a
  * cluster's shared memory, as for os_softmax_rows (one read, one write per
- * element); other rows are streamed twice.
+ * element, the same granule reads at the ends of a row off the grid); other
+ * rows are streamed twice.
  * Errors: OS_ERR_INVALID_ARGUMENT, OS_ERR_MISALIGNED, OS_ERR_CUDA.
  */
 OSS_API os_status os_softmax_rows_16bit(const void* x, void* y, float* m, float* l,

@@ -638,10 +638,25 @@ __device__ __forceinline__ uint32_t neg_inf_word() {
   return (kKind == 0) ? 0xff800000u : h16_neg_inf2<kKind>();
 }
 
-// Chunk c of a row: 16 bytes when complete, else the row's last elements
-// padded with -inf (and -inf beyond the row).
+// The 16-byte chunks of a row of n elements whose first element lies `s`
+// elements past a 16-byte boundary (0 <= s < kEpc; 0 for an aligned row):
+// chunk c holds the elements [c * kEpc - s, (c + 1) * kEpc - s), so every
+// chunk sits on the 16-byte grid and ceil((n + s) / kEpc) chunks cover the
+// row. Every chunk that holds an element of the row is loaded as one 16-byte
+// access; in the partial first and last chunks the elements outside the row
+// are then replaced by -inf. (Those extra bytes share a 16-byte granule, and
+// so a page, with the row's own first or last element: the load reads bytes
+// outside the row but never faults, and nothing outside the row is written.)
+// Chunks wholly outside the row are not read.
 template <int kKind>
-__device__ __forceinline__ uint4 load_chunk16(const char* xr, int c, int nfull, int tail) {
+__device__ __forceinline__ int phase_of(const void* row) {
+  return static_cast<int>((reinterpret_cast<uintptr_t>(row) & 15u) / RowElem<kKind>::kSize);
+}
+
+// Rows on the 16-byte grid (phase 0): chunk c is elements [c * kEpc,
+// (c + 1) * kEpc); nfull whole chunks, then a last chunk of `tail` elements.
+template <int kKind>
+__device__ __forceinline__ uint4 load_chunk16_grid(const char* xr, int c, int nfull, int tail) {
   if (c < nfull) return __ldcs(reinterpret_cast<const uint4*>(xr) + c);
   uint32_t wd[4];
 #pragma unroll
@@ -665,7 +680,7 @@ __device__ __forceinline__ uint4 load_chunk16(const char* xr, int c, int nfull, 
 }
 
 template <int kKind>
-__device__ __forceinline__ void store_chunk16(char* yr, int c, int nfull, int tail, const uint4& o) {
+__device__ __forceinline__ void store_chunk16_grid(char* yr, int c, int nfull, int tail, const uint4& o) {
   if (c < nfull) {
     __stcs(reinterpret_cast<uint4*>(yr) + c, o);
   } else if (c == nfull && tail) {
@@ -680,6 +695,73 @@ __device__ __forceinline__ void store_chunk16(char* yr, int c, int nfull, int ta
 #pragma unroll
       for (int e = 0; e < 7; ++e)
         if (e < tail) p[e] = static_cast<uint16_t>((e & 1) ? (wd[e >> 1] >> 16) : (wd[e >> 1] & 0xffffu));
+    }
+  }
+}
+
+// Chunk c's 16-byte granule when it holds any element of the row, else all
+// -inf (a predicated load: several of them issue back to back).
+template <int kKind>
+__device__ __forceinline__ uint4 ld_granule(const char* xr, int c, int n, int s) {
+  constexpr int kEpc = RowElem<kKind>::kEpc;
+  constexpr int kEsz = RowElem<kKind>::kSize;
+  const int first = c * kEpc - s;
+  const uint32_t ninf = neg_inf_word<kKind>();
+  uint4 v = make_uint4(ninf, ninf, ninf, ninf);
+  if (first < n && first + kEpc > 0) v = __ldcs(reinterpret_cast<const uint4*>(xr + first * kEsz));
+  return v;
+}
+
+// A loaded granule of chunk c with the elements outside the row replaced by
+// -inf (whole chunks pass unchanged).
+template <int kKind>
+__device__ __forceinline__ uint4 fix_granule(uint4 v, int c, int n, int s) {
+  constexpr int kEpc = RowElem<kKind>::kEpc;
+  const int first = c * kEpc - s;
+  if (first >= 0 && first + kEpc <= n) return v;
+  const uint32_t ninf = neg_inf_word<kKind>();
+  uint32_t wd[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int e = 0; e < kEpc; ++e) {
+    const int j = first + e;
+    if (j < 0 || j >= n) {
+      if (kKind == 0)
+        wd[e] = ninf;
+      else
+        wd[e >> 1] = (e & 1) ? ((wd[e >> 1] & 0xffffu) | (ninf & 0xffff0000u))
+                             : ((wd[e >> 1] & 0xffff0000u) | (ninf & 0xffffu));
+    }
+  }
+  return make_uint4(wd[0], wd[1], wd[2], wd[3]);
+}
+
+template <int kKind>
+__device__ __forceinline__ uint4 load_chunk16(const char* xr, int c, int n, int s) {
+  return fix_granule<kKind>(ld_granule<kKind>(xr, c, n, s), c, n, s);
+}
+
+// Chunk c of y (the same phase s as x's row), written for its elements in
+// [0, n) only.
+template <int kKind>
+__device__ __forceinline__ void store_chunk16(char* yr, int c, int n, int s, const uint4& o) {
+  constexpr int kEpc = RowElem<kKind>::kEpc;
+  constexpr int kEsz = RowElem<kKind>::kSize;
+  const int first = c * kEpc - s;
+  if (first >= 0 && first + kEpc <= n) {
+    __stcs(reinterpret_cast<uint4*>(yr + first * kEsz), o);
+    return;
+  }
+  if (first >= n || first + kEpc <= 0) return;
+  const uint32_t wd[4] = {o.x, o.y, o.z, o.w};
+#pragma unroll
+  for (int e = 0; e < kEpc; ++e) {
+    const int j = first + e;
+    if (j >= 0 && j < n) {
+      if (kKind == 0)
+        reinterpret_cast<uint32_t*>(yr)[j] = wd[e];
+      else
+        reinterpret_cast<uint16_t*>(yr)[j] =
+            static_cast<uint16_t>((e & 1) ? (wd[e >> 1] >> 16) : (wd[e >> 1] & 0xffffu));
     }
   }
 }
@@ -765,7 +847,10 @@ __device__ __forceinline__ void group_merge(float& xm, float& ls, const ScaleCon
   ls = l;
 }
 
-template <int kKind, int TPR, int NV, bool kPrefetch, int kMinBlocks>
+// kExtra: one more chunk slot per thread (NV + 1), for rows off the 16-byte
+// grid, which need one chunk more than an aligned row; only the group's
+// first thread ever finds its extra chunk inside the row.
+template <int kKind, int TPR, int NV, bool kPrefetch, int kMinBlocks, bool kExtra>
 __global__ void __launch_bounds__(kThreads, kMinBlocks)
 softmax_rows_grouped_kernel(const void* __restrict__ x, void* __restrict__ y,
                             float* __restrict__ m_out, float* __restrict__ l_out, int64_t rows,
@@ -773,6 +858,7 @@ softmax_rows_grouped_kernel(const void* __restrict__ x, void* __restrict__ y,
   constexpr int kEpc = RowElem<kKind>::kEpc;
   constexpr int kEsz = RowElem<kKind>::kSize;
   constexpr int kGroups = kThreads / TPR;
+  constexpr int kSlots = NV + (kExtra ? 1 : 0);
   // two sets of per-warp states: a warp may start the next row's merge
   // while the group's slower warps still read this row's, and a set is not
   // written again until every warp of the group has passed the barrier
@@ -781,8 +867,6 @@ softmax_rows_grouped_kernel(const void* __restrict__ x, void* __restrict__ y,
   const int tid = threadIdx.x;
   const int g = tid / TPR;
   const int t = tid % TPR;
-  const int nfull = cols / kEpc;
-  const int tail = cols % kEpc;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * kGroups;
   // Groups narrower than a warp share their warp's shuffles, so the warp
   // walks its rows together: the loop runs on the row of the warp's first
@@ -796,35 +880,59 @@ softmax_rows_grouped_kernel(const void* __restrict__ x, void* __restrict__ y,
   const char* xb = static_cast<const char*>(x);
   char* yb = static_cast<char*>(y);
 
-  uint4 nx[NV];
+  // Rows on the grid use the plain chunking; rows off it (kExtra) load each
+  // granule first and mask the partial chunks after, so that a thread's
+  // loads issue back to back.
+  const int nfull = cols / kEpc;
+  const int tail = cols % kEpc;
+  auto load = [&](const char* xr, int c, int s) {
+    if constexpr (kExtra)
+      return ld_granule<kKind>(xr, c, cols, s);
+    else
+      return load_chunk16_grid<kKind>(xr, c, nfull, tail);
+  };
+  auto fix = [&](const uint4& v, int c, int s) {
+    if constexpr (kExtra)
+      return fix_granule<kKind>(v, c, cols, s);
+    else
+      return v;
+  };
+  uint4 nx[kSlots];
+  int nx_s = 0;  // the phase of the row held in nx
   if (kPrefetch && wrow + lead < rows) {
     const char* xr = xb + (wrow + lead) * ld_x * kEsz;
+    nx_s = phase_of<kKind>(xr);
 #pragma unroll
-    for (int i = 0; i < NV; ++i) nx[i] = load_chunk16<kKind>(xr, t + i * TPR, nfull, tail);
+    for (int i = 0; i < kSlots; ++i) nx[i] = load(xr, t + i * TPR, nx_s);
   }
   int buf = 0;
   for (; wrow < rows; wrow += stride) {
     const int64_t row = wrow + lead;
     const bool active = row < rows;
-    float2 w[NV][kEpc / 2];
+    float2 w[kSlots][kEpc / 2];
     if (kPrefetch) {
 #pragma unroll
-      for (int i = 0; i < NV; ++i) unpack_chunk16<kKind>(active ? nx[i] : pad, w[i]);
+      for (int i = 0; i < kSlots; ++i)
+        unpack_chunk16<kKind>(active ? fix(nx[i], t + i * TPR, nx_s) : pad, w[i]);
       const int64_t next = row + stride;
       if (next < rows) {
         const char* xr = xb + next * ld_x * kEsz;
+        nx_s = phase_of<kKind>(xr);
 #pragma unroll
-        for (int i = 0; i < NV; ++i) nx[i] = load_chunk16<kKind>(xr, t + i * TPR, nfull, tail);
+        for (int i = 0; i < kSlots; ++i) nx[i] = load(xr, t + i * TPR, nx_s);
       }
     } else {
       const char* xr = xb + row * ld_x * kEsz;
+      const int s = phase_of<kKind>(xr);
+      uint4 v[kSlots];
 #pragma unroll
-      for (int i = 0; i < NV; ++i)
-        unpack_chunk16<kKind>(active ? load_chunk16<kKind>(xr, t + i * TPR, nfull, tail) : pad, w[i]);
+      for (int i = 0; i < kSlots; ++i) v[i] = active ? load(xr, t + i * TPR, s) : pad;
+#pragma unroll
+      for (int i = 0; i < kSlots; ++i) unpack_chunk16<kKind>(fix(v[i], t + i * TPR, s), w[i]);
     }
     float xa = neg_inf(), xc = neg_inf();
 #pragma unroll
-    for (int i = 0; i < NV; ++i) {
+    for (int i = 0; i < kSlots; ++i) {
 #pragma unroll
       for (int h = 0; h < kEpc / 2; h += 2) {
         xa = fmax3(xa, w[i][h].x, w[i][h].y);
@@ -836,7 +944,7 @@ softmax_rows_grouped_kernel(const void* __restrict__ x, void* __restrict__ y,
     const float2 negM = make_float2(-Mt, -Mt);
     float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
-    for (int i = 0; i < NV; ++i) {
+    for (int i = 0; i < kSlots; ++i) {
 #pragma unroll
       for (int h = 0; h < kEpc / 2; ++h) {
         w[i][h] = weight2(w[i][h], negM, k);
@@ -852,8 +960,14 @@ softmax_rows_grouped_kernel(const void* __restrict__ x, void* __restrict__ y,
     const float2 f2 = make_float2(f, f);
     if (active) {
       char* yr = yb + row * ld_y * kEsz;
+      const int s = phase_of<kKind>(yr);  // x's row has the same phase
 #pragma unroll
-      for (int i = 0; i < NV; ++i) store_chunk16<kKind>(yr, t + i * TPR, nfull, tail, pack_chunk16<kKind>(w[i], f2));
+      for (int i = 0; i < kSlots; ++i) {
+        if constexpr (kExtra)
+          store_chunk16<kKind>(yr, t + i * TPR, cols, s, pack_chunk16<kKind>(w[i], f2));
+        else
+          store_chunk16_grid<kKind>(yr, t + i * TPR, nfull, tail, pack_chunk16<kKind>(w[i], f2));
+      }
       if (t == 0) write_ml(xm, ls, k, row, m_out, l_out);
     }
     buf ^= 1;
@@ -871,14 +985,21 @@ softmax_rows_grouped_kernel(const void* __restrict__ x, void* __restrict__ y,
 // streaming kernel reads the row twice.
 // ---------------------------------------------------------------------------
 
-// Issue the copies of one row's slice into `buf_a` (thread 0 only): the
-// whole 16-byte chunks by bulk copies that complete on `bar_a`, the last
-// partial chunk (if any) by plain loads, padded with -inf. The barrier is
-// told to expect `extra` bytes more than are copied (0 but in the test hook,
-// which makes the wait run out).
+// Issue the copies of one row's slice (n elements at xr, phase s) into
+// `buf_a` (thread 0 only), in the chunks of load_chunk16: the whole 16-byte
+// chunks by bulk copies that complete on `bar_a`, the partial first and last
+// chunks by plain loads, padded with -inf. The barrier is told to expect
+// `extra` bytes more than are copied (0 but in the test hook, which makes the
+// wait run out).
 template <int kKind>
 __device__ __forceinline__ void issue_slice(const char* xr, uint4* buf, uint32_t buf_a, uint32_t bar_a,
-                                            uint32_t bulk, int nfull, int tail, uint32_t extra) {
+                                            int n, int s, uint32_t extra) {
+  constexpr int kEpc = RowElem<kKind>::kEpc;
+  constexpr int kEsz = RowElem<kKind>::kSize;
+  const int nch = (n > 0) ? (n + s + kEpc - 1) / kEpc : 0;
+  const int ca = (s == 0) ? 0 : 1;   // the first whole chunk
+  const int cb = (n + s) / kEpc;     // one past the last whole chunk
+  const uint32_t bulk = (n > 0 && cb > ca) ? static_cast<uint32_t>(cb - ca) * 16u : 0u;
   // the buffer's previous contents were last touched through the generic
   // proxy; order that before the copies' asynchronous writes
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -886,17 +1007,22 @@ __device__ __forceinline__ void issue_slice(const char* xr, uint4* buf, uint32_t
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar_a),
                  "r"(bulk + extra)
                  : "memory");
+    const char* src = xr + (ca * kEpc - s) * kEsz;  // 16-byte aligned
+    const uint32_t dst = buf_a + static_cast<uint32_t>(ca) * 16u;
     for (uint32_t off = 0; off < bulk; off += kClPiece) {
       const uint32_t size = (bulk - off < kClPiece) ? (bulk - off) : kClPiece;
       asm volatile(
           "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
-              "r"(buf_a + off), "l"(xr + off), "r"(size), "r"(bar_a)
+              "r"(dst + off), "l"(src + off), "r"(size), "r"(bar_a)
           : "memory");
     }
   } else {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar_a) : "memory");
   }
-  if (tail) buf[nfull] = load_chunk16<kKind>(xr, nfull, nfull, tail);
+  if (n > 0) {
+    if (s != 0) buf[0] = load_chunk16<kKind>(xr, 0, n, s);
+    if (cb < nch && !(s != 0 && cb == 0)) buf[cb] = load_chunk16<kKind>(xr, cb, n, s);
+  }
 }
 
 // kDouble: two slice buffers; the next row's copies are issued as soon as
@@ -922,11 +1048,8 @@ softmax_rows_cluster_kernel(const void* __restrict__ x, void* __restrict__ y,
   const int64_t lo = static_cast<int64_t>(rank) * slice_elems;
   const int64_t left = cols - lo;
   const int n = static_cast<int>(left <= 0 ? 0 : (left < slice_elems ? left : slice_elems));
-  const int nfull = n / kEpc;
-  const int tail = n % kEpc;
-  const int nch = nfull + (tail ? 1 : 0);
-  const uint32_t bulk = static_cast<uint32_t>(nfull) * 16u;
-  const int stride_chunks = (slice_elems / kEpc + 7) / 8 * 8;  // second buffer 128-byte aligned
+  // a slice whose rows are not 16-byte aligned spans one chunk more
+  const int stride_chunks = (slice_elems / kEpc + 1 + 7) / 8 * 8;  // second buffer 128-byte aligned
   const int64_t row0 = cluster_id();
   const int64_t rstep = cluster_count();
   const char* xb = static_cast<const char*>(x);
@@ -939,9 +1062,11 @@ softmax_rows_cluster_kernel(const void* __restrict__ x, void* __restrict__ y,
   // every CTA of the cluster has started (its shared memory may be written
   // by peers from here on) and the barriers' initialisation is visible
   cluster_sync_all();
-  if (kDouble && tid == 0 && row0 < rows)
-    issue_slice<kKind>(xb + (row0 * ld_x + lo) * kEsz, slices, smem_u32(slices), smem_u32(&bars[0]),
-                       bulk, nfull, tail, fault_tx);
+  if (kDouble && tid == 0 && row0 < rows) {
+    const char* xr0 = xb + (row0 * ld_x + lo) * kEsz;
+    issue_slice<kKind>(xr0, slices, smem_u32(slices), smem_u32(&bars[0]), n, phase_of<kKind>(xr0),
+                       fault_tx);
+  }
 
   uint32_t parity = 0u;  // bit b: the phase parity to wait for on buffer b
   int sbuf = 0;  // cstate set
@@ -951,18 +1076,20 @@ softmax_rows_cluster_kernel(const void* __restrict__ x, void* __restrict__ y,
     const int b = kDouble ? (it & 1) : 0;
     uint4* slice = slices + b * stride_chunks;
     const uint32_t bar_a = smem_u32(&bars[b]);
+    const char* xr = xb + (row * ld_x + lo) * kEsz;
     char* yr = static_cast<char*>(y) + (row * ld_y + lo) * kEsz;
+    const int s = phase_of<kKind>(xr);  // y's slice has the same phase
+    const int nch = (n > 0) ? (n + s + kEpc - 1) / kEpc : 0;
     if (!kDouble && tid == 0 && live)
-      issue_slice<kKind>(xb + (row * ld_x + lo) * kEsz, slice, smem_u32(slice), bar_a, bulk, nfull, tail,
-                         it == 0 ? fault_tx : 0u);
+      issue_slice<kKind>(xr, slice, smem_u32(slice), bar_a, n, s, it == 0 ? fault_tx : 0u);
     if (live) live = mbar_wait_bounded(bar_a, (parity >> b) & 1u, err, timeout_ns);
     parity ^= 1u << b;
     __syncthreads();  // the tail chunk, written by thread 0
     if (kDouble && tid == 0 && live && row + rstep < rows) {
       // the other buffer was read out before the end of the previous row
       uint4* other = slices + (b ^ 1) * stride_chunks;
-      issue_slice<kKind>(xb + ((row + rstep) * ld_x + lo) * kEsz, other, smem_u32(other),
-                         smem_u32(&bars[b ^ 1]), bulk, nfull, tail, 0u);
+      const char* xn = xb + ((row + rstep) * ld_x + lo) * kEsz;
+      issue_slice<kKind>(xn, other, smem_u32(other), smem_u32(&bars[b ^ 1]), n, phase_of<kKind>(xn), 0u);
     }
 
     // The thread's (max, sum) over its chunks, by the online recurrence:
@@ -1038,7 +1165,7 @@ softmax_rows_cluster_kernel(const void* __restrict__ x, void* __restrict__ y,
           unpack_chunk16<kKind>(v[u], w);
 #pragma unroll
           for (int h = 0; h < kEpc / 2; ++h) w[h] = weight2(w[h], negMr, k);
-          store_chunk16<kKind>(yr, c0 + u * kClThreads, nfull, tail, pack_chunk16<kKind>(w, f2));
+          store_chunk16<kKind>(yr, c0 + u * kClThreads, n, s, pack_chunk16<kKind>(w, f2));
         }
       }
     }
@@ -1201,15 +1328,23 @@ void launch_stream(Kernel kernel, const T* x, T* y, float* m, float* l, int64_t 
 
 // Launch of softmax_rows_grouped_kernel: persistent (one wave of kMinBlocks
 // CTAs per SM) when it prefetches, else up to 64 waves of a grid-stride loop.
-template <int kKind, int TPR, int NV, bool kPrefetch, int kMinBlocks>
+template <int kKind, int TPR, int NV, bool kPrefetch, int kMinBlocks, bool kExtra = false>
 void launch_grouped(const void* x, void* y, float* m, float* l, int64_t rows, int cols,
                     int64_t ld_x, int64_t ld_y, const ScaleConsts& k, cudaStream_t stream) {
   constexpr int kGroups = kThreads / TPR;
   const int64_t need = (rows + kGroups - 1) / kGroups;
   const int64_t cap = static_cast<int64_t>(sm_count()) * kMinBlocks * (kPrefetch ? 1 : 64);
   const int g = static_cast<int>(need < cap ? need : cap);
-  softmax_rows_grouped_kernel<kKind, TPR, NV, kPrefetch, kMinBlocks>
+  softmax_rows_grouped_kernel<kKind, TPR, NV, kPrefetch, kMinBlocks, kExtra>
       <<<g, kThreads, 0, stream>>>(x, y, m, l, rows, cols, ld_x, ld_y, k);
+}
+
+// Every row of x starts at the same offset from a 16-byte boundary as the
+// same row of y (the chunks of load_chunk16 then line up for both).
+bool same_phase(const void* x, const void* y, int64_t ld_x, int64_t ld_y, int esz) {
+  const int64_t dx = static_cast<int64_t>(reinterpret_cast<uintptr_t>(x) & 15u);
+  const int64_t dy = static_cast<int64_t>(reinterpret_cast<uintptr_t>(y) & 15u);
+  return dx == dy && ((ld_x - ld_y) * esz) % 16 == 0;
 }
 
 struct ClusterCfg {
@@ -1280,7 +1415,7 @@ bool pick_cluster(int64_t cols, int64_t cap, int max_ctas, ClusterCfg* out) {
     int64_t per = (cols + c - 1) / c;
     per = (per + kEpc - 1) / kEpc * kEpc;
     if (per * kEsz > cap) continue;
-    const int64_t chunks = per / kEpc;
+    const int64_t chunks = per / kEpc + 1;  // + 1: a slice not 16-byte aligned spans one more
     const int64_t stride = (chunks + 7) / 8 * 8;
     ClusterCfg cc{static_cast<int>(c), static_cast<int>(per),
                   static_cast<size_t>((kDouble ? stride + chunks : chunks) * 16)};
@@ -1299,11 +1434,12 @@ template <int kKind, bool kDouble>
 bool launch_cluster_rows_as(const void* x, void* y, float* m, float* l, int64_t rows, int64_t cols,
                             int64_t ld_x, int64_t ld_y, const ScaleConsts& k, const ClusterCfg& cc,
                             unsigned int* err, const RowsFault& fault, cudaStream_t stream) {
-  // the bulk copies need 16-byte aligned rows: x and y aligned, and both
-  // leading dimensions whole chunks
+  // the chunks (and the bulk copies of the whole ones) sit on the 16-byte
+  // grid: x's and y's rows in step, elements aligned, slices whole chunks
   constexpr int kEpc = RowElem<kKind>::kEpc;
-  if (((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y)) & 15u) != 0 ||
-      ld_x % kEpc != 0 || ld_y % kEpc != 0 || cc.slice_elems % kEpc != 0)
+  constexpr int kEsz = RowElem<kKind>::kSize;
+  if (!same_phase(x, y, ld_x, ld_y, kEsz) || (reinterpret_cast<uintptr_t>(x) % kEsz) != 0 ||
+      cc.slice_elems % kEpc != 0)
     return false;
   const int resident = resident_clusters<kKind, kDouble>(cc);
   if (resident < 1) return false;
@@ -1346,7 +1482,35 @@ cudaError_t launch_softmax_rows(const float* x, float* y, float* m, float* l, in
   const bool vec = ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y)) & 15u) == 0 &&
                    (ld_x & 3) == 0 && (ld_y & 3) == 0;
   if (!vec) {
-    launch_stream(softmax_rows_stream_kernel<false>, x, y, m, l, rows, cols, ld_x, ld_y, k, 1, stream);
+    // Rows off the 16-byte grid, x and y in step: 16-byte chunks on the grid
+    // with the partial first and last chunks masked, in the configuration of
+    // an aligned row of the same length plus one chunk slot per thread.
+    // Otherwise stream.
+    const int64_t chunks = (cols + 3) / 4;
+    const int c = static_cast<int>(cols);
+    if (!same_phase(x, y, ld_x, ld_y, 4)) {
+      launch_stream(softmax_rows_stream_kernel<false>, x, y, m, l, rows, cols, ld_x, ld_y, k, 1, stream);
+    } else if (chunks <= 8) {
+      launch_grouped<0, 8, 1, true, 4, true>(x, y, m, l, rows, c, ld_x, ld_y, k, stream);
+    } else if (chunks <= 16) {
+      launch_grouped<0, 16, 1, true, 4, true>(x, y, m, l, rows, c, ld_x, ld_y, k, stream);
+    } else if (chunks <= 32) {
+      launch_grouped<0, 32, 1, true, 4, true>(x, y, m, l, rows, c, ld_x, ld_y, k, stream);
+    } else if (chunks <= 64) {
+      launch_grouped<0, 32, 2, false, 6, true>(x, y, m, l, rows, c, ld_x, ld_y, k, stream);
+    } else if (chunks <= 128) {
+      launch_grouped<0, 32, 4, false, 4, true>(x, y, m, l, rows, c, ld_x, ld_y, k, stream);
+    } else if (chunks <= 256) {
+      launch_grouped<0, 64, 4, false, 4, true>(x, y, m, l, rows, c, ld_x, ld_y, k, stream);
+    } else if (chunks <= 512) {
+      launch_grouped<0, 128, 4, false, 4, true>(x, y, m, l, rows, c, ld_x, ld_y, k, stream);
+    } else if (chunks <= 1024) {
+      launch_grouped<0, 256, 4, false, 4, true>(x, y, m, l, rows, c, ld_x, ld_y, k, stream);
+    } else if (chunks <= 2048) {
+      launch_grouped<0, 256, 8, false, 2, true>(x, y, m, l, rows, c, ld_x, ld_y, k, stream);
+    } else if (!launch_cluster_rows<0>(x, y, m, l, rows, cols, ld_x, ld_y, k, err_word, fault, stream)) {
+      launch_stream(softmax_rows_stream_kernel<false>, x, y, m, l, rows, cols, ld_x, ld_y, k, 1, stream);
+    }
     return cudaGetLastError();
   }
   const int64_t chunks = (cols + 3) / 4;
@@ -1382,17 +1546,13 @@ cudaError_t launch_softmax_rows(const float* x, float* y, float* m, float* l, in
   return cudaGetLastError();
 }
 
-template <int kType>
-void dispatch_rows16(const uint16_t* x, uint16_t* y, float* m, float* l, int64_t rows,
-                     int64_t cols, int64_t ld_x, int64_t ld_y, const ScaleConsts& k,
-                     unsigned int* err_word, const RowsFault& fault, cudaStream_t stream) {
-  const bool vec = ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y)) & 15u) == 0 &&
-                   (ld_x & 7) == 0 && (ld_y & 7) == 0;
-  if (!vec) {
-    launch_stream(softmax_rows16_stream_kernel<kType, false>, x, y, m, l, rows, cols, ld_x, ld_y, k, 1, stream);
-    return;
-  }
-  const int64_t chunks = (cols + 7) / 8;
+// The 16-bit configurations by the aligned chunk count of a row; kExtra
+// adds the slot that a row off the 16-byte grid needs.
+template <int kType, bool kExtra>
+void dispatch_rows16_table(const uint16_t* x, uint16_t* y, float* m, float* l, int64_t rows,
+                           int64_t cols, int64_t chunks, int64_t ld_x, int64_t ld_y,
+                           const ScaleConsts& k, unsigned int* err_word, const RowsFault& fault,
+                           cudaStream_t stream) {
   const int c = static_cast<int>(cols);
   // Rows of up to 16384 elements: persistent CTAs with the next row's chunks
   // prefetched into registers (the widening of fp16 costs a conversion per
@@ -1400,27 +1560,47 @@ void dispatch_rows16(const uint16_t* x, uint16_t* y, float* m, float* l, int64_t
   // 256 / TPR rows per CTA for rows of up to 4096 elements (groups of 8 and
   // 16 threads, without the prefetch, for rows of up to 128).
   if (chunks <= 8) {
-    launch_grouped<kType, 8, 1, false, 8>(x, y, m, l, rows, c, ld_x, ld_y, k, stream);
+    launch_grouped<kType, 8, 1, false, kExtra ? 4 : 8, kExtra>(x, y, m, l, rows, c, ld_x, ld_y, k, stream);
   } else if (chunks <= 16) {
-    launch_grouped<kType, 16, 1, false, 8>(x, y, m, l, rows, c, ld_x, ld_y, k, stream);
+    launch_grouped<kType, 16, 1, false, kExtra ? 4 : 8, kExtra>(x, y, m, l, rows, c, ld_x, ld_y, k, stream);
   } else if (chunks <= 32) {
-    launch_grouped<kType, 32, 1, true, 6>(x, y, m, l, rows, c, ld_x, ld_y, k, stream);
+    launch_grouped<kType, 32, 1, true, kExtra ? 4 : 6, kExtra>(x, y, m, l, rows, c, ld_x, ld_y, k, stream);
   } else if (chunks <= 64) {
-    launch_grouped<kType, 32, 2, true, 5>(x, y, m, l, rows, c, ld_x, ld_y, k, stream);
+    launch_grouped<kType, 32, 2, true, kExtra ? 3 : 5, kExtra>(x, y, m, l, rows, c, ld_x, ld_y, k, stream);
   } else if (chunks <= 128) {
-    launch_grouped<kType, 32, 4, true, 3>(x, y, m, l, rows, c, ld_x, ld_y, k, stream);
+    launch_grouped<kType, 32, 4, true, kExtra ? 2 : 3, kExtra>(x, y, m, l, rows, c, ld_x, ld_y, k, stream);
   } else if (chunks <= 256) {
-    launch_grouped<kType, 64, 4, true, 3>(x, y, m, l, rows, c, ld_x, ld_y, k, stream);
+    launch_grouped<kType, 64, 4, true, kExtra ? 2 : 3, kExtra>(x, y, m, l, rows, c, ld_x, ld_y, k, stream);
   } else if (chunks <= 512) {
-    launch_grouped<kType, 128, 4, true, 3>(x, y, m, l, rows, c, ld_x, ld_y, k, stream);
+    launch_grouped<kType, 128, 4, true, kExtra ? 2 : 3, kExtra>(x, y, m, l, rows, c, ld_x, ld_y, k, stream);
   } else if (chunks <= 1024) {
-    launch_grouped<kType, 256, 4, true, 3>(x, y, m, l, rows, c, ld_x, ld_y, k, stream);
+    launch_grouped<kType, 256, 4, true, kExtra ? 2 : 3, kExtra>(x, y, m, l, rows, c, ld_x, ld_y, k, stream);
   } else if (chunks <= 2048) {
-    launch_grouped<kType, 256, 8, true, 2>(x, y, m, l, rows, c, ld_x, ld_y, k, stream);
-  } else {
-    if (!launch_cluster_rows<kType>(x, y, m, l, rows, cols, ld_x, ld_y, k, err_word, fault, stream))
-      launch_stream(softmax_rows16_stream_kernel<kType, true>, x, y, m, l, rows, cols, ld_x, ld_y, k, 8, stream);
+    launch_grouped<kType, 256, 8, kExtra ? false : true, 2, kExtra>(x, y, m, l, rows, c, ld_x, ld_y, k, stream);
+  } else if (!launch_cluster_rows<kType>(x, y, m, l, rows, cols, ld_x, ld_y, k, err_word, fault, stream)) {
+    // 16-byte accesses only for rows on the grid
+    launch_stream(softmax_rows16_stream_kernel<kType, !kExtra>, x, y, m, l, rows, cols, ld_x, ld_y, k,
+                  kExtra ? 1 : 8, stream);
   }
+}
+
+template <int kType>
+void dispatch_rows16(const uint16_t* x, uint16_t* y, float* m, float* l, int64_t rows,
+                     int64_t cols, int64_t ld_x, int64_t ld_y, const ScaleConsts& k,
+                     unsigned int* err_word, const RowsFault& fault, cudaStream_t stream) {
+  const bool vec = ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y)) & 15u) == 0 &&
+                   (ld_x & 7) == 0 && (ld_y & 7) == 0;
+  if (!vec && !same_phase(x, y, ld_x, ld_y, 2)) {
+    launch_stream(softmax_rows16_stream_kernel<kType, false>, x, y, m, l, rows, cols, ld_x, ld_y, k, 1, stream);
+    return;
+  }
+  // rows off the 16-byte grid (x and y in step) take the configuration of an
+  // aligned row of the same length with one more chunk slot per thread
+  const int64_t chunks = (cols + 7) / 8;
+  if (vec)
+    dispatch_rows16_table<kType, false>(x, y, m, l, rows, cols, chunks, ld_x, ld_y, k, err_word, fault, stream);
+  else
+    dispatch_rows16_table<kType, true>(x, y, m, l, rows, cols, chunks, ld_x, ld_y, k, err_word, fault, stream);
 }
 
 cudaError_t launch_softmax_rows16(const uint16_t* x, uint16_t* y, float* m, float* l,
