@@ -54,20 +54,28 @@ NOMINAL = {"hbm_gbs": 7900.0, "bf16_tflops": 2250.0}
 # "scale" records traffic / algorithmic bytes of a smaller capture of the
 # same kernel, applied to the full launch's algorithmic bytes.
 NCU_TRAFFIC = {
-    "softmax_32k": {"source": "pass_attention_gb300/csrc/softmax_rows.cu",
-                    "sha256": "f2c3cf6a2e23c2a370e6bc8fbb098f0a92b625935b51c26be50756722b76e40b",
-                    "bytes_per_launch": 1073785344 + 1017656064},
-    "softmax_32k_bf16": {"source": "pass_attention_gb300/csrc/softmax_rows.cu",
-                         "sha256": "f2c3cf6a2e23c2a370e6bc8fbb098f0a92b625935b51c26be50756722b76e40b",
-                         "bytes_per_launch": 536911872 + 482367488},
+    "softmax_32k": {"source": ["pass_attention_gb300/csrc/softmax_rows.cu",
+                               "pass_attention_gb300/csrc/softmax_common.cuh",
+                               "pass_attention_gb300/csrc/device_common.cuh"],
+                    "sha256": "79854b8387dad60353dfe42ce7085cb4670f987438e7d52821f005dfc9871292",
+                    "bytes_per_launch": 1073781248 + 1017876224},
+    "softmax_32k_bf16": {"source": ["pass_attention_gb300/csrc/softmax_grouped.cu",
+                                    "pass_attention_gb300/csrc/softmax_common.cuh",
+                                    "pass_attention_gb300/csrc/device_common.cuh"],
+                         "sha256": "ac1bb79bb9714cd101908e2973ed33c4e48b5bf5e496488104c2b81bbb212d98",
+                         "bytes_per_launch": 536921088 + 482647296},
     # the comparators: all sweeps of one call (each reads x from DRAM again)
-    "softmax_32k_3pass": {"source": "pass_attention_gb300/csrc/softmax_rows.cu",
-                          "sha256": "f2c3cf6a2e23c2a370e6bc8fbb098f0a92b625935b51c26be50756722b76e40b",
-                          "bytes_per_launch": (1073818624 + 2815488) + (1073973760 + 166144)
-                          + (1074052352 + 1024768000)},
-    "softmax_32k_2pass": {"source": "pass_attention_gb300/csrc/softmax_rows.cu",
-                          "sha256": "f2c3cf6a2e23c2a370e6bc8fbb098f0a92b625935b51c26be50756722b76e40b",
-                          "bytes_per_launch": (1073793024 + 3014400) + (1074185472 + 1025043456)},
+    "softmax_32k_3pass": {"source": ["pass_attention_gb300/csrc/softmax_rows.cu",
+                                     "pass_attention_gb300/csrc/softmax_common.cuh",
+                                     "pass_attention_gb300/csrc/device_common.cuh"],
+                          "sha256": "79854b8387dad60353dfe42ce7085cb4670f987438e7d52821f005dfc9871292",
+                          "bytes_per_launch": (1073761792 + 2926848) + (1073933056 + 339712)
+                          + (1074051072 + 1024764672)},
+    "softmax_32k_2pass": {"source": ["pass_attention_gb300/csrc/softmax_rows.cu",
+                                     "pass_attention_gb300/csrc/softmax_common.cuh",
+                                     "pass_attention_gb300/csrc/device_common.cuh"],
+                          "sha256": "79854b8387dad60353dfe42ce7085cb4670f987438e7d52821f005dfc9871292",
+                          "bytes_per_launch": (1073761024 + 3011328) + (1074070784 + 1024732160)},
     "attn_4k": {"source": "pass_attention_gb300/csrc/attn_fwd.cu",
                 "sha256": "1de91f1a14f7b69059f99bd37628b4126df733c28a5f205b034826a15235ccec",
                 "bytes_per_launch": 201502976 + 47736320},
@@ -96,15 +104,18 @@ def peaks():
 
 
 def source_sha(rel):
-    """sha256 of a kernel source with its comments and blank lines removed,
-    so that a comment edit keeps the ncu figures taken of the same code."""
+    """sha256 of a kernel's sources (one path, or a list: the kernel's file and
+    the headers it includes) with comments and blank lines removed, so that a
+    comment edit keeps the ncu figures taken of the same code."""
     import re
-    with open(os.path.join(ROOT, rel)) as f:
-        text = f.read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    lines = [re.sub(r"//.*$", "", ln).rstrip() for ln in text.splitlines()]
-    code = "\n".join(ln for ln in lines if ln.strip())
-    return hashlib.sha256(code.encode()).hexdigest()
+    h = hashlib.sha256()
+    for path in ([rel] if isinstance(rel, str) else rel):
+        with open(os.path.join(ROOT, path)) as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        lines = [re.sub(r"//.*$", "", ln).rstrip() for ln in text.splitlines()]
+        h.update("\n".join(ln for ln in lines if ln.strip()).encode())
+    return h.hexdigest()
 
 
 def traffic_for(workload, algorithmic_bytes=None):
@@ -260,13 +271,18 @@ def bench_softmax(args, ctx):
     oss.softmax_rows_from_host(xh, w.scale, out=outs, x_dev=x, y_dev=y)
     torch.cuda.synchronize()
     ctx["barrier"]()
+    # three timed blocks of e2e_steps calls; the median block is reported (a
+    # block that meets contention on the shared host side does not decide it)
     s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    s.record()
-    for _ in range(e2e_steps):
-        oss.softmax_rows_from_host(xh, w.scale, out=outs, x_dev=x, y_dev=y)
-    e.record()
-    torch.cuda.synchronize()
-    e2e_ms = s.elapsed_time(e) / e2e_steps
+    blocks = []
+    for _ in range(3):
+        s.record()
+        for _ in range(e2e_steps):
+            oss.softmax_rows_from_host(xh, w.scale, out=outs, x_dev=x, y_dev=y)
+        e.record()
+        torch.cuda.synchronize()
+        blocks.append(s.elapsed_time(e) / e2e_steps)
+    e2e_ms = statistics.median(blocks)
     # the host link on this machine: plain pinned copies of the same buffers, both
     # directions at once (the e2e step cannot beat this)
     s_up, s_dn = torch.cuda.Stream(), torch.cuda.Stream()
@@ -293,7 +309,8 @@ def bench_softmax(args, ctx):
     del xh, outs
     return {"workload": w, "total_ms": total_ms, "step_ms": step_ms, "median_ms": median_ms,
             "t0": t0, "t1": t1,
-            "nbytes": nbytes, "e2e_ms": e2e_ms, "link_gbs": link_gbs, "h2d": w.rows * w.cols * 4,
+            "nbytes": nbytes, "e2e_ms": e2e_ms, "e2e_blocks_ms": blocks, "link_gbs": link_gbs,
+            "h2d": w.rows * w.cols * 4,
             "d2h": w.rows * w.cols * 4 + 2 * w.rows * 4}
 
 
@@ -714,7 +731,9 @@ def main():
                 "h2d_bytes_per_step": sm["h2d"], "d2h_bytes_per_step": sm["d2h"],
                 "host_link_gbs": sm["link_gbs"],
                 "frac_of_host_link": (sm["nbytes"] / (e2e_ms / 1e3) / 1e9) / sm["link_gbs"],
-                "note": "host_link_gbs: pinned H2D + D2H copies of the same buffers, both at once"},
+                "blocks_gbs": [sm["nbytes"] / (b / 1e3) / 1e9 for b in sm["e2e_blocks_ms"]],
+                "note": "median of three timed blocks of calls (blocks_gbs); host_link_gbs: "
+                        "pinned H2D + D2H copies of the same buffers, both at once"},
         "gpu_launches": args.steps,
         "roofline": {"bound": "hbm", "kernel": kname, "achieved": achieved, "peak": pk["hbm_gbs"],
                      "unit": "GB/s", "frac": achieved / pk["hbm_gbs"],
