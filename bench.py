@@ -57,25 +57,25 @@ NCU_TRAFFIC = {
     "softmax_32k": {"source": ["pass_attention_gb300/csrc/softmax_rows.cu",
                                "pass_attention_gb300/csrc/softmax_common.cuh",
                                "pass_attention_gb300/csrc/device_common.cuh"],
-                    "sha256": "79854b8387dad60353dfe42ce7085cb4670f987438e7d52821f005dfc9871292",
-                    "bytes_per_launch": 1073781248 + 1017876224},
+                    "sha256": "d6ab156378bb084b00f8097ee95196522d4816301b57b1e3996e7114249e689f",
+                    "bytes_per_launch": 1073788928 + 1017820672},
     "softmax_32k_bf16": {"source": ["pass_attention_gb300/csrc/softmax_grouped.cu",
                                     "pass_attention_gb300/csrc/softmax_common.cuh",
                                     "pass_attention_gb300/csrc/device_common.cuh"],
-                         "sha256": "fe6c3c3155c6a16e82fa8e0b0ab120b55143c2e9b5716250c7904ff4477a956a",
-                         "bytes_per_launch": 536915712 + 484293120},
+                         "sha256": "1a829292f655eb21936a73ffa719c786c112e04d568c54e216215a59e249123e",
+                         "bytes_per_launch": 536894976 + 484324864},
     # the comparators: all sweeps of one call (each reads x from DRAM again)
     "softmax_32k_3pass": {"source": ["pass_attention_gb300/csrc/softmax_rows.cu",
                                      "pass_attention_gb300/csrc/softmax_common.cuh",
                                      "pass_attention_gb300/csrc/device_common.cuh"],
-                          "sha256": "79854b8387dad60353dfe42ce7085cb4670f987438e7d52821f005dfc9871292",
-                          "bytes_per_launch": (1073761792 + 2926848) + (1073933056 + 339712)
-                          + (1074051072 + 1024764672)},
+                          "sha256": "d6ab156378bb084b00f8097ee95196522d4816301b57b1e3996e7114249e689f",
+                          "bytes_per_launch": (1073785856 + 2573568) + (1073987840 + 212736)
+                          + (1074051328 + 1024907520)},
     "softmax_32k_2pass": {"source": ["pass_attention_gb300/csrc/softmax_rows.cu",
                                      "pass_attention_gb300/csrc/softmax_common.cuh",
                                      "pass_attention_gb300/csrc/device_common.cuh"],
-                          "sha256": "79854b8387dad60353dfe42ce7085cb4670f987438e7d52821f005dfc9871292",
-                          "bytes_per_launch": (1073761024 + 3011328) + (1074070784 + 1024732160)},
+                          "sha256": "d6ab156378bb084b00f8097ee95196522d4816301b57b1e3996e7114249e689f",
+                          "bytes_per_launch": (1073761280 + 3418112) + (1074050816 + 1025053952)},
     "attn_4k": {"source": "pass_attention_gb300/csrc/attn_fwd.cu",
                 "sha256": "1de91f1a14f7b69059f99bd37628b4126df733c28a5f205b034826a15235ccec",
                 "bytes_per_launch": 201502976 + 47736320},

@@ -536,4 +536,12 @@ bool cluster_rows(int kind, const void* x, void* y, float* m, float* l, int64_t 
                   int64_t ld_x, int64_t ld_y, const ScaleConsts& k, unsigned int* err,
                   const RowsFault& fault, cudaStream_t stream);
 
+// softmax_flat.cu: short rows (at most 512 bytes, or 1 KB off the 16-byte
+// grid) of a matrix whose x rows lie back to back, tiles of whole rows staged
+// in shared memory; x and y at any offset from the grid, y at any leading
+// dimension.
+bool flat_rows(int kind, const void* x, void* y, float* m, float* l, int64_t rows, int64_t cols,
+               int64_t ld_x, int64_t ld_y, const ScaleConsts& k, unsigned int* err,
+               const RowsFault& fault, cudaStream_t stream);
+
 }  // namespace oss

@@ -1,0 +1,328 @@
+// G1, short rows of a dense matrix, staged through shared memory.
+//
+// Rows of at most 1 KB whose x rows lie back to back (leading dimension =
+// row length), so that any run of whole rows is one contiguous byte range.
+// A CTA takes tiles of R consecutive rows. The tile's bytes arrive by bulk
+// asynchronous copies of the 16-byte granules that cover them, into one of
+// three shared-memory buffers, so each CTA has two tiles in flight while it
+// works on a third: short rows then keep as many bytes in flight per SM as
+// long ones, whatever their offset from the 16-byte grid. A granule that a
+// tile shares with its neighbour is copied by both; only the matrix's own
+// partial first and last granules, which reach outside x, are read with plain
+// 16-byte loads (the bytes outside x share a granule, and so a page, with an
+// element of x, and are never used).
+//
+// A group of G threads (1 to 32) owns a row at a time and reads it from
+// shared memory in 16-byte chunks on the grid of its offset s (chunk c holds
+// the elements [c * E - s, (c + 1) * E - s), E elements to a chunk, the
+// partial first and last chunks padded with -inf), NV chunks a thread. G is
+// the narrowest group that holds the row, so that a warp works on 32 / G rows
+// at once and the per-row work (the merge of the group's (max, sum) states
+// by shuffles, the scale factor, m and l) is shared by as many rows as
+// possible; with scalar accesses and groups of 16, that per-row work and one
+// shared-memory load and one store per element left the kernel bound by
+// instruction issue at half the copy peak for 16-bit rows. y is written in
+// 16-byte chunks when its rows have x's offsets, element by element
+// otherwise, so y needs neither x's alignment nor its leading dimension.
+// kKind: 0 = fp32, 1 = bf16, 2 = fp16.
+
+#include "softmax_common.cuh"
+
+namespace oss {
+namespace {
+
+constexpr int kFlBufs = 3;                  // tile buffers per CTA
+constexpr int kFlMinBlocks = 4;             // CTAs per SM
+constexpr int64_t kFlTileBytes = 14 << 10;  // x bytes per tile, at most
+constexpr int64_t kFlMaxRowBytes = 1024;    // the longest row taken
+constexpr int64_t kFlGridRowBytes = 512;    // the longest taken when every row is on the grid
+constexpr int kFlNv = 4;                    // 16-byte chunks a thread holds
+
+template <int kKind>
+__device__ __forceinline__ void flat_store(unsigned char* yr, int j, float v) {
+  if constexpr (kKind == 0)
+    reinterpret_cast<float*>(yr)[j] = v;
+  else
+    reinterpret_cast<uint16_t*>(yr)[j] = h16_round<kKind>(v);
+}
+
+// Thread 0: the copies of tile `tile` (rows [tile * R, tile * R + nr)) into
+// the buffer at shared address buf_a, completing on bar_a. [x0, x1) is the
+// whole matrix. The buffer holds the granules [ga, gb) that cover the tile;
+// those wholly inside x come by bulk copies, the matrix's partial first and
+// last granules by plain loads stored at once. The barrier expects `extra`
+// bytes more than are copied (0 but in the test hook, which makes the wait
+// run out).
+__device__ __forceinline__ void issue_tile(uintptr_t x0, uintptr_t x1, int64_t row_bytes, int64_t R,
+                                           int64_t rows, int64_t tile, unsigned char* buf,
+                                           uint32_t buf_a, uint32_t bar_a, uint32_t extra) {
+  const int64_t r0 = tile * R;
+  const int64_t nr = (rows - r0 < R) ? rows - r0 : R;
+  const uintptr_t a = x0 + static_cast<uintptr_t>(r0 * row_bytes);
+  const uintptr_t b = a + static_cast<uintptr_t>(nr * row_bytes);
+  const uintptr_t ga = a & ~uintptr_t(15);
+  const uintptr_t gb = (b + 15) & ~uintptr_t(15);
+  const uintptr_t in0 = (x0 + 15) & ~uintptr_t(15);  // x's first whole granule
+  const uintptr_t in1 = x1 & ~uintptr_t(15);         // one past its last whole granule
+  const uintptr_t lo = ga > in0 ? ga : in0;
+  const uintptr_t hi = gb < in1 ? gb : in1;
+  const uint32_t bulk = hi > lo ? static_cast<uint32_t>(hi - lo) : 0u;
+  // the buffer was last read through the generic proxy; order that before
+  // the copies' asynchronous writes
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  if (bulk + extra > 0) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar_a),
+                 "r"(bulk + extra)
+                 : "memory");
+    const uint32_t dst = buf_a + static_cast<uint32_t>(lo - ga);
+    for (uint32_t off = 0; off < bulk; off += kClPiece) {
+      const uint32_t size = (bulk - off < kClPiece) ? (bulk - off) : kClPiece;
+      asm volatile(
+          "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+              "r"(dst + off), "l"(lo + off), "r"(size), "r"(bar_a)
+          : "memory");
+    }
+  } else {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar_a) : "memory");
+  }
+  // x's partial first granule (in the buffer when this is the first tile)
+  // and partial last granule (when it is the last), once if they are one
+  const uintptr_t first = x0 & ~uintptr_t(15);
+  const uintptr_t last = (x1 - 1) & ~uintptr_t(15);
+  const bool head = (x0 & 15) != 0 && ga == first;
+  if (head) *reinterpret_cast<uint4*>(buf) = __ldg(reinterpret_cast<const uint4*>(first));
+  if ((x1 & 15) != 0 && gb == last + 16 && !(head && last == first))
+    *reinterpret_cast<uint4*>(buf + (last - ga)) = __ldg(reinterpret_cast<const uint4*>(last));
+}
+
+// G threads per row, NV chunks each (a row spans at most G * NV chunks).
+// kYInStep: y's rows have x's offsets from the 16-byte grid.
+template <int kKind, int G, int NV, bool kYInStep>
+__global__ void __launch_bounds__(kThreads, kFlMinBlocks)
+softmax_rows_flat_kernel(const void* __restrict__ x, void* __restrict__ y,
+                         float* __restrict__ m_out, float* __restrict__ l_out, int64_t rows,
+                         int cols, int64_t ld_y, ScaleConsts k, int64_t R, int64_t tiles,
+                         int buf_stride, unsigned int* err, uint32_t fault_tx, uint64_t timeout_ns) {
+  constexpr int kEpc = RowElem<kKind>::kEpc;
+  constexpr int kEsz = RowElem<kKind>::kSize;
+  constexpr int kGroups = kThreads / G;
+  constexpr int kPerWarp = (G < 32) ? 32 / G : 1;
+  extern __shared__ __align__(128) unsigned char tile_bufs[];
+  __shared__ __align__(8) uint64_t bars[kFlBufs];
+
+  const int tid = threadIdx.x;
+  const int g = tid / G;
+  const int t = tid % G;
+  // a warp's groups walk their rows together (the shuffles take the whole
+  // warp); a group past the tile's last row runs as an empty row
+  const int lead = g % kPerWarp;
+  const int64_t row_bytes = static_cast<int64_t>(cols) * kEsz;
+  const uintptr_t x0 = reinterpret_cast<uintptr_t>(x);
+  const uintptr_t x1 = x0 + static_cast<uintptr_t>(rows * row_bytes);
+  unsigned char* yb = static_cast<unsigned char*>(y);
+
+  if (tid == 0) {
+    for (int b = 0; b < kFlBufs; ++b)
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&bars[b])) : "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  // thread 0's books: buffers with a copy not yet waited for, and the
+  // parity of the phase that copy completes
+  uint32_t pend = 0u, ppar = 0u;
+  if (tid == 0) {
+    for (int b = 0; b < kFlBufs; ++b) {
+      const int64_t tile = blockIdx.x + static_cast<int64_t>(b) * gridDim.x;
+      if (tile < tiles) {
+        unsigned char* buf = tile_bufs + b * buf_stride;
+        issue_tile(x0, x1, row_bytes, R, rows, tile, buf, smem_u32(buf), smem_u32(&bars[b]),
+                   b == 0 ? fault_tx : 0u);
+        pend |= 1u << b;
+      }
+    }
+  }
+  __syncthreads();  // the granules thread 0 stored
+
+  uint32_t par = 0u;  // bit b: the parity of buffer b's next phase
+  bool live = true;   // false once this thread gave up on a wait: no more waits or copies
+  int b = 0;
+  for (int64_t tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
+    const uint32_t bar_a = smem_u32(&bars[b]);
+    if (live) {
+      live = mbar_wait_bounded(bar_a, (par >> b) & 1u, err, timeout_ns);
+      pend &= ~(1u << b);  // landed, or given up on for good
+    }
+    par ^= 1u << b;
+    const unsigned char* buf = tile_bufs + b * buf_stride;
+    const int64_t r0 = tile * R;
+    const int nr = static_cast<int>((rows - r0 < R) ? rows - r0 : R);
+    const int head = static_cast<int>((x0 + static_cast<uintptr_t>(r0 * row_bytes)) & 15u);
+
+    const uint4 pad = make_uint4(neg_inf_word<kKind>(), neg_inf_word<kKind>(), neg_inf_word<kKind>(),
+                                 neg_inf_word<kKind>());
+    for (int ib = g - lead; ib < nr; ib += kGroups) {
+      const int i = ib + lead;
+      const bool active = i < nr;
+      const int o = head + i * static_cast<int>(row_bytes);  // the row's byte offset in the buffer
+      const int sp = (o & 15) / kEsz;                          // its offset from the grid, in elements
+      const uint4* rg = reinterpret_cast<const uint4*>(buf + (o & ~15));
+      const int nch = (cols + sp + kEpc - 1) / kEpc;
+      float2 w[NV][kEpc / 2];
+#pragma unroll
+      for (int v = 0; v < NV; ++v) {
+        const int c = t + v * G;
+        unpack_chunk16<kKind>((active && c < nch) ? fix_granule<kKind>(rg[c], c, cols, sp) : pad, w[v]);
+      }
+      float xa = neg_inf(), xc = neg_inf();
+#pragma unroll
+      for (int v = 0; v < NV; ++v) {
+#pragma unroll
+        for (int h = 0; h < kEpc / 2; h += 2) {
+          xa = fmax3(xa, w[v][h].x, w[v][h].y);
+          if (h + 1 < kEpc / 2) xc = fmax3(xc, w[v][h + 1].x, w[v][h + 1].y);
+        }
+      }
+      const float xm = fmaxf(xa, xc);
+      const float Mt = (xm == neg_inf()) ? 0.f : base2_of(xm, k);
+      const float2 negM = make_float2(-Mt, -Mt);
+      float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int v = 0; v < NV; ++v) {
+#pragma unroll
+        for (int h = 0; h < kEpc / 2; ++h) {
+          w[v][h] = weight2(w[v][h], negM, k);
+          acc = __fadd2_rn(acc, w[v][h]);
+        }
+      }
+      const float ls = acc.x + acc.y;
+      // the group's state: the maximum, then each sum scaled to it
+      float xw = xm, lw = ls;
+      if constexpr (G > 1) {
+#pragma unroll
+        for (int off = G / 2; off > 0; off >>= 1) xw = fmaxf(xw, __shfl_xor_sync(0xffffffffu, xw, off));
+        lw = (xm == neg_inf()) ? 0.f : ls * ex2(base2_of(xm, k) - base2_of(xw, k));
+#pragma unroll
+        for (int off = G / 2; off > 0; off >>= 1) lw += __shfl_xor_sync(0xffffffffu, lw, off);
+      }
+      float f = 0.f;
+      if (xm != neg_inf() && lw > 0.f) f = ex2(base2_of(xm, k) - base2_of(xw, k)) * (1.0f / lw);
+      const float2 f2 = make_float2(f, f);
+      if (active) {
+        const int64_t row = r0 + i;
+        unsigned char* yr = yb + row * ld_y * kEsz;
+#pragma unroll
+        for (int v = 0; v < NV; ++v) {
+          const int c = t + v * G;
+          if (c < nch) {
+            if constexpr (kYInStep) {
+              store_chunk16<kKind>(reinterpret_cast<char*>(yr), c, cols, sp, pack_chunk16<kKind>(w[v], f2));
+            } else {
+#pragma unroll
+              for (int e = 0; e < kEpc; ++e) {
+                const int j = c * kEpc - sp + e;
+                if (j >= 0 && j < cols)
+                  flat_store<kKind>(yr, j, ((e & 1) ? w[v][e >> 1].y : w[v][e >> 1].x) * f);
+              }
+            }
+          }
+        }
+        if (t == 0) write_ml(xw, lw, k, row, m_out, l_out);
+      }
+    }
+
+    __syncthreads();  // buffer b is read out
+    const int64_t next = tile + static_cast<int64_t>(kFlBufs) * gridDim.x;
+    if (tid == 0 && live && next < tiles) {
+      unsigned char* nbuf = tile_bufs + b * buf_stride;
+      issue_tile(x0, x1, row_bytes, R, rows, next, nbuf, smem_u32(nbuf), bar_a, 0u);
+      pend |= 1u << b;
+      ppar = (ppar & ~(1u << b)) | (par & (1u << b));
+    }
+    b = (b + 1 == kFlBufs) ? 0 : b + 1;
+  }
+  // after a give-up: the copies still in flight land before the CTA ends
+  if (tid == 0)
+    for (int c = 0; c < kFlBufs; ++c)
+      if ((pend >> c) & 1u) mbar_wait_bounded(smem_u32(&bars[c]), (ppar >> c) & 1u, err, timeout_ns);
+}
+
+// Tiles of up to kFlTileBytes (fewer rows per tile when the matrix would
+// not give every CTA of one wave a tile), one wave of kFlMinBlocks CTAs per
+// SM, each walking its tiles.
+template <int kKind, int G, bool kYInStep>
+void launch_flat(const void* x, void* y, float* m, float* l, int64_t rows, int64_t cols,
+                 int64_t ld_y, const ScaleConsts& k, unsigned int* err, const RowsFault& fault,
+                 cudaStream_t stream) {
+  constexpr int kEsz = RowElem<kKind>::kSize;
+  const int64_t row_bytes = cols * kEsz;
+  const int64_t cap = static_cast<int64_t>(sm_count()) * kFlMinBlocks;
+  int64_t R = kFlTileBytes / row_bytes;
+  const int64_t spread = (rows + cap - 1) / cap;
+  if (R > spread) R = spread;
+  if (R < 1) R = 1;
+  const int64_t tiles = (rows + R - 1) / R;
+  const int stride = static_cast<int>((R * row_bytes + 32 + 127) / 128 * 128);
+  const int grid = static_cast<int>(tiles < cap ? tiles : cap);
+  const uint64_t timeout = fault.timeout_ns > 0 ? static_cast<uint64_t>(fault.timeout_ns) : kClTimeoutNs;
+  softmax_rows_flat_kernel<kKind, G, kFlNv, kYInStep>
+      <<<grid, kThreads, static_cast<size_t>(stride) * kFlBufs, stream>>>(
+          x, y, m, l, rows, static_cast<int>(cols), ld_y, k, R, tiles, stride, err, fault.extra_tx,
+          timeout);
+}
+
+template <int kKind, bool kYInStep>
+void launch_flat_g(int64_t chunks, const void* x, void* y, float* m, float* l, int64_t rows,
+                   int64_t cols, int64_t ld_y, const ScaleConsts& k, unsigned int* err,
+                   const RowsFault& fault, cudaStream_t stream) {
+  if (chunks <= kFlNv)
+    launch_flat<kKind, 1, kYInStep>(x, y, m, l, rows, cols, ld_y, k, err, fault, stream);
+  else if (chunks <= 2 * kFlNv)
+    launch_flat<kKind, 2, kYInStep>(x, y, m, l, rows, cols, ld_y, k, err, fault, stream);
+  else if (chunks <= 4 * kFlNv)
+    launch_flat<kKind, 4, kYInStep>(x, y, m, l, rows, cols, ld_y, k, err, fault, stream);
+  else if (chunks <= 8 * kFlNv)
+    launch_flat<kKind, 8, kYInStep>(x, y, m, l, rows, cols, ld_y, k, err, fault, stream);
+  else if (chunks <= 16 * kFlNv)
+    launch_flat<kKind, 16, kYInStep>(x, y, m, l, rows, cols, ld_y, k, err, fault, stream);
+  else
+    launch_flat<kKind, 32, kYInStep>(x, y, m, l, rows, cols, ld_y, k, err, fault, stream);
+}
+
+template <int kKind>
+bool flat_rows_as(const void* x, void* y, float* m, float* l, int64_t rows, int64_t cols,
+                  int64_t ld_x, int64_t ld_y, const ScaleConsts& k, unsigned int* err,
+                  const RowsFault& fault, cudaStream_t stream) {
+  constexpr int kEpc = RowElem<kKind>::kEpc;
+  constexpr int kEsz = RowElem<kKind>::kSize;
+  if ((rows > 1 && ld_x != cols) || cols * kEsz > kFlMaxRowBytes) return false;
+  if (((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y)) % kEsz) != 0) return false;
+  // rows on the 16-byte grid longer than kFlGridRowBytes run faster in the
+  // grouped kernel, which reads them straight into registers (GB300, 2^28
+  // elements: fp32 rows of 256 elements at 0.96 of the copy peak there
+  // against 0.85 here, bf16 rows of 512 at 0.88 against 0.87)
+  const bool grid_rows = ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y)) & 15u) == 0 &&
+                         (cols * kEsz) % 16 == 0 && (ld_y * kEsz) % 16 == 0;
+  if (grid_rows && cols * kEsz > kFlGridRowBytes) return false;
+  // the most chunks a row spans: rows 16-byte multiples long all have x's
+  // offset, others may lie at any
+  const int s0 = static_cast<int>((reinterpret_cast<uintptr_t>(x) & 15u) / kEsz);
+  const int smax = ((cols * kEsz) % 16 == 0 || rows == 1) ? s0 : kEpc - 1;
+  const int64_t chunks = (cols + smax + kEpc - 1) / kEpc;
+  if (same_phase(x, y, cols, ld_y, kEsz))
+    launch_flat_g<kKind, true>(chunks, x, y, m, l, rows, cols, ld_y, k, err, fault, stream);
+  else
+    launch_flat_g<kKind, false>(chunks, x, y, m, l, rows, cols, ld_y, k, err, fault, stream);
+  return true;
+}
+
+}  // namespace
+
+bool flat_rows(int kind, const void* x, void* y, float* m, float* l, int64_t rows, int64_t cols,
+               int64_t ld_x, int64_t ld_y, const ScaleConsts& k, unsigned int* err,
+               const RowsFault& fault, cudaStream_t stream) {
+  if (kind == 0) return flat_rows_as<0>(x, y, m, l, rows, cols, ld_x, ld_y, k, err, fault, stream);
+  if (kind == 1) return flat_rows_as<1>(x, y, m, l, rows, cols, ld_x, ld_y, k, err, fault, stream);
+  return flat_rows_as<2>(x, y, m, l, rows, cols, ld_x, ld_y, k, err, fault, stream);
+}
+
+}  // namespace oss

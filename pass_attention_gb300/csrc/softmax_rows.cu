@@ -436,16 +436,21 @@ void launch_stream(Kernel kernel, const T* x, T* y, float* m, float* l, int64_t 
 
 }  // namespace
 
-// The dispatch. Rows whose x and y are not in step on the 16-byte grid are
-// streamed. Aligned fp32 rows of 2049..16384 elements take a CTA each with the
-// row in registers (the kernel the headline workload runs); other rows of up
-// to 2048 fp32 (16384 16-bit, 8192 fp32 off the grid) elements go to the
-// grouped kernel, longer ones of up to 1.6 MB to the cluster-resident kernel,
-// and the rest are streamed.
+// The dispatch. Rows of a matrix whose x rows lie back to back are staged
+// in shared memory by tiles (y at any layout) when they are at most 512 bytes
+// long, or at most 1 KB and off the 16-byte grid. Otherwise, rows
+// whose x and y are not in step on the 16-byte grid are streamed. Aligned fp32
+// rows of 2049..16384 elements take a CTA each with the row in registers (the
+// kernel the headline workload runs); other rows of up to 2048 fp32 (16384
+// 16-bit, 8192 fp32 off the grid) elements go to the grouped kernel, longer
+// ones of up to 1.6 MB to the cluster-resident kernel, and the rest are
+// streamed.
 cudaError_t launch_softmax_rows(const float* x, float* y, float* m, float* l, int64_t rows,
                                 int64_t cols, int64_t ld_x, int64_t ld_y, float scale,
                                 unsigned int* err_word, const RowsFault& fault, cudaStream_t stream) {
   const ScaleConsts k = make_consts(scale);
+  if (flat_rows(0, x, y, m, l, rows, cols, ld_x, ld_y, k, err_word, fault, stream))
+    return cudaGetLastError();
   const bool on_grid = ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y)) & 15u) == 0 &&
                        (ld_x & 3) == 0 && (ld_y & 3) == 0;
   if (!on_grid && !same_phase(x, y, ld_x, ld_y, 4)) {
@@ -478,6 +483,7 @@ template <int kType>
 void dispatch_rows16(const uint16_t* x, uint16_t* y, float* m, float* l, int64_t rows,
                      int64_t cols, int64_t ld_x, int64_t ld_y, const ScaleConsts& k,
                      unsigned int* err_word, const RowsFault& fault, cudaStream_t stream) {
+  if (flat_rows(kType, x, y, m, l, rows, cols, ld_x, ld_y, k, err_word, fault, stream)) return;
   const bool on_grid = ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y)) & 15u) == 0 &&
                        (ld_x & 7) == 0 && (ld_y & 7) == 0;
   if (!on_grid && !same_phase(x, y, ld_x, ld_y, 2)) {

@@ -97,11 +97,12 @@ def timeout_code():
 @pytest.mark.parametrize("kind,cols,rows", [
     ("fp32", 65536, 200),   # 256 KB rows: a cluster of several CTAs, one buffer each
     ("bf16", 20000, 700),   # 40 KB rows: one CTA with two buffers
+    ("bf16", 100, 100000),  # 200-byte rows of a dense matrix: tiles staged in shared memory
 ])
 def test_row_softmax_copy_wait_times_out_and_context_survives(kind, cols, rows):
-    # every CTA's first row expects 16 bytes that never arrive: its wait gives
-    # up after 20 ms, it copies and waits no more but still meets its
-    # cluster's barriers, and the launch ends
+    # every CTA's first row (or tile) expects 16 bytes that never arrive: its
+    # wait gives up after 20 ms, it copies and waits no more but still meets
+    # its barriers, lets the copies already issued land, and the launch ends
     import time
     dtype = torch.float32 if kind == "fp32" else torch.bfloat16
     x = workloads.logits(rows, cols, 10.0, seed=cols, device="cuda").to(dtype)
