@@ -296,13 +296,25 @@ bool flat_rows_as(const void* x, void* y, float* m, float* l, int64_t rows, int6
   constexpr int kEsz = RowElem<kKind>::kSize;
   if ((rows > 1 && ld_x != cols) || cols * kEsz > kFlMaxRowBytes) return false;
   if (((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y)) % kEsz) != 0) return false;
-  // rows on the 16-byte grid longer than kFlGridRowBytes run faster in the
+  // Rows on the 16-byte grid longer than kFlGridRowBytes run faster in the
   // grouped kernel, which reads them straight into registers (GB300, 2^28
   // elements: fp32 rows of 256 elements at 0.96 of the copy peak there
-  // against 0.85 here, bf16 rows of 512 at 0.88 against 0.87)
+  // against 0.85 here, bf16 rows of 512 at 0.88 against 0.87). So do shorter
+  // fp32 rows on the grid that fill at least 80% of the grouped kernel's
+  // chunk slots (a power of two, at least 8, per row): 32, 64 and 128
+  // elements ran at 0.91-0.93 there against 0.85-0.87 here, while 16 (0.51
+  // there, 0.79 here) and 100 (0.77, 0.86) come here. 16-bit rows on the
+  // grid came out ahead here at every length up to 512 bytes (bf16 at 128
+  // elements 0.84 against 0.72), and rows off the grid at every length taken.
   const bool grid_rows = ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y)) & 15u) == 0 &&
                          (cols * kEsz) % 16 == 0 && (ld_y * kEsz) % 16 == 0;
   if (grid_rows && cols * kEsz > kFlGridRowBytes) return false;
+  if (kKind == 0 && grid_rows) {
+    const int64_t chunks = cols * kEsz / 16;
+    int64_t slots = 8;
+    while (slots < chunks) slots *= 2;
+    if (5 * chunks >= 4 * slots) return false;
+  }
   // the most chunks a row spans: rows 16-byte multiples long all have x's
   // offset, others may lie at any
   const int s0 = static_cast<int>((reinterpret_cast<uintptr_t>(x) & 15u) / kEsz);
