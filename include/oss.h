@@ -89,8 +89,14 @@ typedef enum os_status {
  * whose slices' (max, sum) states are merged through distributed shared
  * memory. For a row off the 16-byte grid, the loads of its first and last
  * chunks may read (never write) bytes of the same 16-byte granules outside
- * the row. Rows whose x and y offsets differ, and rows longer than 1.6 MB,
- * are streamed twice (two reads, one write).
+ * the row. Short rows of a matrix whose x rows lie back to back (ld_x ==
+ * cols; rows of up to 512 bytes, or 1 KB off the 16-byte grid) are taken a
+ * tile of whole rows at a time, copied into shared memory by bulk
+ * asynchronous copies whatever their offsets, with y at any offset and
+ * leading dimension; the 16-byte granules holding x's first and last
+ * elements may be read (never written) whole. Other rows whose x and y
+ * offsets differ, and rows longer than 1.6 MB, are streamed twice (two reads,
+ * one write).
  * Errors: OS_ERR_INVALID_ARGUMENT, OS_ERR_MISALIGNED, OS_ERR_CUDA.
  */
 OSS_API os_status os_softmax_rows(const float* x, float* y, float* m, float* l,
@@ -123,8 +129,10 @@ typedef enum os_dtype {
  * y's rows start at the same offsets from a 16-byte boundary, rows of up to
  * 16384 elements are held in registers and longer rows of up to 1.6 MB in a
  * cluster's shared memory, as for os_softmax_rows (one read, one write per
- * element, the same granule reads at the ends of a row off the grid); other
- * rows are streamed twice.
+ * element, the same granule reads at the ends of a row off the grid). Short
+ * rows of a matrix whose x rows lie back to back are staged in shared memory
+ * by tiles as for os_softmax_rows, with y at any layout; other rows are
+ * streamed twice.
  * Errors: OS_ERR_INVALID_ARGUMENT, OS_ERR_MISALIGNED, OS_ERR_CUDA.
  */
 OSS_API os_status os_softmax_rows_16bit(const void* x, void* y, float* m, float* l,
@@ -297,11 +305,12 @@ OSS_API os_status os_check_device_error(void* stream, int32_t* code);
  *           undefined.
  *   kind 2: the next os_softmax_rows or os_softmax_rows_16bit call. If it
  *           holds its rows in a cluster's shared memory (aligned rows longer
- *           than 16384 elements and at most 1.6 MB), every CTA's barrier for
- *           the bulk copies of its first row is told to expect 16 bytes more
+ *           than 16384 elements and at most 1.6 MB) or stages short rows of a
+ *           dense matrix in shared memory, every CTA's barrier for the bulk
+ *           copies of its first row (or tile) is told to expect 16 bytes more
  *           than are copied. The wait gives up after `timeout_ns` (0: 2 s);
  *           from then on each CTA waits and copies no more but still meets
- *           its cluster's barriers, so the launch ends. os_check_device_error
+ *           its barriers, so the launch ends. os_check_device_error
  *           then returns OS_ERR_TIMEOUT with code 2 | (1 << 8). The outputs of
  *           that call are undefined; other paths ignore the hook. `step` is
  *           unused.
