@@ -537,7 +537,8 @@ bool cluster_rows(int kind, const void* x, void* y, float* m, float* l, int64_t 
                   const RowsFault& fault, cudaStream_t stream);
 
 // softmax_flat.cu: short rows (at most 512 bytes, or 1 KB off the 16-byte
-// grid) of a matrix whose x rows lie back to back, tiles of whole rows staged
+// grid; fp32 rows on the grid only where the grouped kernel would leave lanes
+// idle) of a matrix whose x rows lie back to back, tiles of whole rows staged
 // in shared memory; x and y at any offset from the grid, y at any leading
 // dimension.
 bool flat_rows(int kind, const void* x, void* y, float* m, float* l, int64_t rows, int64_t cols,

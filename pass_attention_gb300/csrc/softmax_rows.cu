@@ -438,7 +438,9 @@ void launch_stream(Kernel kernel, const T* x, T* y, float* m, float* l, int64_t 
 
 // The dispatch. Rows of a matrix whose x rows lie back to back are staged
 // in shared memory by tiles (y at any layout) when they are at most 512 bytes
-// long, or at most 1 KB and off the 16-byte grid. Otherwise, rows
+// long, or at most 1 KB and off the 16-byte grid (fp32 rows on the grid only
+// when they would leave a fifth or more of the grouped kernel's lanes idle).
+// Otherwise, rows
 // whose x and y are not in step on the 16-byte grid are streamed. Aligned fp32
 // rows of 2049..16384 elements take a CTA each with the row in registers (the
 // kernel the headline workload runs); other rows of up to 2048 fp32 (16384
