@@ -34,14 +34,11 @@ def rows_for(cols):
     return max(3, min(150001, 3_000_000 // cols))
 
 
-def dense_at(rows, cols, dtype, offset, seed, fill=None):
+def dense_at(rows, cols, dtype, offset, seed):
     """A [rows, cols] view with leading dimension cols, `offset` elements into
-    its buffer (moves the base off the 16-byte grid)."""
+    its buffer (moves the base off the 16-byte grid), and the buffer."""
     n = rows * cols + offset + 7
-    if fill is None:
-        buf = workloads.logits(1, n, 10.0, seed, device="cuda").to(dtype)[0]
-    else:
-        buf = torch.full((n,), fill, dtype=dtype, device="cuda")
+    buf = workloads.logits(1, n, 10.0, seed, device="cuda").to(dtype)[0]
     return buf[offset:offset + rows * cols].view(rows, cols), buf
 
 
