@@ -149,3 +149,36 @@ def test_binding_refuses_cpu_tensors(lib):
         oss.softmax_rows(torch.zeros(2, 4))
     with pytest.raises(ValueError):
         oss.attention_fwd(*(torch.zeros(1, 1, 4, 128, dtype=torch.bfloat16) for _ in range(3)))
+
+
+def test_every_device_call_refuses_host_tensors(lib):
+    # the binding has no CPU path: host tensors are refused before any call
+    # into the library, for every entry point that takes device tensors
+    import torch
+    bf16 = torch.bfloat16
+    x = torch.zeros(4, 64)
+    q = torch.zeros(1, 2, 64, 128, dtype=bf16)
+    qd = torch.zeros(1, 2, 128, dtype=bf16)
+    kd = torch.zeros(1, 2, 32, 128, dtype=bf16)
+    pm = torch.zeros(1, 2, 64, 2)
+    po = torch.zeros(1, 2, 64, 2, 128)
+    calls = [
+        lambda: oss.softmax_rows(x),
+        lambda: oss.softmax_rows_16bit(x.to(bf16)),
+        lambda: oss.softmax_rows_16bit(x.to(torch.float16)),
+        lambda: oss.softmax_rows_multipass(x, 2),
+        lambda: oss.softmax_rows_multipass(x, 3),
+        lambda: oss.attention_fwd(q, q, q),
+        lambda: oss.attention_fwd(q, q, q, causal=True),
+        lambda: oss.attention_fwd_partial(q, q, q, pm, pm, po, 0),
+        lambda: oss.attention_decode_splitkv(qd, kd, kd, torch.ones(1, dtype=torch.int32), 4),
+        lambda: oss.merge_partials(pm, pm, po),
+        lambda: oss.merge_partials(pm, pm, po, finalize=False),
+    ]
+    for i, call in enumerate(calls):
+        with pytest.raises((ValueError, TypeError)):
+            call()
+            pytest.fail(f"call {i} accepted host tensors")
+    # a wrong element type is refused as well
+    with pytest.raises(TypeError):
+        oss.softmax_rows_16bit(x)
