@@ -205,6 +205,27 @@ def device_index_for_smi(local_rank):
 Timing = collections.namedtuple("Timing", "total_ms mean_ms median_ms t0 t1")
 
 
+def headline_config(w):
+    """The headline's ``config`` dict, shared by both arms so that their lines
+    name the same workload in the same words."""
+    return {"workload": f"{w.name} {w.rows}x{w.cols} fp32 N(0,1)*{w.mult:g}, scale {w.scale:g}",
+            "rows": w.rows, "cols": w.cols, "per_rank": "one full matrix per rank",
+            "l2": "inputs larger than L2 (1 GiB per step), no flush"}
+
+
+def max_over_ranks(values, dist=None, device="cpu"):
+    """Element-wise maximum of per-rank timings over all ranks (the slowest
+    rank decides a step's time). ``dist`` is torch.distributed or None for a
+    single process; ``device`` is where the collective's tensor lives (cuda
+    for NCCL, cpu for gloo)."""
+    values = [float(v) for v in values]
+    if dist is None:
+        return values
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
 def time_steps(fn, steps, warmup, stream, barrier):
     """W untimed calls, then K timed calls with per-step events. Returns a
     Timing: the K-step total, the mean and median step (ms), and the wall
@@ -543,8 +564,7 @@ def run_reference(args, rank):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": {"workload": f"{w.name} {w.rows}x{w.cols} fp32 N(0,1)*{w.mult:g}",
-                                        "rows": w.rows, "cols": w.cols},
+        "data": "synthetic", "config": headline_config(w),
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -605,10 +625,7 @@ def main():
     total_ms = sm["total_ms"]
     step_ms = sm["step_ms"]
     e2e_ms = sm["e2e_ms"]
-    if dist:
-        t = torch.tensor([total_ms, step_ms, e2e_ms], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms, step_ms, e2e_ms = t.tolist()
+    total_ms, step_ms, e2e_ms = max_over_ranks([total_ms, step_ms, e2e_ms], dist, "cuda")
     n = world
     w = sm["workload"]
     value = sm["nbytes"] * args.steps * n / (total_ms / 1e3) / 1e9
@@ -723,9 +740,7 @@ def main():
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
         "ms_per_step_median": sm["median_ms"], "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": f"{w.name} {w.rows}x{w.cols} fp32 N(0,1)*{w.mult:g}, scale {w.scale:g}",
-                   "rows": w.rows, "cols": w.cols, "per_rank": "one full matrix per rank",
-                   "l2": "inputs larger than L2 (1 GiB per step), no flush"},
+        "config": headline_config(w),
         "clocks": clocks,
         "e2e": {"value": sm["nbytes"] * n / (e2e_ms / 1e3) / 1e9, "unit": "GB/s",
                 "h2d_bytes_per_step": sm["h2d"], "d2h_bytes_per_step": sm["d2h"],

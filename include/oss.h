@@ -284,6 +284,11 @@ OSS_API os_status os_merge_partials(const float* part_m, const float* part_l, co
  * OS_ERR_TIMEOUT when the word was set, OS_ERR_CUDA when a CUDA call failed,
  * OS_OK otherwise.
  * `code` may be NULL.
+ * The word keeps the FIRST error written since it was last cleared. Call
+ * this after any launch that may have failed, before the next launch: while
+ * an old error sits in the word, a new failing attention launch cannot
+ * publish its own tag there, so its other CTAs no longer stop early and each
+ * waits out its own time limit (the launch still ends; it only ends later).
  */
 OSS_API os_status os_check_device_error(void* stream, int32_t* code);
 

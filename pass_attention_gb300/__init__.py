@@ -118,9 +118,14 @@ def _check(status: int, where: str) -> None:
         raise OssError(status, where)
 
 
-def _stream_ptr(stream) -> int:
-    s = torch.cuda.current_stream() if stream is None else stream
-    return s.cuda_stream
+def _stream_ptr(stream, device: torch.device) -> int:
+    """The CUDA stream to enqueue on: ``stream``, else the current stream of
+    the inputs' device. A stream of another device is refused."""
+    if stream is None:
+        return torch.cuda.current_stream(device).cuda_stream
+    if stream.device != device:
+        raise ValueError(f"stream is on {stream.device}, the tensors on {device}")
+    return stream.cuda_stream
 
 
 def _ptr(t: Optional[torch.Tensor]):
@@ -143,6 +148,32 @@ def _dense(t: torch.Tensor, name: str) -> None:
         raise ValueError(f"{name} must be contiguous")
 
 
+def _same_device(device: torch.device, **tensors) -> None:
+    for name, t in tensors.items():
+        if t is not None and t.device != device:
+            raise ValueError(f"{name} is on {t.device}, the inputs on {device}")
+
+
+def _out(t, name: str, dtype: torch.dtype, shape, device: torch.device) -> torch.Tensor:
+    """A caller-supplied output: a dense CUDA tensor of exactly this dtype and
+    shape on the inputs' device (the kernels write every element of it and
+    nothing around it, so a short, strided, host or foreign-device buffer is
+    refused before the library is called)."""
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (liboss has no CPU path)")
+    if t.device != device:
+        raise ValueError(f"{name} is on {t.device}, the inputs on {device}")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
 # ---------------------------------------------------------------------------
 # os_softmax_rows
 # ---------------------------------------------------------------------------
@@ -158,20 +189,21 @@ def softmax_rows(x: torch.Tensor, scale: float = 1.0, y: Optional[torch.Tensor] 
     if x.stride(1) != 1:
         raise ValueError("x must have unit column stride")
     rows, cols = x.shape
+    dev = x.device
     if y is None:
-        y = torch.empty((rows, cols), dtype=torch.float32, device=x.device)
+        y = torch.empty((rows, cols), dtype=torch.float32, device=dev)
     _need(y, "y", torch.float32, 2)
+    _same_device(dev, y=y)
     if y.stride(1) != 1 or tuple(y.shape) != (rows, cols):
         raise ValueError("y must be [rows, cols] with unit column stride")
-    if m is None:
-        m = torch.empty(rows, dtype=torch.float32, device=x.device)
-    if l is None:
-        l = torch.empty(rows, dtype=torch.float32, device=x.device)
-    _need(m, "m", torch.float32, 1)
-    _need(l, "l", torch.float32, 1)
-    st = load().os_softmax_rows(x.data_ptr(), y.data_ptr(), m.data_ptr(), l.data_ptr(), rows,
-                                cols, x.stride(0), y.stride(0), float(scale),
-                                _stream_ptr(stream))
+    m = _out(torch.empty(rows, dtype=torch.float32, device=dev) if m is None else m,
+             "m", torch.float32, (rows,), dev)
+    l = _out(torch.empty(rows, dtype=torch.float32, device=dev) if l is None else l,
+             "l", torch.float32, (rows,), dev)
+    with torch.cuda.device(dev):
+        st = load().os_softmax_rows(x.data_ptr(), y.data_ptr(), m.data_ptr(), l.data_ptr(), rows,
+                                    cols, x.stride(0), y.stride(0), float(scale),
+                                    _stream_ptr(stream, dev))
     _check(st, "os_softmax_rows")
     return y, m, l
 
@@ -191,20 +223,21 @@ def softmax_rows_16bit(x: torch.Tensor, scale: float = 1.0, y: Optional[torch.Te
     if x.stride(1) != 1:
         raise ValueError("x must have unit column stride")
     rows, cols = x.shape
+    dev = x.device
     if y is None:
-        y = torch.empty((rows, cols), dtype=x.dtype, device=x.device)
+        y = torch.empty((rows, cols), dtype=x.dtype, device=dev)
     _need(y, "y", x.dtype, 2)
+    _same_device(dev, y=y)
     if y.stride(1) != 1 or tuple(y.shape) != (rows, cols):
         raise ValueError("y must be [rows, cols] with unit column stride")
-    if m is None:
-        m = torch.empty(rows, dtype=torch.float32, device=x.device)
-    if l is None:
-        l = torch.empty(rows, dtype=torch.float32, device=x.device)
-    _need(m, "m", torch.float32, 1)
-    _need(l, "l", torch.float32, 1)
-    st = load().os_softmax_rows_16bit(x.data_ptr(), y.data_ptr(), m.data_ptr(), l.data_ptr(),
-                                      rows, cols, x.stride(0), y.stride(0), float(scale),
-                                      _DTYPE_CODES[x.dtype], _stream_ptr(stream))
+    m = _out(torch.empty(rows, dtype=torch.float32, device=dev) if m is None else m,
+             "m", torch.float32, (rows,), dev)
+    l = _out(torch.empty(rows, dtype=torch.float32, device=dev) if l is None else l,
+             "l", torch.float32, (rows,), dev)
+    with torch.cuda.device(dev):
+        st = load().os_softmax_rows_16bit(x.data_ptr(), y.data_ptr(), m.data_ptr(), l.data_ptr(),
+                                          rows, cols, x.stride(0), y.stride(0), float(scale),
+                                          _DTYPE_CODES[x.dtype], _stream_ptr(stream, dev))
     _check(st, "os_softmax_rows_16bit")
     return y, m, l
 
@@ -218,18 +251,21 @@ def softmax_rows_multipass(x: torch.Tensor, passes: int, scale: float = 1.0,
     if x.stride(1) != 1:
         raise ValueError("x must have unit column stride")
     rows, cols = x.shape
+    dev = x.device
     if y is None:
-        y = torch.empty((rows, cols), dtype=torch.float32, device=x.device)
-    if m is None:
-        m = torch.empty(rows, dtype=torch.float32, device=x.device)
-    if l is None:
-        l = torch.empty(rows, dtype=torch.float32, device=x.device)
+        y = torch.empty((rows, cols), dtype=torch.float32, device=dev)
     _need(y, "y", torch.float32, 2)
-    _need(m, "m", torch.float32, 1)
-    _need(l, "l", torch.float32, 1)
-    st = load().os_softmax_rows_multipass(x.data_ptr(), y.data_ptr(), m.data_ptr(), l.data_ptr(),
-                                          rows, cols, x.stride(0), y.stride(0), float(scale),
-                                          int(passes), _stream_ptr(stream))
+    _same_device(dev, y=y)
+    if y.stride(1) != 1 or tuple(y.shape) != (rows, cols):
+        raise ValueError("y must be [rows, cols] with unit column stride")
+    m = _out(torch.empty(rows, dtype=torch.float32, device=dev) if m is None else m,
+             "m", torch.float32, (rows,), dev)
+    l = _out(torch.empty(rows, dtype=torch.float32, device=dev) if l is None else l,
+             "l", torch.float32, (rows,), dev)
+    with torch.cuda.device(dev):
+        st = load().os_softmax_rows_multipass(x.data_ptr(), y.data_ptr(), m.data_ptr(),
+                                              l.data_ptr(), rows, cols, x.stride(0), y.stride(0),
+                                              float(scale), int(passes), _stream_ptr(stream, dev))
     _check(st, "os_softmax_rows_multipass")
     return y, m, l
 
@@ -305,17 +341,17 @@ def attention_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
     Sk = k.shape[2]
     if tuple(k.shape) != (B, H, Sk, D) or tuple(v.shape) != (B, H, Sk, D):
         raise ValueError("k and v must be [B, H, Sk, D] matching q")
+    dev = q.device
+    _same_device(dev, k=k, v=v)
     if scale is None:
         scale = 1.0 / math.sqrt(D)
-    if o is None:
-        o = torch.empty_like(q)
-    _need(o, "o", torch.bfloat16, 4)
-    _dense(o, "o")
-    if lse is None:
-        lse = torch.empty((B, H, Sq), dtype=torch.float32, device=q.device)
-    st = load().os_attention_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
-                                 lse.data_ptr(), B, H, Sq, Sk, D, float(scale), int(bool(causal)),
-                                 _stream_ptr(stream))
+    o = _out(torch.empty_like(q) if o is None else o, "o", torch.bfloat16, q.shape, dev)
+    lse = _out(torch.empty((B, H, Sq), dtype=torch.float32, device=dev) if lse is None else lse,
+               "lse", torch.float32, (B, H, Sq), dev)
+    with torch.cuda.device(dev):
+        st = load().os_attention_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                     lse.data_ptr(), B, H, Sq, Sk, D, float(scale),
+                                     int(bool(causal)), _stream_ptr(stream, dev))
     _check(st, "os_attention_fwd")
     return o, lse
 
@@ -336,21 +372,23 @@ def attention_fwd_partial(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
     Sk = k.shape[2]
     if tuple(k.shape) != (B, H, Sk, D) or tuple(v.shape) != (B, H, Sk, D):
         raise ValueError("k and v must be [B, H, Sk, D] matching q")
+    dev = q.device
+    _same_device(dev, k=k, v=v)
     _need(part_m, "part_m", torch.float32, 4)
-    _need(part_l, "part_l", torch.float32, 4)
-    _need(part_o, "part_o", torch.float32, 5)
-    for t, n in ((part_m, "part_m"), (part_l, "part_l"), (part_o, "part_o")):
-        _dense(t, n)
     stride = part_m.shape[-1]
-    if (tuple(part_m.shape) != (B, H, Sq, stride) or tuple(part_l.shape) != (B, H, Sq, stride)
-            or tuple(part_o.shape) != (B, H, Sq, stride, D)):
-        raise ValueError("partials must be [B, H, Sq, S] and [B, H, Sq, S, D]")
+    _out(part_m, "part_m", torch.float32, (B, H, Sq, stride), dev)
+    _out(part_l, "part_l", torch.float32, (B, H, Sq, stride), dev)
+    _out(part_o, "part_o", torch.float32, (B, H, Sq, stride, D), dev)
+    if not 0 <= int(index) < stride:
+        raise ValueError(f"index {index} outside the {stride} partial slots")
     if scale is None:
         scale = 1.0 / math.sqrt(D)
-    st = load().os_attention_fwd_partial(q.data_ptr(), k.data_ptr(), v.data_ptr(), B, H, Sq, Sk, D,
-                                         float(scale), int(bool(causal)), part_m.data_ptr(),
-                                         part_l.data_ptr(), part_o.data_ptr(), stride, int(index),
-                                         _stream_ptr(stream))
+    with torch.cuda.device(dev):
+        st = load().os_attention_fwd_partial(q.data_ptr(), k.data_ptr(), v.data_ptr(), B, H, Sq,
+                                             Sk, D, float(scale), int(bool(causal)),
+                                             part_m.data_ptr(), part_l.data_ptr(),
+                                             part_o.data_ptr(), stride, int(index),
+                                             _stream_ptr(stream, dev))
     _check(st, "os_attention_fwd_partial")
 
 
@@ -391,20 +429,24 @@ def attention_decode_splitkv(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
         raise ValueError("k and v must be [B, H, Lmax, D] matching q")
     if kv_len.numel() != B:
         raise ValueError("kv_len must have B entries")
+    dev = q.device
+    _same_device(dev, k=k, v=v, kv_len=kv_len)
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     S = int(num_splits)
-    dev = q.device
-    if part_m is None:
-        part_m = torch.empty((B, H, S), dtype=torch.float32, device=dev)
-    if part_l is None:
-        part_l = torch.empty((B, H, S), dtype=torch.float32, device=dev)
-    if part_o is None:
-        part_o = torch.empty((B, H, S, D), dtype=torch.float32, device=dev)
-    st = load().os_attention_decode_splitkv(q.data_ptr(), k.data_ptr(), v.data_ptr(),
-                                            kv_len.data_ptr(), B, H, Lmax, D, S, float(scale),
-                                            part_m.data_ptr(), part_l.data_ptr(),
-                                            part_o.data_ptr(), _stream_ptr(stream))
+    if S < 1:
+        raise ValueError("num_splits must be >= 1")
+    part_m = _out(torch.empty((B, H, S), dtype=torch.float32, device=dev) if part_m is None
+                  else part_m, "part_m", torch.float32, (B, H, S), dev)
+    part_l = _out(torch.empty((B, H, S), dtype=torch.float32, device=dev) if part_l is None
+                  else part_l, "part_l", torch.float32, (B, H, S), dev)
+    part_o = _out(torch.empty((B, H, S, D), dtype=torch.float32, device=dev) if part_o is None
+                  else part_o, "part_o", torch.float32, (B, H, S, D), dev)
+    with torch.cuda.device(dev):
+        st = load().os_attention_decode_splitkv(q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                                kv_len.data_ptr(), B, H, Lmax, D, S, float(scale),
+                                                part_m.data_ptr(), part_l.data_ptr(),
+                                                part_o.data_ptr(), _stream_ptr(stream, dev))
     _check(st, "os_attention_decode_splitkv")
     return part_m, part_l, part_o
 
@@ -428,18 +470,21 @@ def merge_partials(part_m: torch.Tensor, part_l: torch.Tensor, part_o: torch.Ten
     for n in lead:
         groups *= n
     dev = part_m.device
-    if o_out is None:
-        o_out = torch.empty(lead + (D,), dtype=torch.bfloat16 if finalize else torch.float32,
-                            device=dev)
-    if m_out is None:
-        m_out = torch.empty(lead, dtype=torch.float32, device=dev)
-    if l_out is None:
-        l_out = torch.empty(lead, dtype=torch.float32, device=dev)
-    if lse_out is None:
-        lse_out = torch.empty(lead, dtype=torch.float32, device=dev)
-    st = load().os_merge_partials(part_m.data_ptr(), part_l.data_ptr(), part_o.data_ptr(), groups,
-                                  S, D, int(bool(finalize)), o_out.data_ptr(), _ptr(m_out),
-                                  _ptr(l_out), _ptr(lse_out), _stream_ptr(stream))
+    _same_device(dev, part_l=part_l, part_o=part_o)
+    o_dtype = torch.bfloat16 if finalize else torch.float32
+    o_out = _out(torch.empty(lead + (D,), dtype=o_dtype, device=dev) if o_out is None else o_out,
+                 "o_out", o_dtype, lead + (D,), dev)
+    m_out = _out(torch.empty(lead, dtype=torch.float32, device=dev) if m_out is None else m_out,
+                 "m_out", torch.float32, lead, dev)
+    l_out = _out(torch.empty(lead, dtype=torch.float32, device=dev) if l_out is None else l_out,
+                 "l_out", torch.float32, lead, dev)
+    lse_out = _out(torch.empty(lead, dtype=torch.float32, device=dev) if lse_out is None
+                   else lse_out, "lse_out", torch.float32, lead, dev)
+    with torch.cuda.device(dev):
+        st = load().os_merge_partials(part_m.data_ptr(), part_l.data_ptr(), part_o.data_ptr(),
+                                      groups, S, D, int(bool(finalize)), o_out.data_ptr(),
+                                      _ptr(m_out), _ptr(l_out), _ptr(lse_out),
+                                      _stream_ptr(stream, dev))
     _check(st, "os_merge_partials")
     return o_out, m_out, l_out, lse_out
 
@@ -472,6 +517,8 @@ def check_device_error(stream=None) -> int:
     """Synchronise ``stream`` and read/clear the device error word; raises
     OssError(OS_ERR_TIMEOUT) when a kernel gave up on a bounded wait."""
     code = _i32(0)
-    st = load().os_check_device_error(_stream_ptr(stream), ctypes.byref(code))
+    dev = torch.device("cuda", torch.cuda.current_device()) if stream is None else stream.device
+    with torch.cuda.device(dev):
+        st = load().os_check_device_error(_stream_ptr(stream, dev), ctypes.byref(code))
     _check(st, f"os_check_device_error (code {code.value:#x})")
     return int(code.value)

@@ -1,6 +1,7 @@
 // The C ABI of liboss (include/oss.h): host-side validation, then launch.
 // Nothing here synchronises, allocates or prints.
 
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -17,17 +18,22 @@ __device__ unsigned int g_oss_error_word;
 namespace {
 
 constexpr int kMaxDevices = 64;
-unsigned int* g_err_ptr[kMaxDevices];  // device address of g_oss_error_word, per device
+// Device address of g_oss_error_word, per device, filled on first use. Host
+// threads may race to fill a slot; they store the same address, and the
+// atomic makes that race well defined.
+std::atomic<unsigned int*> g_err_ptr[kMaxDevices];
 
 unsigned int* error_word() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-  if (!g_err_ptr[dev]) {
+  unsigned int* cached = g_err_ptr[dev].load(std::memory_order_acquire);
+  if (!cached) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_oss_error_word) != cudaSuccess) return nullptr;
-    g_err_ptr[dev] = static_cast<unsigned int*>(p);
+    cached = static_cast<unsigned int*>(p);
+    g_err_ptr[dev].store(cached, std::memory_order_release);
   }
-  return g_err_ptr[dev];
+  return cached;
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -143,6 +149,7 @@ os_status os_attention_fwd_partial(const os_bf16* q, const os_bf16* k, const os_
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(part_o)) return OS_ERR_MISALIGNED;
   if (D != 128) return OS_ERR_UNSUPPORTED;
   if (causal && Sq != Sk) return OS_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(B) * H > 65535 * 64) return OS_ERR_UNSUPPORTED;
   unsigned int* err = error_word();
   if (!err) return OS_ERR_CUDA;
   const oss::AttnFault fault = t_fault;

@@ -182,3 +182,21 @@ def test_every_device_call_refuses_host_tensors(lib):
     # a wrong element type is refused as well
     with pytest.raises(TypeError):
         oss.softmax_rows_16bit(x)
+
+
+def test_binding_refuses_host_outputs(lib):
+    # the output check itself (device tensors are not available here): a
+    # host tensor, a wrong shape or type is refused before any library call
+    import torch
+    dev = torch.device("cuda", 0)
+    with pytest.raises(ValueError):
+        oss._out(torch.zeros(3), "m", torch.float32, (3,), dev)
+    with pytest.raises(TypeError):
+        oss._out(None, "m", torch.float32, (3,), dev)
+
+
+def test_partial_rejects_too_many_heads(lib):
+    f = lib.os_attention_fwd_partial
+    # B * H beyond the kernel's grid bound, as os_attention_fwd
+    assert f(A, A, A, 65535, 65, 64, 64, 128, 0.1, 0, A, A, A, 1, 0, None) == UNSUPPORTED
+    assert lib.os_attention_fwd(A, A, A, A, None, 65535, 65, 64, 64, 128, 0.1, 0, None) == UNSUPPORTED

@@ -10,7 +10,8 @@ import torch
 import oracle
 import pass_attention_gb300 as oss
 from pass_attention_gb300 import workloads
-from parity import check_attn
+from parity import (check_attn, check_lse_tight, check_o_tight, lse_bar, o_bar, report,
+                    score_error_bound)
 
 pytestmark = pytest.mark.gpu
 
@@ -29,22 +30,51 @@ def run(B, H, Sq, Sk, causal, seed, mult=1.0):
     return q, k, v, o, lse, scale
 
 
-def check_all_rows(q, k, v, o, lse, scale, causal, what):
+def check_all_rows(q, k, v, o, lse, scale, causal, what, tight=True):
+    """Every row against the oracle: the spec bar, and (tight) the
+    secondary bars of tests/parity.py derived from the kernel's arithmetic."""
     qh, kh, vh = f64(q), f64(k), f64(v)
     B, H = q.shape[:2]
+    Sk = k.shape[2]
 
     def one(bh):
         b, h = divmod(bh, H)
-        O, L = oracle.attention(qh[b:b + 1, h:h + 1], kh[b:b + 1, h:h + 1], vh[b:b + 1, h:h + 1],
-                                scale, causal)
-        return bh, O[0, 0], L[0, 0]
+        sl = (slice(b, b + 1), slice(h, h + 1))
+        O, L = oracle.attention(qh[sl], kh[sl], vh[sl], scale, causal)
+        A = oracle.attention(qh[sl], kh[sl], np.abs(vh[sl]), scale, causal)[0] if tight else None
+        return bh, O[0, 0], L[0, 0], None if A is None else A[0, 0]
 
     on, ln = f64(o), f64(lse)
+    worst = {"lse": 0.0, "O": 0.0}
     with ThreadPoolExecutor(max_workers=4) as ex:
-        for bh, O, L in ex.map(one, range(B * H)):
+        for bh, O, L, A in ex.map(one, range(B * H)):
             b, h = divmod(bh, H)
             check_attn(on[b, h], O, f"{what} O b{b} h{h}")
             check_attn(ln[b, h], L, f"{what} lse b{b} h{h}")
+            if tight:
+                e_s = score_error_bound(qh[b, h], kh[b, h], scale)
+                worst["lse"] = max(worst["lse"], check_lse_tight(ln[b, h], L, lse_bar(e_s),
+                                                                 f"{what} lse b{b} h{h}"))
+                worst["O"] = max(worst["O"], check_o_tight(on[b, h], O, o_bar(O, A, e_s, Sk),
+                                                           f"{what} b{b} h{h}"))
+    if tight:
+        report(what, **worst)
+
+
+def check_rows(q, k, v, o, lse, scale, causal, rows, what):
+    """Sampled rows (b, h, i) against the oracle, both bars."""
+    qh, kh, vh = f64(q), f64(k), f64(v)
+    O, L = oracle.attention(qh, kh, vh, scale, causal, rows=rows)
+    A, _ = oracle.attention(qh, kh, np.abs(vh), scale, causal, rows=rows)
+    on, ln = f64(o), f64(lse)
+    got_o = np.stack([on[b, h, i] for b, h, i in rows])
+    got_l = np.array([ln[b, h, i] for b, h, i in rows])
+    check_attn(got_o, O, f"{what} O")
+    check_attn(got_l, L, f"{what} lse")
+    e_s = np.array([score_error_bound(qh[b, h, i][None], kh[b, h], scale)[0] for b, h, i in rows])
+    r_l = check_lse_tight(got_l, L, lse_bar(e_s), f"{what} lse")
+    r_o = check_o_tight(got_o, O, o_bar(O, A, e_s, k.shape[2]), what)
+    report(what, lse=r_l, O=r_o)
 
 
 @pytest.mark.parametrize("B,H,Sq,Sk", [
@@ -135,13 +165,7 @@ def test_full_size_attn_causal_sampled_rows():
     n = 4096
     rows = list(zip(rng.integers(0, w.B, n), rng.integers(0, w.H, n), rng.integers(0, w.S, n)))
     rows += [(0, h, i) for h in (0, w.H - 1) for i in (0, 1, 127, 128, 255, 256, w.S - 1)]
-    qh, kh, vh = f64(q), f64(k), f64(v)
-    O, L = oracle.attention(qh, kh, vh, w.scale, True, rows=rows)
-    on, ln = f64(o), f64(lse)
-    got_o = np.stack([on[b, h, i] for b, h, i in rows])
-    got_l = np.array([ln[b, h, i] for b, h, i in rows])
-    check_attn(got_o, O, "attn_causal O")
-    check_attn(got_l, L, "attn_causal lse")
+    check_rows(q, k, v, o, lse, w.scale, True, rows, "attn_causal")
 
 
 def test_causal_beyond_the_schedule_size():
@@ -157,7 +181,4 @@ def test_causal_beyond_the_schedule_size():
     n = 2048
     rows = list(zip(rng.integers(0, B, n), rng.integers(0, H, n), rng.integers(0, S, n)))
     rows += [(b, h, i) for b, h in ((0, 0), (B - 1, H - 1)) for i in (0, 63, 64, 127)]
-    O, L = oracle.attention(f64(q), f64(k), f64(v), scale, True, rows=rows)
-    on, ln = f64(o), f64(lse)
-    check_attn(np.stack([on[b, h, i] for b, h, i in rows]), O, "15200 tiles O")
-    check_attn(np.array([ln[b, h, i] for b, h, i in rows]), L, "15200 tiles lse")
+    check_rows(q, k, v, o, lse, scale, True, rows, "15200 tiles")
