@@ -187,6 +187,40 @@ OSS_API os_status os_attention_fwd(const os_bf16* q, const os_bf16* k, const os_
                            float scale, int causal, void* stream);
 
 /*
+ * Rescale policies of the attention forward: when a tile raises a row's
+ * maximum, the running sum l and the accumulator O are multiplied by
+ * exp(m_old - m_new) (metalworking "Online Softmax", the five-line
+ * recurrence). The same page's "Recognition guide" sets two kernels side by
+ * side that disagree on when to do it: MLX multiplies on every tile,
+ * metal-flash-attention only when the maximum rose. Here O lives in tensor
+ * memory, so each rescale costs a wait for the previous P V and a round trip
+ * of O; the decision is taken per warp of 16 rows. All three policies compute
+ * the same O and lse in exact arithmetic (the reference maximum cancels in
+ * O / l); their rounding differs within the documented tolerance.
+ */
+typedef enum os_rescale_policy {
+  OS_RESCALE_THRESHOLD = 0, /* default: move the reference maximum only when a
+                               row of the warp rose by more than 8 (base 2), so
+                               the weights stay below 2^8; rarely rescales */
+  OS_RESCALE_ON_RISE = 1,   /* metal-flash-attention's guard: whenever a row of
+                               the warp rose at all */
+  OS_RESCALE_ALWAYS = 2     /* MLX's form: on every tile */
+} os_rescale_policy;
+
+/*
+ * os_attention_set_rescale_policy -- choose the rescale policy of the
+ * os_attention_fwd and os_attention_fwd_partial calls the calling host
+ * thread makes from now on (other threads keep theirs; a new thread starts
+ * with OS_RESCALE_THRESHOLD, the fastest measured). Provided to measure the
+ * trade named above; results agree within the attention tolerance.
+ * Errors: OS_ERR_INVALID_ARGUMENT for another value (the setting is kept).
+ */
+OSS_API os_status os_attention_set_rescale_policy(int32_t policy);
+
+/* The calling host thread's current os_rescale_policy. */
+OSS_API int32_t os_attention_rescale_policy(void);
+
+/*
  * os_attention_fwd_partial -- the attention forward over one shard of the
  * keys, written as partial softmax states instead of O / l, so that shards of
  * a long sequence (processed one after another, or on different devices) can

@@ -34,6 +34,9 @@ __all__ = [
     "decode_from_host",
     "check_device_error",
     "debug_inject_fault",
+    "set_rescale_policy",
+    "rescale_policy",
+    "RESCALE_POLICIES",
     "abi_version",
     "EXPORTED_SYMBOLS",
 ]
@@ -71,6 +74,8 @@ _SIGNATURES = {
     "os_merge_partials": (_i32, [_vp, _vp, _vp, _i64, _i32, _i32, ctypes.c_int, _vp, _vp, _vp,
                                  _vp, _vp]),
     "os_check_device_error": (_i32, [_vp, ctypes.POINTER(_i32)]),
+    "os_attention_set_rescale_policy": (_i32, [_i32]),
+    "os_attention_rescale_policy": (_i32, []),
     "os_debug_inject_fault": (_i32, [_i32, _i32, _i64]),
     "os_status_string": (ctypes.c_char_p, [_i32]),
     "os_abi_version": (_i32, []),
@@ -503,6 +508,22 @@ def decode_from_host(q_host, k_host, v_host, kv_len_host, num_splits, scale=None
     out[1].copy_(lse, non_blocking=True)
     torch.cuda.current_stream().synchronize()
     return out
+
+
+RESCALE_POLICIES = {"threshold": 0, "on_rise": 1, "always": 2}
+
+
+def set_rescale_policy(policy) -> None:
+    """Rescale policy of this thread's later attention calls: "threshold"
+    (default), "on_rise" or "always" (or the os_rescale_policy value). See
+    ``os_attention_set_rescale_policy``."""
+    code = RESCALE_POLICIES.get(policy, policy)
+    _check(load().os_attention_set_rescale_policy(int(code)), "os_attention_set_rescale_policy")
+
+
+def rescale_policy() -> str:
+    code = int(load().os_attention_rescale_policy())
+    return {v: k for k, v in RESCALE_POLICIES.items()}[code]
 
 
 def debug_inject_fault(kind: int, step: int = 0, timeout_ns: int = 0) -> None:

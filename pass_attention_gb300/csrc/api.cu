@@ -52,6 +52,9 @@ thread_local oss::AttnFault t_fault;
 // Armed by os_debug_inject_fault (kind 2), consumed by the next
 // os_softmax_rows or os_softmax_rows_16bit on the same host thread.
 thread_local oss::RowsFault t_rows_fault;
+// Set by os_attention_set_rescale_policy; kept for the host thread's later
+// attention calls.
+thread_local int t_rescale_policy = OS_RESCALE_THRESHOLD;
 
 }  // namespace
 
@@ -133,7 +136,7 @@ os_status os_attention_fwd(const os_bf16* q, const os_bf16* k, const os_bf16* v,
   const oss::AttnFault fault = t_fault;
   t_fault = oss::AttnFault();
   return from_cuda(oss::launch_attention_fwd(q, k, v, o, lse, B, H, Sq, Sk, D, scale,
-                                             causal != 0, err, fault, nullptr,
+                                             causal != 0, err, fault, nullptr, t_rescale_policy,
                                              static_cast<cudaStream_t>(stream)));
 }
 
@@ -156,7 +159,7 @@ os_status os_attention_fwd_partial(const os_bf16* q, const os_bf16* k, const os_
   t_fault = oss::AttnFault();
   const oss::AttnPartialOut out{part_m, part_l, part_o, part_stride, part_index};
   return from_cuda(oss::launch_attention_fwd(q, k, v, nullptr, nullptr, B, H, Sq, Sk, D, scale,
-                                             causal != 0, err, fault, &out,
+                                             causal != 0, err, fault, &out, t_rescale_policy,
                                              static_cast<cudaStream_t>(stream)));
 }
 
@@ -187,6 +190,15 @@ os_status os_merge_partials(const float* part_m, const float* part_l, const floa
                                               finalize, o_out, m_out, l_out, lse_out,
                                               static_cast<cudaStream_t>(stream)));
 }
+
+os_status os_attention_set_rescale_policy(int32_t policy) {
+  if (policy != OS_RESCALE_THRESHOLD && policy != OS_RESCALE_ON_RISE && policy != OS_RESCALE_ALWAYS)
+    return OS_ERR_INVALID_ARGUMENT;
+  t_rescale_policy = policy;
+  return OS_OK;
+}
+
+int32_t os_attention_rescale_policy(void) { return t_rescale_policy; }
 
 os_status os_debug_inject_fault(int32_t kind, int32_t step, int64_t timeout_ns) {
   if (kind < 0 || kind > 2 || step < 0 || timeout_ns < 0) return OS_ERR_INVALID_ARGUMENT;

@@ -106,8 +106,21 @@ constexpr uint32_t kTmemCols = 512;
 __device__ __forceinline__ uint32_t col_s(int b) { return 128u * b; }
 constexpr uint32_t kColO = 384;
 
-// The reference maximum of a warp's rows moves only when one of them rises
-// by more than this (base-2 units): weights stay below 2^8 = 256.
+// When the rows' maxima are moved and O rescaled (the policy is a template
+// parameter; the metalworking page, "Recognition guide", sets two real
+// kernels side by side here: MLX multiplies O by the correction on every
+// tile, metal-flash-attention only when the maximum rose). O lives in tensor
+// memory, so a rescale costs the softmax warp a wait for the previous P V and
+// a round trip of its rows of O; the decision is per warp (tensor-memory
+// access is warp-wide):
+//   kRescaleThreshold -- move a warp's reference maxima only when one of its
+//                        rows rose by more than kRescaleSlack (base 2); weights
+//                        stay below 2^kRescaleSlack. The default.
+//   kRescaleOnRise    -- move them whenever one of its rows rose at all.
+//   kRescaleAlways    -- move them (and rescale O) on every tile.
+// Any reference below the true maximum gives the same O / l in exact
+// arithmetic (it cancels), so all three compute the same result.
+enum RescalePolicy : int { kRescaleThreshold = 0, kRescaleOnRise = 1, kRescaleAlways = 2 };
 constexpr float kRescaleSlack = 8.0f;
 
 constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s per wait
@@ -494,7 +507,7 @@ __device__ __forceinline__ int tile_of(int k, const AttnParams& p, const TileSch
   }
 }
 
-template <bool kSched>
+template <bool kSched, int kPolicy>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
                 const __grid_constant__ CUtensorMap tmap_k,
@@ -800,12 +813,17 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
         const float mnew_a = fmaxf(m_a, mtile_a), mnew_b = fmaxf(m_b, mtile_b);
         mt_a = fmaxf(mt_a, mtile_a);
         mt_b = fmaxf(mt_b, mtile_b);
-        // Move the reference maxima only when some row of this warp has risen
-        // by more than kRescaleSlack (base 2). Otherwise keep them: the same
-        // O / l in exact arithmetic (the reference cancels), weights stay
-        // <= 2^kRescaleSlack, and the O round trip is skipped.
-        const bool rescale = __any_sync(0xffffffffu, (mnew_a > m_a + kRescaleSlack) ||
-                                                         (mnew_b > m_b + kRescaleSlack));
+        // Move the reference maxima (and rescale O) as the policy says;
+        // between moves the weights are taken relative to a reference at most
+        // kRescaleSlack below the true maximum (threshold policy).
+        bool rescale;
+        if constexpr (kPolicy == kRescaleAlways)
+          rescale = true;
+        else if constexpr (kPolicy == kRescaleOnRise)
+          rescale = __any_sync(0xffffffffu, (mnew_a > m_a) || (mnew_b > m_b));
+        else
+          rescale = __any_sync(0xffffffffu, (mnew_a > m_a + kRescaleSlack) ||
+                                                (mnew_b > m_b + kRescaleSlack));
         float corr_a = 1.f, corr_b = 1.f;
         if (rescale) {
           corr_a = ex2(m_a - ((mnew_a == neg_inf()) ? 0.f : mnew_a));  // 0 while m = -inf
@@ -1045,6 +1063,21 @@ bool build_schedule(const AttnParams& prm, int G, TileSched<true>* sc) {
   return true;
 }
 
+// Launch of the kernel instance for a rescale policy (grid of `grid` CTAs).
+template <bool kSched>
+void launch_policy(int policy, int grid, cudaStream_t stream, const CUtensorMap& mq,
+                   const CUtensorMap& mk, const CUtensorMap& mv, const AttnParams& prm,
+                   const TileSched<kSched>& sched) {
+  const dim3 g(static_cast<unsigned>(grid));
+  if (policy == kRescaleOnRise)
+    attn_fwd_kernel<kSched, kRescaleOnRise><<<g, kThreads, kSmemBytes, stream>>>(mq, mk, mv, prm, sched);
+  else if (policy == kRescaleAlways)
+    attn_fwd_kernel<kSched, kRescaleAlways><<<g, kThreads, kSmemBytes, stream>>>(mq, mk, mv, prm, sched);
+  else
+    attn_fwd_kernel<kSched, kRescaleThreshold><<<g, kThreads, kSmemBytes, stream>>>(mq, mk, mv, prm,
+                                                                                    sched);
+}
+
 // The last schedule built by this host thread, reused while the shape stays.
 struct SchedCache {
   int bh = -1, n_qblocks = -1, sk = -1, grid = -1;
@@ -1057,7 +1090,9 @@ cudaError_t launch_attention_fwd(const uint16_t* q, const uint16_t* k, const uin
                                  uint16_t* o, float* lse, int B, int H, int Sq, int Sk, int D,
                                  float scale, bool causal, unsigned int* err_word,
                                  const AttnFault& fault, const AttnPartialOut* partial,
-                                 cudaStream_t stream) {
+                                 int rescale_policy, cudaStream_t stream) {
+  if (rescale_policy < kRescaleThreshold || rescale_policy > kRescaleAlways)
+    return cudaErrorInvalidValue;
   if (D != kD) return cudaErrorNotSupported;
   const int BH = B * H;
   CUtensorMap mq, mk, mv;
@@ -1071,12 +1106,17 @@ cudaError_t launch_attention_fwd(const uint16_t* q, const uint16_t* k, const uin
   constexpr int kMaxDevices = 64;
   static std::atomic<bool> smem_set[kMaxDevices];
   if (dev < 0 || dev >= kMaxDevices || !smem_set[dev].load(std::memory_order_acquire)) {
-    e = cudaFuncSetAttribute(attn_fwd_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kSmemBytes);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(attn_fwd_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               kSmemBytes);
-    if (e != cudaSuccess) return e;
+    const void* kernels[] = {
+        reinterpret_cast<const void*>(attn_fwd_kernel<false, kRescaleThreshold>),
+        reinterpret_cast<const void*>(attn_fwd_kernel<true, kRescaleThreshold>),
+        reinterpret_cast<const void*>(attn_fwd_kernel<false, kRescaleOnRise>),
+        reinterpret_cast<const void*>(attn_fwd_kernel<true, kRescaleOnRise>),
+        reinterpret_cast<const void*>(attn_fwd_kernel<false, kRescaleAlways>),
+        reinterpret_cast<const void*>(attn_fwd_kernel<true, kRescaleAlways>)};
+    for (const void* kf : kernels) {
+      e = cudaFuncSetAttribute(kf, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+      if (e != cudaSuccess) return e;
+    }
     if (dev >= 0 && dev < kMaxDevices) smem_set[dev].store(true, std::memory_order_release);
   }
   AttnParams prm;
@@ -1119,19 +1159,16 @@ cudaError_t launch_attention_fwd(const uint16_t* q, const uint16_t* k, const uin
       cache.n_qblocks = prm.n_qblocks;
       cache.sk = Sk;
       cache.grid = G;
-      attn_fwd_kernel<true><<<static_cast<unsigned>(G), kThreads, kSmemBytes, stream>>>(
-          mq, mk, mv, prm, cache.sched);
+      launch_policy<true>(rescale_policy, G, stream, mq, mk, mv, prm, cache.sched);
       return cudaGetLastError();
     }
     cache.bh = -1;  // not schedulable: one CTA per tile
     TileSched<false> none{};
-    attn_fwd_kernel<false><<<static_cast<unsigned>(tiles), kThreads, kSmemBytes, stream>>>(
-        mq, mk, mv, prm, none);
+    launch_policy<false>(rescale_policy, static_cast<int>(tiles), stream, mq, mk, mv, prm, none);
     return cudaGetLastError();
   }
   TileSched<false> none{};
-  attn_fwd_kernel<false><<<static_cast<unsigned>(G), kThreads, kSmemBytes, stream>>>(mq, mk, mv,
-                                                                                     prm, none);
+  launch_policy<false>(rescale_policy, G, stream, mq, mk, mv, prm, none);
   return cudaGetLastError();
 }
 

@@ -68,11 +68,13 @@ struct AttnPartialOut {
 
 // Returns cudaErrorNotSupported for shapes the kernel does not cover. With
 // partial != nullptr the kernel writes partial states instead of o and lse.
+// rescale_policy: an os_rescale_policy value (0 threshold, 1 on rise, 2
+// every tile).
 cudaError_t launch_attention_fwd(const uint16_t* q, const uint16_t* k, const uint16_t* v,
                                  uint16_t* o, float* lse, int B, int H, int Sq, int Sk, int D,
                                  float scale, bool causal, unsigned int* err_word,
                                  const AttnFault& fault, const AttnPartialOut* partial,
-                                 cudaStream_t stream);
+                                 int rescale_policy, cudaStream_t stream);
 
 // log2(e) split into a float and the float nearest to the remainder, so that
 // hi + lo carries about 48 bits of it.

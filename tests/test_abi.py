@@ -200,3 +200,16 @@ def test_partial_rejects_too_many_heads(lib):
     # B * H beyond the kernel's grid bound, as os_attention_fwd
     assert f(A, A, A, 65535, 65, 64, 64, 128, 0.1, 0, A, A, A, 1, 0, None) == UNSUPPORTED
     assert lib.os_attention_fwd(A, A, A, A, None, 65535, 65, 64, 64, 128, 0.1, 0, None) == UNSUPPORTED
+
+
+def test_rescale_policy_selector(lib):
+    f = lib.os_attention_set_rescale_policy
+    assert lib.os_attention_rescale_policy() == 0          # threshold by default
+    for bad in (-1, 3, 100):
+        assert f(bad) == INVALID
+        assert lib.os_attention_rescale_policy() == 0      # a refused value changes nothing
+    for p in (1, 2, 0):
+        assert f(p) == 0 and lib.os_attention_rescale_policy() == p
+    oss.set_rescale_policy("on_rise")
+    assert oss.rescale_policy() == "on_rise"
+    oss.set_rescale_policy("threshold")

@@ -182,3 +182,46 @@ def test_causal_beyond_the_schedule_size():
     rows = list(zip(rng.integers(0, B, n), rng.integers(0, H, n), rng.integers(0, S, n)))
     rows += [(b, h, i) for b, h in ((0, 0), (B - 1, H - 1)) for i in (0, 63, 64, 127)]
     check_rows(q, k, v, o, lse, scale, True, rows, "15200 tiles")
+
+
+@pytest.mark.parametrize("policy", ["threshold", "on_rise", "always"])
+@pytest.mark.parametrize("B,H,Sq,Sk,causal", [(2, 2, 1000, 700, False), (1, 2, 1000, 1000, True),
+                                               (3, 40, 300, 300, False), (2, 3, 1, 129, False)])
+def test_rescale_policies(policy, B, H, Sq, Sk, causal):
+    # the three rescale policies compute the same result within the bars
+    oss.set_rescale_policy(policy)
+    try:
+        assert oss.rescale_policy() == policy
+        q, k, v, o, lse, scale = run(B, H, Sq, Sk, causal, seed=Sq + Sk + B)
+    finally:
+        oss.set_rescale_policy("threshold")
+    check_all_rows(q, k, v, o, lse, scale, causal, f"{policy} {B}x{H}x{Sq}x{Sk}")
+
+
+@pytest.mark.parametrize("policy", ["on_rise", "always"])
+@pytest.mark.parametrize("causal", [False, True])
+def test_rescale_policies_rising_max(policy, causal):
+    # every tile raises every row's maximum: all policies rescale O each tile
+    B, H, S = 1, 2, 1536
+    q, k, v = workloads.qkv(B, H, S, S, 128, seed=12, device="cuda")
+    grow = (1.0 + torch.arange(S, device="cuda", dtype=torch.float32) / 24.0)[None, None, :, None]
+    k = (k.float() * grow).to(torch.bfloat16)
+    scale = 1.0 / math.sqrt(128)
+    oss.set_rescale_policy(policy)
+    try:
+        o, lse = oss.attention_fwd(q, k, v, scale, causal)
+        assert oss.check_device_error() == 0
+    finally:
+        oss.set_rescale_policy("threshold")
+    check_all_rows(q, k, v, o, lse, scale, causal, f"{policy} rising max")
+
+
+def test_rescale_policy_is_per_thread():
+    import threading
+    oss.set_rescale_policy("always")
+    seen = []
+    t = threading.Thread(target=lambda: seen.append(oss.rescale_policy()))
+    t.start()
+    t.join()
+    oss.set_rescale_policy("threshold")
+    assert seen == ["threshold"]
