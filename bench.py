@@ -370,6 +370,30 @@ def bench_softmax16(args, ctx):
     return tm, nbytes
 
 
+def bench_softmax_long(args, ctx):
+    """Rows beyond a cluster's shared memory: 64 x 2^22 fp32 (16 MB rows,
+    1 GiB) and the same matrix in bf16, through os_softmax_rows_ws /
+    os_softmax_rows_16bit_ws (the binding supplies the workspace). Returns
+    {name: (Timing, algorithmic bytes)}."""
+    import pass_attention_gb300 as oss
+    out = {}
+    stream = torch.cuda.current_stream()
+    rows, cols = 64, 1 << 22
+    for name, dtype in (("fp32", torch.float32), ("bf16", torch.bfloat16)):
+        x = workloads.logits(rows, cols, 10.0, 11 + ctx["rank"], device="cuda").to(dtype)
+        y = torch.empty_like(x)
+        m = torch.empty(rows, device="cuda")
+        l = torch.empty(rows, device="cuda")
+        if dtype == torch.float32:
+            fn = lambda: oss.softmax_rows(x, 1.0, y=y, m=m, l=l, stream=stream)
+        else:
+            fn = lambda: oss.softmax_rows_16bit(x, 1.0, y=y, m=m, l=l, stream=stream)
+        tm = time_steps(fn, max(3, min(args.steps, 20)), 3, stream, ctx["barrier"])
+        out[name] = (tm, rows * cols * 2 * x.element_size() + rows * 8)
+        del x, y
+    return out
+
+
 def bench_softmax_lengths(args, ctx):
     """os_softmax_rows / os_softmax_rows_16bit over row lengths from 128 to
     131072 at 2^28 elements per matrix (1 GiB fp32, 512 MiB 16-bit: larger
@@ -684,6 +708,22 @@ def main():
             }
         except Exception as e:
             extra["softmax_row_lengths"] = {"unavailable": f"{type(e).__name__}: {e}"}
+        try:
+            for name, (tm, nb) in bench_softmax_long(args, ctx).items():
+                gbs = nb / (tm.mean_ms / 1e3) / 1e9
+                extra[f"softmax_64x4m_{name}"] = {
+                    "value": gbs, "unit": "GB/s", "ms_per_step": tm.mean_ms,
+                    "ms_per_step_median": tm.median_ms,
+                    "workload": f"64 x 2^22 {name} rows (16 MB fp32 / 8 MB bf16 a row), N(0,1)*10, "
+                                "scale 1, with a workspace",
+                    "roofline": {"bound": "hbm", "kernel": "softmax_rows_wide_kernel (cooperative)",
+                                 "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                                 "frac": gbs / pk["hbm_gbs"], "traffic": traffic_for(f"softmax_64x4m_{name}"),
+                                 "peak_kind": f"{pk_kind} HBM copy", "nominal_peak": NOMINAL["hbm_gbs"],
+                                 "frac_nominal": gbs / NOMINAL["hbm_gbs"]},
+                    "window": (tm.t0, tm.t1)}
+        except Exception as e:
+            extra["softmax_64x4m"] = {"unavailable": f"{type(e).__name__}: {e}"}
         for aw in (workloads.ATTN_4K, workloads.ATTN_CAUSAL):
             try:
                 tm, flops, cpu_a = bench_attention(args, ctx, aw)

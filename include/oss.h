@@ -96,12 +96,49 @@ typedef enum os_status {
  * leading dimension; the 16-byte granules holding x's first and last
  * elements may be read (never written) whole. Other rows whose x and y
  * offsets differ, and rows longer than 1.6 MB, are streamed twice (two reads,
- * one write).
+ * one write; os_softmax_rows_ws reads them once).
  * Errors: OS_ERR_INVALID_ARGUMENT, OS_ERR_MISALIGNED, OS_ERR_CUDA.
  */
 OSS_API os_status os_softmax_rows(const float* x, float* y, float* m, float* l,
                           int64_t rows, int64_t cols, int64_t ld_x, int64_t ld_y,
                           float scale, void* stream);
+
+/*
+ * os_softmax_rows_workspace_bytes -- bytes of workspace os_softmax_rows_ws /
+ * os_softmax_rows_16bit_ws use for rows of `cols` elements of type `dtype`
+ * (0 = fp32, OS_DTYPE_BF16, OS_DTYPE_F16) on the current device: a few tens
+ * of KB for rows longer than the 1.6 MB a thread-block cluster holds, 0 for
+ * shorter rows (they never use it); -1 when the device cannot be queried.
+ */
+OSS_API int64_t os_softmax_rows_workspace_bytes(int64_t rows, int64_t cols, int32_t dtype);
+
+/*
+ * os_softmax_rows_ws -- os_softmax_rows with a caller-owned device
+ * workspace. Rows longer than a cluster's shared memory holds (over 1.6 MB)
+ * then take the whole GPU a few rows at a time (as many as fit in L2):
+ * every CTA streams one slice of a row once, forming the slice's (max, sum)
+ * state of the online normaliser; the slices' states meet in the workspace
+ * at a grid-wide barrier of a cooperative launch and are merged in slice
+ * order with the pairwise identity (curionode "The Online Softmax.", "One
+ * pass, exactly"); each CTA then reads its slice again, from L2, to write y.
+ * HBM sees one read and one write per element; without a workspace such rows
+ * are read twice from HBM. Results are those of os_softmax_rows, within its
+ * tolerance; shorter rows ignore the workspace.
+ *
+ *   workspace        device memory of at least os_softmax_rows_workspace_bytes
+ *                    bytes, 16-byte aligned (contents need no initialising:
+ *                    the call zeroes what it needs, with an asynchronous
+ *                    memset on `stream`), or NULL with workspace_bytes 0.
+ *   workspace_bytes  its size; too small: the rows are streamed twice.
+ * Calls that may run at the same time (other streams) need workspaces of
+ * their own. Other arguments and errors as os_softmax_rows; a grid barrier
+ * that waits longer than 2 s gives up and os_check_device_error then reports
+ * OS_ERR_TIMEOUT with code 2 | (2 << 8).
+ */
+OSS_API os_status os_softmax_rows_ws(const float* x, float* y, float* m, float* l,
+                                     int64_t rows, int64_t cols, int64_t ld_x, int64_t ld_y,
+                                     float scale, void* workspace, int64_t workspace_bytes,
+                                     void* stream);
 
 /* Element type of a 16-bit row (os_softmax_rows_16bit). */
 typedef enum os_dtype {
@@ -138,6 +175,15 @@ typedef enum os_dtype {
 OSS_API os_status os_softmax_rows_16bit(const void* x, void* y, float* m, float* l,
                                         int64_t rows, int64_t cols, int64_t ld_x, int64_t ld_y,
                                         float scale, int32_t dtype, void* stream);
+
+/*
+ * os_softmax_rows_16bit_ws -- os_softmax_rows_16bit with a workspace, as
+ * os_softmax_rows_ws (the same single read from HBM for rows over 1.6 MB).
+ */
+OSS_API os_status os_softmax_rows_16bit_ws(const void* x, void* y, float* m, float* l,
+                                           int64_t rows, int64_t cols, int64_t ld_x,
+                                           int64_t ld_y, float scale, int32_t dtype,
+                                           void* workspace, int64_t workspace_bytes, void* stream);
 
 /*
  * os_softmax_rows_multipass -- the same outputs as os_softmax_rows, computed
@@ -185,6 +231,43 @@ OSS_API os_status os_attention_fwd(const os_bf16* q, const os_bf16* k, const os_
                            os_bf16* o, float* lse,
                            int32_t B, int32_t H, int32_t Sq, int32_t Sk, int32_t D,
                            float scale, int causal, void* stream);
+
+/*
+ * os_attention_fwd_workspace_bytes -- bytes of workspace os_attention_fwd_ws
+ * uses for this shape on the current device; 0 when it uses none (causal
+ * launches, and launches whose query tiles fill whole rounds of the GPU's
+ * SMs), -1 when the device cannot be queried.
+ */
+OSS_API int64_t os_attention_fwd_workspace_bytes(int32_t B, int32_t H, int32_t Sq, int32_t Sk,
+                                                 int32_t D, int causal);
+
+/*
+ * os_attention_fwd_ws -- os_attention_fwd with a caller-owned device
+ * workspace, which lets a non-causal launch keep every SM busy to the end:
+ * the kernel walks the 128-row query tiles in rounds of one tile per SM;
+ * when the last round would leave SMs idle, its tiles are cut along the keys
+ * into 2..8 parts, one per SM, each part's partial state (m, l, O) goes to
+ * the workspace, and the last part of a tile to finish combines them with
+ * the pairwise merge identity of the curionode page ("One pass, exactly"),
+ * always in part order, so results do not depend on which SM finishes last.
+ * The outputs are those of os_attention_fwd, within its tolerance.
+ *
+ *   workspace        device memory of at least os_attention_fwd_workspace_bytes
+ *                    bytes, 16-byte aligned, or NULL with workspace_bytes 0
+ *                    (then the call is os_attention_fwd). It must be all
+ *                    zeros the first time it is used (fill it with zeros
+ *                    once): it holds the per-tile counters of finished parts,
+ *                    which every call that completes leaves at zero again.
+ *                    After a call that reported OS_ERR_TIMEOUT, zero it again
+ *                    before reuse.
+ *   workspace_bytes  its size; smaller than required: OS_ERR_INVALID_ARGUMENT.
+ * Calls that may run at the same time (other streams) need workspaces of
+ * their own. Other arguments and errors as os_attention_fwd.
+ */
+OSS_API os_status os_attention_fwd_ws(const os_bf16* q, const os_bf16* k, const os_bf16* v,
+                                      os_bf16* o, float* lse, int32_t B, int32_t H, int32_t Sq,
+                                      int32_t Sk, int32_t D, float scale, int causal,
+                                      void* workspace, int64_t workspace_bytes, void* stream);
 
 /*
  * Rescale policies of the attention forward: when a tile raises a row's

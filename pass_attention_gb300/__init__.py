@@ -26,9 +26,11 @@ __all__ = [
     "softmax_rows_from_host",
     "softmax_rows_multipass",
     "softmax_rows_16bit",
+    "softmax_rows_workspace_bytes",
     "attention_fwd",
     "attention_fwd_from_host",
     "attention_fwd_partial",
+    "attention_fwd_workspace_bytes",
     "attention_decode_splitkv",
     "merge_partials",
     "decode_from_host",
@@ -63,10 +65,17 @@ _f32 = ctypes.c_float
 _SIGNATURES = {
     "os_softmax_rows": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _f32, _vp]),
     "os_softmax_rows_16bit": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _f32, _i32, _vp]),
+    "os_softmax_rows_ws": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _f32, _vp, _i64, _vp]),
+    "os_softmax_rows_16bit_ws": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _f32, _i32, _vp,
+                                        _i64, _vp]),
+    "os_softmax_rows_workspace_bytes": (_i64, [_i64, _i64, _i32]),
     "os_softmax_rows_multipass": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _f32, _i32,
                                          _vp]),
     "os_attention_fwd": (_i32, [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _f32,
                                 ctypes.c_int, _vp]),
+    "os_attention_fwd_ws": (_i32, [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _f32,
+                                   ctypes.c_int, _vp, _i64, _vp]),
+    "os_attention_fwd_workspace_bytes": (_i64, [_i32, _i32, _i32, _i32, _i32, ctypes.c_int]),
     "os_attention_fwd_partial": (_i32, [_vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _f32,
                                         ctypes.c_int, _vp, _vp, _vp, _i32, _i32, _vp]),
     "os_attention_decode_splitkv": (_i32, [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32,
@@ -179,9 +188,33 @@ def _out(t, name: str, dtype: torch.dtype, shape, device: torch.device) -> torch
     return t
 
 
+# Workspaces of the *_ws entry points, one per (device, stream, kind): calls
+# on one stream run one after another and may share one; calls on other
+# streams get their own. Each is zero-filled when made, and the calls leave
+# what must start at zero at zero again.
+_WORKSPACES: dict = {}
+
+
+def _workspace(device: torch.device, stream_ptr: int, nbytes: int, kind: str = "attn") -> torch.Tensor:
+    key = (device.index, stream_ptr, kind)
+    ws = _WORKSPACES.get(key)
+    if ws is None or ws.numel() < nbytes:
+        ws = torch.zeros(max(nbytes, 16), dtype=torch.uint8, device=device)
+        _WORKSPACES[key] = ws
+    return ws
+
+
 # ---------------------------------------------------------------------------
 # os_softmax_rows
 # ---------------------------------------------------------------------------
+
+def softmax_rows_workspace_bytes(rows: int, cols: int, dtype=torch.float32) -> int:
+    """Workspace bytes os_softmax_rows_ws uses for such rows (0: none)."""
+    code = 0 if dtype == torch.float32 else _DTYPE_CODES[dtype]
+    n = int(load().os_softmax_rows_workspace_bytes(int(rows), int(cols), code))
+    if n < 0:
+        raise OssError(4, "os_softmax_rows_workspace_bytes")
+    return n
 
 def softmax_rows(x: torch.Tensor, scale: float = 1.0, y: Optional[torch.Tensor] = None,
                  m: Optional[torch.Tensor] = None, l: Optional[torch.Tensor] = None,
@@ -206,10 +239,13 @@ def softmax_rows(x: torch.Tensor, scale: float = 1.0, y: Optional[torch.Tensor] 
     l = _out(torch.empty(rows, dtype=torch.float32, device=dev) if l is None else l,
              "l", torch.float32, (rows,), dev)
     with torch.cuda.device(dev):
-        st = load().os_softmax_rows(x.data_ptr(), y.data_ptr(), m.data_ptr(), l.data_ptr(), rows,
-                                    cols, x.stride(0), y.stride(0), float(scale),
-                                    _stream_ptr(stream, dev))
-    _check(st, "os_softmax_rows")
+        sp = _stream_ptr(stream, dev)
+        need = softmax_rows_workspace_bytes(rows, cols)
+        ws = _workspace(dev, sp, need, "rows") if need > 0 else None
+        st = load().os_softmax_rows_ws(x.data_ptr(), y.data_ptr(), m.data_ptr(), l.data_ptr(), rows,
+                                       cols, x.stride(0), y.stride(0), float(scale), _ptr(ws),
+                                       need if ws is not None else 0, sp)
+    _check(st, "os_softmax_rows_ws")
     return y, m, l
 
 
@@ -240,10 +276,14 @@ def softmax_rows_16bit(x: torch.Tensor, scale: float = 1.0, y: Optional[torch.Te
     l = _out(torch.empty(rows, dtype=torch.float32, device=dev) if l is None else l,
              "l", torch.float32, (rows,), dev)
     with torch.cuda.device(dev):
-        st = load().os_softmax_rows_16bit(x.data_ptr(), y.data_ptr(), m.data_ptr(), l.data_ptr(),
-                                          rows, cols, x.stride(0), y.stride(0), float(scale),
-                                          _DTYPE_CODES[x.dtype], _stream_ptr(stream, dev))
-    _check(st, "os_softmax_rows_16bit")
+        sp = _stream_ptr(stream, dev)
+        need = softmax_rows_workspace_bytes(rows, cols, x.dtype)
+        ws = _workspace(dev, sp, need, "rows") if need > 0 else None
+        st = load().os_softmax_rows_16bit_ws(x.data_ptr(), y.data_ptr(), m.data_ptr(), l.data_ptr(),
+                                             rows, cols, x.stride(0), y.stride(0), float(scale),
+                                             _DTYPE_CODES[x.dtype], _ptr(ws),
+                                             need if ws is not None else 0, sp)
+    _check(st, "os_softmax_rows_16bit_ws")
     return y, m, l
 
 
@@ -331,6 +371,16 @@ def softmax_rows_from_host(x_host: torch.Tensor, scale: float = 1.0, out=None, d
 # os_attention_fwd
 # ---------------------------------------------------------------------------
 
+def attention_fwd_workspace_bytes(B: int, H: int, Sq: int, Sk: int, D: int = 128,
+                                  causal: bool = False) -> int:
+    """Workspace bytes os_attention_fwd_ws uses for this shape on the current
+    device (0: none)."""
+    n = int(load().os_attention_fwd_workspace_bytes(B, H, Sq, Sk, D, int(bool(causal))))
+    if n < 0:
+        raise OssError(4, "os_attention_fwd_workspace_bytes")
+    return n
+
+
 def attention_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
                   scale: Optional[float] = None, causal: bool = False,
                   o: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
@@ -354,10 +404,14 @@ def attention_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
     lse = _out(torch.empty((B, H, Sq), dtype=torch.float32, device=dev) if lse is None else lse,
                "lse", torch.float32, (B, H, Sq), dev)
     with torch.cuda.device(dev):
-        st = load().os_attention_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
-                                     lse.data_ptr(), B, H, Sq, Sk, D, float(scale),
-                                     int(bool(causal)), _stream_ptr(stream, dev))
-    _check(st, "os_attention_fwd")
+        sp = _stream_ptr(stream, dev)
+        need = attention_fwd_workspace_bytes(B, H, Sq, Sk, D, causal)
+        ws = _workspace(dev, sp, need, "attn") if need > 0 else None
+        st = load().os_attention_fwd_ws(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                        lse.data_ptr(), B, H, Sq, Sk, D, float(scale),
+                                        int(bool(causal)), _ptr(ws), need if ws is not None else 0,
+                                        sp)
+    _check(st, "os_attention_fwd_ws")
     return o, lse
 
 
@@ -541,5 +595,9 @@ def check_device_error(stream=None) -> int:
     dev = torch.device("cuda", torch.cuda.current_device()) if stream is None else stream.device
     with torch.cuda.device(dev):
         st = load().os_check_device_error(_stream_ptr(stream, dev), ctypes.byref(code))
+    if st != OS_OK:
+        # a launch that gave up may have left counters in its workspace:
+        # later calls get fresh zero-filled ones
+        _WORKSPACES.clear()
     _check(st, f"os_check_device_error (code {code.value:#x})")
     return int(code.value)

@@ -74,37 +74,62 @@ const char* os_status_string(os_status status) {
   return "OS_ERR_UNKNOWN";
 }
 
-os_status os_softmax_rows(const float* x, float* y, float* m, float* l, int64_t rows,
-                          int64_t cols, int64_t ld_x, int64_t ld_y, float scale, void* stream) {
+os_status os_softmax_rows_ws(const float* x, float* y, float* m, float* l, int64_t rows,
+                             int64_t cols, int64_t ld_x, int64_t ld_y, float scale, void* workspace,
+                             int64_t workspace_bytes, void* stream) {
   if (!x || !y) return OS_ERR_INVALID_ARGUMENT;
   if (rows <= 0 || cols <= 0 || ld_x < cols || ld_y < cols) return OS_ERR_INVALID_ARGUMENT;
   if (cols > (int64_t(1) << 30) || rows > (int64_t(1) << 40)) return OS_ERR_INVALID_ARGUMENT;
   if (!valid_scale(scale)) return OS_ERR_INVALID_ARGUMENT;
+  if (workspace_bytes < 0 || (!workspace && workspace_bytes != 0)) return OS_ERR_INVALID_ARGUMENT;
   if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y) |
        reinterpret_cast<uintptr_t>(m) | reinterpret_cast<uintptr_t>(l)) & 3u)
     return OS_ERR_MISALIGNED;
+  if (!aligned16(workspace)) return OS_ERR_MISALIGNED;
   const oss::RowsFault fault = t_rows_fault;
   t_rows_fault = oss::RowsFault();
   return from_cuda(oss::launch_softmax_rows(x, y, m, l, rows, cols, ld_x, ld_y, scale,
-                                            error_word(), fault, static_cast<cudaStream_t>(stream)));
+                                            error_word(), fault, workspace, workspace_bytes,
+                                            static_cast<cudaStream_t>(stream)));
 }
 
-os_status os_softmax_rows_16bit(const void* x, void* y, float* m, float* l, int64_t rows,
-                                int64_t cols, int64_t ld_x, int64_t ld_y, float scale,
-                                int32_t dtype, void* stream) {
+os_status os_softmax_rows(const float* x, float* y, float* m, float* l, int64_t rows,
+                          int64_t cols, int64_t ld_x, int64_t ld_y, float scale, void* stream) {
+  return os_softmax_rows_ws(x, y, m, l, rows, cols, ld_x, ld_y, scale, nullptr, 0, stream);
+}
+
+os_status os_softmax_rows_16bit_ws(const void* x, void* y, float* m, float* l, int64_t rows,
+                                   int64_t cols, int64_t ld_x, int64_t ld_y, float scale,
+                                   int32_t dtype, void* workspace, int64_t workspace_bytes,
+                                   void* stream) {
   if (!x || !y) return OS_ERR_INVALID_ARGUMENT;
   if (rows <= 0 || cols <= 0 || ld_x < cols || ld_y < cols) return OS_ERR_INVALID_ARGUMENT;
   if (cols > (int64_t(1) << 30) || rows > (int64_t(1) << 40)) return OS_ERR_INVALID_ARGUMENT;
   if (!valid_scale(scale) || (dtype != OS_DTYPE_BF16 && dtype != OS_DTYPE_F16))
     return OS_ERR_INVALID_ARGUMENT;
+  if (workspace_bytes < 0 || (!workspace && workspace_bytes != 0)) return OS_ERR_INVALID_ARGUMENT;
   if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y)) & 1u) return OS_ERR_MISALIGNED;
   if ((reinterpret_cast<uintptr_t>(m) | reinterpret_cast<uintptr_t>(l)) & 3u) return OS_ERR_MISALIGNED;
+  if (!aligned16(workspace)) return OS_ERR_MISALIGNED;
   const oss::RowsFault fault = t_rows_fault;
   t_rows_fault = oss::RowsFault();
   return from_cuda(oss::launch_softmax_rows16(static_cast<const uint16_t*>(x),
                                               static_cast<uint16_t*>(y), m, l, rows, cols, ld_x,
-                                              ld_y, scale, dtype, error_word(), fault,
-                                              static_cast<cudaStream_t>(stream)));
+                                              ld_y, scale, dtype, error_word(), fault, workspace,
+                                              workspace_bytes, static_cast<cudaStream_t>(stream)));
+}
+
+os_status os_softmax_rows_16bit(const void* x, void* y, float* m, float* l, int64_t rows,
+                                int64_t cols, int64_t ld_x, int64_t ld_y, float scale,
+                                int32_t dtype, void* stream) {
+  return os_softmax_rows_16bit_ws(x, y, m, l, rows, cols, ld_x, ld_y, scale, dtype, nullptr, 0,
+                                  stream);
+}
+
+int64_t os_softmax_rows_workspace_bytes(int64_t rows, int64_t cols, int32_t dtype) {
+  if (rows <= 0 || cols <= 0) return 0;
+  if (dtype != 0 && dtype != OS_DTYPE_BF16 && dtype != OS_DTYPE_F16) return 0;
+  return oss::softmax_workspace_bytes(cols * (dtype == 0 ? 4 : 2));
 }
 
 os_status os_softmax_rows_multipass(const float* x, float* y, float* m, float* l, int64_t rows,
@@ -137,6 +162,39 @@ os_status os_attention_fwd(const os_bf16* q, const os_bf16* k, const os_bf16* v,
   t_fault = oss::AttnFault();
   return from_cuda(oss::launch_attention_fwd(q, k, v, o, lse, B, H, Sq, Sk, D, scale,
                                              causal != 0, err, fault, nullptr, t_rescale_policy,
+                                             nullptr, 0, static_cast<cudaStream_t>(stream)));
+}
+
+int64_t os_attention_fwd_workspace_bytes(int32_t B, int32_t H, int32_t Sq, int32_t Sk, int32_t D,
+                                         int causal) {
+  if (B <= 0 || H <= 0 || Sq <= 0 || Sk <= 0 || D != 128) return 0;
+  if (static_cast<int64_t>(B) * H > 65535 * 64) return 0;
+  return oss::attention_workspace_bytes(B, H, Sq, Sk, causal != 0);
+}
+
+os_status os_attention_fwd_ws(const os_bf16* q, const os_bf16* k, const os_bf16* v, os_bf16* o,
+                              float* lse, int32_t B, int32_t H, int32_t Sq, int32_t Sk, int32_t D,
+                              float scale, int causal, void* workspace, int64_t workspace_bytes,
+                              void* stream) {
+  if (!q || !k || !v || !o) return OS_ERR_INVALID_ARGUMENT;
+  if (B <= 0 || H <= 0 || Sq <= 0 || Sk <= 0 || D <= 0) return OS_ERR_INVALID_ARGUMENT;
+  if (!valid_scale(scale)) return OS_ERR_INVALID_ARGUMENT;
+  if (workspace_bytes < 0 || (!workspace && workspace_bytes != 0)) return OS_ERR_INVALID_ARGUMENT;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(workspace))
+    return OS_ERR_MISALIGNED;
+  if (D != 128) return OS_ERR_UNSUPPORTED;
+  if (causal && Sq != Sk) return OS_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(B) * H > 65535 * 64) return OS_ERR_UNSUPPORTED;
+  const int64_t need = oss::attention_workspace_bytes(B, H, Sq, Sk, causal != 0);
+  if (need < 0) return OS_ERR_CUDA;
+  if (need > 0 && workspace && workspace_bytes < need) return OS_ERR_INVALID_ARGUMENT;
+  unsigned int* err = error_word();
+  if (!err) return OS_ERR_CUDA;
+  const oss::AttnFault fault = t_fault;
+  t_fault = oss::AttnFault();
+  return from_cuda(oss::launch_attention_fwd(q, k, v, o, lse, B, H, Sq, Sk, D, scale,
+                                             causal != 0, err, fault, nullptr, t_rescale_policy,
+                                             workspace, workspace_bytes,
                                              static_cast<cudaStream_t>(stream)));
 }
 
@@ -160,7 +218,7 @@ os_status os_attention_fwd_partial(const os_bf16* q, const os_bf16* k, const os_
   const oss::AttnPartialOut out{part_m, part_l, part_o, part_stride, part_index};
   return from_cuda(oss::launch_attention_fwd(q, k, v, nullptr, nullptr, B, H, Sq, Sk, D, scale,
                                              causal != 0, err, fault, &out, t_rescale_policy,
-                                             static_cast<cudaStream_t>(stream)));
+                                             nullptr, 0, static_cast<cudaStream_t>(stream)));
 }
 
 os_status os_attention_decode_splitkv(const os_bf16* q, const os_bf16* k, const os_bf16* v,

@@ -409,6 +409,15 @@ struct AttnParams {
   float* part_l;
   float* part_o;
   int part_stride, part_index;
+  // Split tail (non-causal, with a workspace): after full_rounds rounds of
+  // whole query tiles, the remaining tiles from split_first on are cut along
+  // the keys into split_f parts, one part per CTA; each part writes its
+  // (m, l, O) to the workspace and the last part of a tile to finish merges
+  // them. split_f < 2: no split.
+  int full_rounds, split_first, split_f, split_items;
+  float* ws_o;            // [split tiles][split_f][16][softmax threads][4]: unnormalised O
+  float* ws_ml;           // [split tiles][split_f][softmax threads][4]: base-2 m, l of rows a, b
+  unsigned int* ws_cnt;   // [split tiles][softmax warps]: (launch tag << 8) | parts done
 };
 
 struct Barriers {
@@ -422,10 +431,18 @@ struct Barriers {
   uint64_t drain[2];  // one per issuing thread
 };
 
+// A unit of work: query tile `lin`, whole (part < 0) or part `part` of a tile
+// split along the keys.
+struct Work {
+  int lin, part;
+};
+
 // A query tile: (b, h), first query row, number of KV tiles and how many of
-// them (the diagonal ones, causal only) are visited first.
+// them (the diagonal ones, causal only) are visited first; the work unit
+// visits n_steps of them, from position kv_lo of that order.
 struct TileInfo {
   int bh, q0, n_kv, n_diag;
+  int kv_lo, n_steps, part, tail;
 };
 
 // Query tile number lin of the launch. Causal tiles start kCausalShift rows
@@ -437,7 +454,8 @@ struct TileInfo {
 __host__ __device__ __forceinline__ int imin(int a, int b) { return a < b ? a : b; }
 __host__ __device__ __forceinline__ int imax(int a, int b) { return a > b ? a : b; }
 
-__host__ __device__ __forceinline__ TileInfo tile_info(const AttnParams& p, int lin) {
+__host__ __device__ __forceinline__ TileInfo tile_info(const AttnParams& p, Work w) {
+  const int lin = w.lin;
   int bh, qb;
   if (!p.causal) {
     bh = lin / p.n_qblocks;
@@ -461,12 +479,23 @@ __host__ __device__ __forceinline__ TileInfo tile_info(const AttnParams& p, int 
   // first one is masked for all of the tile's first kCausalShift rows.
   const int diag_first = p.causal ? imax(0, t.q0) / kBN : t.n_kv;
   t.n_diag = t.n_kv - diag_first;
+  t.part = w.part;
+  if (w.part < 0) {
+    t.kv_lo = 0;
+    t.n_steps = t.n_kv;
+    t.tail = -1;
+  } else {  // keys of part i: KV tiles [i n / f, (i + 1) n / f)
+    t.kv_lo = w.part * t.n_kv / p.split_f;
+    t.n_steps = (w.part + 1) * t.n_kv / p.split_f - t.kv_lo;
+    t.tail = lin - p.split_first;
+  }
   return t;
 }
 
-// KV tile visited at step j of a query tile.
+// KV tile visited at step j of a work unit.
 __device__ __forceinline__ int kv_tile(const TileInfo& t, int j) {
-  return j < t.n_diag ? (t.n_kv - 1 - j) : (j - t.n_diag);
+  const int v = t.kv_lo + j;
+  return v < t.n_diag ? (t.n_kv - 1 - v) : (v - t.n_diag);
 }
 
 // The k-th query tile of this CTA, or -1. With G CTAs, round k hands tiles
@@ -495,15 +524,75 @@ struct TileSched<true> {
   uint16_t list[kSchedMaxTiles];
 };
 
-// The k-th query tile of this CTA, or -1: from the host's lists, or by the
-// round rule of work_tile.
+// The k-th work unit of this CTA (lin < 0: none left): from the host's lists,
+// or by the round rule of work_tile, then, with a split tail, one part of a
+// split tile per CTA.
 template <bool kSched>
-__device__ __forceinline__ int tile_of(int k, const AttnParams& p, const TileSched<kSched>& sc) {
+__device__ __forceinline__ Work tile_of(int k, const AttnParams& p, const TileSched<kSched>& sc) {
   if constexpr (kSched) {
     const int b = sc.off[blockIdx.x];
-    return (b + k < static_cast<int>(sc.off[blockIdx.x + 1])) ? static_cast<int>(sc.list[b + k]) : -1;
+    return {(b + k < static_cast<int>(sc.off[blockIdx.x + 1])) ? static_cast<int>(sc.list[b + k]) : -1,
+            -1};
   } else {
-    return work_tile(k, p.n_tiles);
+    if (p.split_f < 2) return {work_tile(k, p.n_tiles), -1};
+    if (k < p.full_rounds) return {work_tile(k, p.n_tiles), -1};
+    const int seg = static_cast<int>(blockIdx.x);
+    if (k == p.full_rounds && seg < p.split_items)
+      return {p.split_first + seg / p.split_f, seg % p.split_f};
+    return {-1, -1};
+  }
+}
+
+constexpr int kMaxSplit = 8;  // parts a split tile is cut into at most
+
+// Counts one finished part of a split tile on its counter and returns how
+// many of the tile's parts are done, this one included. The counter holds
+// (launch tag << 8) | parts done; a value left by another launch (one that
+// gave up on a wait, say) carries another tag and counts as zero. The
+// compare-and-swap has acquire-release semantics at GPU scope: it publishes
+// the part this warp has written (its lanes' stores are ordered before it
+// by the warp barrier the caller takes) and, for the last part, makes every
+// other part's stores visible. At most kMaxSplit threads contend for a
+// counter, so the loop ends within that many rounds; the bound only guards
+// against the impossible.
+__device__ __forceinline__ unsigned int count_part(unsigned int* c, unsigned int tag) {
+  unsigned int cur;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(cur) : "l"(c) : "memory");
+  for (int round = 0; round < 4 * kMaxSplit; ++round) {
+    const unsigned int n = ((cur >> 8) == tag) ? (cur & 0xffu) + 1u : 1u;
+    unsigned int seen;
+    asm volatile("atom.acq_rel.gpu.global.cas.b32 %0, [%1], %2, %3;"
+                 : "=r"(seen)
+                 : "l"(c), "r"(cur), "r"((tag << 8) | n)
+                 : "memory");
+    if (seen == cur) return n;
+    cur = seen;
+  }
+  return 0;
+}
+
+// Stores half h (head dims 64 h .. 64 h + 63) of two rows of O in bf16:
+// va[2 k + e], vb[2 k + e] hold dims 64 h + 8 k + cq + e of rows a and b,
+// scaled by inv_a, inv_b. Each 8-dim chunk of a row is spread over the row's
+// four threads (2 dims each); a 4 x 4 transpose among them hands every
+// thread whole chunks, written with 16-byte stores.
+__device__ __forceinline__ void store_o_half(uint4* oa, uint4* ob, const float (&va)[16],
+                                             const float (&vb)[16], float inv_a, float inv_b,
+                                             int h, int jj, bool live_a, bool live_b) {
+#pragma unroll
+  for (int mb = 0; mb < 2; ++mb) {
+    uint32_t wa[4], wb[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int k = 4 * mb + i;  // chunk 8 h + k of the row
+      wa[i] = pack_bf16x2(va[2 * k] * inv_a, va[2 * k + 1] * inv_a);
+      wb[i] = pack_bf16x2(vb[2 * k] * inv_b, vb[2 * k + 1] * inv_b);
+    }
+    lane_transpose4(wa, jj);
+    lane_transpose4(wb, jj);
+    const int chunk = 8 * h + 4 * mb + jj;
+    if (live_a) oa[chunk] = make_uint4(wa[0], wa[1], wa[2], wa[3]);
+    if (live_b) ob[chunk] = make_uint4(wb[0], wb[1], wb[2], wb[3]);
   }
 }
 
@@ -575,9 +664,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
       int k_issued = 0, v_issued = 0, q_loads = 0, skipped_v = -1;
       int key_row[kStages] = {0, 0, 0}, key_bh[kStages] = {0, 0, 0};
       int kt = 0, j = 0;  // K stream: tile ordinal, step within the tile
-      int lin = tile_of(0, p, sched);
+      Work wk = tile_of(0, p, sched);
       TileInfo t{};
-      if (lin >= 0) t = tile_info(p, lin);
+      if (wk.lin >= 0) t = tile_info(p, wk);
       for (int g = 0;; ++g) {
         // V of step g - kKLead first: it is the load the P V thread waits on
         // soonest, and the Q wait below may block until this tile's QK^T end
@@ -599,7 +688,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
             v_issued = gv + 1;
           }
         }
-        if (lin < 0) {
+        if (wk.lin < 0) {
           if (gv + 1 >= k_issued) break;  // the last V load has been issued
           continue;
         }
@@ -626,10 +715,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
           tma_load_3d(sbase + kOffK + s * kTile + h * kHalf, &tmap_k, kb, h * 64, key_row[s],
                       key_bh[s]);
         k_issued = g + 1;
-        if (++j == t.n_kv) {
+        if (++j == t.n_steps) {
           j = 0;
-          lin = tile_of(++kt, p, sched);
-          if (lin >= 0) t = tile_info(p, lin);
+          wk = tile_of(++kt, p, sched);
+          if (wk.lin >= 0) t = tile_info(p, wk);
         }
       }
       // drain: every issued copy must land before the CTA may exit
@@ -651,9 +740,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
       const uint64_t dq = smem_desc(sbase + kOffQ, 16, 1024);
       int g = 0;
       for (int kt = 0; ok; ++kt) {
-        const int lin = tile_of(kt, p, sched);
-        if (lin < 0) break;
-        const TileInfo t = tile_info(p, lin);
+        const Work wk = tile_of(kt, p, sched);
+        if (wk.lin < 0) break;
+        const TileInfo t = tile_info(p, wk);
         if (!(ok = wait_bar(smem_addr(&bars.q_full), kt & 1, abort_flag, p.err, kSiteQFull)))
           break;
         // The previous tile's last P V goes through the tensor pipe before this
@@ -664,7 +753,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
         if (kt > 0 && !(ok = wait_bar(smem_addr(&bars.o_done[(g - 1) % kStages]),
                                       ((g - 1) / kStages) & 1, abort_flag, p.err, kSiteODone)))
           break;
-        for (int j = 0; j < t.n_kv; ++j, ++g) {
+        for (int j = 0; j < t.n_steps; ++j, ++g) {
           const int s = g % kStages;  // K stage = score buffer
           if (!(ok = wait_bar(smem_addr(&bars.k_full[s]), (g / kStages) & 1, abort_flag, p.err,
                               kSiteKFull)))
@@ -697,10 +786,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
       const uint32_t d_o = tbase + kColO;
       int g = 0;
       for (int kt = 0; ok; ++kt) {
-        const int lin = tile_of(kt, p, sched);
-        if (lin < 0) break;
-        const TileInfo t = tile_info(p, lin);
-        for (int j = 0; j < t.n_kv; ++j, ++g) {
+        const Work wk = tile_of(kt, p, sched);
+        if (wk.lin < 0) break;
+        const TileInfo t = tile_info(p, wk);
+        for (int j = 0; j < t.n_steps; ++j, ++g) {
           const int s = g % kStages;
           if (!(ok = wait_bar(smem_addr(&bars.v_full[s]), (g / kStages) & 1, abort_flag, p.err,
                               kSiteVFull)))
@@ -750,14 +839,14 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
     bool ok = true;
     int g = 0;
     for (int kt = 0; ok; ++kt) {
-      const int lin = tile_of(kt, p, sched);
-      if (lin < 0) break;
-      const TileInfo t = tile_info(p, lin);
+      const Work wk = tile_of(kt, p, sched);
+      if (wk.lin < 0) break;
+      const TileInfo t = tile_info(p, wk);
       const int row_a = t.q0 + ra, row_b = t.q0 + rb;  // query indices (may be < 0: padding)
       float m_a = neg_inf(), m_b = neg_inf();       // reference maxima, base 2
       float mt_a = neg_inf(), mt_b = neg_inf();     // true row maxima, base 2 (partial states)
       float l_a = 0.f, l_b = 0.f;                   // this thread's share of the row sums
-      for (int j = 0; j < t.n_kv; ++j, ++g) {
+      for (int j = 0; j < t.n_steps; ++j, ++g) {
         const int b = g % kSBuf;
         const uint32_t colS = col_s(b);
         ok = __all_sync(0xffffffffu, wait_bar(smem_addr(&bars.s_full[b]), (g / kSBuf) & 1,
@@ -940,37 +1029,131 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
             p.part_l[slot_b] = empty_b ? 0.f : l_b * f_b;
           }
         }
+      } else if (ok && t.part >= 0) {
+        // A part of a split tile: its (m, l, O) go to the workspace; the last
+        // part of the tile to finish merges every part, in part order, so the
+        // result does not depend on which CTA merges. A thread's 64 values of
+        // O (rows a, b; the 16x256b layout) are 16 vectors of 4; vector e of
+        // the CTA's 256 threads lies contiguous, so every warp access is 512
+        // contiguous bytes, and the part that merges reads the same thread's
+        // vectors of the other parts.
+        tc_fence_after();
+        const int f = p.split_f;
+        const int me = warp * 32 + lane;                       // this thread's slot in a part
+        const size_t part0 = static_cast<size_t>(t.tail) * f;  // part 0 of this tile
+        {
+          // O of this part, [h][k][a0 a1 b0 b1]: 16 float4 per thread
+          float4* wo = reinterpret_cast<float4*>(p.ws_o) + (part0 + t.part) * 16 * kSoftThreads + me;
+#pragma unroll 1
+          for (int h = 0; h < 2; ++h) {
+            uint32_t ov[32];
+            tmem_ld16x256_x8(tl + kColO + 64 * h, ov);
+            tmem_ld_wait(ov);
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              wo[(8 * h + e) * kSoftThreads] = make_float4(__uint_as_float(ov[4 * e]), __uint_as_float(ov[4 * e + 1]),
+                                          __uint_as_float(ov[4 * e + 2]), __uint_as_float(ov[4 * e + 3]));
+          }
+          reinterpret_cast<float4*>(p.ws_ml)[(part0 + t.part) * kSoftThreads + me] =
+              make_float4(m_a, l_a, m_b, l_b);
+        }
+        __syncwarp();
+        unsigned int* cnt = p.ws_cnt + static_cast<size_t>(t.tail) * kSoftWarps + warp;
+        unsigned int done = 0;
+        if (lane == 0) done = count_part(cnt, p.tag);
+        done = __shfl_sync(0xffffffffu, done, 0);
+        __syncwarp();  // the lanes' reads below come after lane 0's acquire
+        if (done == static_cast<unsigned int>(f)) {
+          // the merge identity over the parts: M = max m_i, weights 2^(m_i - M)
+          float4 st[kMaxSplit];
+#pragma unroll
+          for (int i = 0; i < kMaxSplit; ++i)
+            st[i] = (i < f) ? __ldcg(reinterpret_cast<const float4*>(p.ws_ml) + (part0 + i) * kSoftThreads + me)
+                            : make_float4(neg_inf(), 0.f, neg_inf(), 0.f);
+          float Ma = neg_inf(), Mb = neg_inf();
+#pragma unroll
+          for (int i = 0; i < kMaxSplit; ++i) {
+            Ma = fmaxf(Ma, st[i].x);
+            Mb = fmaxf(Mb, st[i].z);
+          }
+          float La = 0.f, Lb = 0.f;
+          float wpa[kMaxSplit], wpb[kMaxSplit];
+#pragma unroll
+          for (int i = 0; i < kMaxSplit; ++i) {
+            wpa[i] = (st[i].x == neg_inf()) ? 0.f : ex2(st[i].x - Ma);
+            wpb[i] = (st[i].z == neg_inf()) ? 0.f : ex2(st[i].z - Mb);
+            La = fmaf(wpa[i], st[i].y, La);
+            Lb = fmaf(wpb[i], st[i].w, Lb);
+          }
+          // acc = sum_i w_i O_i in part order, so every CTA that merges
+          // rounds the same way
+          float acc[64];
+#pragma unroll
+          for (int e = 0; e < 64; ++e) acc[e] = 0.f;
+#pragma unroll 1
+          for (int i = 0; i < f; ++i) {
+            float xa = 0.f, xb = 0.f;
+#pragma unroll
+            for (int q = 0; q < kMaxSplit; ++q)
+              if (q == i) { xa = wpa[q]; xb = wpb[q]; }
+            float4 v4[16];
+            const float4* po = reinterpret_cast<const float4*>(p.ws_o) + (part0 + i) * 16 * kSoftThreads + me;
+#pragma unroll
+            for (int e = 0; e < 16; ++e) v4[e] = __ldcg(po + e * kSoftThreads);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              acc[4 * e] = fmaf(xa, v4[e].x, acc[4 * e]);
+              acc[4 * e + 1] = fmaf(xa, v4[e].y, acc[4 * e + 1]);
+              acc[4 * e + 2] = fmaf(xb, v4[e].z, acc[4 * e + 2]);
+              acc[4 * e + 3] = fmaf(xb, v4[e].w, acc[4 * e + 3]);
+            }
+          }
+          const float inv_a = (La > 0.f) ? 1.0f / La : 0.f;
+          const float inv_b = (Lb > 0.f) ? 1.0f / Lb : 0.f;
+          uint4* oa = reinterpret_cast<uint4*>(p.o + (static_cast<size_t>(t.bh) * p.Sq + row_a) * kD);
+          uint4* ob = reinterpret_cast<uint4*>(p.o + (static_cast<size_t>(t.bh) * p.Sq + row_b) * kD);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            float va[16], vb[16];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              va[2 * k] = acc[32 * h + 4 * k];
+              va[2 * k + 1] = acc[32 * h + 4 * k + 1];
+              vb[2 * k] = acc[32 * h + 4 * k + 2];
+              vb[2 * k + 1] = acc[32 * h + 4 * k + 3];
+            }
+            store_o_half(oa, ob, va, vb, inv_a, inv_b, h, lane & 3, live_a, live_b);
+          }
+          if (writes_row && p.lse) {
+            const float kLn2 = 0.69314718055994530942f;
+            if (live_a)
+              p.lse[static_cast<size_t>(t.bh) * p.Sq + row_a] = (La > 0.f) ? (Ma + __log2f(La)) * kLn2 : neg_inf();
+            if (live_b)
+              p.lse[static_cast<size_t>(t.bh) * p.Sq + row_b] = (Lb > 0.f) ? (Mb + __log2f(Lb)) * kLn2 : neg_inf();
+          }
+          __syncwarp();
+          if (lane == 0) *cnt = 0u;  // ready for the next launch
+        }
       } else if (ok) {
         tc_fence_after();
         const float inv_a = (l_a > 0.f) ? 1.0f / l_a : 0.f;
         const float inv_b = (l_b > 0.f) ? 1.0f / l_b : 0.f;
-        // Each 8-column chunk of a row is spread over the row's four threads
-        // (2 columns each); a 4 x 4 transpose among them hands every thread
-        // whole chunks, written with 16-byte stores (whole sectors for each
-        // pair of threads instead of 16-byte pieces).
         uint4* oa = reinterpret_cast<uint4*>(p.o + (static_cast<size_t>(t.bh) * p.Sq + row_a) * kD);
         uint4* ob = reinterpret_cast<uint4*>(p.o + (static_cast<size_t>(t.bh) * p.Sq + row_b) * kD);
-        const int jj = lane & 3;
 #pragma unroll 1
         for (int h = 0; h < 2; ++h) {
           uint32_t ov[32];
           tmem_ld16x256_x8(tl + kColO + 64 * h, ov);
           tmem_ld_wait(ov);
+          float va[16], vb[16];
 #pragma unroll
-          for (int mb = 0; mb < 2; ++mb) {
-            uint32_t wa[4], wb[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const int k = 4 * mb + i;  // chunk 8 h + k of the row
-              wa[i] = pack_bf16x2(__uint_as_float(ov[4 * k]) * inv_a, __uint_as_float(ov[4 * k + 1]) * inv_a);
-              wb[i] = pack_bf16x2(__uint_as_float(ov[4 * k + 2]) * inv_b, __uint_as_float(ov[4 * k + 3]) * inv_b);
-            }
-            lane_transpose4(wa, jj);
-            lane_transpose4(wb, jj);
-            const int chunk = 8 * h + 4 * mb + jj;
-            if (live_a) oa[chunk] = make_uint4(wa[0], wa[1], wa[2], wa[3]);
-            if (live_b) ob[chunk] = make_uint4(wb[0], wb[1], wb[2], wb[3]);
+          for (int k = 0; k < 8; ++k) {
+            va[2 * k] = __uint_as_float(ov[4 * k]);
+            va[2 * k + 1] = __uint_as_float(ov[4 * k + 1]);
+            vb[2 * k] = __uint_as_float(ov[4 * k + 2]);
+            vb[2 * k + 1] = __uint_as_float(ov[4 * k + 3]);
           }
+          store_o_half(oa, ob, va, vb, inv_a, inv_b, h, lane & 3, live_a, live_b);
         }
         if (writes_row && p.lse) {
           const float kLn2 = 0.69314718055994530942f;
@@ -1053,7 +1236,7 @@ bool build_schedule(const AttnParams& prm, int G, TileSched<true>* sc) {
     heap.pop();
     owner[lin] = l.second;
     ++count[l.second];
-    heap.push({l.first + tile_info(prm, lin).n_kv + kTileOverheadSteps, l.second});
+    heap.push({l.first + tile_info(prm, Work{lin, -1}).n_kv + kTileOverheadSteps, l.second});
   }
   sc->off[0] = 0;
   for (int c = 0; c < G; ++c) sc->off[c + 1] = static_cast<uint16_t>(sc->off[c] + count[c]);
@@ -1078,6 +1261,47 @@ void launch_policy(int policy, int grid, cudaStream_t stream, const CUtensorMap&
                                                                                     sched);
 }
 
+// The split tail of a non-causal launch on `sms` SMs: whole query tiles in
+// full rounds of one tile per CTA, then the remaining tiles cut along the keys
+// into f parts so that every CTA gets one part (f = sms / remaining, at most
+// kMaxSplit and at most the tile's KV tiles). No split when the tiles fill
+// the rounds exactly or f < 2.
+struct SplitPlan {
+  int full_rounds = 0, split_first = 0, split_f = 0, split_items = 0;
+  long long tail = 0;
+};
+
+SplitPlan split_plan(long long tiles, int n_kv, int sms) {
+  SplitPlan sp;
+  if (tiles <= 0 || sms <= 0) return sp;
+  const long long rounds = tiles / sms;
+  const long long tail = tiles - rounds * sms;
+  if (tail == 0) return sp;
+  long long f = sms / tail;
+  if (f > kMaxSplit) f = kMaxSplit;
+  if (f > n_kv) f = n_kv;
+  if (f < 2) return sp;
+  sp.full_rounds = static_cast<int>(rounds);
+  sp.split_first = static_cast<int>(rounds * sms);
+  sp.split_f = static_cast<int>(f);
+  sp.split_items = static_cast<int>(f * tail);
+  sp.tail = tail;
+  return sp;
+}
+
+// Workspace of a split tail: O, then (m, l), then the counters.
+size_t split_bytes_o(const SplitPlan& sp) {
+  return static_cast<size_t>(sp.tail) * sp.split_f * kBM * kD * sizeof(float);
+}
+size_t split_bytes_ml(const SplitPlan& sp) {
+  return static_cast<size_t>(sp.tail) * sp.split_f * kSoftThreads * 4 * sizeof(float);
+}
+size_t split_bytes(const SplitPlan& sp) {
+  if (sp.split_f < 2) return 0;
+  return split_bytes_o(sp) + split_bytes_ml(sp) +
+         static_cast<size_t>(sp.tail) * kSoftWarps * sizeof(unsigned int);
+}
+
 // The last schedule built by this host thread, reused while the shape stays.
 struct SchedCache {
   int bh = -1, n_qblocks = -1, sk = -1, grid = -1;
@@ -1090,7 +1314,8 @@ cudaError_t launch_attention_fwd(const uint16_t* q, const uint16_t* k, const uin
                                  uint16_t* o, float* lse, int B, int H, int Sq, int Sk, int D,
                                  float scale, bool causal, unsigned int* err_word,
                                  const AttnFault& fault, const AttnPartialOut* partial,
-                                 int rescale_policy, cudaStream_t stream) {
+                                 int rescale_policy, void* workspace, int64_t workspace_bytes,
+                                 cudaStream_t stream) {
   if (rescale_policy < kRescaleThreshold || rescale_policy > kRescaleAlways)
     return cudaErrorInvalidValue;
   if (D != kD) return cudaErrorNotSupported;
@@ -1138,6 +1363,9 @@ cudaError_t launch_attention_fwd(const uint16_t* q, const uint16_t* k, const uin
   prm.part_o = partial ? partial->o : nullptr;
   prm.part_stride = partial ? partial->stride : 1;
   prm.part_index = partial ? partial->index : 0;
+  prm.full_rounds = prm.split_first = prm.split_f = prm.split_items = 0;
+  prm.ws_o = prm.ws_ml = nullptr;
+  prm.ws_cnt = nullptr;
   const long long tiles = static_cast<long long>(prm.n_qblocks) * BH;
   if (tiles > 0x7fffffffLL) return cudaErrorNotSupported;
   prm.n_tiles = static_cast<int>(tiles);
@@ -1168,8 +1396,34 @@ cudaError_t launch_attention_fwd(const uint16_t* q, const uint16_t* k, const uin
     return cudaGetLastError();
   }
   TileSched<false> none{};
-  launch_policy<false>(rescale_policy, G, stream, mq, mk, mv, prm, none);
+  int grid = G;
+  if (workspace && !partial) {
+    const SplitPlan sp = split_plan(tiles, (Sk + kBN - 1) / kBN, sms);
+    const size_t need = split_bytes(sp);
+    if (need > 0 && static_cast<uint64_t>(workspace_bytes) >= need) {
+      uint8_t* w = static_cast<uint8_t*>(workspace);
+      prm.full_rounds = sp.full_rounds;
+      prm.split_first = sp.split_first;
+      prm.split_f = sp.split_f;
+      prm.split_items = sp.split_items;
+      prm.ws_o = reinterpret_cast<float*>(w);
+      prm.ws_ml = reinterpret_cast<float*>(w + split_bytes_o(sp));
+      prm.ws_cnt = reinterpret_cast<unsigned int*>(w + split_bytes_o(sp) + split_bytes_ml(sp));
+      grid = sms;  // one part of a split tile for every CTA
+    }
+  }
+  launch_policy<false>(rescale_policy, grid, stream, mq, mk, mv, prm, none);
   return cudaGetLastError();
+}
+
+int64_t attention_workspace_bytes(int B, int H, int Sq, int Sk, bool causal) {
+  if (causal || B <= 0 || H <= 0 || Sq <= 0 || Sk <= 0) return 0;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return -1;
+  const long long tiles = static_cast<long long>((Sq + kBM - 1) / kBM) * B * H;
+  return static_cast<int64_t>(split_bytes(split_plan(tiles, (Sk + kBN - 1) / kBN, sms)));
 }
 
 }  // namespace oss

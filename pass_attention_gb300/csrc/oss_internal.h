@@ -21,16 +21,24 @@ struct RowsFault {
 
 // err_word: the device error word (the cluster-resident kernel records a
 // give-up on its bounded wait there); may be null.
+// ws (may be null, ws_bytes 0): a workspace of softmax_workspace_bytes()
+// bytes; with it, rows beyond the cluster path's 1.6 MB are read once from
+// HBM instead of twice.
 cudaError_t launch_softmax_rows(const float* x, float* y, float* m, float* l,
                                 int64_t rows, int64_t cols, int64_t ld_x, int64_t ld_y,
                                 float scale, unsigned int* err_word, const RowsFault& fault,
-                                cudaStream_t stream);
+                                void* ws, int64_t ws_bytes, cudaStream_t stream);
 
 // 16-bit rows: dtype 1 = bf16, 2 = fp16 (x and y); m, l fp32 or null.
 cudaError_t launch_softmax_rows16(const uint16_t* x, uint16_t* y, float* m, float* l,
                                   int64_t rows, int64_t cols, int64_t ld_x, int64_t ld_y,
                                   float scale, int dtype, unsigned int* err_word,
-                                  const RowsFault& fault, cudaStream_t stream);
+                                  const RowsFault& fault, void* ws, int64_t ws_bytes,
+                                  cudaStream_t stream);
+
+// Workspace the row softmax of rows of `row_bytes` bytes uses on the current
+// device (0: none; -1: the device could not be queried).
+int64_t softmax_workspace_bytes(int64_t row_bytes);
 
 // Comparators: passes = 2 (online (m, l) pass, then a write pass) or 3 (max
 // pass, sum pass, write pass); each pass re-reads x from HBM. m, l required.
@@ -69,12 +77,19 @@ struct AttnPartialOut {
 // Returns cudaErrorNotSupported for shapes the kernel does not cover. With
 // partial != nullptr the kernel writes partial states instead of o and lse.
 // rescale_policy: an os_rescale_policy value (0 threshold, 1 on rise, 2
-// every tile).
+// every tile). workspace (may be null): at least attention_workspace_bytes
+// bytes, counters zero; with it, a non-causal launch whose query tiles do not
+// fill the last round splits that round's tiles along the keys.
 cudaError_t launch_attention_fwd(const uint16_t* q, const uint16_t* k, const uint16_t* v,
                                  uint16_t* o, float* lse, int B, int H, int Sq, int Sk, int D,
                                  float scale, bool causal, unsigned int* err_word,
                                  const AttnFault& fault, const AttnPartialOut* partial,
-                                 int rescale_policy, cudaStream_t stream);
+                                 int rescale_policy, void* workspace, int64_t workspace_bytes,
+                                 cudaStream_t stream);
+
+// Workspace the attention forward of this shape uses on the current device
+// (0: none; -1: the device could not be queried).
+int64_t attention_workspace_bytes(int B, int H, int Sq, int Sk, bool causal);
 
 // log2(e) split into a float and the float nearest to the remainder, so that
 // hi + lo carries about 48 bits of it.

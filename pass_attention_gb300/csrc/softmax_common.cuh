@@ -536,6 +536,16 @@ bool cluster_rows(int kind, const void* x, void* y, float* m, float* l, int64_t 
                   int64_t ld_x, int64_t ld_y, const ScaleConsts& k, unsigned int* err,
                   const RowsFault& fault, cudaStream_t stream);
 
+// softmax_wide.cu: rows the cluster path does not hold (over 1.6 MB), a
+// group of rows at a time over the whole GPU (cooperative launch), slice
+// states merged at a grid barrier through the workspace `ws` (at least
+// wide_workspace_bytes() bytes); x is read once from HBM and once more from
+// L2. Returns false (launching nothing) without a workspace.
+bool wide_rows(int kind, const void* x, void* y, float* m, float* l, int64_t rows, int64_t cols,
+               int64_t ld_x, int64_t ld_y, const ScaleConsts& k, bool on_grid, void* ws,
+               int64_t ws_bytes, unsigned int* err, cudaStream_t stream);
+int64_t wide_workspace_bytes();
+
 // softmax_flat.cu: short rows (at most 512 bytes, or 1 KB off the 16-byte
 // grid; fp32 rows on the grid only where the grouped kernel would leave lanes
 // idle) of a matrix whose x rows lie back to back, tiles of whole rows staged

@@ -449,7 +449,8 @@ void launch_stream(Kernel kernel, const T* x, T* y, float* m, float* l, int64_t 
 // streamed.
 cudaError_t launch_softmax_rows(const float* x, float* y, float* m, float* l, int64_t rows,
                                 int64_t cols, int64_t ld_x, int64_t ld_y, float scale,
-                                unsigned int* err_word, const RowsFault& fault, cudaStream_t stream) {
+                                unsigned int* err_word, const RowsFault& fault, void* ws,
+                                int64_t ws_bytes, cudaStream_t stream) {
   const ScaleConsts k = make_consts(scale);
   if (flat_rows(0, x, y, m, l, rows, cols, ld_x, ld_y, k, err_word, fault, stream))
     return cudaGetLastError();
@@ -470,7 +471,9 @@ cudaError_t launch_softmax_rows(const float* x, float* y, float* m, float* l, in
     else
       softmax_rows_reg_kernel<16><<<grid_for(rows, 2), kThreads, 0, stream>>>(x, y, m, l, rows, c, ld_x, ld_y, k);
   } else if (!grouped_rows(0, x, y, m, l, rows, cols, ld_x, ld_y, k, on_grid, stream) &&
-             !cluster_rows(0, x, y, m, l, rows, cols, ld_x, ld_y, k, err_word, fault, stream)) {
+             !cluster_rows(0, x, y, m, l, rows, cols, ld_x, ld_y, k, err_word, fault, stream) &&
+             !wide_rows(0, x, y, m, l, rows, cols, ld_x, ld_y, k, on_grid, ws, ws_bytes, err_word,
+                        stream)) {
     if (on_grid)
       launch_stream(softmax_rows_stream_kernel<true>, x, y, m, l, rows, cols, ld_x, ld_y, k, 4, stream);
     else
@@ -484,7 +487,8 @@ namespace {
 template <int kType>
 void dispatch_rows16(const uint16_t* x, uint16_t* y, float* m, float* l, int64_t rows,
                      int64_t cols, int64_t ld_x, int64_t ld_y, const ScaleConsts& k,
-                     unsigned int* err_word, const RowsFault& fault, cudaStream_t stream) {
+                     unsigned int* err_word, const RowsFault& fault, void* ws, int64_t ws_bytes,
+                     cudaStream_t stream) {
   if (flat_rows(kType, x, y, m, l, rows, cols, ld_x, ld_y, k, err_word, fault, stream)) return;
   const bool on_grid = ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y)) & 15u) == 0 &&
                        (ld_x & 7) == 0 && (ld_y & 7) == 0;
@@ -493,7 +497,8 @@ void dispatch_rows16(const uint16_t* x, uint16_t* y, float* m, float* l, int64_t
     return;
   }
   if (grouped_rows(kType, x, y, m, l, rows, cols, ld_x, ld_y, k, on_grid, stream) ||
-      cluster_rows(kType, x, y, m, l, rows, cols, ld_x, ld_y, k, err_word, fault, stream))
+      cluster_rows(kType, x, y, m, l, rows, cols, ld_x, ld_y, k, err_word, fault, stream) ||
+      wide_rows(kType, x, y, m, l, rows, cols, ld_x, ld_y, k, on_grid, ws, ws_bytes, err_word, stream))
     return;
   // 16-byte accesses only for rows on the grid
   if (on_grid)
@@ -507,12 +512,13 @@ void dispatch_rows16(const uint16_t* x, uint16_t* y, float* m, float* l, int64_t
 cudaError_t launch_softmax_rows16(const uint16_t* x, uint16_t* y, float* m, float* l,
                                   int64_t rows, int64_t cols, int64_t ld_x, int64_t ld_y,
                                   float scale, int dtype, unsigned int* err_word,
-                                  const RowsFault& fault, cudaStream_t stream) {
+                                  const RowsFault& fault, void* ws, int64_t ws_bytes,
+                                  cudaStream_t stream) {
   const ScaleConsts k = make_consts(scale);
   if (dtype == 1)
-    dispatch_rows16<1>(x, y, m, l, rows, cols, ld_x, ld_y, k, err_word, fault, stream);
+    dispatch_rows16<1>(x, y, m, l, rows, cols, ld_x, ld_y, k, err_word, fault, ws, ws_bytes, stream);
   else
-    dispatch_rows16<2>(x, y, m, l, rows, cols, ld_x, ld_y, k, err_word, fault, stream);
+    dispatch_rows16<2>(x, y, m, l, rows, cols, ld_x, ld_y, k, err_word, fault, ws, ws_bytes, stream);
   return cudaGetLastError();
 }
 

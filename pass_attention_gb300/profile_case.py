@@ -5,6 +5,12 @@
     python -m pass_attention_gb300.profile_case multipass --passes 2|3 [--rows R --cols C]
     python -m pass_attention_gb300.profile_case attn [--B --H --S] [--causal] [--reps N]
     python -m pass_attention_gb300.profile_case decode [--B --H --Lmax --splits] [--reps N]
+    python -m pass_attention_gb300.profile_case merge [--B --H --Lmax --splits] [--reps N]
+
+``merge`` runs the split-KV decode once and then the merge ``--reps`` times on
+its partials: the merge's inputs are the decode's (B, H, splits) partial
+arrays, whose size does not depend on Lmax, so a short cache gives the same
+merge launch with little memory held.
 
 Inputs are the seeded synthetic ones of ``workloads``; every call is
 followed by a device synchronise, so a profiler filter such as
@@ -24,7 +30,7 @@ from pass_attention_gb300 import workloads
 
 def main(argv=None):
     ap = argparse.ArgumentParser()
-    ap.add_argument("case", choices=["softmax", "softmax16", "multipass", "attn", "decode"])
+    ap.add_argument("case", choices=["softmax", "softmax16", "multipass", "attn", "decode", "merge"])
     ap.add_argument("--passes", type=int, default=3)
     ap.add_argument("--rows", type=int, default=32768)
     ap.add_argument("--cols", type=int, default=8192)
@@ -64,6 +70,16 @@ def main(argv=None):
             oss.attention_fwd(q, k, v, 1.0 / math.sqrt(128), a.causal)
             torch.cuda.synchronize()
         oss.check_device_error()
+    elif a.case == "merge":
+        B, H = a.B or 64, a.H or 32
+        q, k, v, kv = workloads.decode_inputs(B, H, a.Lmax, 128, seed=4, device="cuda")
+        pm, pl, po = oss.attention_decode_splitkv(q, k, v, kv, a.splits)
+        del k, v
+        torch.cuda.synchronize()
+        o = torch.empty((B, H, 128), dtype=torch.bfloat16, device="cuda")
+        for _ in range(a.reps):
+            oss.merge_partials(pm, pl, po, finalize=True, o_out=o)
+            torch.cuda.synchronize()
     else:
         B, H = a.B or 8, a.H or 32
         q, k, v, kv = workloads.decode_inputs(B, H, a.Lmax, 128, seed=4, device="cuda")

@@ -225,3 +225,69 @@ def test_rescale_policy_is_per_thread():
     t.join()
     oss.set_rescale_policy("threshold")
     assert seen == ["threshold"]
+
+
+def _attn_no_split(q, k, v, scale):
+    """os_attention_fwd without a workspace (whole query tiles only)."""
+    import ctypes
+    B, H, Sq, D = q.shape
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, Sq), device=q.device)
+    st = oss.load().os_attention_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                     lse.data_ptr(), B, H, Sq, k.shape[2], D, ctypes.c_float(scale),
+                                     0, ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert st == 0
+    return o, lse
+
+
+@pytest.mark.parametrize("B,H,Sq,Sk", [
+    (1, 1, 1024, 4096),   # 8 query tiles: each cut into 8 parts of 4 KV tiles
+    (1, 2, 256, 129),     # 2 KV tiles, one key in the second: parts of one tile
+    (2, 3, 300, 200),     # 18 ragged query tiles, 2 parts each
+    (5, 16, 2000, 1000),  # 1280 tiles: 8 full rounds, then 64 tiles in 2 parts
+    (4, 16, 4096, 640),   # the attn_4k tile count with fewer keys: 72 tiles split in 2
+])
+def test_split_tail_matches_oracle_and_unsplit(B, H, Sq, Sk):
+    scale = 1.0 / math.sqrt(128)
+    q, k, v = workloads.qkv(B, H, Sq, Sk, 128, seed=B * 7 + Sq + Sk, device="cuda")
+    need = oss.attention_fwd_workspace_bytes(B, H, Sq, Sk)
+    assert need > 0, "this shape was chosen to take the split tail"
+    o, lse = oss.attention_fwd(q, k, v, scale)          # with the workspace
+    o1, lse1 = _attn_no_split(q, k, v, scale)
+    assert oss.check_device_error() == 0
+    # the split result differs from the unsplit one only by the rounding of
+    # the merge: lse within the tight bar of both, O within bf16 rounding
+    assert torch.allclose(lse, lse1, atol=1e-4, rtol=0)
+    assert (o.float() - o1.float()).abs().max().item() <= 2.0 ** -7 * (o1.float().abs().max().item() + 1e-3)
+    if B * H * Sq <= 4096:
+        check_all_rows(q, k, v, o, lse, scale, False, f"split {B}x{H}x{Sq}x{Sk}")
+    else:
+        rng = np.random.default_rng(Sq)
+        rows = list(zip(rng.integers(0, B, 2048), rng.integers(0, H, 2048), rng.integers(0, Sq, 2048)))
+        check_rows(q, k, v, o, lse, scale, False, rows, f"split {B}x{H}x{Sq}x{Sk}")
+    # every completed call leaves the workspace's counters at zero
+    sp = torch.cuda.current_stream().cuda_stream
+    ws = oss._WORKSPACES[(q.device.index, sp, "attn")]
+    torch.cuda.synchronize()
+    tiles = B * H * ((Sq + 127) // 128)
+    sms = torch.cuda.get_device_properties(q.device).multi_processor_count
+    tail = tiles - (tiles // sms) * sms
+    cnt = ws[need - tail * 8 * 4:need].view(torch.int32)
+    assert int(cnt.abs().sum().item()) == 0
+
+
+def test_split_tail_repeat_calls_identical():
+    # the merge runs over the parts in part order, whichever SM merges
+    q, k, v = workloads.qkv(2, 3, 640, 1500, 128, seed=21, device="cuda")
+    assert oss.attention_fwd_workspace_bytes(2, 3, 640, 1500) > 0
+    o1, l1 = oss.attention_fwd(q, k, v, 0.1)
+    o2, l2 = oss.attention_fwd(q, k, v, 0.1)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_no_workspace_for_causal_or_full_rounds():
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert oss.attention_fwd_workspace_bytes(1, 32, 16384, 16384, causal=True) == 0
+    # tiles that fill whole rounds: sms query tiles of 128 rows
+    assert oss.attention_fwd_workspace_bytes(1, sms, 128, 4096) == 0
