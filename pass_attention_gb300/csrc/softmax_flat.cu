@@ -24,6 +24,13 @@
 // instruction issue at half the copy peak for 16-bit rows. y is written in
 // 16-byte chunks when its rows have x's offsets, element by element
 // otherwise, so y needs neither x's alignment nor its leading dimension.
+// When y is laid out like x (the same offsets, rows back to back), a tile of
+// y is one byte range with x's alignment: the groups write their y chunks
+// into the tile's buffer in place of x (whole chunks as 16-byte stores; at a
+// row boundary a granule holds two rows, and each group writes only its own
+// elements) and one bulk copy sends the tile's whole granules out; only the
+// tile's partial first and last granules are stored element by element.
+// Rows off the 16-byte grid then cost no divergent per-element stores.
 // kKind: 0 = fp32, 1 = bf16, 2 = fp16.
 
 #include "softmax_common.cuh"
@@ -95,9 +102,25 @@ __device__ __forceinline__ void issue_tile(uintptr_t x0, uintptr_t x1, int64_t r
     *reinterpret_cast<uint4*>(buf + (last - ga)) = __ldg(reinterpret_cast<const uint4*>(last));
 }
 
+// y's elements [lo, hi) of the tile from the tile's buffer, element by
+// element (the partial granules at the ends of a tile of y).
+template <int kKind>
+__device__ __forceinline__ void store_elems_from(unsigned char* ybase, const unsigned char* bufbase,
+                                                 uintptr_t lo, uintptr_t hi) {
+  constexpr int kEsz = RowElem<kKind>::kSize;
+  for (uintptr_t a = lo; a < hi; a += kEsz) {
+    if (kEsz == 4)
+      *reinterpret_cast<uint32_t*>(ybase + a) = *reinterpret_cast<const uint32_t*>(bufbase + a);
+    else
+      *reinterpret_cast<uint16_t*>(ybase + a) = *reinterpret_cast<const uint16_t*>(bufbase + a);
+  }
+}
+
 // G threads per row, NV chunks each (a row spans at most G * NV chunks).
-// kYInStep: y's rows have x's offsets from the 16-byte grid.
-template <int kKind, int G, int NV, bool kYInStep>
+// kYInStep: y's rows have x's offsets from the 16-byte grid. kYBulk (with
+// kYInStep): y's rows also lie back to back, and tiles of y leave through the
+// buffers by bulk copies.
+template <int kKind, int G, int NV, bool kYInStep, bool kYBulk>
 __global__ void __launch_bounds__(kThreads, kFlMinBlocks)
 softmax_rows_flat_kernel(const void* __restrict__ x, void* __restrict__ y,
                          float* __restrict__ m_out, float* __restrict__ l_out, int64_t rows,
@@ -153,7 +176,7 @@ softmax_rows_flat_kernel(const void* __restrict__ x, void* __restrict__ y,
       pend &= ~(1u << b);  // landed, or given up on for good
     }
     par ^= 1u << b;
-    const unsigned char* buf = tile_bufs + b * buf_stride;
+    unsigned char* buf = tile_bufs + b * buf_stride;
     const int64_t r0 = tile * R;
     const int nr = static_cast<int>((rows - r0 < R) ? rows - r0 : R);
     const int head = static_cast<int>((x0 + static_cast<uintptr_t>(r0 * row_bytes)) & 15u);
@@ -165,7 +188,7 @@ softmax_rows_flat_kernel(const void* __restrict__ x, void* __restrict__ y,
       const bool active = i < nr;
       const int o = head + i * static_cast<int>(row_bytes);  // the row's byte offset in the buffer
       const int sp = (o & 15) / kEsz;                          // its offset from the grid, in elements
-      const uint4* rg = reinterpret_cast<const uint4*>(buf + (o & ~15));
+      uint4* rg = reinterpret_cast<uint4*>(buf + (o & ~15));
       const int nch = (cols + sp + kEpc - 1) / kEpc;
       float2 w[NV][kEpc / 2];
 #pragma unroll
@@ -214,7 +237,29 @@ softmax_rows_flat_kernel(const void* __restrict__ x, void* __restrict__ y,
         for (int v = 0; v < NV; ++v) {
           const int c = t + v * G;
           if (c < nch) {
-            if constexpr (kYInStep) {
+            if constexpr (kYBulk) {
+              // y in place of x: whole chunks at once, a chunk shared with a
+              // neighbouring row element by element (this row's elements only)
+              const uint4 ov = pack_chunk16<kKind>(w[v], f2);
+              const int first = c * kEpc - sp;
+              if (first >= 0 && first + kEpc <= cols) {
+                rg[c] = ov;
+              } else {
+                const uint32_t wd[4] = {ov.x, ov.y, ov.z, ov.w};
+                unsigned char* gp = reinterpret_cast<unsigned char*>(rg + c);
+#pragma unroll
+                for (int e = 0; e < kEpc; ++e) {
+                  const int j = first + e;
+                  if (j >= 0 && j < cols) {
+                    if (kKind == 0)
+                      reinterpret_cast<uint32_t*>(gp)[e] = wd[e];
+                    else
+                      reinterpret_cast<uint16_t*>(gp)[e] =
+                          static_cast<uint16_t>((e & 1) ? (wd[e >> 1] >> 16) : (wd[e >> 1] & 0xffffu));
+                  }
+                }
+              }
+            } else if constexpr (kYInStep) {
               store_chunk16<kKind>(reinterpret_cast<char*>(yr), c, cols, sp, pack_chunk16<kKind>(w[v], f2));
             } else {
 #pragma unroll
@@ -230,10 +275,40 @@ softmax_rows_flat_kernel(const void* __restrict__ x, void* __restrict__ y,
       }
     }
 
-    __syncthreads();  // buffer b is read out
+    if constexpr (kYBulk) {
+      // this thread's y writes into the buffer, before the copy reads them
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    __syncthreads();  // buffer b is read out (and, kYBulk, holds the tile's y)
+    if constexpr (kYBulk) {
+      if (tid == 0) {
+        // y's tile [ys, ye): the buffer's byte 0 is the granule of ys
+        const uintptr_t ys = reinterpret_cast<uintptr_t>(y) + static_cast<uintptr_t>(r0 * row_bytes);
+        const uintptr_t ye = ys + static_cast<uintptr_t>(nr * row_bytes);
+        const uintptr_t g0 = ys & ~uintptr_t(15);
+        const uintptr_t a0 = (ys + 15) & ~uintptr_t(15);
+        const uintptr_t a1 = ye & ~uintptr_t(15);
+        unsigned char* ybase = reinterpret_cast<unsigned char*>(g0);
+        if (a1 > a0) {
+          asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(a0),
+                       "r"(smem_u32(buf) + static_cast<uint32_t>(a0 - g0)),
+                       "r"(static_cast<uint32_t>(a1 - a0))
+                       : "memory");
+          asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+          // the partial granules at the ends: this tile's elements only (the
+          // rest of each belongs to the neighbouring tile)
+          store_elems_from<kKind>(ybase, buf, ys - g0, a0 - g0);
+          store_elems_from<kKind>(ybase, buf, a1 - g0, ye - g0);
+        } else {
+          store_elems_from<kKind>(ybase, buf, ys - g0, ye - g0);
+        }
+      }
+    }
     const int64_t next = tile + static_cast<int64_t>(kFlBufs) * gridDim.x;
     if (tid == 0 && live && next < tiles) {
       unsigned char* nbuf = tile_bufs + b * buf_stride;
+      // the bulk copy of y out of this buffer has read it
+      if constexpr (kYBulk) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
       issue_tile(x0, x1, row_bytes, R, rows, next, nbuf, smem_u32(nbuf), bar_a, 0u);
       pend |= 1u << b;
       ppar = (ppar & ~(1u << b)) | (par & (1u << b));
@@ -244,12 +319,15 @@ softmax_rows_flat_kernel(const void* __restrict__ x, void* __restrict__ y,
   if (tid == 0)
     for (int c = 0; c < kFlBufs; ++c)
       if ((pend >> c) & 1u) mbar_wait_bounded(smem_u32(&bars[c]), (ppar >> c) & 1u, err, timeout_ns);
+  // the bulk copies of y are complete before the CTA ends
+  if constexpr (kYBulk)
+    if (tid == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
 // Tiles of up to kFlTileBytes (fewer rows per tile when the matrix would
 // not give every CTA of one wave a tile), one wave of kFlMinBlocks CTAs per
 // SM, each walking its tiles.
-template <int kKind, int G, bool kYInStep>
+template <int kKind, int G, bool kYInStep, bool kYBulk>
 void launch_flat(const void* x, void* y, float* m, float* l, int64_t rows, int64_t cols,
                  int64_t ld_y, const ScaleConsts& k, unsigned int* err, const RowsFault& fault,
                  cudaStream_t stream) {
@@ -264,28 +342,28 @@ void launch_flat(const void* x, void* y, float* m, float* l, int64_t rows, int64
   const int stride = static_cast<int>((R * row_bytes + 32 + 127) / 128 * 128);
   const int grid = static_cast<int>(tiles < cap ? tiles : cap);
   const uint64_t timeout = fault.timeout_ns > 0 ? static_cast<uint64_t>(fault.timeout_ns) : kClTimeoutNs;
-  softmax_rows_flat_kernel<kKind, G, kFlNv, kYInStep>
+  softmax_rows_flat_kernel<kKind, G, kFlNv, kYInStep, kYBulk>
       <<<grid, kThreads, static_cast<size_t>(stride) * kFlBufs, stream>>>(
           x, y, m, l, rows, static_cast<int>(cols), ld_y, k, R, tiles, stride, err, fault.extra_tx,
           timeout);
 }
 
-template <int kKind, bool kYInStep>
+template <int kKind, bool kYInStep, bool kYBulk>
 void launch_flat_g(int64_t chunks, const void* x, void* y, float* m, float* l, int64_t rows,
                    int64_t cols, int64_t ld_y, const ScaleConsts& k, unsigned int* err,
                    const RowsFault& fault, cudaStream_t stream) {
   if (chunks <= kFlNv)
-    launch_flat<kKind, 1, kYInStep>(x, y, m, l, rows, cols, ld_y, k, err, fault, stream);
+    launch_flat<kKind, 1, kYInStep, kYBulk>(x, y, m, l, rows, cols, ld_y, k, err, fault, stream);
   else if (chunks <= 2 * kFlNv)
-    launch_flat<kKind, 2, kYInStep>(x, y, m, l, rows, cols, ld_y, k, err, fault, stream);
+    launch_flat<kKind, 2, kYInStep, kYBulk>(x, y, m, l, rows, cols, ld_y, k, err, fault, stream);
   else if (chunks <= 4 * kFlNv)
-    launch_flat<kKind, 4, kYInStep>(x, y, m, l, rows, cols, ld_y, k, err, fault, stream);
+    launch_flat<kKind, 4, kYInStep, kYBulk>(x, y, m, l, rows, cols, ld_y, k, err, fault, stream);
   else if (chunks <= 8 * kFlNv)
-    launch_flat<kKind, 8, kYInStep>(x, y, m, l, rows, cols, ld_y, k, err, fault, stream);
+    launch_flat<kKind, 8, kYInStep, kYBulk>(x, y, m, l, rows, cols, ld_y, k, err, fault, stream);
   else if (chunks <= 16 * kFlNv)
-    launch_flat<kKind, 16, kYInStep>(x, y, m, l, rows, cols, ld_y, k, err, fault, stream);
+    launch_flat<kKind, 16, kYInStep, kYBulk>(x, y, m, l, rows, cols, ld_y, k, err, fault, stream);
   else
-    launch_flat<kKind, 32, kYInStep>(x, y, m, l, rows, cols, ld_y, k, err, fault, stream);
+    launch_flat<kKind, 32, kYInStep, kYBulk>(x, y, m, l, rows, cols, ld_y, k, err, fault, stream);
 }
 
 template <int kKind>
@@ -320,10 +398,16 @@ bool flat_rows_as(const void* x, void* y, float* m, float* l, int64_t rows, int6
   const int s0 = static_cast<int>((reinterpret_cast<uintptr_t>(x) & 15u) / kEsz);
   const int smax = ((cols * kEsz) % 16 == 0 || rows == 1) ? s0 : kEpc - 1;
   const int64_t chunks = (cols + smax + kEpc - 1) / kEpc;
-  if (same_phase(x, y, cols, ld_y, kEsz))
-    launch_flat_g<kKind, true>(chunks, x, y, m, l, rows, cols, ld_y, k, err, fault, stream);
+  // y laid out like x, rows back to back: tiles of y leave by bulk copies
+  // when its rows are off the 16-byte grid (on the grid every chunk is whole
+  // and goes out as one 16-byte store already)
+  const bool y_like_x = ld_y == cols && ((reinterpret_cast<uintptr_t>(x) ^ reinterpret_cast<uintptr_t>(y)) & 15u) == 0;
+  if (y_like_x && !grid_rows)
+    launch_flat_g<kKind, true, true>(chunks, x, y, m, l, rows, cols, ld_y, k, err, fault, stream);
+  else if (same_phase(x, y, cols, ld_y, kEsz))
+    launch_flat_g<kKind, true, false>(chunks, x, y, m, l, rows, cols, ld_y, k, err, fault, stream);
   else
-    launch_flat_g<kKind, false>(chunks, x, y, m, l, rows, cols, ld_y, k, err, fault, stream);
+    launch_flat_g<kKind, false, false>(chunks, x, y, m, l, rows, cols, ld_y, k, err, fault, stream);
   return true;
 }
 

@@ -159,3 +159,25 @@ def test_repeat_identical():
     b = oss.softmax_rows_16bit(x, 1.0)
     torch.cuda.synchronize()
     assert all(torch.equal(p, q) for p, q in zip(a, b))
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16, torch.float16])
+@pytest.mark.parametrize("cols", [3, 7, 33, 100, 101, 255, 300])
+@pytest.mark.parametrize("off", [1, 3, 5])
+def test_y_like_x_tiles_leave_by_bulk_copies(dtype, cols, off):
+    # x and y at the same offset from the 16-byte grid, rows back to back, row
+    # lengths off the grid: tiles of y leave through shared memory by bulk
+    # copies, and the granules where two tiles meet are shared by two CTAs
+    # (each stores its own elements); the canaries around y stay intact
+    esz = torch.tensor([], dtype=dtype).element_size()
+    if dtype == torch.float32 and cols * esz > 1024:
+        pytest.skip("longer than the staged rows")
+    rows = max(7, min(120001, 2_000_000 // cols))
+    x, _ = dense_at(rows, cols, dtype, off, seed=cols * 3 + off)
+    ybuf = torch.full((rows * cols + off + 16,), 7.0, dtype=dtype, device="cuda")
+    y = ybuf[off:off + rows * cols].view(rows, cols)
+    if off == 5:
+        x = masked(x, cols)
+    y, m, l = run(x, 0.8, y)
+    check(x, y, m, l, 0.8, f"{dtype} {rows}x{cols} y like x +{off}")
+    assert bool((ybuf[:off] == 7.0).all()) and bool((ybuf[off + rows * cols:] == 7.0).all())
