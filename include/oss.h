@@ -270,6 +270,41 @@ OSS_API os_status os_attention_fwd_ws(const os_bf16* q, const os_bf16* k, const 
                                       void* workspace, int64_t workspace_bytes, void* stream);
 
 /*
+ * os_attention_fwd_noalloc -- os_attention_fwd_ws for callers that cannot
+ * allocate device memory. The online-softmax pages this library follows have
+ * no counterpart to this call: it exists because some callers cannot hand
+ * over a workspace, such as a plugin that its host framework gives only the
+ * input and output buffers while the framework's own pool owns the rest of
+ * device memory, or a latency-critical thread that must not call cudaMalloc
+ * (which can block and synchronise the device).
+ *
+ * The split tail's workspace comes from a fixed 16 MiB array in device
+ * memory that the library declares statically; every GPU that loads the
+ * library holds those 16 MiB until the process exits. The call itself
+ * allocates nothing (no cudaMalloc, no cudaFree, no allocating library
+ * routine). The first call on a device looks up the array's device address
+ * on that device (cudaGetSymbolAddress, once per device); make that first
+ * call before any stream capture.
+ *
+ * Arguments, layout, outputs and tolerance are os_attention_fwd's; the
+ * caller still owns and passes q, k, v, o and lse. Every call clears the
+ * counters it needs at zero (an asynchronous memset on `stream`), so the
+ * array's leftover contents from an earlier call, even one that timed out,
+ * do no harm. All calls on a device share the one array: calls whose work
+ * overlaps on the GPU (other streams, other threads) race on it and give
+ * wrong results, so order them on one stream or with events.
+ *
+ * Errors: those of os_attention_fwd; OS_ERR_UNSUPPORTED also when the shape
+ * needs more than the 16 MiB array holds (the split tail takes about 68 KB
+ * per SM, 10.4 MB on a GPU with 152 SMs); OS_ERR_CUDA when the device or the
+ * array's address cannot be queried.
+ */
+OSS_API os_status os_attention_fwd_noalloc(const os_bf16* q, const os_bf16* k, const os_bf16* v,
+                                           os_bf16* o, float* lse, int32_t B, int32_t H,
+                                           int32_t Sq, int32_t Sk, int32_t D, float scale,
+                                           int causal, void* stream);
+
+/*
  * Rescale policies of the attention forward: when a tile raises a row's
  * maximum, the running sum l and the accumulator O are multiplied by
  * exp(m_old - m_new) (metalworking "Online Softmax", the five-line

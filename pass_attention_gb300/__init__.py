@@ -76,6 +76,8 @@ _SIGNATURES = {
     "os_attention_fwd_ws": (_i32, [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _f32,
                                    ctypes.c_int, _vp, _i64, _vp]),
     "os_attention_fwd_workspace_bytes": (_i64, [_i32, _i32, _i32, _i32, _i32, ctypes.c_int]),
+    "os_attention_fwd_noalloc": (_i32, [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32,
+                                        _f32, ctypes.c_int, _vp]),
     "os_attention_fwd_partial": (_i32, [_vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _f32,
                                         ctypes.c_int, _vp, _vp, _vp, _i32, _i32, _vp]),
     "os_attention_decode_splitkv": (_i32, [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32,

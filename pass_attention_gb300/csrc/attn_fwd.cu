@@ -1416,6 +1416,19 @@ cudaError_t launch_attention_fwd(const uint16_t* q, const uint16_t* k, const uin
   return cudaGetLastError();
 }
 
+int64_t attention_workspace_counters(int B, int H, int Sq, int Sk, bool causal, int64_t* bytes) {
+  *bytes = 0;
+  if (causal || B <= 0 || H <= 0 || Sq <= 0 || Sk <= 0) return 0;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return -1;
+  const long long tiles = static_cast<long long>((Sq + kBM - 1) / kBM) * B * H;
+  const SplitPlan sp = split_plan(tiles, (Sk + kBN - 1) / kBN, sms);
+  if (sp.split_f >= 2) *bytes = static_cast<int64_t>(sp.tail) * kSoftWarps * sizeof(unsigned int);
+  return 0;
+}
+
 int64_t attention_workspace_bytes(int B, int H, int Sq, int Sk, bool causal) {
   if (causal || B <= 0 || H <= 0 || Sq <= 0 || Sk <= 0) return 0;
   int dev = 0, sms = 0;

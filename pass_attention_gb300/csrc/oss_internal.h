@@ -91,6 +91,10 @@ cudaError_t launch_attention_fwd(const uint16_t* q, const uint16_t* k, const uin
 // (0: none; -1: the device could not be queried).
 int64_t attention_workspace_bytes(int B, int H, int Sq, int Sk, bool causal);
 
+// Bytes of per-tile counters at the end of that workspace (*bytes; 0 when it
+// uses none). Returns -1 when the device could not be queried, else 0.
+int64_t attention_workspace_counters(int B, int H, int Sq, int Sk, bool causal, int64_t* bytes);
+
 // log2(e) split into a float and the float nearest to the remainder, so that
 // hi + lo carries about 48 bits of it.
 void split_constant(double c, float* hi, float* lo);
