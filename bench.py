@@ -53,39 +53,44 @@ NOMINAL = {"hbm_gbs": 7900.0, "bf16_tflops": 2250.0}
 # blank lines removed) when it was captured: changed code reports null. Summaries live under profiles/.
 # "scale" records traffic / algorithmic bytes of a smaller capture of the
 # same kernel, applied to the full launch's algorithmic bytes.
+_SRC_COMMON = ["pass_attention_gb300/csrc/softmax_common.cuh",
+               "pass_attention_gb300/csrc/device_common.cuh"]
+_SRC_ROWS = ["pass_attention_gb300/csrc/softmax_rows.cu"] + _SRC_COMMON
+_SRC_GROUPED = ["pass_attention_gb300/csrc/softmax_grouped.cu"] + _SRC_COMMON
+_SRC_WIDE = ["pass_attention_gb300/csrc/softmax_wide.cu"] + _SRC_COMMON
 NCU_TRAFFIC = {
-    "softmax_32k": {"source": ["pass_attention_gb300/csrc/softmax_rows.cu",
-                               "pass_attention_gb300/csrc/softmax_common.cuh",
-                               "pass_attention_gb300/csrc/device_common.cuh"],
-                    "sha256": "d6ab156378bb084b00f8097ee95196522d4816301b57b1e3996e7114249e689f",
-                    "bytes_per_launch": 1073788928 + 1017820672},
-    "softmax_32k_bf16": {"source": ["pass_attention_gb300/csrc/softmax_grouped.cu",
-                                    "pass_attention_gb300/csrc/softmax_common.cuh",
-                                    "pass_attention_gb300/csrc/device_common.cuh"],
-                         "sha256": "1a829292f655eb21936a73ffa719c786c112e04d568c54e216215a59e249123e",
-                         "bytes_per_launch": 536894976 + 484324864},
+    "softmax_32k": {"source": _SRC_ROWS,
+                    "sha256": "73995524e85db31d7c3bf8d58cf01f5782d07ad3a36db8fe5429e33fcd182570",
+                    "bytes_per_launch": 1073778688 + 1017928448},
+    "softmax_32k_bf16": {"source": _SRC_GROUPED,
+                         "sha256": "bf6578f2881c77b13dca4a2fed113a752c6b6bb837750b1a704b7cc421b4cf9d",
+                         "bytes_per_launch": 536895744 + 484455424},
     # the comparators: all sweeps of one call (each reads x from DRAM again)
-    "softmax_32k_3pass": {"source": ["pass_attention_gb300/csrc/softmax_rows.cu",
-                                     "pass_attention_gb300/csrc/softmax_common.cuh",
-                                     "pass_attention_gb300/csrc/device_common.cuh"],
-                          "sha256": "d6ab156378bb084b00f8097ee95196522d4816301b57b1e3996e7114249e689f",
-                          "bytes_per_launch": (1073785856 + 2573568) + (1073987840 + 212736)
-                          + (1074051328 + 1024907520)},
-    "softmax_32k_2pass": {"source": ["pass_attention_gb300/csrc/softmax_rows.cu",
-                                     "pass_attention_gb300/csrc/softmax_common.cuh",
-                                     "pass_attention_gb300/csrc/device_common.cuh"],
-                          "sha256": "d6ab156378bb084b00f8097ee95196522d4816301b57b1e3996e7114249e689f",
-                          "bytes_per_launch": (1073761280 + 3418112) + (1074050816 + 1025053952)},
+    "softmax_32k_3pass": {"source": _SRC_ROWS,
+                          "sha256": "73995524e85db31d7c3bf8d58cf01f5782d07ad3a36db8fe5429e33fcd182570",
+                          "bytes_per_launch": (1073760768 + 2916608) + (1073907712 + 246528)
+                          + (1074052608 + 1024674048)},
+    "softmax_32k_2pass": {"source": _SRC_ROWS,
+                          "sha256": "73995524e85db31d7c3bf8d58cf01f5782d07ad3a36db8fe5429e33fcd182570",
+                          "bytes_per_launch": (1073760000 + 2976000) + (1074086656 + 1024858624)},
+    # rows over 1.6 MB, the cooperative kernel (one read from HBM, one from L2)
+    "softmax_64x4m_fp32": {"source": _SRC_WIDE,
+                           "sha256": "000a531d0350e02d4b200d688b0f4d30451417e78868412d770f4d6aa58b0d5b",
+                           "bytes_per_launch": 1101548800 + 1013168896},
+    "softmax_64x4m_bf16": {"source": _SRC_WIDE,
+                           "sha256": "000a531d0350e02d4b200d688b0f4d30451417e78868412d770f4d6aa58b0d5b",
+                           "bytes_per_launch": 548189696 + 476873472},
     "attn_4k": {"source": "pass_attention_gb300/csrc/attn_fwd.cu",
-                "sha256": "1de91f1a14f7b69059f99bd37628b4126df733c28a5f205b034826a15235ccec",
-                "bytes_per_launch": 201502976 + 47736320},
+                "sha256": "1be6e0f202facc625839827f2a87382ddd1d773a7096bf3895c42b0e52cfff77",
+                "bytes_per_launch": 201534464 + 49693952},
     "attn_causal": {"source": "pass_attention_gb300/csrc/attn_fwd.cu",
-                    "sha256": "1de91f1a14f7b69059f99bd37628b4126df733c28a5f205b034826a15235ccec",
-                    "bytes_per_launch": 406748672 + 119554048},
+                    "sha256": "1be6e0f202facc625839827f2a87382ddd1d773a7096bf3895c42b0e52cfff77",
+                    "bytes_per_launch": 405638400 + 119282688},
     "decode_64x32": {"source": "pass_attention_gb300/csrc/decode_merge.cu",
                      "sha256": "0d345bb183c174c3248d68638b3899f9499e35b1a5ceb04884c68dbc28755393",
-                     "scale": (2484805000 + 4145664) / (151653 * 32 * 512 + 8 * 32 * 128 * 2
-                                                         + 8 * 32 * 16 * 130 * 4)},
+                     # B 8, H 32, Lmax 8192 (kv_len sum 36965), 16 splits
+                     "scale": (605719552 + 3959040) / (36965 * 32 * 512 + 8 * 32 * 128 * 2
+                                                       + 8 * 32 * 16 * 130 * 4)},
 }
 
 
