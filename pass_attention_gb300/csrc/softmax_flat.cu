@@ -43,7 +43,8 @@ constexpr int kFlMinBlocks = 4;             // CTAs per SM
 constexpr int64_t kFlTileBytes = 14 << 10;  // x bytes per tile, at most
 constexpr int64_t kFlMaxRowBytes = 1024;    // the longest row taken
 constexpr int64_t kFlGridRowBytes = 512;    // the longest taken when every row is on the grid
-constexpr int kFlNv = 4;                    // 16-byte chunks a thread holds
+constexpr int kFlNvA = 4;                   // 16-byte chunks a thread holds: 4 or 6
+constexpr int kFlNvB = 6;
 
 template <int kKind>
 __device__ __forceinline__ void flat_store(unsigned char* yr, int j, float v) {
@@ -121,7 +122,7 @@ __device__ __forceinline__ void store_elems_from(unsigned char* ybase, const uns
 // kYInStep): y's rows also lie back to back, and tiles of y leave through the
 // buffers by bulk copies.
 template <int kKind, int G, int NV, bool kYInStep, bool kYBulk>
-__global__ void __launch_bounds__(kThreads, kFlMinBlocks)
+__global__ void __launch_bounds__(kThreads, (NV > kFlNvA) ? kFlMinBlocks - 1 : kFlMinBlocks)
 softmax_rows_flat_kernel(const void* __restrict__ x, void* __restrict__ y,
                          float* __restrict__ m_out, float* __restrict__ l_out, int64_t rows,
                          int cols, int64_t ld_y, ScaleConsts k, int64_t R, int64_t tiles,
@@ -327,13 +328,13 @@ softmax_rows_flat_kernel(const void* __restrict__ x, void* __restrict__ y,
 // Tiles of up to kFlTileBytes (fewer rows per tile when the matrix would
 // not give every CTA of one wave a tile), one wave of kFlMinBlocks CTAs per
 // SM, each walking its tiles.
-template <int kKind, int G, bool kYInStep, bool kYBulk>
+template <int kKind, int G, int NV, bool kYInStep, bool kYBulk>
 void launch_flat(const void* x, void* y, float* m, float* l, int64_t rows, int64_t cols,
                  int64_t ld_y, const ScaleConsts& k, unsigned int* err, const RowsFault& fault,
                  cudaStream_t stream) {
   constexpr int kEsz = RowElem<kKind>::kSize;
   const int64_t row_bytes = cols * kEsz;
-  const int64_t cap = static_cast<int64_t>(sm_count()) * kFlMinBlocks;
+  const int64_t cap = static_cast<int64_t>(sm_count()) * ((NV > kFlNvA) ? kFlMinBlocks - 1 : kFlMinBlocks);
   int64_t R = kFlTileBytes / row_bytes;
   const int64_t spread = (rows + cap - 1) / cap;
   if (R > spread) R = spread;
@@ -342,28 +343,53 @@ void launch_flat(const void* x, void* y, float* m, float* l, int64_t rows, int64
   const int stride = static_cast<int>((R * row_bytes + 32 + 127) / 128 * 128);
   const int grid = static_cast<int>(tiles < cap ? tiles : cap);
   const uint64_t timeout = fault.timeout_ns > 0 ? static_cast<uint64_t>(fault.timeout_ns) : kClTimeoutNs;
-  softmax_rows_flat_kernel<kKind, G, kFlNv, kYInStep, kYBulk>
+  softmax_rows_flat_kernel<kKind, G, NV, kYInStep, kYBulk>
       <<<grid, kThreads, static_cast<size_t>(stride) * kFlBufs, stream>>>(
           x, y, m, l, rows, static_cast<int>(cols), ld_y, k, R, tiles, stride, err, fault.extra_tx,
           timeout);
 }
 
+template <int kKind, int NV, bool kYInStep, bool kYBulk>
+void launch_flat_nv(int G, const void* x, void* y, float* m, float* l, int64_t rows, int64_t cols,
+                    int64_t ld_y, const ScaleConsts& k, unsigned int* err, const RowsFault& fault,
+                    cudaStream_t stream) {
+  switch (G) {
+    case 1: launch_flat<kKind, 1, NV, kYInStep, kYBulk>(x, y, m, l, rows, cols, ld_y, k, err, fault, stream); break;
+    case 2: launch_flat<kKind, 2, NV, kYInStep, kYBulk>(x, y, m, l, rows, cols, ld_y, k, err, fault, stream); break;
+    case 4: launch_flat<kKind, 4, NV, kYInStep, kYBulk>(x, y, m, l, rows, cols, ld_y, k, err, fault, stream); break;
+    case 8: launch_flat<kKind, 8, NV, kYInStep, kYBulk>(x, y, m, l, rows, cols, ld_y, k, err, fault, stream); break;
+    case 16: launch_flat<kKind, 16, NV, kYInStep, kYBulk>(x, y, m, l, rows, cols, ld_y, k, err, fault, stream); break;
+    default: launch_flat<kKind, 32, NV, kYInStep, kYBulk>(x, y, m, l, rows, cols, ld_y, k, err, fault, stream); break;
+  }
+}
+
+// The group for a row spanning `chunks` 16-byte chunks: G threads of NV
+// chunks each (G a power of two up to 32, NV 4 or 6), the pair whose G * NV
+// slots leave the fewest unused, then the one with fewer threads a row (the
+// per-row work -- the group's shuffles, the scale factor, m and l -- is
+// repeated by each of its threads).
 template <int kKind, bool kYInStep, bool kYBulk>
 void launch_flat_g(int64_t chunks, const void* x, void* y, float* m, float* l, int64_t rows,
                    int64_t cols, int64_t ld_y, const ScaleConsts& k, unsigned int* err,
                    const RowsFault& fault, cudaStream_t stream) {
-  if (chunks <= kFlNv)
-    launch_flat<kKind, 1, kYInStep, kYBulk>(x, y, m, l, rows, cols, ld_y, k, err, fault, stream);
-  else if (chunks <= 2 * kFlNv)
-    launch_flat<kKind, 2, kYInStep, kYBulk>(x, y, m, l, rows, cols, ld_y, k, err, fault, stream);
-  else if (chunks <= 4 * kFlNv)
-    launch_flat<kKind, 4, kYInStep, kYBulk>(x, y, m, l, rows, cols, ld_y, k, err, fault, stream);
-  else if (chunks <= 8 * kFlNv)
-    launch_flat<kKind, 8, kYInStep, kYBulk>(x, y, m, l, rows, cols, ld_y, k, err, fault, stream);
-  else if (chunks <= 16 * kFlNv)
-    launch_flat<kKind, 16, kYInStep, kYBulk>(x, y, m, l, rows, cols, ld_y, k, err, fault, stream);
+  int best_g = 32, best_nv = kFlNvA;
+  int64_t best_waste = -1;
+  for (int g = 1; g <= 32; g *= 2) {
+    for (int nv : {kFlNvA, kFlNvB}) {
+      const int64_t slots = static_cast<int64_t>(g) * nv;
+      if (slots < chunks) continue;
+      const int64_t waste = slots - chunks;
+      if (best_waste < 0 || waste < best_waste || (waste == best_waste && g < best_g)) {
+        best_waste = waste;
+        best_g = g;
+        best_nv = nv;
+      }
+    }
+  }
+  if (best_nv == kFlNvA)
+    launch_flat_nv<kKind, kFlNvA, kYInStep, kYBulk>(best_g, x, y, m, l, rows, cols, ld_y, k, err, fault, stream);
   else
-    launch_flat<kKind, 32, kYInStep, kYBulk>(x, y, m, l, rows, cols, ld_y, k, err, fault, stream);
+    launch_flat_nv<kKind, kFlNvB, kYInStep, kYBulk>(best_g, x, y, m, l, rows, cols, ld_y, k, err, fault, stream);
 }
 
 template <int kKind>
