@@ -75,11 +75,11 @@ NCU_TRAFFIC = {
                           "bytes_per_launch": (1073760000 + 2976000) + (1074086656 + 1024858624)},
     # rows over 1.6 MB, the cooperative kernel (one read from HBM, one from L2)
     "softmax_64x4m_fp32": {"source": _SRC_WIDE,
-                           "sha256": "000a531d0350e02d4b200d688b0f4d30451417e78868412d770f4d6aa58b0d5b",
-                           "bytes_per_launch": 1101548800 + 1013168896},
+                           "sha256": "9abfeac38fb9931ea4f304e1c199c04d026e43d90bd0e247fea097ca74f14fc8",
+                           "bytes_per_launch": 1289380608 + 1013640960},
     "softmax_64x4m_bf16": {"source": _SRC_WIDE,
-                           "sha256": "000a531d0350e02d4b200d688b0f4d30451417e78868412d770f4d6aa58b0d5b",
-                           "bytes_per_launch": 548189696 + 476873472},
+                           "sha256": "9abfeac38fb9931ea4f304e1c199c04d026e43d90bd0e247fea097ca74f14fc8",
+                           "bytes_per_launch": 633526272 + 478089472},
     "attn_4k": {"source": "pass_attention_gb300/csrc/attn_fwd.cu",
                 "sha256": "1be6e0f202facc625839827f2a87382ddd1d773a7096bf3895c42b0e52cfff77",
                 "bytes_per_launch": 201534464 + 49693952},

@@ -26,7 +26,7 @@
 namespace oss {
 namespace {
 
-constexpr int64_t kWideL2Budget = int64_t(48) << 20;        // bytes of x a group may hold
+constexpr int64_t kWideL2Budget = int64_t(64) << 20;        // bytes of x a group may hold
 constexpr unsigned long long kWideTimeoutNs = 2000000000ull;  // wait at the grid barrier
 constexpr int kWideCtasPerSm = 8;
 constexpr int kWideUnroll = 4;  // 16-byte chunks each thread has in flight

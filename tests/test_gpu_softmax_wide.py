@@ -36,7 +36,7 @@ def no_workspace(x, scale):
 
 
 @pytest.mark.parametrize("rows,cols", [
-    (7, 1 << 21),      # 8 MB rows: six to a group, the second group has one live row
+    (9, 1 << 21),      # 8 MB rows: eight to a group, the second group has one live row
     (1, 3_000_001),    # one row, ragged last chunk
     (40, 500_000),     # 2 MB rows, several groups
     (3, 409_601),      # just beyond the cluster path
