@@ -33,6 +33,8 @@
 // Rows off the 16-byte grid then cost no divergent per-element stores.
 // kKind: 0 = fp32, 1 = bf16, 2 = fp16.
 
+#include <atomic>
+
 #include "softmax_common.cuh"
 
 namespace oss {
@@ -43,8 +45,9 @@ constexpr int kFlMinBlocks = 4;             // CTAs per SM
 constexpr int64_t kFlTileBytes = 14 << 10;  // x bytes per tile, at most
 constexpr int64_t kFlMaxRowBytes = 1024;    // the longest row taken
 constexpr int64_t kFlGridRowBytes = 512;    // the longest taken when every row is on the grid
-constexpr int kFlNvA = 4;                   // 16-byte chunks a thread holds: 4 or 6
-constexpr int kFlNvB = 6;
+constexpr int kFlNvA = 4;                   // 16-byte chunks a thread holds: 4 or 6,
+constexpr int kFlNvB = 6;                   // or 8 for 16-bit rows on the grid that fill
+constexpr int kFlNvC = 8;                   // groups of 2 or 4 threads exactly
 
 template <int kKind>
 __device__ __forceinline__ void flat_store(unsigned char* yr, int j, float v) {
@@ -121,8 +124,14 @@ __device__ __forceinline__ void store_elems_from(unsigned char* ybase, const uns
 // kYInStep: y's rows have x's offsets from the 16-byte grid. kYBulk (with
 // kYInStep): y's rows also lie back to back, and tiles of y leave through the
 // buffers by bulk copies.
+// CTAs per SM for NV chunks a thread (the registers they need) and the
+// x bytes a tile holds (eight-chunk kernels take twice the tile, to keep as
+// many bytes in flight per SM with half the CTAs).
+constexpr int flat_blocks(int nv) { return nv > kFlNvB ? kFlMinBlocks - 2 : nv > kFlNvA ? kFlMinBlocks - 1 : kFlMinBlocks; }
+constexpr int64_t flat_tile_bytes(int nv) { return nv > kFlNvB ? 2 * kFlTileBytes : kFlTileBytes; }
+
 template <int kKind, int G, int NV, bool kYInStep, bool kYBulk>
-__global__ void __launch_bounds__(kThreads, (NV > kFlNvA) ? kFlMinBlocks - 1 : kFlMinBlocks)
+__global__ void __launch_bounds__(kThreads, flat_blocks(NV))
 softmax_rows_flat_kernel(const void* __restrict__ x, void* __restrict__ y,
                          float* __restrict__ m_out, float* __restrict__ l_out, int64_t rows,
                          int cols, int64_t ld_y, ScaleConsts k, int64_t R, int64_t tiles,
@@ -334,8 +343,8 @@ void launch_flat(const void* x, void* y, float* m, float* l, int64_t rows, int64
                  cudaStream_t stream) {
   constexpr int kEsz = RowElem<kKind>::kSize;
   const int64_t row_bytes = cols * kEsz;
-  const int64_t cap = static_cast<int64_t>(sm_count()) * ((NV > kFlNvA) ? kFlMinBlocks - 1 : kFlMinBlocks);
-  int64_t R = kFlTileBytes / row_bytes;
+  const int64_t cap = static_cast<int64_t>(sm_count()) * flat_blocks(NV);
+  int64_t R = flat_tile_bytes(NV) / row_bytes;
   const int64_t spread = (rows + cap - 1) / cap;
   if (R > spread) R = spread;
   if (R < 1) R = 1;
@@ -343,8 +352,17 @@ void launch_flat(const void* x, void* y, float* m, float* l, int64_t rows, int64
   const int stride = static_cast<int>((R * row_bytes + 32 + 127) / 128 * 128);
   const int grid = static_cast<int>(tiles < cap ? tiles : cap);
   const uint64_t timeout = fault.timeout_ns > 0 ? static_cast<uint64_t>(fault.timeout_ns) : kClTimeoutNs;
+  const size_t smem = static_cast<size_t>(stride) * kFlBufs;
+  if (smem > (48u << 10)) {  // above the default limit: raise it once
+    static std::atomic<bool> raised{false};
+    if (!raised.load(std::memory_order_acquire)) {
+      cudaFuncSetAttribute(softmax_rows_flat_kernel<kKind, G, NV, kYInStep, kYBulk>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, 100 << 10);
+      raised.store(true, std::memory_order_release);
+    }
+  }
   softmax_rows_flat_kernel<kKind, G, NV, kYInStep, kYBulk>
-      <<<grid, kThreads, static_cast<size_t>(stride) * kFlBufs, stream>>>(
+      <<<grid, kThreads, smem, stream>>>(
           x, y, m, l, rows, static_cast<int>(cols), ld_y, k, R, tiles, stride, err, fault.extra_tx,
           timeout);
 }
@@ -418,6 +436,20 @@ bool flat_rows_as(const void* x, void* y, float* m, float* l, int64_t rows, int6
     int64_t slots = 8;
     while (slots < chunks) slots *= 2;
     if (5 * chunks >= 4 * slots) return false;
+  }
+  // 16-bit rows on the grid of 16 or 32 chunks: groups of 2 or 4 threads of
+  // eight chunks, no chunk slot left over (GB300, 2^28 elements: bf16 rows
+  // of 128 elements 0.83 -> 0.94 of the copy peak, 256 0.82 -> 0.86; rows of
+  // 64, one thread a row, fell to 0.62, and rows that leave slots over, such
+  // as 200, lost 3%)
+  if constexpr (kKind != 0) {
+    if (grid_rows && same_phase(x, y, cols, ld_y, kEsz) && (cols * kEsz == 256 || cols * kEsz == 512)) {
+      if (cols * kEsz == 256)
+        launch_flat<kKind, 2, kFlNvC, true, false>(x, y, m, l, rows, cols, ld_y, k, err, fault, stream);
+      else
+        launch_flat<kKind, 4, kFlNvC, true, false>(x, y, m, l, rows, cols, ld_y, k, err, fault, stream);
+      return true;
+    }
   }
   // the most chunks a row spans: rows 16-byte multiples long all have x's
   // offset, others may lie at any
