@@ -57,8 +57,8 @@ __device__ __forceinline__ void issue_slice(const char* xr, uint4* buf, uint32_t
 // kDouble: two slice buffers; the next row's copies are issued as soon as
 // the current row's have landed, so they are in flight while the current row
 // is reduced and written.
-template <int kKind, bool kDouble>
-__global__ void __launch_bounds__(kClThreads, 2)
+template <int kKind, bool kDouble, int kThr>
+__global__ void __launch_bounds__(kThr, 1024 / kThr)
 softmax_rows_cluster_kernel(const void* __restrict__ x, void* __restrict__ y,
                             float* __restrict__ m_out, float* __restrict__ l_out, int64_t rows,
                             int64_t cols, int64_t ld_x, int64_t ld_y, ScaleConsts k,
@@ -67,7 +67,7 @@ softmax_rows_cluster_kernel(const void* __restrict__ x, void* __restrict__ y,
   constexpr int kEpc = RowElem<kKind>::kEpc;
   constexpr int kEsz = RowElem<kKind>::kSize;
   extern __shared__ __align__(128) uint4 slices[];  // this CTA's slice buffer(s), 16-byte chunks
-  __shared__ float2 wstate[kClWarps];
+  __shared__ float2 wstate[kThr / 32];
   __shared__ float2 cstate[2][kClMaxCtas];         // the cluster's CTA states, by row parity
   __shared__ __align__(8) uint64_t bars[2];
 
@@ -130,11 +130,11 @@ softmax_rows_cluster_kernel(const void* __restrict__ x, void* __restrict__ y,
     float xm = neg_inf();
     float2 negM = make_float2(0.f, 0.f);
     float2 acc = make_float2(0.f, 0.f);
-    for (int c0 = tid; c0 < nch; c0 += kClThreads * kClUnroll) {
+    for (int c0 = tid; c0 < nch; c0 += kThr * kClUnroll) {
       float2 w[kClUnroll][kEpc / 2];
 #pragma unroll
       for (int u = 0; u < kClUnroll; ++u)
-        unpack_chunk16<kKind>((c0 + u * kClThreads < nch) ? slice[c0 + u * kClThreads] : pad, w[u]);
+        unpack_chunk16<kKind>((c0 + u * kThr < nch) ? slice[c0 + u * kThr] : pad, w[u]);
       float cm = xm;
 #pragma unroll
       for (int u = 0; u < kClUnroll; ++u)
@@ -166,7 +166,7 @@ softmax_rows_cluster_kernel(const void* __restrict__ x, void* __restrict__ y,
     for (int off = 16; off > 0; off >>= 1) lw += __shfl_xor_sync(0xffffffffu, lw, off);
     if ((tid & 31) == 0) wstate[tid >> 5] = make_float2(xw, lw);
     __syncthreads();
-    float2 st = merge_states_warp(wstate, kClWarps, k);
+    float2 st = merge_states_warp(wstate, kThr / 32, k);
     if (C > 1) {
       if (tid == 0)
         for (uint32_t r = 0; r < C; ++r) st_peer_f2(&cstate[sbuf][rank], r, st.x, st.y);
@@ -183,18 +183,18 @@ softmax_rows_cluster_kernel(const void* __restrict__ x, void* __restrict__ y,
     const float2 negMr = make_float2(-Mr, -Mr);
     const float inv = nonempty ? 1.0f / ls : 0.f;
     const float2 f2 = make_float2(inv, inv);
-    for (int c0 = tid; c0 < nch; c0 += kClThreads * kClUnroll) {
+    for (int c0 = tid; c0 < nch; c0 += kThr * kClUnroll) {
       uint4 v[kClUnroll];
 #pragma unroll
-      for (int u = 0; u < kClUnroll; ++u) v[u] = (c0 + u * kClThreads < nch) ? slice[c0 + u * kClThreads] : pad;
+      for (int u = 0; u < kClUnroll; ++u) v[u] = (c0 + u * kThr < nch) ? slice[c0 + u * kThr] : pad;
 #pragma unroll
       for (int u = 0; u < kClUnroll; ++u) {
-        if (c0 + u * kClThreads < nch) {
+        if (c0 + u * kThr < nch) {
           float2 w[kEpc / 2];
           unpack_chunk16<kKind>(v[u], w);
 #pragma unroll
           for (int h = 0; h < kEpc / 2; ++h) w[h] = weight2(w[h], negMr, k);
-          store_chunk16<kKind>(yr, c0 + u * kClThreads, n, s, pack_chunk16<kKind>(w, f2));
+          store_chunk16<kKind>(yr, c0 + u * kThr, n, s, pack_chunk16<kKind>(w, f2));
         }
       }
     }
@@ -209,7 +209,7 @@ struct ClusterCfg {
   size_t smem;
 };
 
-template <int kKind, bool kDouble>
+template <int kKind, bool kDouble, int kThr>
 cudaLaunchConfig_t cluster_launch_cfg(const ClusterCfg& cc, cudaLaunchAttribute* attr,
                                       cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
@@ -217,7 +217,7 @@ cudaLaunchConfig_t cluster_launch_cfg(const ClusterCfg& cc, cudaLaunchAttribute*
   attr[0].val.clusterDim.x = cc.ctas;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
-  cfg.blockDim = dim3(kClThreads, 1, 1);
+  cfg.blockDim = dim3(kThr, 1, 1);
   cfg.gridDim = dim3(cc.ctas, 1, 1);
   cfg.dynamicSmemBytes = cc.smem;
   cfg.stream = stream;
@@ -228,7 +228,7 @@ cudaLaunchConfig_t cluster_launch_cfg(const ClusterCfg& cc, cudaLaunchAttribute*
 
 // Clusters of `ctas` CTAs that can be resident at once (0 when none can),
 // cached per device, cluster size and shared-memory size in 8 KB steps.
-template <int kKind, bool kDouble>
+template <int kKind, bool kDouble, int kThr>
 int resident_clusters(const ClusterCfg& cc) {
   static std::atomic<int> cache[64][kClMaxCtas + 1][32];  // resident + 1; 0 = not asked yet
   int dev = 0;
@@ -239,13 +239,13 @@ int resident_clusters(const ClusterCfg& cc) {
     const int v = cache[dev][cc.ctas][kb8].load();
     if (v > 0) return v - 1;
   }
-  auto kernel = softmax_rows_cluster_kernel<kKind, kDouble>;
+  auto kernel = softmax_rows_cluster_kernel<kKind, kDouble, kThr>;
   if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 210 << 10) != cudaSuccess) {
     cudaGetLastError();
     return 0;
   }
   cudaLaunchAttribute attr[1];
-  cudaLaunchConfig_t cfg = cluster_launch_cfg<kKind, kDouble>(cc, attr, nullptr);
+  cudaLaunchConfig_t cfg = cluster_launch_cfg<kKind, kDouble, kThr>(cc, attr, nullptr);
   int resident = 0;
   if (cudaOccupancyMaxActiveClusters(&resident, kernel, &cfg) != cudaSuccess) {
     cudaGetLastError();
@@ -260,7 +260,7 @@ int resident_clusters(const ClusterCfg& cc) {
 // among the cluster sizes that hold the row the one that keeps the most SMs
 // busy (clusters resident at once x CTAs per cluster; a GPC's SMs need not
 // divide into clusters evenly), the smallest on a tie.
-template <int kKind, bool kDouble>
+template <int kKind, bool kDouble, int kThr>
 bool pick_cluster(int64_t cols, int64_t cap, int max_ctas, ClusterCfg* out) {
   constexpr int kEpc = RowElem<kKind>::kEpc;
   constexpr int kEsz = RowElem<kKind>::kSize;
@@ -275,7 +275,7 @@ bool pick_cluster(int64_t cols, int64_t cap, int max_ctas, ClusterCfg* out) {
     const int64_t stride = (chunks + 7) / 8 * 8;
     ClusterCfg cc{static_cast<int>(c), static_cast<int>(per),
                   static_cast<size_t>((kDouble ? stride + chunks : chunks) * 16)};
-    const int used = resident_clusters<kKind, kDouble>(cc) * cc.ctas;
+    const int used = resident_clusters<kKind, kDouble, kThr>(cc) * cc.ctas;
     if (used > best_used) {
       best_used = used;
       *out = cc;
@@ -286,7 +286,7 @@ bool pick_cluster(int64_t cols, int64_t cap, int max_ctas, ClusterCfg* out) {
 
 // Launch of softmax_rows_cluster_kernel, as many clusters as can be resident
 // at once (each loops over its rows).
-template <int kKind, bool kDouble>
+template <int kKind, bool kDouble, int kThr>
 bool launch_cluster_rows_as(const void* x, void* y, float* m, float* l, int64_t rows, int64_t cols,
                             int64_t ld_x, int64_t ld_y, const ScaleConsts& k, const ClusterCfg& cc,
                             unsigned int* err, const RowsFault& fault, cudaStream_t stream) {
@@ -297,15 +297,15 @@ bool launch_cluster_rows_as(const void* x, void* y, float* m, float* l, int64_t 
   if (!same_phase(x, y, ld_x, ld_y, kEsz) || (reinterpret_cast<uintptr_t>(x) % kEsz) != 0 ||
       cc.slice_elems % kEpc != 0)
     return false;
-  const int resident = resident_clusters<kKind, kDouble>(cc);
+  const int resident = resident_clusters<kKind, kDouble, kThr>(cc);
   if (resident < 1) return false;
   cudaLaunchAttribute attr[1];
-  cudaLaunchConfig_t cfg = cluster_launch_cfg<kKind, kDouble>(cc, attr, stream);
+  cudaLaunchConfig_t cfg = cluster_launch_cfg<kKind, kDouble, kThr>(cc, attr, stream);
   const int64_t nclusters = rows < resident ? rows : resident;
   cfg.gridDim = dim3(static_cast<unsigned int>(nclusters * cc.ctas), 1, 1);
   const int64_t c64 = cols;
   const uint64_t timeout = fault.timeout_ns > 0 ? static_cast<uint64_t>(fault.timeout_ns) : kClTimeoutNs;
-  return cudaLaunchKernelEx(&cfg, softmax_rows_cluster_kernel<kKind, kDouble>, x, y, m, l, rows, c64,
+  return cudaLaunchKernelEx(&cfg, softmax_rows_cluster_kernel<kKind, kDouble, kThr>, x, y, m, l, rows, c64,
                             ld_x, ld_y, k, cc.slice_elems, err, fault.extra_tx, timeout) == cudaSuccess;
 }
 
@@ -321,12 +321,23 @@ bool launch_cluster_rows(const void* x, void* y, float* m, float* l, int64_t row
                          int64_t ld_x, int64_t ld_y, const ScaleConsts& k, unsigned int* err,
                          const RowsFault& fault, cudaStream_t stream) {
   ClusterCfg cc;
-  if (pick_cluster<kKind, true>(cols, kClDoubleCap, 1, &cc))
-    return launch_cluster_rows_as<kKind, true>(x, y, m, l, rows, cols, ld_x, ld_y, k, cc, err, fault,
-                                               stream);
-  if (pick_cluster<kKind, false>(cols, kClSingleCap, kClMaxCtas, &cc))
-    return launch_cluster_rows_as<kKind, false>(x, y, m, l, rows, cols, ld_x, ld_y, k, cc, err, fault,
-                                                stream);
+  if (pick_cluster<kKind, true, kClThreads>(cols, kClDoubleCap, 1, &cc))
+    return launch_cluster_rows_as<kKind, true, kClThreads>(x, y, m, l, rows, cols, ld_x, ld_y, k, cc,
+                                                           err, fault, stream);
+  // fp32 rows of 32768 to 131072 elements: CTAs of 256 threads, up to four an
+  // SM, overlap their rows' copy waits and exchanges better (GB300, 2^28
+  // elements, fraction of the copy peak: 32768 columns 0.770 -> 0.805, 65536
+  // 0.755 -> 0.776, 131072 0.847 -> 0.870); 16-bit rows, shorter fp32 rows and
+  // longer ones ran slower that way (bf16 and fp16 at 32768 by 6-8%, fp32 at
+  // 20000 by 8%, at 262144 by 3%, at 409600 by 7%)
+  if constexpr (kKind == 0) {
+    if (cols >= 32768 && cols <= 131072 && pick_cluster<kKind, false, kClThreads / 2>(cols, kClSingleCap, kClMaxCtas, &cc))
+      return launch_cluster_rows_as<kKind, false, kClThreads / 2>(x, y, m, l, rows, cols, ld_x, ld_y, k,
+                                                                  cc, err, fault, stream);
+  }
+  if (pick_cluster<kKind, false, kClThreads>(cols, kClSingleCap, kClMaxCtas, &cc))
+    return launch_cluster_rows_as<kKind, false, kClThreads>(x, y, m, l, rows, cols, ld_x, ld_y, k, cc,
+                                                            err, fault, stream);
   return false;
 }
 
