@@ -181,3 +181,19 @@ def test_y_like_x_tiles_leave_by_bulk_copies(dtype, cols, off):
     y, m, l = run(x, 0.8, y)
     check(x, y, m, l, 0.8, f"{dtype} {rows}x{cols} y like x +{off}")
     assert bool((ybuf[:off] == 7.0).all()) and bool((ybuf[off + rows * cols:] == 7.0).all())
+
+
+@pytest.mark.parametrize("kind", ["bf16", "f16"])
+@pytest.mark.parametrize("cols", [128, 256])
+@pytest.mark.parametrize("rows", [1, 2, 55, 56, 57, 111, 112, 113, 5000])
+def test_16bit_rows_on_the_grid_in_eight_chunk_groups(kind, cols, rows):
+    # 16-bit rows of 128 or 256 elements on the 16-byte grid take groups of 2
+    # or 4 threads of eight chunks and tiles of 28 KB (112 or 56 rows): row
+    # counts around a tile, masked entries and whole masked rows
+    dtype = torch.bfloat16 if kind == "bf16" else torch.float16
+    x, _ = dense_at(rows, cols, dtype, 0, seed=rows * 3 + cols)
+    assert x.data_ptr() % 16 == 0
+    if rows > 3:
+        x = masked(x, rows + cols)
+    y, m, l = run(x, 1.1, None)
+    check(x, y, m, l, 1.1, f"{kind} {rows}x{cols} eight-chunk groups")
