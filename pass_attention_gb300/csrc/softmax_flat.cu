@@ -353,12 +353,15 @@ void launch_flat(const void* x, void* y, float* m, float* l, int64_t rows, int64
   const int grid = static_cast<int>(tiles < cap ? tiles : cap);
   const uint64_t timeout = fault.timeout_ns > 0 ? static_cast<uint64_t>(fault.timeout_ns) : kClTimeoutNs;
   const size_t smem = static_cast<size_t>(stride) * kFlBufs;
-  if (smem > (48u << 10)) {  // above the default limit: raise it once
-    static std::atomic<bool> raised{false};
-    if (!raised.load(std::memory_order_acquire)) {
+  if (smem > (48u << 10)) {  // above the default limit: raised once per device
+    constexpr int kMaxDevices = 64;
+    static std::atomic<bool> raised[kMaxDevices];
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= kMaxDevices || !raised[dev].load(std::memory_order_acquire)) {
       cudaFuncSetAttribute(softmax_rows_flat_kernel<kKind, G, NV, kYInStep, kYBulk>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize, 100 << 10);
-      raised.store(true, std::memory_order_release);
+      if (dev >= 0 && dev < kMaxDevices) raised[dev].store(true, std::memory_order_release);
     }
   }
   softmax_rows_flat_kernel<kKind, G, NV, kYInStep, kYBulk>
