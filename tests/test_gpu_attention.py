@@ -291,3 +291,29 @@ def test_no_workspace_for_causal_or_full_rounds():
     assert oss.attention_fwd_workspace_bytes(1, 32, 16384, 16384, causal=True) == 0
     # tiles that fill whole rounds: sms query tiles of 128 rows
     assert oss.attention_fwd_workspace_bytes(1, sms, 128, 4096) == 0
+
+
+def test_split_tail_on_two_streams_keeps_workspaces_apart():
+    # two launches that both take the split tail, on two streams with no
+    # ordering between them: each stream gets its own workspace (counters and
+    # partial states), and each result equals the same call made alone
+    B, H, Sq, Sk = 2, 3, 640, 1500
+    assert oss.attention_fwd_workspace_bytes(B, H, Sq, Sk) > 0
+    q1, k1, v1 = workloads.qkv(B, H, Sq, Sk, 128, seed=31, device="cuda")
+    q2, k2, v2 = workloads.qkv(B, H, Sq, Sk, 128, seed=32, device="cuda")
+    ref1 = oss.attention_fwd(q1, k1, v1, 0.1)
+    ref2 = oss.attention_fwd(q2, k2, v2, 0.1)
+    torch.cuda.synchronize()
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    for _ in range(3):
+        with torch.cuda.stream(s1):
+            o1, l1 = oss.attention_fwd(q1, k1, v1, 0.1, stream=s1)
+        with torch.cuda.stream(s2):
+            o2, l2 = oss.attention_fwd(q2, k2, v2, 0.1, stream=s2)
+    torch.cuda.synchronize()
+    assert oss.check_device_error() == 0
+    assert torch.equal(o1, ref1[0]) and torch.equal(l1, ref1[1])
+    assert torch.equal(o2, ref2[0]) and torch.equal(l2, ref2[1])
+    dev = q1.device.index
+    keys = {key for key in oss._WORKSPACES if key[0] == dev and key[2] == "attn"}
+    assert (dev, s1.cuda_stream, "attn") in keys and (dev, s2.cuda_stream, "attn") in keys
