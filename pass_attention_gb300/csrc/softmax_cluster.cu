@@ -217,7 +217,21 @@ softmax_rows_cluster_kernel(const void* __restrict__ x, void* __restrict__ y,
           float2 w[kEpc / 2];
           unpack_chunk16_cl<kKind>(v[u], w);
 #pragma unroll
-          for (int h = 0; h < kEpc / 2; ++h) w[h] = weight2(w[h], negMr, k);
+          for (int h = 0; h < kEpc / 2; ++h) {
+            if constexpr (kKind == 1) {
+              // bf16 y: the exponent from c_hi alone (one FMA, not weight2's
+              // two). Dropping c_lo (< one fp32 ulp of c) moves y by at most
+              // |x c| 2^-24 ln 2 relative before its rounding to 8 bits: under
+              // 5e-4 even for logits of 10^4, against a rounding step of
+              // 2^-8. m and l, from the exact form above, are unchanged.
+              // (GB300, 2^28 elements: 32768 columns 0.830 -> 0.856 of the
+              // copy peak, 20000 0.737 -> 0.758.)
+              const float2 t = __ffma2_rn(w[h], make_float2(k.c_hi, k.c_hi), negMr);
+              w[h] = make_float2(ex2(t.x), ex2(t.y));
+            } else {
+              w[h] = weight2(w[h], negMr, k);
+            }
+          }
           store_chunk16<kKind>(yr, c0 + u * kThr, n, s, pack_chunk16<kKind>(w, f2));
         }
       }
