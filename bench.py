@@ -63,8 +63,8 @@ NCU_TRAFFIC = {
                     "sha256": "73995524e85db31d7c3bf8d58cf01f5782d07ad3a36db8fe5429e33fcd182570",
                     "bytes_per_launch": 1073778688 + 1017928448},
     "softmax_32k_bf16": {"source": _SRC_GROUPED,
-                         "sha256": "bf6578f2881c77b13dca4a2fed113a752c6b6bb837750b1a704b7cc421b4cf9d",
-                         "bytes_per_launch": 536895744 + 484455424},
+                         "sha256": "edca4d93214216b2621d11a822fc211291dd35ffdef21c5c7f9f9b25c782109f",
+                         "bytes_per_launch": 536895488 + 484645376},
     # the comparators: all sweeps of one call (each reads x from DRAM again)
     "softmax_32k_3pass": {"source": _SRC_ROWS,
                           "sha256": "73995524e85db31d7c3bf8d58cf01f5782d07ad3a36db8fe5429e33fcd182570",

@@ -275,19 +275,21 @@ bool grouped_rows_f32(const void* x, void* y, float* m, float* l, int64_t rows, 
 }
 
 // 16-bit rows of up to 16384 elements: persistent CTAs with the next row's
-// chunks prefetched into registers (the widening of fp16 costs a conversion
-// per element, and without the prefetch that arithmetic stalled the loads);
-// 256 / TPR rows per CTA for rows of up to 4096 elements (groups of 8 and 16
-// threads, without the prefetch, for rows of up to 128). kExtra: the slot a
-// row off the 16-byte grid needs, with fewer CTAs per SM.
+// chunks prefetched into registers, or, for the lengths where that measured
+// slower, more CTAs per SM without it; 256 / TPR rows per CTA for rows of up
+// to 4096 elements (groups of 8 and 16 threads, without the prefetch, for
+// rows of up to 128). kExtra: the slot a row off the 16-byte grid needs, with
+// fewer CTAs per SM.
 template <int kType, bool kExtra>
 bool grouped_rows16(const void* x, void* y, float* m, float* l, int64_t rows, int64_t cols,
                     int64_t ld_x, int64_t ld_y, const ScaleConsts& k, cudaStream_t stream) {
   const int64_t chunks = (cols + 7) / 8;
   const int c = static_cast<int>(cols);
-  if (kType == 1 && !kExtra && chunks > 32 && chunks <= 1024) {
-    // bf16 widens with a shift, not a conversion: on the grid these rows ran
-    // 3-11% faster on the GB300 without the prefetch, with more CTAs per SM
+  if (!kExtra && chunks > 32 && chunks <= (kType == 1 ? 1024 : 256)) {
+    // On the grid these rows ran faster on the GB300 without the prefetch,
+    // with more CTAs per SM: bf16 by 3-11%, fp16 of 33-256 chunks by 2-10%
+    // (at 512 and 1024 chunks fp16 kept the prefetch, level or up to 0.6%
+    // ahead). Rows off the grid lost 5-9% without it, for both types.
     if (chunks <= 64)
       launch_grouped<kType, 32, 2, false, 6>(x, y, m, l, rows, c, ld_x, ld_y, k, stream);
     else if (chunks <= 128)
