@@ -85,9 +85,10 @@ typedef enum os_status {
  * kernel moves the row in 16-byte chunks on that grid and reads each element
  * once and writes it once: rows of up to 16384 elements are held in
  * registers (several rows per CTA up to 2048 elements); longer rows of up to
- * 1.6 MB in the shared memory of a thread-block cluster of up to eight CTAs,
- * whose slices' (max, sum) states are merged through distributed shared
- * memory. For a row off the 16-byte grid, the loads of its first and last
+ * 1.6 MB by a thread-block cluster of up to eight CTAs, whose slices' (max,
+ * sum) states are merged through distributed shared memory: in the cluster's
+ * registers for rows on the 16-byte grid of 20481..65536 elements, in its
+ * shared memory otherwise. For a row off the 16-byte grid, the loads of its first and last
  * chunks may read (never write) bytes of the same 16-byte granules outside
  * the row. Short rows of a matrix whose x rows lie back to back (ld_x ==
  * cols; rows of up to 512 bytes, or 1 KB off the 16-byte grid) are taken a
@@ -164,8 +165,9 @@ typedef enum os_dtype {
  *   finite and > 0; dtype an os_dtype.
  * Alignment: x and y 2-byte aligned, m and l 4-byte aligned. When x's and
  * y's rows start at the same offsets from a 16-byte boundary, rows of up to
- * 16384 elements are held in registers and longer rows of up to 1.6 MB in a
- * cluster's shared memory, as for os_softmax_rows (one read, one write per
+ * 16384 elements are held in registers and longer rows of up to 1.6 MB by a
+ * cluster, as for os_softmax_rows (in its registers for rows on the 16-byte
+ * grid of up to 131072 elements; one read, one write per
  * element, the same granule reads at the ends of a row off the grid). Short
  * rows of a matrix whose x rows lie back to back are staged in shared memory
  * by tiles as for os_softmax_rows, with y at any layout; other rows are
@@ -432,7 +434,9 @@ OSS_API os_status os_merge_partials(const float* part_m, const float* part_l, co
  * wait since the last check, otherwise an OS_ERR_TIMEOUT detail code
  * (bits 0..7 = kernel id, bits 8..15 = wait site): kernel 1 is the attention
  * forward (see os_debug_inject_fault); 2 | (1 << 8) is a row softmax whose
- * wait for its row's bulk copies into shared memory gave up. Returns
+ * wait for its row's bulk copies into shared memory gave up, 2 | (2 << 8) one
+ * whose wait for the (max, sum) states of the other CTAs of its cluster gave
+ * up. Returns
  * OS_ERR_TIMEOUT when the word was set, OS_ERR_CUDA when a CUDA call failed,
  * OS_OK otherwise.
  * `code` may be NULL.
@@ -461,16 +465,21 @@ OSS_API os_status os_check_device_error(void* stream, int32_t* code);
  *           The CUDA context stays usable; the outputs of that call are
  *           undefined.
  *   kind 2: the next os_softmax_rows or os_softmax_rows_16bit call. If it
- *           holds its rows in a cluster's shared memory (aligned rows longer
- *           than 16384 elements and at most 1.6 MB) or stages short rows of a
- *           dense matrix in shared memory, every CTA's barrier for the bulk
- *           copies of its first row (or tile) is told to expect 16 bytes more
- *           than are copied. The wait gives up after `timeout_ns` (0: 2 s);
- *           from then on each CTA waits and copies no more but still meets
- *           its barriers, so the launch ends. os_check_device_error
- *           then returns OS_ERR_TIMEOUT with code 2 | (1 << 8). The outputs of
- *           that call are undefined; other paths ignore the hook. `step` is
- *           unused.
+ *           holds its rows in a cluster's shared memory (rows longer than
+ *           16384 elements and at most 1.6 MB that the register path below
+ *           does not take) or stages short rows of a dense matrix in shared
+ *           memory, every CTA's barrier for the bulk copies of its first row
+ *           (or tile) is told to expect 16 bytes more than are copied; the
+ *           code is then 2 | (1 << 8). If it holds its rows in a cluster's
+ *           registers (rows on the 16-byte grid of 16385..131072 16-bit or
+ *           20481..65536 fp32 elements), every CTA's barrier for the
+ *           cluster's states of its first row expects 16 bytes more than
+ *           the states; the code is then 2 | (2 << 8). The wait gives up
+ *           after `timeout_ns` (0: 2 s); from then on each CTA waits (and
+ *           copies or sends) no more but still meets its barriers, so the
+ *           launch ends. os_check_device_error then returns OS_ERR_TIMEOUT
+ *           with that code. The outputs of that call are undefined; other
+ *           paths ignore the hook. `step` is unused.
  * No GPU fault, trap or endless wait is involved.
  * Errors: OS_ERR_INVALID_ARGUMENT (kind not 0/1/2, step < 0, timeout_ns < 0).
  */

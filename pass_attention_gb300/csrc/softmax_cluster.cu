@@ -2,14 +2,22 @@
 //
 // Cluster-resident rows: rows too long for registers (more than 16384
 // elements) but short enough to fit in the shared memory of a thread-block
-// cluster of C <= 8 CTAs. CTA r of a cluster holds slice r of the row, copied
-// in by bulk asynchronous copies; each CTA reduces its slice to a (max, sum)
-// state, the CTAs exchange their states through distributed shared memory and
-// merge them (the merge identity of partial results), and each CTA then
-// writes its slice once. One HBM read and one write per element, where the
-// streaming kernel reads the row twice.
+// cluster of C <= 8 CTAs, where the register path (softmax_cluster_regs.cu)
+// does not take them. CTA r of a cluster holds slice r of the row, copied in
+// by bulk asynchronous copies; each CTA reduces its slice to a (max, sum)
+// state, the CTAs exchange their states through distributed shared memory on
+// mbarriers (cluster_exchange.cuh) and merge them (the merge identity of
+// partial results), and each CTA then writes its slice once. One HBM read and
+// one write per element, where the streaming kernel reads the row twice.
+//
+// The exchange was a cluster barrier, warp 0 arriving with release, until
+// the mbarrier form measured faster everywhere it applies (GB300, 2^28
+// elements, fraction of the copy peak: fp32 rows of 98304, 131072, 204800 and
+// 409600 columns 0.884 / 0.870 / 0.837 / 0.658 -> 0.952 / 0.929 / 0.927 /
+// 0.689; bf16 262144 0.745 -> 0.771, fp16 262144 0.717 -> 0.755, bf16 819200
+// 0.558 -> 0.582; rows held by one CTA unchanged).
 
-#include "softmax_common.cuh"
+#include "cluster_exchange.cuh"
 
 namespace oss {
 namespace {
@@ -94,6 +102,7 @@ softmax_rows_cluster_kernel(const void* __restrict__ x, void* __restrict__ y,
   __shared__ float2 wstate[kThr / 32];
   __shared__ float2 cstate[2][kClMaxCtas];         // the cluster's CTA states, by row parity
   __shared__ __align__(8) uint64_t bars[2];
+  __shared__ __align__(8) uint64_t xbar[2];  // the states' barriers, by exchange parity
 
   const int tid = threadIdx.x;
   const uint32_t C = cluster_size();
@@ -110,6 +119,8 @@ softmax_rows_cluster_kernel(const void* __restrict__ x, void* __restrict__ y,
   if (tid == 0) {
     for (int b = 0; b < (kDouble ? 2 : 1); ++b)
       asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&bars[b])) : "memory");
+    for (int b = 0; b < 2; ++b)
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&xbar[b])) : "memory");
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   // every CTA of the cluster has started (its shared memory may be written
@@ -122,7 +133,7 @@ softmax_rows_cluster_kernel(const void* __restrict__ x, void* __restrict__ y,
   }
 
   uint32_t parity = 0u;  // bit b: the phase parity to wait for on buffer b
-  int sbuf = 0;  // cstate set
+  int xe = 0;  // exchanges so far: slot set and barrier xe & 1, parity (xe >> 1) & 1
   int it = 0;
   bool live = true;  // false once this thread gave up on a wait: no more waits or copies
   for (int64_t row = row0; row < rows; row += rstep, ++it) {
@@ -192,11 +203,11 @@ softmax_rows_cluster_kernel(const void* __restrict__ x, void* __restrict__ y,
     __syncthreads();
     float2 st = merge_states_warp(wstate, kThr / 32, k);
     if (C > 1) {
-      if (tid == 0)
-        for (uint32_t r = 0; r < C; ++r) st_peer_f2(&cstate[sbuf][rank], r, st.x, st.y);
-      cluster_sync_warp0_wrote();
-      st = merge_states_warp(cstate[sbuf], static_cast<int>(C), k);
-      sbuf ^= 1;
+      const int xs = xe & 1;
+      if (tid == 0 && live) send_state(cstate[xs], &xbar[xs], C, rank, st.x, st.y, 0u);
+      if (live) live = wait_states_bounded(smem_u32(&xbar[xs]), (xe >> 1) & 1, err, timeout_ns);
+      st = merge_states_warp(cstate[xs], static_cast<int>(C), k);
+      ++xe;
     }
     xm = st.x;
     ls = st.y;
@@ -239,6 +250,8 @@ softmax_rows_cluster_kernel(const void* __restrict__ x, void* __restrict__ y,
     if (rank == 0 && tid == 0) write_ml(xm, ls, k, row, m_out, l_out);
     __syncthreads();  // the slice is read out before its buffer is refilled
   }
+  // no CTA leaves while a peer may still store into its shared memory
+  if (C > 1) cluster_sync_all();
 }
 
 struct ClusterCfg {
@@ -381,9 +394,18 @@ bool launch_cluster_rows(const void* x, void* y, float* m, float* l, int64_t row
 
 }  // namespace
 
+// softmax_cluster_regs.cu: aligned rows short enough for a cluster's
+// registers (16-bit up to 131072 elements, fp32 20481..65536), with one
+// exponential per element and the states exchanged on mbarriers; false,
+// launching nothing, for other rows.
+bool cluster_reg_rows(int kind, const void* x, void* y, float* m, float* l, int64_t rows, int64_t cols,
+                      int64_t ld_x, int64_t ld_y, const ScaleConsts& k, unsigned int* err,
+                      const RowsFault& fault, cudaStream_t stream);
+
 bool cluster_rows(int kind, const void* x, void* y, float* m, float* l, int64_t rows, int64_t cols,
                   int64_t ld_x, int64_t ld_y, const ScaleConsts& k, unsigned int* err,
                   const RowsFault& fault, cudaStream_t stream) {
+  if (cluster_reg_rows(kind, x, y, m, l, rows, cols, ld_x, ld_y, k, err, fault, stream)) return true;
   if (kind == 0) return launch_cluster_rows<0>(x, y, m, l, rows, cols, ld_x, ld_y, k, err, fault, stream);
   if (kind == 1) return launch_cluster_rows<1>(x, y, m, l, rows, cols, ld_x, ld_y, k, err, fault, stream);
   return launch_cluster_rows<2>(x, y, m, l, rows, cols, ld_x, ld_y, k, err, fault, stream);

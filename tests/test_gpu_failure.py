@@ -110,6 +110,7 @@ def test_timeout_stops_the_whole_launch():
 
 KERNEL_SOFTMAX_ROWS = 2
 SITE_COPIES = 1
+SITE_STATES = 2
 
 
 def timeout_code():
@@ -119,15 +120,20 @@ def timeout_code():
     return int(str(info.value).split("code ")[1].split(")")[0], 16)
 
 
-@pytest.mark.parametrize("kind,cols,rows", [
-    ("fp32", 65536, 200),   # 256 KB rows: a cluster of several CTAs, one buffer each
-    ("bf16", 20000, 700),   # 40 KB rows: one CTA with two buffers
-    ("bf16", 100, 100000),  # 200-byte rows of a dense matrix: tiles staged in shared memory
+@pytest.mark.parametrize("kind,cols,rows,site", [
+    ("fp32", 65536, 200, SITE_STATES),   # 256 KB rows in the registers of a cluster of 8
+    ("bf16", 131072, 64, SITE_STATES),   # the same, 16-bit
+    ("bf16", 20000, 700, SITE_STATES),   # 40 KB rows in the registers of a cluster of 2
+    ("fp32", 100000, 60, SITE_COPIES),   # 400 KB rows in a cluster's shared memory
+    ("bf16", 20001, 700, SITE_COPIES),   # off the 16-byte grid, 40 KB: one CTA, two buffers
+    ("bf16", 100, 100000, SITE_COPIES),  # 200-byte rows of a dense matrix: tiles staged
 ])
-def test_row_softmax_copy_wait_times_out_and_context_survives(kind, cols, rows):
-    # every CTA's first row (or tile) expects 16 bytes that never arrive: its
-    # wait gives up after 20 ms, it copies and waits no more but still meets
-    # its barriers, lets the copies already issued land, and the launch ends
+def test_row_softmax_wait_times_out_and_context_survives(kind, cols, rows, site):
+    # every CTA's first row (or tile) expects 16 bytes that never arrive,
+    # on its copies' barrier or on the barrier of the cluster's states: its
+    # wait gives up after 20 ms, it waits (and copies or sends) no more, so
+    # a peer waiting for it gives up too; every CTA still meets its barriers
+    # and the launch ends
     import time
     dtype = torch.float32 if kind == "fp32" else torch.bfloat16
     x = workloads.logits(rows, cols, 10.0, seed=cols, device="cuda").to(dtype)
@@ -140,7 +146,7 @@ def test_row_softmax_copy_wait_times_out_and_context_survives(kind, cols, rows):
     code = timeout_code()
     assert time.perf_counter() - t0 < 1.0
     assert code & 0xFF == KERNEL_SOFTMAX_ROWS
-    assert (code >> 8) & 0xFF == SITE_COPIES
+    assert (code >> 8) & 0xFF == site
     # the word was cleared, the hook consumed, and the context computes correctly
     assert oss.check_device_error() == 0
     y, m, l = call(x, 1.0)

@@ -1,14 +1,18 @@
 """Rows longer than 16384 elements against the oracle (GPU).
 
-Aligned rows of up to 8 x 200 KB are held in the shared memory of a
+Aligned rows of up to 8 x 2048 chunks of 16 bytes (131072 16-bit elements,
+65536 fp32; fp32 rows of more than 80 KB) are held in the registers of a
 thread-block cluster: CTA r of a cluster of C CTAs holds slice r, the CTAs
-merge their (max, sum) states through distributed shared memory, and each
-writes its slice once. A row of at most 48 KB takes one CTA with two slice
-buffers (the next row's copies overlap the current row). Longer rows fall back
-to the streaming kernel. The lengths below take one CTA with two buffers, one
-with one buffer, and clusters of up to eight, with ragged last slices and
-slices that are empty; the row counts exceed the clusters resident at once,
-so each cluster walks several rows."""
+send their (max, sum) states to each other by asynchronous stores into
+distributed shared memory, and each writes its slice once. Other rows of up
+to 8 x 200 KB are held in the shared memory of a cluster, merged through a
+cluster barrier; a row of at most 48 KB takes one CTA with two slice buffers
+(the next row's copies overlap the current row). Longer rows fall back to the
+streaming kernel. The lengths below take every cluster size of both paths,
+5 to 8 chunks a thread in the register path, one CTA with two buffers, one
+with one buffer, ragged last slices and slices that are empty; most row counts
+exceed the clusters resident at once, so each cluster walks several rows,
+and some are fewer than the clusters."""
 
 import numpy as np
 import pytest
@@ -25,9 +29,15 @@ pytestmark = pytest.mark.gpu
 F32_CASES = [
     (16385, 301),    # 64 KB, one CTA, ragged tail
     (20000, 401),    # 80 KB; more rows than resident CTAs
-    (25601, 160),    # 100 KB, one element past a 16-byte chunk
-    (32768, 160),    # 128 KB
-    (65536, 130),    # 256 KB: two or more CTAs
+    (20481, 150),    # registers: 3 CTAs of 7 chunks a thread
+    (24576, 150),    # registers: 3 CTAs of 8
+    (25601, 160),    # 100 KB, one element past a 16-byte chunk (registers: 4 of 7)
+    (32768, 160),    # 128 KB (registers: 4 of 8)
+    (40000, 100),    # registers: 5 CTAs
+    (57345, 50),     # registers: 8 CTAs, the last one short
+    (65536, 130),    # 256 KB (registers: 8 CTAs)
+    (65536, 3),      # fewer rows than clusters
+    (65537, 40),     # one element past the register path: shared memory
     (100003, 41),    # 391 KB, ragged
     (204800, 21),    # 800 KB: four or more
     (204801, 21),    # one element more: five or more
@@ -35,10 +45,15 @@ F32_CASES = [
     (409601, 9),     # beyond: the streaming kernel
 ]
 H16_CASES = [
-    (16385, 301),    # 32 KB: one CTA, two buffers
-    (20000, 401),    # 40 KB: one CTA, two buffers
-    (51201, 160),    # 100 KB: one buffer
-    (131072, 64),    # 256 KB
+    (16385, 301),    # registers: 2 CTAs of 5 chunks a thread
+    (20000, 401),    # registers: 2 CTAs of 5
+    (24000, 301),    # registers: 2 CTAs of 6
+    (32768, 200),    # registers: 2 CTAs of 8
+    (51201, 160),    # registers: 4 CTAs of 7, ragged
+    (100000, 40),    # registers: 7 CTAs of 7
+    (131072, 64),    # 256 KB: registers, 8 CTAs of 8
+    (131072, 3),     # fewer rows than clusters
+    (131073, 30),    # one element past the register path: shared memory
     (409600, 12), (409601, 12),
     (819200, 6),     # 1.6 MB: eight
     (819201, 6),     # beyond: the streaming kernel
