@@ -344,7 +344,21 @@ void launch_flat(const void* x, void* y, float* m, float* l, int64_t rows, int64
   constexpr int kEsz = RowElem<kKind>::kSize;
   const int64_t row_bytes = cols * kEsz;
   const int64_t cap = static_cast<int64_t>(sm_count()) * flat_blocks(NV);
+  // R a multiple of the CTA's groups: a tile of 71 rows for 64 groups took
+  // two rounds of the groups, the second with 7 rows, while the CTA's other
+  // warps waited at the tile's barrier. Below one round, a tile of one row a
+  // group when that stays within twice the tile's bytes (not for the
+  // eight-chunk groups, whose rows of 128 and 256 elements lost 2-4% so).
+  // GB300, 2^28 elements, fraction of the copy peak: bf16 100 columns 0.600
+  // -> 0.686, 200 0.708 -> 0.820, 300 0.644 -> 0.775, 75 0.623 -> 0.746, 33
+  // 0.612 -> 0.729; fp32 101 0.767 -> 0.913, 50 0.800 -> 0.891; fp32 100
+  // 0.861 -> 0.841.
+  constexpr int64_t kGroups = kThreads / G;
   int64_t R = flat_tile_bytes(NV) / row_bytes;
+  if (R >= kGroups)
+    R = R / kGroups * kGroups;
+  else if (NV <= kFlNvB && kGroups * row_bytes <= 2 * flat_tile_bytes(NV))
+    R = kGroups;
   const int64_t spread = (rows + cap - 1) / cap;
   if (R > spread) R = spread;
   if (R < 1) R = 1;
@@ -353,7 +367,8 @@ void launch_flat(const void* x, void* y, float* m, float* l, int64_t rows, int64
   const int grid = static_cast<int>(tiles < cap ? tiles : cap);
   const uint64_t timeout = fault.timeout_ns > 0 ? static_cast<uint64_t>(fault.timeout_ns) : kClTimeoutNs;
   const size_t smem = static_cast<size_t>(stride) * kFlBufs;
-  if (smem > (48u << 10)) {  // above the default limit: raised once per device
+  // above the default limit with the static barriers: raised once per device
+  if (smem + sizeof(uint64_t) * kFlBufs > (48u << 10)) {
     constexpr int kMaxDevices = 64;
     static std::atomic<bool> raised[kMaxDevices];
     int dev = 0;
