@@ -45,9 +45,9 @@ constexpr int kFlMinBlocks = 4;             // CTAs per SM
 constexpr int64_t kFlTileBytes = 14 << 10;  // x bytes per tile, at most
 constexpr int64_t kFlMaxRowBytes = 1024;    // the longest row taken
 constexpr int64_t kFlGridRowBytes = 512;    // the longest taken when every row is on the grid
-constexpr int kFlNvA = 4;                   // 16-byte chunks a thread holds: 4 or 6,
-constexpr int kFlNvB = 6;                   // or 8 for 16-bit rows on the grid that fill
-constexpr int kFlNvC = 8;                   // groups of 2 or 4 threads exactly
+constexpr int kFlNvA = 4;                   // 16-byte chunks a thread holds: 4, 6
+constexpr int kFlNvB = 6;                   // or 8 (the eight-chunk kernels: two
+constexpr int kFlNvC = 8;                   // CTAs an SM, tiles of twice the bytes)
 
 template <int kKind>
 __device__ __forceinline__ void flat_store(unsigned char* yr, int j, float v) {
@@ -400,18 +400,25 @@ void launch_flat_nv(int G, const void* x, void* y, float* m, float* l, int64_t r
 }
 
 // The group for a row spanning `chunks` 16-byte chunks: G threads of NV
-// chunks each (G a power of two up to 32, NV 4 or 6), the pair whose G * NV
-// slots leave the fewest unused, then the one with fewer threads a row (the
-// per-row work -- the group's shuffles, the scale factor, m and l -- is
-// repeated by each of its threads).
+// chunks each (G a power of two up to 32, NV 4, 6 or 8), the pair whose
+// G * NV slots leave the fewest unused, then the one with fewer threads a row
+// (the per-row work -- the group's shuffles, the scale factor, m and l -- is
+// repeated by each of its threads). Eight chunks a thread (two CTAs an SM,
+// tiles of twice the bytes) for rows off the grid, and on it for groups of
+// four threads or more: GB300, 2^28 elements, fraction of the copy peak, bf16
+// rows of 100 columns (off the grid, 4 x 4 -> 2 x 8) 0.685 -> 0.788, fp16 100
+// 0.691 -> 0.807, fp32 101 0.897 -> 0.963, fp32 50 0.881 -> 0.930; on the
+// grid bf16 200 (8 x 4 -> 4 x 8) 0.817 -> 0.863 and fp32 100 0.838 -> 0.869,
+// but bf16 120 (4 x 4 -> 2 x 8) 0.826 -> 0.782.
 template <int kKind, bool kYInStep, bool kYBulk>
-void launch_flat_g(int64_t chunks, const void* x, void* y, float* m, float* l, int64_t rows,
+void launch_flat_g(int64_t chunks, bool on_grid, const void* x, void* y, float* m, float* l, int64_t rows,
                    int64_t cols, int64_t ld_y, const ScaleConsts& k, unsigned int* err,
                    const RowsFault& fault, cudaStream_t stream) {
   int best_g = 32, best_nv = kFlNvA;
   int64_t best_waste = -1;
   for (int g = 1; g <= 32; g *= 2) {
-    for (int nv : {kFlNvA, kFlNvB}) {
+    for (int nv : {kFlNvA, kFlNvB, kFlNvC}) {
+      if (nv == kFlNvC && on_grid && g < 4) continue;
       const int64_t slots = static_cast<int64_t>(g) * nv;
       if (slots < chunks) continue;
       const int64_t waste = slots - chunks;
@@ -424,8 +431,10 @@ void launch_flat_g(int64_t chunks, const void* x, void* y, float* m, float* l, i
   }
   if (best_nv == kFlNvA)
     launch_flat_nv<kKind, kFlNvA, kYInStep, kYBulk>(best_g, x, y, m, l, rows, cols, ld_y, k, err, fault, stream);
-  else
+  else if (best_nv == kFlNvB)
     launch_flat_nv<kKind, kFlNvB, kYInStep, kYBulk>(best_g, x, y, m, l, rows, cols, ld_y, k, err, fault, stream);
+  else
+    launch_flat_nv<kKind, kFlNvC, kYInStep, kYBulk>(best_g, x, y, m, l, rows, cols, ld_y, k, err, fault, stream);
 }
 
 template <int kKind>
@@ -479,11 +488,11 @@ bool flat_rows_as(const void* x, void* y, float* m, float* l, int64_t rows, int6
   // and goes out as one 16-byte store already)
   const bool y_like_x = ld_y == cols && ((reinterpret_cast<uintptr_t>(x) ^ reinterpret_cast<uintptr_t>(y)) & 15u) == 0;
   if (y_like_x && !grid_rows)
-    launch_flat_g<kKind, true, true>(chunks, x, y, m, l, rows, cols, ld_y, k, err, fault, stream);
+    launch_flat_g<kKind, true, true>(chunks, grid_rows, x, y, m, l, rows, cols, ld_y, k, err, fault, stream);
   else if (same_phase(x, y, cols, ld_y, kEsz))
-    launch_flat_g<kKind, true, false>(chunks, x, y, m, l, rows, cols, ld_y, k, err, fault, stream);
+    launch_flat_g<kKind, true, false>(chunks, grid_rows, x, y, m, l, rows, cols, ld_y, k, err, fault, stream);
   else
-    launch_flat_g<kKind, false, false>(chunks, x, y, m, l, rows, cols, ld_y, k, err, fault, stream);
+    launch_flat_g<kKind, false, false>(chunks, grid_rows, x, y, m, l, rows, cols, ld_y, k, err, fault, stream);
   return true;
 }
 
