@@ -530,8 +530,9 @@ inline bool same_phase(const void* x, const void* y, int64_t ld_x, int64_t ld_y,
 bool grouped_rows(int kind, const void* x, void* y, float* m, float* l, int64_t rows, int64_t cols,
                   int64_t ld_x, int64_t ld_y, const ScaleConsts& k, bool on_grid, cudaStream_t stream);
 
-// softmax_cluster.cu: a row per thread-block cluster, held in its shared
-// memory (up to 1.6 MB).
+// softmax_cluster.cu: a row per thread-block cluster, held in its registers
+// (softmax_cluster_regs.cu: aligned rows of up to 131072 16-bit or 65536
+// fp32 elements) or in its shared memory (up to 1.6 MB).
 bool cluster_rows(int kind, const void* x, void* y, float* m, float* l, int64_t rows, int64_t cols,
                   int64_t ld_x, int64_t ld_y, const ScaleConsts& k, unsigned int* err,
                   const RowsFault& fault, cudaStream_t stream);

@@ -17,8 +17,9 @@
 // one read and one write per element. This file holds the kernel for aligned
 // fp32 rows of 2049..16384 elements (a CTA of 256 threads per row);
 // softmax_grouped.cu the kernel for shorter rows (several per CTA) and for
-// 16-bit rows; softmax_cluster.cu the kernel for rows held in a
-// thread-block cluster's shared memory.
+// 16-bit rows; softmax_cluster_regs.cu the kernel for rows held in a
+// thread-block cluster's registers, softmax_cluster.cu the one for rows held
+// in a cluster's shared memory.
 //
 // Streaming path (rows beyond those, or whose x and y are not in step on
 // the 16-byte grid): each thread runs the recurrence over its chunks of the
@@ -445,8 +446,9 @@ void launch_stream(Kernel kernel, const T* x, T* y, float* m, float* l, int64_t 
 // rows of 2049..16384 elements take a CTA each with the row in registers (the
 // kernel the headline workload runs); other rows of up to 2048 fp32 (16384
 // 16-bit, 8192 fp32 off the grid) elements go to the grouped kernel, longer
-// ones of up to 1.6 MB to the cluster-resident kernel, and the rest are
-// streamed.
+// ones of up to 1.6 MB to a cluster (its registers for aligned rows of up to
+// 131072 16-bit or 65536 fp32 elements, else its shared memory), and the rest
+// are streamed.
 cudaError_t launch_softmax_rows(const float* x, float* y, float* m, float* l, int64_t rows,
                                 int64_t cols, int64_t ld_x, int64_t ld_y, float scale,
                                 unsigned int* err_word, const RowsFault& fault, void* ws,
