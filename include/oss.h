@@ -471,7 +471,7 @@ OSS_API os_status os_check_device_error(void* stream, int32_t* code);
  *           memory, every CTA's barrier for the bulk copies of its first row
  *           (or tile) is told to expect 16 bytes more than are copied; the
  *           code is then 2 | (1 << 8). If it holds its rows in a cluster's
- *           registers (rows on the 16-byte grid of 16385..131072 16-bit or
+ *           registers (rows on the 16-byte grid of 18433..131072 16-bit or
  *           20481..65536 fp32 elements), every CTA's barrier for the
  *           cluster's states of its first row expects 16 bytes more than
  *           the states; the code is then 2 | (2 << 8). The wait gives up

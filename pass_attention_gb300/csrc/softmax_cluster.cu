@@ -395,7 +395,7 @@ bool launch_cluster_rows(const void* x, void* y, float* m, float* l, int64_t row
 }  // namespace
 
 // softmax_cluster_regs.cu: aligned rows short enough for a cluster's
-// registers (16-bit up to 131072 elements, fp32 20481..65536), with one
+// registers (16-bit 18433..131072 elements, fp32 20481..65536), with one
 // exponential per element and the states exchanged on mbarriers; false,
 // launching nothing, for other rows.
 bool cluster_reg_rows(int kind, const void* x, void* y, float* m, float* l, int64_t rows, int64_t cols,

@@ -1,6 +1,6 @@
 // G1, rows held in a cluster's registers.
 //
-// Aligned rows of 16385..131072 16-bit or 20481..65536 fp32 elements: a
+// Aligned rows of 18433..131072 16-bit or 20481..65536 fp32 elements: a
 // thread-block cluster of C <= 8 CTAs of 256 threads holds one row, CTA r
 // holding slice r (at most 256 * 8 chunks of 16 bytes, NV chunks a thread).
 // Each thread widens its chunks, forms its weights 2^(x*c - M_t) once (one
@@ -255,6 +255,10 @@ bool cluster_reg_rows(int kind, const void* x, void* y, float* m, float* l, int6
   // holds them in one CTA without an exchange (fp32 17000 columns: 0.96 of
   // the copy peak there, 0.92 here)
   if (kind == 0) return cols > 20480 && clreg_rows<0>(x, y, m, l, rows, cols, ld_x, ld_y, k, err, fault, stream);
+  // 16-bit rows of at most 36 KB likewise (one CTA there, with two buffers;
+  // here two CTAs of five chunks a thread, a fifth of them empty: bf16 16400
+  // columns 0.785 there, 0.714 here; 20000 0.757 there, 0.846 here)
+  if (cols <= 18432) return false;
   if (kind == 1) return clreg_rows<1>(x, y, m, l, rows, cols, ld_x, ld_y, k, err, fault, stream);
   return clreg_rows<2>(x, y, m, l, rows, cols, ld_x, ld_y, k, err, fault, stream);
 }

@@ -45,7 +45,9 @@ F32_CASES = [
     (409601, 9),     # beyond: the streaming kernel
 ]
 H16_CASES = [
-    (16385, 301),    # registers: 2 CTAs of 5 chunks a thread
+    (16385, 301),    # 32 KB: one CTA, two buffers
+    (18432, 301),    # 36 KB: the longest that stays in one CTA's two buffers
+    (18440, 301),    # registers: 2 CTAs of 5 chunks a thread
     (20000, 401),    # registers: 2 CTAs of 5
     (24000, 301),    # registers: 2 CTAs of 6
     (32768, 200),    # registers: 2 CTAs of 8
