@@ -167,7 +167,7 @@ typedef enum os_dtype {
  * y's rows start at the same offsets from a 16-byte boundary, rows of up to
  * 16384 elements are held in registers and longer rows of up to 1.6 MB by a
  * cluster, as for os_softmax_rows (in its registers for rows on the 16-byte
- * grid of up to 131072 elements; one read, one write per
+ * grid of 18433..131072 elements; one read, one write per
  * element, the same granule reads at the ends of a row off the grid). Short
  * rows of a matrix whose x rows lie back to back are staged in shared memory
  * by tiles as for os_softmax_rows, with y at any layout; other rows are
