@@ -188,6 +188,44 @@ OSS_API os_status os_softmax_rows_16bit_ws(const void* x, void* y, float* m, flo
                                            void* workspace, int64_t workspace_bytes, void* stream);
 
 /*
+ * os_softmax_rows_from_host -- os_softmax_rows on rows that sit in host
+ * memory: the library copies x up, runs the row softmax and copies y (and m,
+ * l) back. The pages define no host-side call; this is the end-to-end form
+ * of the row softmax (the curionode page's "one pass, exactly": the row is
+ * read once), for a caller whose rows live on the host.
+ *   x_host [rows, cols] fp32, host, dense (leading dimension cols); read.
+ *   y_host [rows, cols] fp32, host, dense; written.
+ *   m_host, l_host [rows] fp32, host, or NULL to skip (natural units, as
+ *         os_softmax_rows).
+ *   x_dev, y_dev [rows, cols] fp32, device, dense, owned by the caller: the
+ *         staging copies (x_dev ends up holding x, y_dev holding y).
+ *   m_dev, l_dev [rows] fp32, device, owned by the caller; required when
+ *         m_host (l_host) is given, else may be NULL.
+ *   rows >= 1; cols >= 1; scale finite and > 0; chunk_rows >= 0 (rows per
+ *   block; 0: about 64 MiB of x a block).
+ * The rows go in blocks of chunk_rows: block b's upload, kernel and
+ * download run on three streams (two copy streams the library makes once
+ * per device, and `stream` for the kernels), so block b + 1 uploads while
+ * block b computes and block b - 1 downloads. The copies start after the
+ * work already enqueued on `stream`, and `stream` waits for the last
+ * download: the call returns at once, and the host outputs are complete when
+ * `stream` is (synchronise it before reading them or freeing any buffer).
+ * Host buffers must be page-locked (cudaHostAlloc, or pinned by the caller)
+ * for the copies to overlap; pageable memory gives the same results, with
+ * copies that do not overlap. Every row gets the kernel os_softmax_rows gives
+ * it, so the results equal those of os_softmax_rows on x_dev. Creates and
+ * releases four CUDA events per call; allocates no memory.
+ * Errors: OS_ERR_INVALID_ARGUMENT (null x_host, y_host, x_dev or y_dev; a
+ *         host m or l without its device buffer; a bad size or scale),
+ *         OS_ERR_MISALIGNED (a device buffer not 4-byte aligned),
+ *         OS_ERR_CUDA (a copy, an event or a launch failed; outputs undefined).
+ */
+OSS_API os_status os_softmax_rows_from_host(const float* x_host, float* y_host, float* m_host,
+                                            float* l_host, float* x_dev, float* y_dev, float* m_dev,
+                                            float* l_dev, int64_t rows, int64_t cols, float scale,
+                                            int64_t chunk_rows, void* stream);
+
+/*
  * os_softmax_rows_multipass -- the same outputs as os_softmax_rows, computed
  * the way the curionode page describes the methods the online form replaces
  * (introduction): passes = 3 is the safe softmax -- a maximum pass, a sum pass

@@ -69,6 +69,8 @@ _SIGNATURES = {
     "os_softmax_rows_16bit_ws": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _f32, _i32, _vp,
                                         _i64, _vp]),
     "os_softmax_rows_workspace_bytes": (_i64, [_i64, _i64, _i32]),
+    "os_softmax_rows_from_host": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _f32, _i64,
+                                         _vp]),
     "os_softmax_rows_multipass": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _f32, _i32,
                                          _vp]),
     "os_attention_fwd": (_i32, [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _f32,
@@ -320,52 +322,46 @@ def softmax_rows_multipass(x: torch.Tensor, passes: int, scale: float = 1.0,
 def softmax_rows_from_host(x_host: torch.Tensor, scale: float = 1.0, out=None, device="cuda",
                            chunk_rows: Optional[int] = None, x_dev: Optional[torch.Tensor] = None,
                            y_dev: Optional[torch.Tensor] = None):
-    """End-to-end call on host memory: copy x to the GPU, run os_softmax_rows,
-    copy y, m and l back into (pinned) host tensors. Returns host (y, m, l).
-
-    The rows are processed in blocks of ``chunk_rows`` (default: about 64 MiB
-    of x per block) on three streams: the upload of block i + 1, the kernel
-    on block i and the download of block i - 1 overlap, so the host link
-    carries both directions at once. ``x_dev`` / ``y_dev`` are optional
-    device buffers of x's shape to reuse across calls."""
-    if x_host.dim() != 2 or x_host.dtype != torch.float32 or x_host.is_cuda:
+    """End-to-end call on host memory through os_softmax_rows_from_host: the
+    library copies x to the GPU, runs the row softmax and copies y, m and l
+    back into (pinned) host tensors, in blocks of ``chunk_rows`` rows (default:
+    about 64 MiB of x a block) whose upload, kernel and download overlap.
+    Returns host (y, m, l) once the stream has finished them. ``x_dev`` /
+    ``y_dev`` are optional device buffers of x's shape to reuse across calls."""
+    if not isinstance(x_host, torch.Tensor) or x_host.dim() != 2 or x_host.dtype != torch.float32 \
+            or x_host.is_cuda:
         raise ValueError("x_host must be a 2-D float32 host tensor")
+    _dense(x_host, "x_host")
     rows, cols = x_host.shape
+    dev = torch.device(device)
+    if dev.type == "cuda" and dev.index is None:
+        dev = torch.device("cuda", torch.cuda.current_device())
     if out is None:
         out = (torch.empty((rows, cols), dtype=torch.float32, pin_memory=True),
                torch.empty(rows, dtype=torch.float32, pin_memory=True),
                torch.empty(rows, dtype=torch.float32, pin_memory=True))
     y_host, m_host, l_host = out
-    if x_dev is None:
-        x_dev = torch.empty((rows, cols), dtype=torch.float32, device=device)
-    if y_dev is None:
-        y_dev = torch.empty((rows, cols), dtype=torch.float32, device=device)
-    m_dev = torch.empty(rows, dtype=torch.float32, device=device)
-    l_dev = torch.empty(rows, dtype=torch.float32, device=device)
-    if chunk_rows is None:
-        chunk_rows = max(1, (64 << 20) // max(1, cols * 4))
-    main = torch.cuda.current_stream(x_dev.device)
-    s_in = torch.cuda.Stream(device=x_dev.device)
-    s_out = torch.cuda.Stream(device=x_dev.device)
-    s_in.wait_stream(main)   # buffers may still be in use by earlier work on main
-    s_out.wait_stream(main)
-    for r0 in range(0, rows, chunk_rows):
-        r1 = min(rows, r0 + chunk_rows)
-        with torch.cuda.stream(s_in):
-            x_dev[r0:r1].copy_(x_host[r0:r1], non_blocking=True)
-        main.wait_stream(s_in)
-        softmax_rows(x_dev[r0:r1], scale, y=y_dev[r0:r1], m=m_dev[r0:r1], l=l_dev[r0:r1],
-                     stream=main)
-        s_out.wait_stream(main)
-        with torch.cuda.stream(s_out):
-            y_host[r0:r1].copy_(y_dev[r0:r1], non_blocking=True)
-            m_host[r0:r1].copy_(m_dev[r0:r1], non_blocking=True)
-            l_host[r0:r1].copy_(l_dev[r0:r1], non_blocking=True)
-    main.wait_stream(s_out)
-    for t in (x_dev, y_dev, m_dev, l_dev):
-        t.record_stream(s_in)
-        t.record_stream(s_out)
-    s_out.synchronize()
+    for name, t, shape in (("y_host", y_host, (rows, cols)), ("m_host", m_host, (rows,)),
+                           ("l_host", l_host, (rows,))):
+        if not isinstance(t, torch.Tensor) or t.is_cuda or t.dtype != torch.float32 \
+                or tuple(t.shape) != shape or not t.is_contiguous():
+            raise ValueError(f"{name} must be a dense float32 host tensor of shape {shape}")
+    x_dev = torch.empty((rows, cols), dtype=torch.float32, device=dev) if x_dev is None \
+        else _out(x_dev, "x_dev", torch.float32, (rows, cols), dev)
+    y_dev = torch.empty((rows, cols), dtype=torch.float32, device=dev) if y_dev is None \
+        else _out(y_dev, "y_dev", torch.float32, (rows, cols), dev)
+    m_dev = torch.empty(rows, dtype=torch.float32, device=dev)
+    l_dev = torch.empty(rows, dtype=torch.float32, device=dev)
+    if chunk_rows is not None and chunk_rows < 1:
+        raise ValueError("chunk_rows must be at least 1")
+    with torch.cuda.device(dev):
+        stream = torch.cuda.current_stream(dev)
+        st = load().os_softmax_rows_from_host(
+            x_host.data_ptr(), y_host.data_ptr(), m_host.data_ptr(), l_host.data_ptr(),
+            x_dev.data_ptr(), y_dev.data_ptr(), m_dev.data_ptr(), l_dev.data_ptr(), rows, cols,
+            ctypes.c_float(scale), 0 if chunk_rows is None else int(chunk_rows), stream.cuda_stream)
+        _check(st, "os_softmax_rows_from_host")
+        stream.synchronize()
     return out
 
 

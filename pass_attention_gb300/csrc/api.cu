@@ -1,10 +1,13 @@
 // The C ABI of liboss (include/oss.h): host-side validation, then launch.
-// Nothing here synchronises, allocates or prints.
+// Nothing here synchronises, allocates device memory or prints.
+// os_softmax_rows_from_host creates four CUDA events per call (released at
+// its end) and, once per device, two copy streams.
 
 #include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 
 #include <cuda_runtime.h>
 
@@ -55,6 +58,70 @@ thread_local oss::RowsFault t_rows_fault;
 // Set by os_attention_set_rescale_policy; kept for the host thread's later
 // attention calls.
 thread_local int t_rescale_policy = OS_RESCALE_THRESHOLD;
+
+// The two copy streams of os_softmax_rows_from_host on the current device
+// (non-blocking, made on first use and kept for the process).
+cudaError_t copy_streams(cudaStream_t* up, cudaStream_t* down) {
+  static std::mutex mu;
+  static cudaStream_t streams[kMaxDevices][2];
+  static bool made[kMaxDevices];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!made[dev]) {
+    if ((e = cudaStreamCreateWithFlags(&streams[dev][0], cudaStreamNonBlocking)) != cudaSuccess) return e;
+    if ((e = cudaStreamCreateWithFlags(&streams[dev][1], cudaStreamNonBlocking)) != cudaSuccess) {
+      cudaStreamDestroy(streams[dev][0]);
+      return e;
+    }
+    made[dev] = true;
+  }
+  *up = streams[dev][0];
+  *down = streams[dev][1];
+  return cudaSuccess;
+}
+
+// The pipeline of os_softmax_rows_from_host over blocks of chunk_rows rows:
+// a block's upload on `up`, its kernel on `main` once the upload landed, its
+// downloads on `down` once the kernel ended. `up` and `down` start after the
+// work already on `main`, and `main` ends after the last download. A wait
+// enqueued on an event keeps the record it saw, so each event is recorded
+// again for the next block.
+cudaError_t from_host_pipeline(const float* x_host, float* y_host, float* m_host, float* l_host,
+                               float* x_dev, float* y_dev, float* m_dev, float* l_dev, int64_t rows,
+                               int64_t cols, float scale, int64_t chunk_rows, cudaStream_t main,
+                               cudaStream_t up, cudaStream_t down, const cudaEvent_t* ev) {
+  cudaError_t e;
+  if ((e = cudaEventRecord(ev[0], main)) != cudaSuccess) return e;
+  if ((e = cudaStreamWaitEvent(up, ev[0], 0)) != cudaSuccess) return e;
+  if ((e = cudaStreamWaitEvent(down, ev[0], 0)) != cudaSuccess) return e;
+  for (int64_t r0 = 0; r0 < rows; r0 += chunk_rows) {
+    const int64_t n = (rows - r0 < chunk_rows) ? rows - r0 : chunk_rows;
+    const int64_t off = r0 * cols;
+    const size_t bytes = static_cast<size_t>(n * cols) * sizeof(float);
+    const size_t vb = static_cast<size_t>(n) * sizeof(float);
+    if ((e = cudaMemcpyAsync(x_dev + off, x_host + off, bytes, cudaMemcpyHostToDevice, up)) != cudaSuccess)
+      return e;
+    if ((e = cudaEventRecord(ev[1], up)) != cudaSuccess) return e;
+    if ((e = cudaStreamWaitEvent(main, ev[1], 0)) != cudaSuccess) return e;
+    if ((e = oss::launch_softmax_rows(x_dev + off, y_dev + off, m_dev ? m_dev + r0 : nullptr,
+                                      l_dev ? l_dev + r0 : nullptr, n, cols, cols, cols, scale,
+                                      error_word(), oss::RowsFault(), nullptr, 0, main)) != cudaSuccess)
+      return e;
+    if ((e = cudaEventRecord(ev[2], main)) != cudaSuccess) return e;
+    if ((e = cudaStreamWaitEvent(down, ev[2], 0)) != cudaSuccess) return e;
+    if ((e = cudaMemcpyAsync(y_host + off, y_dev + off, bytes, cudaMemcpyDeviceToHost, down)) != cudaSuccess)
+      return e;
+    if (m_host && (e = cudaMemcpyAsync(m_host + r0, m_dev + r0, vb, cudaMemcpyDeviceToHost, down)) != cudaSuccess)
+      return e;
+    if (l_host && (e = cudaMemcpyAsync(l_host + r0, l_dev + r0, vb, cudaMemcpyDeviceToHost, down)) != cudaSuccess)
+      return e;
+  }
+  if ((e = cudaEventRecord(ev[3], down)) != cudaSuccess) return e;
+  return cudaStreamWaitEvent(main, ev[3], 0);
+}
 
 }  // namespace
 
@@ -130,6 +197,37 @@ int64_t os_softmax_rows_workspace_bytes(int64_t rows, int64_t cols, int32_t dtyp
   if (rows <= 0 || cols <= 0) return 0;
   if (dtype != 0 && dtype != OS_DTYPE_BF16 && dtype != OS_DTYPE_F16) return 0;
   return oss::softmax_workspace_bytes(cols * (dtype == 0 ? 4 : 2));
+}
+
+os_status os_softmax_rows_from_host(const float* x_host, float* y_host, float* m_host, float* l_host,
+                                    float* x_dev, float* y_dev, float* m_dev, float* l_dev,
+                                    int64_t rows, int64_t cols, float scale, int64_t chunk_rows,
+                                    void* stream) {
+  if (!x_host || !y_host || !x_dev || !y_dev) return OS_ERR_INVALID_ARGUMENT;
+  if ((m_host && !m_dev) || (l_host && !l_dev)) return OS_ERR_INVALID_ARGUMENT;
+  if (rows <= 0 || cols <= 0 || chunk_rows < 0) return OS_ERR_INVALID_ARGUMENT;
+  if (cols > (int64_t(1) << 30) || rows > (int64_t(1) << 40)) return OS_ERR_INVALID_ARGUMENT;
+  if (!valid_scale(scale)) return OS_ERR_INVALID_ARGUMENT;
+  if ((reinterpret_cast<uintptr_t>(x_dev) | reinterpret_cast<uintptr_t>(y_dev) |
+       reinterpret_cast<uintptr_t>(m_dev) | reinterpret_cast<uintptr_t>(l_dev)) & 3u)
+    return OS_ERR_MISALIGNED;
+  if (chunk_rows == 0) {  // about 64 MiB of x a block
+    chunk_rows = (int64_t(64) << 20) / (cols * 4);
+    if (chunk_rows < 1) chunk_rows = 1;
+  }
+  cudaStream_t up = nullptr, down = nullptr;
+  cudaError_t e = copy_streams(&up, &down);
+  if (e != cudaSuccess) return from_cuda(e);
+  cudaEvent_t ev[4] = {nullptr, nullptr, nullptr, nullptr};
+  for (int i = 0; i < 4 && e == cudaSuccess; ++i) e = cudaEventCreateWithFlags(&ev[i], cudaEventDisableTiming);
+  if (e == cudaSuccess)
+    e = from_host_pipeline(x_host, y_host, m_host, l_host, x_dev, y_dev, m_dev, l_dev, rows, cols, scale,
+                           chunk_rows, static_cast<cudaStream_t>(stream), up, down, ev);
+  // an event destroyed while work it was recorded on is pending is released
+  // once that work completes: this does not wait
+  for (int i = 0; i < 4; ++i)
+    if (ev[i]) cudaEventDestroy(ev[i]);
+  return from_cuda(e);
 }
 
 os_status os_softmax_rows_multipass(const float* x, float* y, float* m, float* l, int64_t rows,

@@ -63,6 +63,29 @@ def test_softmax_rows_rejects_bad_arguments(lib):
     assert f(A, A, None, A + 1, 4, 8, 8, 8, 1.0, None) == MISALIGNED   # l
 
 
+def test_softmax_rows_from_host_rejects_bad_arguments(lib):
+    f = lib.os_softmax_rows_from_host
+    ok = dict(xh=A, yh=A, mh=A, lh=A, xd=A, yd=A, md=A, ld=A)
+
+    def call(rows=4, cols=8, scale=1.0, chunk=0, **kw):
+        a = dict(ok, **kw)
+        return f(a["xh"], a["yh"], a["mh"], a["lh"], a["xd"], a["yd"], a["md"], a["ld"], rows, cols,
+                 ctypes.c_float(scale), chunk, None)
+    assert call(xh=None) == INVALID
+    assert call(yh=None) == INVALID
+    assert call(xd=None) == INVALID
+    assert call(yd=None) == INVALID
+    assert call(md=None) == INVALID            # host m without its device buffer
+    assert call(ld=None) == INVALID            # host l without its device buffer
+    assert call(rows=0) == INVALID
+    assert call(cols=0) == INVALID
+    assert call(chunk=-1) == INVALID
+    assert call(scale=0.0) == INVALID
+    assert call(scale=float("nan")) == INVALID
+    assert call(xd=A + 2) == MISALIGNED
+    assert call(ld=A + 1) == MISALIGNED
+
+
 def test_softmax_rows_multipass_rejects_bad_arguments(lib):
     f = lib.os_softmax_rows_multipass
     for passes in (2, 3):

@@ -110,10 +110,35 @@ def test_full_size_softmax_32k_every_row():
 
 @pytest.mark.parametrize("rows,cols,chunk", [(1000, 4096, 300), (37, 1000, None), (5, 7, 2)])
 def test_from_host_pipelined_matches_device_call(rows, cols, chunk):
-    # the host-buffer path copies and computes in row blocks on three streams;
-    # every row sees the same kernel, so the results are identical
+    # os_softmax_rows_from_host copies and computes in row blocks on three
+    # streams; every row sees the same kernel, so the results are identical
     x = workloads.logits(rows, cols, 10.0, seed=rows + cols, device="cuda")
     y_ref, m_ref, l_ref = oss.softmax_rows(x, 0.5)
     torch.cuda.synchronize()
     yh, mh, lh = oss.softmax_rows_from_host(x.cpu().pin_memory(), 0.5, chunk_rows=chunk)
     assert torch.equal(yh, y_ref.cpu()) and torch.equal(mh, m_ref.cpu()) and torch.equal(lh, l_ref.cpu())
+
+
+def test_from_host_c_call_without_m_and_l_after_prior_work():
+    # the C call with no m and l, in blocks that do not divide the rows; the
+    # device staging buffer is overwritten on the stream just before the call,
+    # so an upload that did not wait for that work would leave NaN behind
+    import ctypes
+    rows, cols = 301, 2500
+    x = workloads.logits(rows, cols, 10.0, seed=17, device="cuda")
+    y_ref, _, _ = oss.softmax_rows(x, 0.7)
+    torch.cuda.synchronize()
+    xh = x.cpu().pin_memory()
+    yh = torch.empty((rows, cols), dtype=torch.float32, pin_memory=True)
+    x_dev = torch.empty_like(x)
+    y_dev = torch.empty_like(x)
+    stream = torch.cuda.current_stream()
+    x_dev.fill_(float("nan"))
+    st = oss.load().os_softmax_rows_from_host(
+        xh.data_ptr(), yh.data_ptr(), None, None, x_dev.data_ptr(), y_dev.data_ptr(), None, None,
+        rows, cols, ctypes.c_float(0.7), 64, stream.cuda_stream)
+    assert st == 0, oss.load().os_status_string(st)
+    stream.synchronize()
+    assert oss.check_device_error() == 0
+    assert torch.equal(yh, y_ref.cpu())
+    assert torch.equal(x_dev, x) and torch.equal(y_dev, y_ref)
