@@ -13,8 +13,9 @@
  *
  * Conventions shared by every call
  * --------------------------------
- * - Tensors are DEVICE pointers allocated and owned by the caller. The
- *   library never allocates, frees or keeps them.
+ * - Tensors are DEVICE pointers allocated and owned by the caller (besides
+ *   them, os_softmax_rows_from_host takes host pointers). The library never
+ *   allocates, frees or keeps them.
  * - Layouts are row-major; the attention tensors are dense [B, H, S, D].
  * - Each call validates its arguments on the host, then enqueues its kernels
  *   on `stream` (a cudaStream_t passed as void*; NULL = the legacy default
